@@ -1,0 +1,16 @@
+"""Float64 CPU oracle for the attention forward -- test infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline and
+reference legs may import this package.  The library never does.
+"""
+
+from .attention import (  # noqa: F401
+    attention_dense,
+    attention_paged,
+    attention_single,
+    attention_varlen,
+    check_cu_seqlens,
+    paged_gather,
+    softmax_weights,
+    visible_mask,
+)

@@ -1,0 +1,213 @@
+"""Float64 CPU oracle for the fused scaled-dot-product attention forward.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the library imports this module; only
+``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may call it.  It shares no code with
+the CUDA path.
+
+What it computes (the plain definition, score matrix materialised):
+
+    s[i, j]  = scale * <q[i, h], k[j, kv(h)]>           for visible (i, j)
+    out[i,h] = sum_j exp(s[i,j] - M_i) v[j, kv(h)] / sum_j exp(s[i,j] - M_i)
+    lse[h,i] = M_i + ln sum_j exp(s[i,j] - M_i),        M_i = max_j s[i,j]
+
+Sources, by page and section:
+
+* Output and log-sum-exp pair: vllm-omni ``flash_attn.py``,
+  ``FlashAttentionImpl._unwrap_flash_output`` (the FlashAttention call may
+  return ``(out, lse)``); vllm-ascend ``attention_v1.py``,
+  ``AscendAttentionBackendImpl.full_graph_fia`` (``softmax_lse`` output).
+* Explicit softmax scale: ``flash_attn.py``, ``FlashAttentionImpl.__init__``.
+* Causal masking is bottom-right aligned: ``flash_attn.py``,
+  ``FlashAttentionImpl.forward_fa_npu`` -- key position kp is blocked for query
+  position qp iff ``kp > qp + (Sk - Sq)``.
+* Rows with no visible key ("invalid-row handling" in ``forward_fa_npu``):
+  reading taken here -- out = 0 and lse = -inf, which also matches the
+  "padded rows come back zero" convention of vllm-omni ``fastvideo_vsa.py``
+  (SDPA fallback with packed padding).
+* GQA: ``attention_v1.py``, ``AscendAttentionBackendImpl.__init__``
+  (``num_heads % num_kv_heads == 0``, ``num_queries_per_kv``); reading taken
+  here -- query head h reads KV head ``h // (Hq // Hkv)``.
+* Packed documents: ``flash_attn.py``, ``FlashAttentionImpl._forward_varlen_packed``
+  (attention only inside ``[cu_seqlens[i], cu_seqlens[i+1])``) and
+  ``FlashAttentionImpl._flash_varlen_wrapper`` (dense == varlen with
+  ``arange`` cu_seqlens).
+* Paged cache ``(2, num_blocks, block_size, num_kv_heads, head_size)``:
+  ``attention_v1.py``, ``AscendAttentionBackend.get_kv_cache_shape``; token t
+  of sequence s sits at slot ``block_table[s, t // block_size] * block_size +
+  t % block_size`` (``AscendMetadata.slot_mapping`` comment);
+  ``AscendAttentionBackendImpl.forward_paged_attention`` reads the cache
+  through ``block_tables`` and ``seq_lens`` (``context_lens``).
+
+Every array argument is converted to float64 first; bf16 inputs convert
+exactly, so the oracle sees the same numbers the kernels see.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(x) -> np.ndarray:
+    """Exact conversion to a float64 ndarray (torch tensors go through float32)."""
+    if hasattr(x, "detach"):  # torch tensor; bf16 -> fp32 is exact
+        x = x.detach().to("cpu").float().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def _i64(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.asarray(x, dtype=np.int64)
+
+
+def visible_mask(lq: int, lk: int, causal: bool, rows=None) -> np.ndarray:
+    """Boolean [len(rows), lk]: True where query row i may attend key j.
+
+    Non-causal: every key of the document.  Causal: bottom-right aligned,
+    j <= i + (lk - lq) (``flash_attn.py``, ``FlashAttentionImpl.forward_fa_npu``).
+    """
+    i = np.arange(lq) if rows is None else np.asarray(rows, dtype=np.int64)
+    j = np.arange(lk)
+    if not causal:
+        return np.ones((i.size, lk), dtype=bool)
+    return j[None, :] <= i[:, None] + (lk - lq)
+
+
+def attention_single(q, k, v, scale: float, causal: bool, rows=None):
+    """One document.
+
+    q: [Lq, Hq, D]; k, v: [Lk, Hkv, D] (any float dtype).
+    rows: optional iterable of query rows to evaluate (default: all).
+    Returns out [R, Hq, D] and lse [Hq, R] (float64), R = number of rows.
+    Rows that see no key get out = 0 and lse = -inf.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    lq, hq, d = q.shape
+    lk, hkv, dk = k.shape
+    if dk != d or v.shape != k.shape:
+        raise ValueError("k and v must both be [Lk, Hkv, D] with D matching q")
+    if hkv == 0 or hq % hkv != 0:
+        raise ValueError("num_heads must be a multiple of num_kv_heads")
+    group = hq // hkv
+    rows = np.arange(lq) if rows is None else np.asarray(rows, dtype=np.int64)
+    r = rows.size
+    out = np.zeros((r, hq, d))
+    lse = np.full((hq, r), -np.inf)
+    if r == 0 or lk == 0:
+        return out, lse
+    vis = visible_mask(lq, lk, causal, rows)
+    live = vis.any(axis=1)
+    for h in range(hq):
+        kv = h // group
+        s = scale * (q[rows, h, :] @ k[:, kv, :].T)  # [R, Lk]
+        s = np.where(vis, s, -np.inf)
+        m = np.where(live, s.max(axis=1), 0.0)
+        p = np.where(vis, np.exp(s - m[:, None]), 0.0)
+        l = p.sum(axis=1)
+        num = p @ v[:, kv, :]
+        out[live, h, :] = num[live] / l[live, None]
+        lse[h, live] = m[live] + np.log(l[live])
+    return out, lse
+
+
+def attention_dense(q, k, v, scale: float, causal: bool):
+    """Fixed-length batch (vllm-omni ``flash_attn.py``, dense ``flash_attn_func`` route).
+
+    q: [B, Sq, Hq, D]; k, v: [B, Sk, Hkv, D].
+    Returns out [B, Sq, Hq, D] and lse [B, Hq, Sq].
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    b, sq, hq, d = q.shape
+    out = np.zeros((b, sq, hq, d))
+    lse = np.full((b, hq, sq), -np.inf)
+    for bi in range(b):
+        out[bi], lse[bi] = attention_single(q[bi], k[bi], v[bi], scale, causal)
+    return out, lse
+
+
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool):
+    """Packed documents (``flash_attn.py``, ``FlashAttentionImpl._forward_varlen_packed``).
+
+    q: [Tq, Hq, D]; k, v: [Tk, Hkv, D]; cu_seqlens_q/k: [N+1] non-decreasing,
+    starting at 0 and ending at Tq / Tk.  Document n owns query rows
+    [cu_q[n], cu_q[n+1]) and key rows [cu_k[n], cu_k[n+1]); nothing attends
+    across documents.  Returns out [Tq, Hq, D] and lse [Hq, Tq].
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    cq, ck = _i64(cu_seqlens_q), _i64(cu_seqlens_k)
+    check_cu_seqlens(cq, q.shape[0])
+    check_cu_seqlens(ck, k.shape[0])
+    if cq.size != ck.size:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k describe different document counts")
+    tq, hq, d = q.shape
+    out = np.zeros((tq, hq, d))
+    lse = np.full((hq, tq), -np.inf)
+    for n in range(cq.size - 1):
+        qs, qe, ks, ke = cq[n], cq[n + 1], ck[n], ck[n + 1]
+        o, l = attention_single(q[qs:qe], k[ks:ke], v[ks:ke], scale, causal)
+        out[qs:qe] = o
+        lse[:, qs:qe] = l
+    return out, lse
+
+
+def check_cu_seqlens(cu, total: int) -> None:
+    cu = _i64(cu)
+    if cu.ndim != 1 or cu.size < 1 or cu[0] != 0 or cu[-1] != total or np.any(np.diff(cu) < 0):
+        raise ValueError(f"cu_seqlens must start at 0, be non-decreasing and end at {total}")
+
+
+def paged_gather(kv_cache, block_table, seq_lens):
+    """Contiguous K and V of each sequence read through its block table.
+
+    kv_cache: [2, num_blocks, block_size, Hkv, D]; block_table: [S, max_blocks];
+    seq_lens: [S].  Token t of sequence s is slot ``block_table[s, t // bs] *
+    bs + t % bs`` (``attention_v1.py``, ``AscendMetadata.slot_mapping``).
+    Returns two lists of [L_s, Hkv, D] float64 arrays.
+    """
+    cache = _f64(kv_cache)
+    bt, sl = _i64(block_table), _i64(seq_lens)
+    _, nb, bs, hkv, d = cache.shape
+    ks, vs = [], []
+    for s in range(sl.size):
+        t = np.arange(sl[s])
+        blocks = bt[s, t // bs]
+        if t.size and (blocks.min() < 0 or blocks.max() >= nb):
+            raise ValueError(f"block_table row {s} points outside the cache")
+        ks.append(cache[0, blocks, t % bs])
+        vs.append(cache[1, blocks, t % bs])
+    return ks, vs
+
+
+def attention_paged(q, kv_cache, block_table, seq_lens, scale: float):
+    """Decode over a paged cache (``attention_v1.py``, ``forward_paged_attention``).
+
+    q: [S, Hq, D], one query token per sequence.  With one query the
+    bottom-right causal mask shows it the whole context, so causal has no
+    effect here.  Returns out [S, Hq, D] and lse [S, Hq].
+    """
+    q = _f64(q)
+    s_count, hq, d = q.shape
+    ks, vs = paged_gather(kv_cache, block_table, seq_lens)
+    out = np.zeros((s_count, hq, d))
+    lse = np.full((s_count, hq), -np.inf)
+    for s in range(s_count):
+        o, l = attention_single(q[s:s + 1], ks[s], vs[s], scale, causal=False)
+        out[s] = o[0]
+        lse[s] = l[:, 0]
+    return out, lse
+
+
+def softmax_weights(q, k, scale: float, causal: bool, head: int):
+    """The attention weights of one head, [Lq, Lk] (for invariant checks)."""
+    q, k = _f64(q), _f64(k)
+    lq, hq, _ = q.shape
+    lk, hkv, _ = k.shape
+    kv = head // (hq // hkv)
+    vis = visible_mask(lq, lk, causal)
+    s = np.where(vis, scale * (q[:, head, :] @ k[:, kv, :].T), -np.inf)
+    live = vis.any(axis=1)
+    m = np.where(live, s.max(axis=1), 0.0)
+    p = np.where(vis, np.exp(s - m[:, None]), 0.0)
+    l = p.sum(axis=1)
+    return np.where(live[:, None], p / np.where(live, l, 1.0)[:, None], 0.0)

@@ -1,0 +1,330 @@
+"""Pins of the float64 oracle against facts fixed outside it.
+
+Each pin is chosen so that a plausible slip in the oracle fails it: a wrong
+mask offset (causal pins, q = 0 closed form), a wrong GQA head map (one-hot
+routing), K and V indices mixed up (joint vs V-only permutation), a dropped
+normalisation (V = const, weights sum to one), a wrong LSE (hand-worked
+values, Decimal brute force, scipy's logsumexp), broken document or block
+indexing (pack vs separate runs, paged scatter vs contiguous).
+"""
+
+import json
+import math
+import os
+from decimal import Decimal, getcontext
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+def _rand(*shape):
+    return rng.standard_normal(shape)
+
+
+# ---------------------------------------------------------------- hand-worked
+
+def _golden_cases():
+    with open(os.path.join(GOLDEN, "hand_worked.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c["name"])
+def test_hand_worked(case):
+    q = np.array(case["q_full"], dtype=np.float64)
+    k = np.array(case["k"], dtype=np.float64)
+    v = np.array(case["v"], dtype=np.float64)
+    out, lse = oracle.attention_single(q, k, v, case["scale"], case["causal"])
+    want_lse = np.array([[float(x) for x in row] for row in case["lse"]])
+    np.testing.assert_allclose(out, np.array(case["out"]), rtol=0, atol=1e-13)
+    fin = np.isfinite(want_lse)
+    assert np.array_equal(np.isfinite(lse), fin)
+    np.testing.assert_allclose(lse[fin], want_lse[fin], rtol=0, atol=1e-13)
+    assert np.all(lse[~fin] == -np.inf)
+
+
+# --------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("lq,lk", [(5, 5), (3, 7), (7, 3), (1, 9)])
+def test_zero_query_is_mean_of_visible_values(causal, lq, lk):
+    """q = 0 makes every visible score 0: out = mean of the visible V rows and
+    lse = ln(number visible); the bottom-right rule gives row i
+    clip(i + 1 + lk - lq, 0, lk) visible keys."""
+    hq, hkv, d = 6, 3, 4
+    q = np.zeros((lq, hq, d))
+    k, v = _rand(lk, hkv, d), _rand(lk, hkv, d)
+    out, lse = oracle.attention_single(q, k, v, 0.3, causal)
+    for i in range(lq):
+        n = lk if not causal else min(lk, max(0, i + 1 + lk - lq))
+        for h in range(hq):
+            kv = h // (hq // hkv)
+            if n == 0:
+                assert np.all(out[i, h] == 0) and lse[h, i] == -np.inf
+            else:
+                np.testing.assert_allclose(out[i, h], v[:n, kv].mean(axis=0), atol=1e-13)
+                assert abs(lse[h, i] - math.log(n)) < 1e-13
+
+
+def test_single_key_returns_its_value_row():
+    d = 16
+    q, k, v = _rand(4, 2, d), _rand(1, 1, d), _rand(1, 1, d)
+    out, lse = oracle.attention_single(q, k, v, 0.25, False)
+    for h in range(2):
+        np.testing.assert_array_equal(out[:, h], np.repeat(v[:, 0], 4, axis=0))
+        np.testing.assert_allclose(lse[h], 0.25 * q[:, h] @ k[0, 0], atol=1e-13)
+
+
+def test_identical_value_rows_and_constant_values():
+    lq, lk, d = 6, 11, 8
+    q, k = _rand(lq, 2, d), _rand(lk, 2, d)
+    row = _rand(d)
+    v = np.broadcast_to(row, (lk, 2, d)).copy()
+    out, _ = oracle.attention_single(q, k, v, 0.5, True)
+    np.testing.assert_allclose(out, np.broadcast_to(row, out.shape), atol=1e-13)
+    out1, _ = oracle.attention_single(q, k, np.ones((lk, 2, d)), 0.5, False)
+    np.testing.assert_allclose(out1, 1.0, atol=1e-14)
+
+
+def test_one_hot_routing_pins_gqa_head_map():
+    """Query head h puts all its weight on key h; out[h] must then be V row h
+    of KV head h // (Hq/Hkv) -- not h % Hkv, not another key."""
+    hq, hkv, d = 8, 2, 8
+    q = np.zeros((1, hq, d))
+    for h in range(hq):
+        q[0, h, h] = 60.0
+    k = np.zeros((d, hkv, d))
+    for j in range(d):
+        k[j, :, j] = 1.0
+    v = _rand(d, hkv, d)
+    out, _ = oracle.attention_single(q, k, v, 1.0, False)
+    for h in range(hq):
+        np.testing.assert_allclose(out[0, h], v[h, h // (hq // hkv)], atol=1e-20 + 1e-12)
+        assert not np.allclose(out[0, h], v[h, h % hkv]) or h // 4 == h % 2
+
+
+def test_weights_sum_to_one_and_vanish_where_masked():
+    lq, lk, d = 9, 13, 5
+    q, k = _rand(lq, 4, d), _rand(lk, 2, d)
+    for causal in (False, True):
+        for h in range(4):
+            w = oracle.softmax_weights(q, k, 0.7, causal, h)
+            assert np.all(w >= 0)
+            np.testing.assert_allclose(w.sum(axis=1), 1.0, atol=1e-12)
+            if causal:
+                vis = oracle.visible_mask(lq, lk, True)
+                assert np.all(w[~vis] == 0)
+
+
+def test_permutation_invariance_and_value_sensitivity():
+    lq, lk, d = 4, 10, 6
+    q, k, v = _rand(lq, 1, d), _rand(lk, 1, d), _rand(lk, 1, d)
+    perm = rng.permutation(lk)
+    out, lse = oracle.attention_single(q, k, v, 0.4, False)
+    out_p, lse_p = oracle.attention_single(q, k[perm], v[perm], 0.4, False)
+    np.testing.assert_allclose(out_p, out, atol=1e-13)
+    np.testing.assert_allclose(lse_p, lse, atol=1e-13)
+    out_v, _ = oracle.attention_single(q, k, v[perm], 0.4, False)
+    assert np.max(np.abs(out_v - out)) > 1e-3
+
+
+def test_affine_in_values():
+    lq, lk, d = 5, 7, 4
+    q, k, v = _rand(lq, 2, d), _rand(lk, 2, d), _rand(lk, 2, d)
+    c = _rand(d)
+    out, _ = oracle.attention_single(q, k, v, 0.5, True)
+    out2, _ = oracle.attention_single(q, k, 3.0 * v + c, 0.5, True)
+    np.testing.assert_allclose(out2, 3.0 * out + c, atol=1e-12)
+
+
+# ------------------------------------------------- brute force / library pins
+
+def _decimal_attention(q, k, v, scale, causal):
+    """Direct sum of exponentials at 50 digits (no max subtraction)."""
+    getcontext().prec = 50
+    lq, lk = len(q), len(k)
+    out, lse = [], []
+    for i in range(lq):
+        w = []
+        for j in range(lk):
+            if causal and j > i + (lk - lq):
+                continue
+            s = Decimal(scale) * sum(Decimal(a) * Decimal(b) for a, b in zip(q[i], k[j]))
+            w.append((j, s.exp()))
+        z = sum(x for _, x in w)
+        out.append([float(sum(x * Decimal(v[j][c]) for j, x in w) / z) for c in range(len(v[0]))])
+        lse.append(float(z.ln()))
+    return np.array(out), np.array(lse)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_decimal_brute_force_tiny(causal):
+    lq, lk, d = 4, 6, 3
+    q, k, v = _rand(lq, 1, d) * 2, _rand(lk, 1, d) * 2, _rand(lk, 1, d)
+    out, lse = oracle.attention_single(q, k, v, 0.9, causal)
+    bo, bl = _decimal_attention(q[:, 0].tolist(), k[:, 0].tolist(), v[:, 0].tolist(), 0.9, causal)
+    np.testing.assert_allclose(out[:, 0], bo, atol=1e-12)
+    np.testing.assert_allclose(lse[0], bl, atol=1e-12)
+
+
+def test_lse_matches_scipy_logsumexp():
+    scipy_special = pytest.importorskip("scipy.special")
+    lq, lk, d = 7, 12, 8
+    q, k = _rand(lq, 1, d) * 3, _rand(lk, 1, d)
+    _, lse = oracle.attention_single(q, k, _rand(lk, 1, d), 0.35, True)
+    for i in range(lq):
+        n = i + 1 + lk - lq
+        scores = [0.35 * float(np.dot(q[i, 0], k[j, 0])) for j in range(n)]
+        assert abs(lse[0, i] - scipy_special.logsumexp(scores)) < 1e-12
+
+
+# ------------------------------------------------------------ mask identities
+
+def test_causal_last_row_equals_full_single_query():
+    lq, lk, d = 6, 9, 8
+    q, k, v = _rand(lq, 2, d), _rand(lk, 2, d), _rand(lk, 2, d)
+    out_c, lse_c = oracle.attention_single(q, k, v, 0.3, True)
+    out_1, lse_1 = oracle.attention_single(q[-1:], k, v, 0.3, False)
+    np.testing.assert_allclose(out_c[-1], out_1[0], atol=1e-13)
+    np.testing.assert_allclose(lse_c[:, -1], lse_1[:, 0], atol=1e-13)
+
+
+def test_causal_square_row_is_prefix_attention():
+    l, d = 8, 4
+    q, k, v = _rand(l, 1, d), _rand(l, 1, d), _rand(l, 1, d)
+    out, lse = oracle.attention_single(q, k, v, 0.6, True)
+    for i in range(l):
+        o, s = oracle.attention_single(q[i:i + 1], k[:i + 1], v[:i + 1], 0.6, False)
+        np.testing.assert_allclose(out[i], o[0], atol=1e-13)
+        assert abs(lse[0, i] - s[0, 0]) < 1e-13
+
+
+def test_fully_masked_rows_and_empty_keys():
+    q, k, v = _rand(5, 2, 4), _rand(2, 2, 4), _rand(2, 2, 4)
+    out, lse = oracle.attention_single(q, k, v, 0.5, True)  # rows 0..2 see nothing
+    assert np.all(out[:3] == 0) and np.all(lse[:, :3] == -np.inf)
+    assert np.all(np.isfinite(lse[:, 3:]))
+    out0, lse0 = oracle.attention_single(q, k[:0], v[:0], 0.5, False)
+    assert np.all(out0 == 0) and np.all(lse0 == -np.inf)
+
+
+def test_power_of_two_prescale_is_exact():
+    """Laser-attention prescale (flash_attn.py, FlashAttentionImpl.
+    _forward_prefix_kv_slice_npu): q, k, v divided by s = 2 with the scale
+    multiplied by s^2, output multiplied back by s, is the same attention."""
+    q, k, v = _rand(7, 2, 8), _rand(9, 2, 8), _rand(9, 2, 8)
+    out, lse = oracle.attention_single(q, k, v, 0.125, True)
+    out2, lse2 = oracle.attention_single(q / 2, k / 2, v / 2, 0.5, True)
+    np.testing.assert_array_equal(out2 * 2, out)
+    np.testing.assert_array_equal(lse2, lse)
+
+
+# ------------------------------------------------------ varlen / dense / paged
+
+def test_dense_equals_varlen_with_arange_cu_seqlens():
+    """flash_attn.py, FlashAttentionImpl._flash_varlen_wrapper: a dense batch
+    is the varlen call with cu_seqlens = arange(0, (B+1)*L, L)."""
+    b, sq, sk, hq, hkv, d = 3, 5, 7, 4, 2, 8
+    q, k, v = _rand(b, sq, hq, d), _rand(b, sk, hkv, d), _rand(b, sk, hkv, d)
+    for causal in (False, True):
+        out, lse = oracle.attention_dense(q, k, v, 0.3, causal)
+        cq, ck = np.arange(0, (b + 1) * sq, sq), np.arange(0, (b + 1) * sk, sk)
+        out_v, lse_v = oracle.attention_varlen(
+            q.reshape(b * sq, hq, d), k.reshape(b * sk, hkv, d), v.reshape(b * sk, hkv, d), cq, ck, 0.3, causal)
+        np.testing.assert_array_equal(out_v.reshape(out.shape), out)
+        np.testing.assert_array_equal(lse_v.reshape(hq, b, sq).transpose(1, 0, 2), lse)
+
+
+def test_varlen_pack_equals_documents_run_alone():
+    lens_q, lens_k = [3, 0, 7, 1], [4, 2, 7, 5]
+    hq, hkv, d = 4, 1, 8
+    q, k, v = _rand(sum(lens_q), hq, d), _rand(sum(lens_k), hkv, d), _rand(sum(lens_k), hkv, d)
+    cq, ck = np.cumsum([0] + lens_q), np.cumsum([0] + lens_k)
+    for causal in (False, True):
+        out, lse = oracle.attention_varlen(q, k, v, cq, ck, 0.4, causal)
+        for n in range(len(lens_q)):
+            o, s = oracle.attention_single(q[cq[n]:cq[n + 1]], k[ck[n]:ck[n + 1]], v[ck[n]:ck[n + 1]], 0.4, causal)
+            np.testing.assert_array_equal(out[cq[n]:cq[n + 1]], o)
+            np.testing.assert_array_equal(lse[:, cq[n]:cq[n + 1]], s)
+        # a mistake that lets documents see each other changes the answer
+        o_all, _ = oracle.attention_single(q, k, v, 0.4, False)
+        assert np.max(np.abs(o_all - out)) > 1e-3
+
+
+def test_varlen_rejects_bad_cu_seqlens():
+    q, k = _rand(4, 1, 2), _rand(4, 1, 2)
+    with pytest.raises(ValueError):
+        oracle.attention_varlen(q, k, k, [0, 3, 2, 4], [0, 1, 2, 4], 1.0, False)
+    with pytest.raises(ValueError):
+        oracle.attention_varlen(q, k, k, [0, 4], [0, 3], 1.0, False)
+
+
+def _scatter_to_pages(ks, vs, nb, bs, seed):
+    """Build a paged cache by writing each token to slot block*bs + offset
+    through a randomly permuted block table (the inverse of the gather)."""
+    r = np.random.default_rng(seed)
+    hkv, d = ks[0].shape[1:]
+    cache = np.full((2, nb, bs, hkv, d), np.nan)
+    perm = r.permutation(nb)
+    maxb = max(-(-len(x) // bs) for x in ks)
+    bt = np.full((len(ks), maxb), -1)
+    at = 0
+    for s, (kk, vv) in enumerate(zip(ks, vs)):
+        nblk = -(-len(kk) // bs)
+        bt[s, :nblk] = perm[at:at + nblk]
+        at += nblk
+        for t in range(len(kk)):
+            slot = bt[s, t // bs] * bs + t % bs
+            cache[0].reshape(nb * bs, hkv, d)[slot] = kk[t]
+            cache[1].reshape(nb * bs, hkv, d)[slot] = vv[t]
+    return cache, bt
+
+
+def test_paged_equals_contiguous_and_ignores_unused_slots():
+    bs, hq, hkv, d = 4, 4, 2, 8
+    lens = [5, 1, 8, 11]
+    ks = [_rand(n, hkv, d) for n in lens]
+    vs = [_rand(n, hkv, d) for n in lens]
+    nb = sum(-(-n // bs) for n in lens) + 3
+    q = _rand(len(lens), hq, d)
+    outs = []
+    for seed in (0, 1):
+        cache, bt = _scatter_to_pages(ks, vs, nb, bs, seed)
+        cache = np.nan_to_num(cache, nan=0.0) + np.where(np.isnan(cache), 1e6, 0.0)  # poison unused slots
+        out, lse = oracle.attention_paged(q, cache, bt, lens, 0.3)
+        for s in range(len(lens)):
+            o, l = oracle.attention_single(q[s:s + 1], ks[s], vs[s], 0.3, False)
+            np.testing.assert_array_equal(out[s], o[0])
+            np.testing.assert_array_equal(lse[s], l[:, 0])
+        outs.append(out)
+    np.testing.assert_array_equal(outs[0], outs[1])
+
+
+def test_paged_gather_rejects_out_of_range_block():
+    cache = np.zeros((2, 2, 4, 1, 2))
+    with pytest.raises(ValueError):
+        oracle.paged_gather(cache, np.array([[0, 5]]), [6])
+
+
+# ----------------------------------------------------------------- workloads
+
+def test_workload_shapes_and_index_structures():
+    w3 = workloads.varlen_causal_gqa()
+    assert len(w3.lens_q) == 8 and sum(w3.lens_q) <= 32768
+    assert all(512 <= n <= 8192 for n in w3.lens_q)
+    w4 = workloads.paged_decode()
+    assert len(w4.seq_lens) == 64 and all(1024 <= n <= 32768 for n in w4.seq_lens)
+    bt = w4.block_table()
+    used = [int(b) for s, n in enumerate(w4.seq_lens) for b in bt[s, :-(-n // 128)]]
+    assert sorted(used) == list(range(w4.num_blocks))  # every physical block used exactly once
+    assert all(int(x) == -1 for s, n in enumerate(w4.seq_lens) for x in bt[s, -(-n // 128):])
+    w1 = workloads.tiny_varlen()
+    q, k, v, cq, ck = w1.make()
+    assert q.shape == (128, 4, 64) and cq.tolist() == [0, 37, 128]
+    assert abs(w1.flops() - 4 * 64 * 4 * (37 ** 2 + 91 ** 2)) < 1
+    assert abs(workloads.dit_self().flops() - 412.3e9) / 412.3e9 < 1e-3
