@@ -1,0 +1,181 @@
+"""GB300 (sm_103a) fused attention forward -- Python binding of libgbattn.so.
+
+The functions here only marshal arguments (shapes, pointers, the current
+CUDA stream) into the C ABI declared in ``include/gbattn.h``; every step of
+the computation runs in the library's CUDA kernels.  There is no CPU or
+PyTorch fallback: if the library is missing, or the device is not a GB300,
+the calls raise.
+
+Entry points (same names as the C ABI):
+    attn_fwd_dense(q, k, v, ...)    q [B, Sq, Hq, D], k/v [B, Sk, Hkv, D]
+    attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, ...)
+    attn_fwd_paged(q, kv_cache, block_table, seq_lens, max_seq_len, ...)
+    attn_fwd_paged_workspace_size(num_seqs, Hq, Hkv, D, max_seq_len)
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgbattn.so")
+
+OUT_BF16, OUT_F32 = 0, 1
+DEV_BAD_INDEX, DEV_TIMEOUT, DEV_BAD_SEQLEN = 1, 2, 4
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "workspace",
+                5: "cuda", 6: "device"}
+
+# (name, restype, argtypes) for every symbol of include/gbattn.h
+_P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "attn_fwd_dense": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _P]),
+    "attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _P]),
+    "attn_fwd_paged_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "attn_fwd_paged": (_I, [_P, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _Z, _P, _P]),
+    "attn_status_string": (ctypes.c_char_p, [_I]),
+}
+
+_lib = None
+
+
+class GbattnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: status {status} ({STATUS_NAMES.get(status, '?')})")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libgbattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with attention_forward_09_gb300._build.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, st):
+    if st != 0:
+        raise GbattnError(fn, st)
+
+
+def _out_code(dtype):
+    if dtype == torch.float32:
+        return OUT_F32
+    if dtype == torch.bfloat16:
+        return OUT_BF16
+    raise ValueError("out dtype must be float32 or bfloat16")
+
+
+def _bf16_cuda(name, t):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+
+
+def attn_fwd_dense(q, k, v, softmax_scale=None, causal=False, out=None, lse=None, out_dtype=torch.float32,
+                   dev_status=None, stream=None):
+    """Dense batch.  Returns (out [B, Sq, Hq, D], lse [B, Hq, Sq] or None).
+    Pass ``lse=True`` to allocate the LSE output, or a float32 tensor."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _bf16_cuda(n, t)
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Sk, Hkv, D] matching q")
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    if out is None:
+        out = torch.empty(B, Sq, Hq, D, dtype=out_dtype, device=q.device)
+    if lse is True:
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device=q.device)
+    st = load_library().attn_fwd_dense(_ptr(q), _ptr(k), _ptr(v), B, Sq, Sk, Hq, Hkv, D, scale, int(bool(causal)),
+                                       _ptr(out), _out_code(out.dtype), _ptr(lse), _ptr(dev_status),
+                                       _stream_handle(stream))
+    _check("attn_fwd_dense", st)
+    return out, lse
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, softmax_scale=None,
+                    causal=False, out=None, lse=None, out_dtype=torch.float32, dev_status=None, stream=None):
+    """Packed documents.  q [Tq, Hq, D], k/v [Tk, Hkv, D], cu_seqlens int32
+    CUDA tensors [N+1]; max_seqlen_q/k are host ints.  Returns (out [Tq, Hq, D],
+    lse [Hq, Tq] or None)."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _bf16_cuda(n, t)
+    for n, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    Tq, Hq, D = q.shape
+    Tk, Hkv, _ = k.shape
+    if k.shape != v.shape or k.shape[2] != D:
+        raise ValueError("k and v must be [Tk, Hkv, D] matching q")
+    n_docs = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() - 1 != n_docs:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k describe different document counts")
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    if out is None:
+        out = torch.empty(Tq, Hq, D, dtype=out_dtype, device=q.device)
+    if lse is True:
+        lse = torch.empty(Hq, Tq, dtype=torch.float32, device=q.device)
+    st = load_library().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), n_docs,
+                                        Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, scale,
+                                        int(bool(causal)), _ptr(out), _out_code(out.dtype), _ptr(lse),
+                                        _ptr(dev_status), _stream_handle(stream))
+    _check("attn_fwd_varlen", st)
+    return out, lse
+
+
+def attn_fwd_paged_workspace_size(num_seqs, Hq, Hkv, D, max_seq_len) -> int:
+    return int(load_library().attn_fwd_paged_workspace_size(num_seqs, Hq, Hkv, D, max_seq_len))
+
+
+def attn_fwd_paged(q, kv_cache, block_table, seq_lens, max_seq_len, softmax_scale=None, causal=True, out=None,
+                   lse=None, out_dtype=torch.float32, workspace=None, dev_status=None, stream=None):
+    """Decode over a paged cache.  q [S, Hq, D]; kv_cache [2, nb, 128, Hkv, D];
+    block_table int32 [S, max_blocks]; seq_lens int32 [S]; max_seq_len host int.
+    Returns (out [S, Hq, D], lse [S, Hq] or None).  A workspace tensor of at
+    least ``attn_fwd_paged_workspace_size`` bytes may be passed (it is
+    allocated here otherwise)."""
+    _bf16_cuda("q", q)
+    _bf16_cuda("kv_cache", kv_cache)
+    S, Hq, D = q.shape
+    two, nb, bs, Hkv, Dk = kv_cache.shape
+    if two != 2 or Dk != D:
+        raise ValueError("kv_cache must be [2, num_blocks, block_size, Hkv, D]")
+    for n, t in (("block_table", block_table), ("seq_lens", seq_lens)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    need = attn_fwd_paged_workspace_size(S, Hq, Hkv, D, int(max_seq_len))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty(S, Hq, D, dtype=out_dtype, device=q.device)
+    if lse is True:
+        lse = torch.empty(S, Hq, dtype=torch.float32, device=q.device)
+    st = load_library().attn_fwd_paged(_ptr(q), _ptr(kv_cache), nb, bs, _ptr(block_table), block_table.shape[1],
+                                       _ptr(seq_lens), S, int(max_seq_len), Hq, Hkv, D, scale, int(bool(causal)),
+                                       _ptr(out), _out_code(out.dtype), _ptr(lse), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                                       _stream_handle(stream))
+    _check("attn_fwd_paged", st)
+    return out, lse

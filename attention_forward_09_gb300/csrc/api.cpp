@@ -1,0 +1,256 @@
+// api.cpp -- the extern "C" entry points of gbattn.h: argument validation,
+// TMA tensor-map encoding and kernel launches.  No allocation, no
+// synchronisation; every launch goes to the caller's stream.
+#include "../../include/gbattn.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <mutex>
+
+#include "kernels.h"
+
+namespace {
+
+using gbattn::PagedParams;
+using gbattn::PagedPlan;
+using gbattn::PrefillParams;
+
+bool head_size_ok(int d) { return d == 64 || d == 96 || d == 128 || d == 192 || d == 256; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool scale_ok(float s) { return isfinite(s) && s > 0.f; }
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---- driver entry point for cuTensorMapEncodeTiled (no link against libcuda)
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Per-device facts: compute capability 10.3 and the SM count.
+struct DeviceInfo {
+    bool ok;
+    int sms;
+};
+
+gbattn_status device_info(DeviceInfo* out) {
+    static DeviceInfo cache[64];
+    static bool have[64];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GBATTN_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return GBATTN_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return GBATTN_ERR_CUDA;
+        cache[dev] = DeviceInfo{major == 10 && minor == 3, sms};
+        have[dev] = true;
+    }
+    *out = cache[dev];
+    return out->ok ? GBATTN_OK : GBATTN_ERR_DEVICE;
+}
+
+// bf16 tensor [rows, heads, D] (D contiguous) as a 3-D TMA map with box
+// {64, 1, box_rows} and 128-byte swizzle; out-of-range elements read as zero.
+bool encode_rows_heads_d(CUtensorMap* m, const void* base, long long rows, int heads, int d, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                          static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(heads) * d * 2};
+    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Shared by the dense and varlen entries: validation of what they have in common.
+// k and v may be null only when there are no keys at all (has_keys == false).
+gbattn_status check_common(const void* q, const void* k, const void* v, const void* out, int Hq, int Hkv, int D,
+                           float scale, gbattn_dtype odt, bool has_keys) {
+    if (!q || !out || (has_keys && (!k || !v))) return GBATTN_ERR_INVALID_ARG;
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
+    if (!scale_ok(scale)) return GBATTN_ERR_INVALID_ARG;
+    if (!head_size_ok(D)) return GBATTN_ERR_UNSUPPORTED;
+    if (odt != GBATTN_OUT_BF16 && odt != GBATTN_OUT_F32) return GBATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return GBATTN_ERR_ALIGNMENT;
+    return GBATTN_OK;
+}
+
+gbattn_status run_prefill(const void* q, const void* k, const void* v, long long Tq, long long Tk, int D,
+                          PrefillParams& p, int q_tiles, cudaStream_t st) {
+    DeviceInfo di;
+    gbattn_status s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    CUtensorMap tq, tk, tv;
+    const int bn = gbattn::prefill_block_n(D);
+    // With no keys at all no KV tile is ever loaded; point the K/V maps at q
+    // so that they are still well-formed.
+    const bool no_keys = Tk == 0;
+    if (!encode_rows_heads_d(&tq, q, Tq, p.Hq, D, 128) ||
+        !encode_rows_heads_d(&tk, no_keys ? q : k, no_keys ? Tq : Tk, no_keys ? p.Hq : p.Hkv, D, bn) ||
+        !encode_rows_heads_d(&tv, no_keys ? q : v, no_keys ? Tq : Tk, no_keys ? p.Hq : p.Hkv, D, bn))
+        return GBATTN_ERR_CUDA;
+    return gbattn::launch_prefill(D, tq, tk, tv, p, q_tiles, st) == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(gbattn_status s) {
+    switch (s) {
+        case GBATTN_OK: return "ok";
+        case GBATTN_ERR_INVALID_ARG: return "invalid argument";
+        case GBATTN_ERR_UNSUPPORTED: return "unsupported head size, block size or dtype";
+        case GBATTN_ERR_ALIGNMENT: return "tensor pointer not 16-byte aligned";
+        case GBATTN_ERR_WORKSPACE: return "workspace missing or too small";
+        case GBATTN_ERR_CUDA: return "CUDA error";
+        case GBATTN_ERR_DEVICE: return "device is not compute capability 10.3 (GB300)";
+        default: return "unknown status";
+    }
+}
+
+gbattn_status attn_fwd_dense(const void* q, const void* k, const void* v, int B, int Sq, int Sk, int Hq, int Hkv,
+                             int D, float softmax_scale, int causal, void* out, gbattn_dtype out_dtype, float* lse,
+                             uint32_t* dev_status, void* stream) {
+    gbattn_status s = check_common(q, k, v, out, Hq, Hkv, D, softmax_scale, out_dtype, Sk != 0);
+    if (s != GBATTN_OK) return s;
+    if (B < 0 || Sq < 0 || Sk < 0) return GBATTN_ERR_INVALID_ARG;
+    if (B > 65535) return GBATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Sq == 0) return GBATTN_OK;
+    PrefillParams p{};
+    p.out = out;
+    p.lse = lse;
+    p.status = dev_status;
+    p.cu_q = p.cu_k = nullptr;
+    p.num_docs = B;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.Tq = B * Sq;
+    p.Tk = B * Sk;
+    p.max_seqlen_q = Sq;
+    p.max_seqlen_k = Sk;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.group = Hq / Hkv;
+    p.scale_log2 = softmax_scale * kLog2e;
+    p.causal = causal ? 1 : 0;
+    p.out_f32 = out_dtype == GBATTN_OUT_F32;
+    p.lse_bstride = static_cast<long long>(Hq) * Sq;
+    p.lse_hstride = Sq;
+    p.lse_row_global = 0;
+    return run_prefill(q, k, v, static_cast<long long>(B) * Sq, static_cast<long long>(B) * Sk, D, p,
+                       (Sq + 127) / 128, static_cast<cudaStream_t>(stream));
+}
+
+gbattn_status attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                              const int32_t* cu_seqlens_k, int num_docs, int Tq, int Tk, int max_seqlen_q,
+                              int max_seqlen_k, int Hq, int Hkv, int D, float softmax_scale, int causal, void* out,
+                              gbattn_dtype out_dtype, float* lse, uint32_t* dev_status, void* stream) {
+    gbattn_status s = check_common(q, k, v, out, Hq, Hkv, D, softmax_scale, out_dtype, Tk != 0);
+    if (s != GBATTN_OK) return s;
+    if (!cu_seqlens_q || !cu_seqlens_k) return GBATTN_ERR_INVALID_ARG;
+    if (num_docs < 0 || Tq < 0 || Tk < 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return GBATTN_ERR_INVALID_ARG;
+    if (max_seqlen_q > Tq || max_seqlen_k > Tk) return GBATTN_ERR_INVALID_ARG;
+    if (num_docs > 65535) return GBATTN_ERR_UNSUPPORTED;
+    if (num_docs == 0 || Tq == 0 || max_seqlen_q == 0) return GBATTN_OK;
+    PrefillParams p{};
+    p.out = out;
+    p.lse = lse;
+    p.status = dev_status;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.num_docs = num_docs;
+    p.Sq = p.Sk = 0;
+    p.Tq = Tq;
+    p.Tk = Tk;
+    p.max_seqlen_q = max_seqlen_q;
+    p.max_seqlen_k = max_seqlen_k;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.group = Hq / Hkv;
+    p.scale_log2 = softmax_scale * kLog2e;
+    p.causal = causal ? 1 : 0;
+    p.out_f32 = out_dtype == GBATTN_OUT_F32;
+    p.lse_bstride = 0;
+    p.lse_hstride = Tq;
+    p.lse_row_global = 1;
+    return run_prefill(q, k, v, Tq, Tk, D, p, (max_seqlen_q + 127) / 128, static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_fwd_paged_workspace_size(int num_seqs, int Hq, int Hkv, int D, int max_seq_len) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || !head_size_ok(D)) return 0;
+    return gbattn::paged_plan(num_seqs, Hq, Hkv, D, max_seq_len).workspace_bytes;
+}
+
+gbattn_status attn_fwd_paged(const void* q, const void* kv_cache, int num_blocks, int block_size,
+                             const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                             int num_seqs, int max_seq_len, int Hq, int Hkv, int D, float softmax_scale,
+                             int causal, void* out, gbattn_dtype out_dtype, float* lse, void* workspace,
+                             size_t workspace_bytes, uint32_t* dev_status, void* stream) {
+    (void)causal;  // one query token sees its whole context under the bottom-right rule
+    if (!q || !kv_cache || !block_table || !seq_lens || !out) return GBATTN_ERR_INVALID_ARG;
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || !scale_ok(softmax_scale)) return GBATTN_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || max_blocks_per_seq <= 0 || num_seqs < 0 || max_seq_len < 0)
+        return GBATTN_ERR_INVALID_ARG;
+    if (!head_size_ok(D)) return GBATTN_ERR_UNSUPPORTED;
+    if (block_size != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (out_dtype != GBATTN_OUT_BF16 && out_dtype != GBATTN_OUT_F32) return GBATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) return GBATTN_ERR_ALIGNMENT;
+    if (2LL * num_blocks * 128 > 0x7FFFFFFFLL) return GBATTN_ERR_UNSUPPORTED;  // TMA row coordinate is int32
+    if (num_seqs == 0) return GBATTN_OK;
+    const int group = Hq / Hkv;
+    const int hg = group % 8 == 0 ? 8 : (group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1));
+    const PagedPlan plan = gbattn::paged_plan(num_seqs, Hq, Hkv, D, max_seq_len > 0 ? max_seq_len : 1);
+    if (!workspace || workspace_bytes < plan.workspace_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return GBATTN_ERR_WORKSPACE;
+    DeviceInfo di;
+    gbattn_status s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    CUtensorMap tm;
+    if (!encode_rows_heads_d(&tm, kv_cache, 2LL * num_blocks * 128, Hkv, D, 128)) return GBATTN_ERR_CUDA;
+    PagedParams p{};
+    p.q = q;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.lse = lse;
+    p.status = dev_status;
+    const size_t rows = static_cast<size_t>(num_seqs) * Hq * plan.max_splits;
+    p.part_o = static_cast<float*>(workspace);
+    p.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * D * 4 + 255) & ~size_t(255)));
+    p.num_seqs = num_seqs;
+    p.num_blocks = num_blocks;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.max_seq_len = max_seq_len;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.group = group;
+    p.heads_per_cta = hg;
+    p.blocks_per_split = plan.blocks_per_split;
+    p.max_splits = plan.max_splits;
+    p.scale_log2 = softmax_scale * kLog2e;
+    p.out_f32 = out_dtype == GBATTN_OUT_F32;
+    return gbattn::launch_paged(D, tm, p, di.sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GBATTN_OK
+               : GBATTN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,70 @@
+// kernels.h -- private interface between the host API and the CUDA kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gbattn {
+
+constexpr uint32_t kDevBadIndex = 1u;
+constexpr uint32_t kDevTimeout = 2u;
+constexpr uint32_t kDevBadSeqlen = 4u;
+
+// One launch of the prefill kernel.  Dense batches use cu_q == cu_k == nullptr
+// and fixed lengths Sq / Sk per batch entry; packed documents use cu_seqlens.
+struct PrefillParams {
+    void* out;
+    float* lse;
+    uint32_t* status;
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    int num_docs;      // B (dense) or number of documents
+    int Sq, Sk;        // dense per-batch lengths
+    int Tq, Tk;        // total rows of q and of k/v
+    int max_seqlen_q;  // bound checked on the device
+    int max_seqlen_k;
+    int Hq, Hkv, group;
+    float scale_log2;  // softmax_scale * log2(e)
+    int causal;
+    int out_f32;
+    long long lse_bstride;  // lse offset = b*lse_bstride + h*lse_hstride + row
+    long long lse_hstride;
+    int lse_row_global;     // row counted from the start of the packed tensor (varlen)
+};
+
+// Tensor maps are built by the host (see api.cpp) over q [Tq, Hq, D] and
+// k / v [Tk, Hkv, D]; box {64, 1, rows}, 128-byte swizzle.
+cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                           const CUtensorMap& tmV, const PrefillParams& p, int num_q_tiles,
+                           cudaStream_t stream);
+int prefill_block_n(int D);  // keys per KV tile for head size D
+
+struct PagedParams {
+    const void* q;          // [S, Hq, D] bf16
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    void* out;
+    float* lse;
+    uint32_t* status;
+    float* part_o;          // [S, Hq, max_splits, D]
+    float* part_lse;        // [S, Hq, max_splits]
+    int num_seqs, num_blocks, max_blocks_per_seq, max_seq_len;
+    int Hq, Hkv, group, heads_per_cta;
+    int blocks_per_split, max_splits;
+    float scale_log2;
+    int out_f32;
+};
+
+struct PagedPlan {
+    int blocks_per_split;
+    int max_splits;
+    size_t workspace_bytes;
+};
+PagedPlan paged_plan(int num_seqs, int Hq, int Hkv, int D, int max_seq_len);
+
+cudaError_t launch_paged(int D, const CUtensorMap& tmKV, const PagedParams& p, int num_sms,
+                         cudaStream_t stream);
+
+}  // namespace gbattn

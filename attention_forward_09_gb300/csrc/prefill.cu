@@ -1,0 +1,391 @@
+// prefill.cu -- fused attention forward for sm_103a (dense and packed varlen).
+//
+// One CTA computes one 128-row query tile of one (document, query head):
+//   S_j = Q K_j^T          tcgen05.mma, bf16 x bf16 -> fp32 in TMEM (double-buffered)
+//   P_j = exp2(S_j*c - m)  softmax warps, one thread per query row (TMEM lane)
+//   O  += P_j V_j          tcgen05.mma, P staged in shared memory as bf16
+//   out = O / l, lse = (m + log2 l) ln 2
+// This is the online-softmax form of the plain definition (vllm-omni
+// flash_attn.py, FlashAttentionImpl: flash_attn_func / flash_attn_varlen_func
+// with softmax_scale and causal; the (out, lse) pair of _unwrap_flash_output).
+//
+// Warp roles (192 threads):
+//   warps 0-3  softmax + O correction + epilogue; warp w owns TMEM lanes 32w..32w+31
+//   warp 4     TMA producer: Q once, then K_0 V_0 K_1 V_1 ... into a ring of slots
+//   warp 5     TMEM allocator and (lane 0) MMA issuer
+// The MMA warp issues S_{j+1} before PV_j, so the tensor core works on the
+// next scores while the softmax warps exponentiate the current ones.
+//
+// Causal masking is bottom-right aligned (FlashAttentionImpl.forward_fa_npu:
+// key kp is blocked for query qp iff kp > qp + Sk - Sq); KV tiles past the
+// last visible key of the tile's last row are never loaded.
+//
+// Shared-memory operand layout: every operand is a stack of 64-column
+// chunks, each chunk [rows x 128 B] with the 128-byte swizzle that TMA
+// writes (16-byte piece c of row r at position c ^ (r % 8)).  Q and K are
+// K-major operands; V is the MN-major B operand of P V; P is written by the
+// softmax threads in the same K-major layout as Q.
+#include <math.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gbattn {
+
+template <int D_, int BN_, int STAGES_>
+struct PrefillCfg {
+    static constexpr int D = D_;
+    static constexpr int BN = BN_;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int BM = 128;
+    static constexpr int NCH = (D + 63) / 64;           // 64-column chunks per row
+    static constexpr int Q_BYTES = NCH * BM * 128;
+    static constexpr int KV_BYTES = NCH * BN * 128;     // one K or one V tile
+    static constexpr int P_BYTES = (BN / 64) * BM * 128;
+    static constexpr int NUM_BARS = 2 * STAGES + 6;
+    static constexpr int SMEM_BYTES = 1024 + Q_BYTES + STAGES * KV_BYTES + P_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int TMEM_S = 0;        // S buffers at columns [0, BN) and [BN, 2BN)
+    static constexpr int TMEM_O = 2 * BN;   // O at [2BN, 2BN + D)
+    static constexpr int TMEM_COLS = (2 * BN + D) <= 256 ? 256 : 512;
+    static_assert(2 * BN + D <= 512, "TMEM budget");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(D % 32 == 0 && BN % 64 == 0, "tile shape");
+};
+
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: tolerate P up to 2^8 before rescaling O
+
+template <class C>
+__global__ void __launch_bounds__(192, 1)
+    fmha_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+    constexpr int D = C::D, BN = C::BN, STAGES = C::STAGES, BM = C::BM, NCH = C::NCH;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sQ = smem_u32(smem);
+    const uint32_t sKV = sQ + C::Q_BYTES;
+    const uint32_t sP = sKV + STAGES * C::KV_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Q_BYTES + STAGES * C::KV_BYTES + C::P_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t b_q_full = smem_u32(&bars[0]);
+    auto b_kv_full = [&](int s) { return smem_u32(&bars[1 + s]); };
+    auto b_kv_empty = [&](int s) { return smem_u32(&bars[1 + STAGES + s]); };
+    auto b_s_full = [&](int b) { return smem_u32(&bars[1 + 2 * STAGES + b]); };
+    const uint32_t b_p_full = smem_u32(&bars[3 + 2 * STAGES]);
+    const uint32_t b_pv_done = smem_u32(&bars[4 + 2 * STAGES]);
+    const uint32_t b_drain = smem_u32(&bars[5 + 2 * STAGES]);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ------------------------------------------------------------ tile coordinates
+    const int tile = p.causal ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;  // heavy causal tiles first
+    const int h = blockIdx.y;
+    const int doc = blockIdx.z;
+    const int kvh = h / p.group;
+    int q_start, Lq, k_start, Lk;
+    if (p.cu_q) {
+        q_start = p.cu_q[doc];
+        k_start = p.cu_k[doc];
+        const int q_end = p.cu_q[doc + 1], k_end = p.cu_k[doc + 1];
+        Lq = q_end - q_start;
+        Lk = k_end - k_start;
+        const bool bad = q_start < 0 || Lq < 0 || q_end > p.Tq || k_start < 0 || Lk < 0 ||
+                         k_end > p.Tk || Lq > p.max_seqlen_q || Lk > p.max_seqlen_k;
+        if (bad) {
+            if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0 && p.status) atomicOr(p.status, kDevBadSeqlen);
+            return;
+        }
+    } else {
+        q_start = doc * p.Sq;
+        Lq = p.Sq;
+        k_start = doc * p.Sk;
+        Lk = p.Sk;
+    }
+    const int q0 = tile * BM;
+    if (q0 >= Lq) return;  // CTA-uniform, before any barrier or TMEM use
+    if (status_has_timeout(p.status, kDevTimeout)) return;
+    const int diag = Lk - Lq;
+    int kend = Lk;
+    if (p.causal) kend = min(Lk, min(q0 + BM - 1, Lq - 1) + diag + 1);
+    const int n_kv = kend > 0 ? (kend + BN - 1) / BN : 0;
+
+    // ------------------------------------------------------------------ setup
+    if (threadIdx.x == 0) {
+        mbar_init(b_q_full, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(b_kv_full(s), 1);
+            mbar_init(b_kv_empty(s), 1);
+        }
+        mbar_init(b_s_full(0), 1);
+        mbar_init(b_s_full(1), 1);
+        mbar_init(b_p_full, 128);
+        mbar_init(b_pv_done, 1);
+        mbar_init(b_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            mbar_arrive_expect_tx(b_q_full, C::Q_BYTES);
+            for (int c = 0; c < NCH; ++c) tma_load_3d(sQ + c * BM * 128, &tmQ, b_q_full, c * 64, h, q_start + q0);
+            int issued = 0;
+            for (int t = 0; t < 2 * n_kv; ++t) {
+                const int s = t % STAGES, u = t / STAGES;
+                if (u > 0 && !mbar_wait(b_kv_empty(s), (u - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const CUtensorMap* m = (t & 1) ? &tmV : &tmK;
+                const int row = k_start + (t >> 1) * BN;
+                mbar_arrive_expect_tx(b_kv_full(s), C::KV_BYTES);
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_3d(sKV + s * C::KV_BYTES + c * BN * 128, m, b_kv_full(s), c * 64, kvh, row);
+                ++issued;
+            }
+            if (!ok || *abort_flag) {
+                // Let every copy this thread started land before the CTA retires.
+                mbar_wait_drain(b_q_full, 0);
+                for (int t = (issued > STAGES ? issued - STAGES : 0); t < issued; ++t)
+                    mbar_wait_drain(b_kv_full(t % STAGES), (t / STAGES) & 1);
+            }
+        }
+    } else if (warp == 5) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc_bf16_f32(BM, BN, false, false);
+            constexpr uint32_t kIdO = idesc_bf16_f32(BM, D, false, true);
+            ok = mbar_wait(b_q_full, 0, abort_flag);
+            auto issue_s = [&](int j) -> bool {
+                const int t = 2 * j, s = t % STAGES;
+                if (!mbar_wait(b_kv_full(s), (t / STAGES) & 1, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t dS = tmem + C::TMEM_S + (j & 1) * BN;
+                const uint32_t kb = sKV + s * C::KV_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;  // 16 bf16 = 32 B step inside a 128-B row
+                    const uint64_t a = sdesc_sw128(sQ + (kk >> 2) * BM * 128 + off, 16, 1024);
+                    const uint64_t b = sdesc_sw128(kb + (kk >> 2) * BN * 128 + off, 16, 1024);
+                    mma_bf16_ss(dS, a, b, kIdS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(b_s_full(j & 1));
+                mma_commit(b_kv_empty(s));
+                return true;
+            };
+            if (ok && n_kv > 0) ok = issue_s(0);
+            for (int j = 0; ok && j < n_kv; ++j) {
+                if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
+                if (!(ok = mbar_wait(b_p_full, j & 1, abort_flag))) break;
+                const int t = 2 * j + 1, s = t % STAGES;
+                if (!(ok = mbar_wait(b_kv_full(s), (t / STAGES) & 1, abort_flag))) break;
+                tc_fence_after();
+                const uint32_t vb = sKV + s * C::KV_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t a = sdesc_sw128(sP + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = sdesc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
+                    mma_bf16_ss(tmem + C::TMEM_O, a, b, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(b_pv_done);
+                mma_commit(b_kv_empty(s));
+            }
+            // Everything issued above must finish before TMEM is released.
+            mma_commit(b_drain);
+            mbar_wait_drain(b_drain, 0);
+        }
+    } else {
+        // ------------------------------------------------------------- softmax
+        const int r = threadIdx.x;  // row within the tile == TMEM lane
+        const int row = q0 + r;     // row within the document
+        const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const int row_lim = p.causal ? min(Lk, row + diag + 1) : Lk;  // keys [0, row_lim) visible
+        const float c2 = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        for (int j = 0; j < n_kv; ++j) {
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_s_full(j & 1), (j >> 1) & 1, abort_flag)))) break;
+            tc_fence_after();
+            uint32_t sr[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c)
+                tmem_ld32(tl + C::TMEM_S + (j & 1) * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+            tmem_wait_ld();
+            const int kbase = j * BN;
+            const bool edge = (kbase + BN > Lk) || (p.causal && kbase + BN - 1 > q0 + diag);
+            if (edge) {
+                const int lim = row_lim - kbase;
+#pragma unroll
+                for (int c = 0; c < BN; ++c)
+                    if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+            const float m_new = fmaxf(m, mx * c2);
+            const bool need = m_new > m + kRescaleThreshold;
+            const bool warp_need = __any_sync(0xffffffffu, need);
+            float alpha = 1.f;
+            if (warp_need && m_new > m) {
+                alpha = ex2(m - m_new);
+                m = m_new;
+            }
+            l *= alpha;
+            const float msub = (m == -INFINITY) ? 0.f : m;
+            uint32_t pk[BN / 2];
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < BN; c += 2) {
+                const float p0 = ex2(fmaf(__uint_as_float(sr[c]), c2, -msub));
+                const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), c2, -msub));
+                rs += p0 + p1;
+                pk[c >> 1] = pack_bf16x2(p0, p1);
+            }
+            l += rs;
+            // PV_{j-1} has to be finished before O is rescaled or P overwritten.
+            if (j > 0) {
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_pv_done, (j - 1) & 1, abort_flag)))) break;
+                tc_fence_after();
+                if (warp_need) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tl + C::TMEM_O + c * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(tl + C::TMEM_O + c * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < BN / 64; ++a) {
+                const uint32_t rowp = sP + a * BM * 128 + r * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_shared_v4(rowp + ((q ^ (r & 7)) << 4), pk[a * 32 + q * 4 + 0], pk[a * 32 + q * 4 + 1],
+                                 pk[a * 32 + q * 4 + 2], pk[a * 32 + q * 4 + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(b_p_full);
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok && n_kv > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(b_pv_done, (n_kv - 1) & 1, abort_flag));
+            tc_fence_after();
+        }
+        // ------------------------------------------------------------ epilogue
+        const bool row_valid = ok && row < Lq;
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const long long orow = static_cast<long long>(q_start + row) * p.Hq + h;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            if (n_kv > 0 && ok) {
+                tmem_ld32(tl + C::TMEM_O + c * 32, o);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = 0u;
+            }
+            if (row_valid) {
+                if (p.out_f32) {
+                    float* dst = reinterpret_cast<float*>(p.out) + orow * D + c * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        st_global_v4(dst + e, __float_as_uint(__uint_as_float(o[e]) * inv_l),
+                                     __float_as_uint(__uint_as_float(o[e + 1]) * inv_l),
+                                     __float_as_uint(__uint_as_float(o[e + 2]) * inv_l),
+                                     __float_as_uint(__uint_as_float(o[e + 3]) * inv_l));
+                } else {
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + orow * D + c * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8)
+                        st_global_v4(dst + e,
+                                     pack_bf16x2(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l),
+                                     pack_bf16x2(__uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l),
+                                     pack_bf16x2(__uint_as_float(o[e + 4]) * inv_l, __uint_as_float(o[e + 5]) * inv_l),
+                                     pack_bf16x2(__uint_as_float(o[e + 6]) * inv_l, __uint_as_float(o[e + 7]) * inv_l));
+                }
+            }
+        }
+        if (row_valid && p.lse) {
+            const long long lrow = p.lse_row_global ? (q_start + row) : row;
+            p.lse[doc * p.lse_bstride + h * p.lse_hstride + lrow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        }
+    }
+
+    // --------------------------------------------------------------- teardown
+    if (!ok) {
+        *abort_flag = 1;
+        if (p.status) atomicOr(p.status, kDevTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- launchers
+using Cfg64 = PrefillCfg<64, 128, 6>;
+using Cfg96 = PrefillCfg<96, 128, 4>;
+using Cfg128 = PrefillCfg<128, 128, 4>;
+using Cfg192 = PrefillCfg<192, 128, 3>;
+using Cfg256 = PrefillCfg<256, 128, 2>;
+
+template <class C>
+static cudaError_t launch_cfg(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                              const PrefillParams& p, int num_q_tiles, cudaStream_t stream) {
+    static bool attr_done = false;  // attribute is per function; setting it twice is harmless
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(fmha_fwd_sm103a<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    dim3 grid(num_q_tiles, p.Hq, p.num_docs);
+    fmha_fwd_sm103a<C><<<grid, 192, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
+    return cudaGetLastError();
+}
+
+int prefill_block_n(int D) {
+    switch (D) {
+        case 64: return Cfg64::BN;
+        case 96: return Cfg96::BN;
+        case 128: return Cfg128::BN;
+        case 192: return Cfg192::BN;
+        case 256: return Cfg256::BN;
+        default: return 0;
+    }
+}
+
+cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                           const PrefillParams& p, int num_q_tiles, cudaStream_t stream) {
+    switch (D) {
+        case 64: return launch_cfg<Cfg64>(tmQ, tmK, tmV, p, num_q_tiles, stream);
+        case 96: return launch_cfg<Cfg96>(tmQ, tmK, tmV, p, num_q_tiles, stream);
+        case 128: return launch_cfg<Cfg128>(tmQ, tmK, tmV, p, num_q_tiles, stream);
+        case 192: return launch_cfg<Cfg192>(tmQ, tmK, tmV, p, num_q_tiles, stream);
+        case 256: return launch_cfg<Cfg256>(tmQ, tmK, tmV, p, num_q_tiles, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gbattn

@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention forward hot path on one GB300 (or N, as
+independent weak-scaled replicas under torchrun).
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  1. prefill: dense diffusion-transformer self-attention, B=2, S=4096,
+     24 heads, D=128, non-causal (attn_fwd_dense, tcgen05 kernel);
+  2. paged decode: 64 sequences, contexts U[1024, 32768], 32 query / 8 KV
+     heads, D=128, cache (2, nb, 128, 8, 128) (attn_fwd_paged: split-K kernel
+     + LSE-merge combine).
+The headline `value` is the prefill's TFLOP/s (4*B*H*S^2*D algorithmic
+flops over the kernel's CUDA-event time); the decode's HBM GB/s sits in
+`paged_decode`.  Between steps a 512 MiB buffer is rewritten so that L2
+(129 MB) holds nothing of the previous step.
+
+`--impl reference` times the float64 CPU oracle on a bounded sample of the
+same workload on this machine's host cores (there is no other reference
+implementation of this path).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s & % bf16 TC peak; paged-decode HBM GB/s & % of HBM peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_for(kernel: str, source_file: str):
+    """DRAM bytes per launch from a committed ncu summary, only while the
+    kernel source still matches the one the counters were taken on."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d:
+        return None
+    with open(os.path.join(ROOT, "attention_forward_09_gb300", "csrc", source_file), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return d["bytes_per_launch"] if d.get("source_sha") == sha else None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *a):
+        self.text = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.text = self.proc.communicate(timeout=5)[0]
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "text", "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over the ranks (timing only; no data moves)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def oracle_prefill_sample(w: workloads.Dense, budget_s: float):
+    """Time the float64 oracle on whole (batch, head) slices of the dense
+    workload until budget_s has passed; returns (TFLOP/s, description)."""
+    import oracle
+
+    q, k, v = w.make()
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        b, h = divmod(done % (w.B * w.Hq), w.Hq)
+        oracle.attention_single(q[b, :, h:h + 1], k[b, :, h // (w.Hq // w.Hkv):h // (w.Hq // w.Hkv) + 1],
+                                v[b, :, h // (w.Hq // w.Hkv):h // (w.Hq // w.Hkv) + 1], w.scale, w.causal)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    flops = 4.0 * w.D * w.Sq * w.Sk * done
+    return flops / el / 1e12, f"{done} of {w.B * w.Hq} (batch, head) slices of {w.name}, all {w.Sq} query rows", el
+
+
+def oracle_paged_sample(w: workloads.Paged, q, cache, bt, sl, budget_s: float):
+    import oracle
+
+    done, nbytes = 0, 0
+    t0 = time.perf_counter()
+    order = np.argsort(w.seq_lens)
+    while True:
+        s = int(order[done % len(order)])
+        oracle.attention_paged(q[s:s + 1], cache, bt[s:s + 1], sl[s:s + 1], w.scale)
+        nbytes += 2 * w.seq_lens[s] * w.Hkv * w.D * 2
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or done >= len(order):
+            break
+    return nbytes / el / 1e9, f"{done} of {len(order)} sequences of {w.name} (shortest first)", el
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# --------------------------------------------------------------------- arms
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = workloads.dit_self()
+    steps = []
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        tf, desc, el = oracle_prefill_sample(w, per_step)
+        if i >= args.warmup:
+            steps.append((tf, el))
+    value = statistics.median(t for t, _ in steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(e for _, e in steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "seq_len": w.Sq, "heads": w.Hq, "head_dim": w.D},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": desc + f"; {per_step:.0f} s of oracle work per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import attention_forward_09_gb300 as gb
+    from attention_forward_09_gb300 import _build
+
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier(world)
+    gb.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk, peak_kind = peaks()
+
+    # ---- inputs (CPU, seeded), then resident in HBM
+    wp = workloads.dit_self()
+    q, k, v = wp.make()
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    outd = torch.empty(wp.B, wp.Sq, wp.Hq, wp.D, dtype=torch.float32, device=dev)
+    lsed = torch.empty(wp.B, wp.Hq, wp.Sq, dtype=torch.float32, device=dev)
+    wd = workloads.paged_decode()
+    pq, cache, bt, sl = wd.make(chunk_rows=256)
+    pqd, cached, btd, sld = pq.to(dev), cache.to(dev), bt.to(dev), sl.to(dev)
+    max_len = max(wd.seq_lens)
+    ws = torch.empty(gb.attn_fwd_paged_workspace_size(len(wd.seq_lens), wd.Hq, wd.Hkv, wd.D, max_len),
+                     dtype=torch.uint8, device=dev)
+    pout = torch.empty(len(wd.seq_lens), wd.Hq, wd.D, dtype=torch.float32, device=dev)
+    plse = torch.empty(len(wd.seq_lens), wd.Hq, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill():
+        gb.attn_fwd_dense(qd, kd, vd, wp.scale, wp.causal, out=outd, lse=lsed, dev_status=status, stream=stream)
+
+    def decode():
+        gb.attn_fwd_paged(pqd, cached, btd, sld, max_len, wd.scale, out=pout, lse=plse, workspace=ws,
+                          dev_status=status, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        prefill()
+        decode()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            prefill()
+            ev[i][1].record(stream)
+            decode()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the timed region")
+    pre_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    pre_avg = max_over_ranks(statistics.mean(pre_ms), world)
+    dec_avg = max_over_ranks(statistics.mean(dec_ms), world)
+    step_ms = max_over_ranks(statistics.mean(p + d for p, d in zip(pre_ms, dec_ms)), world)
+
+    flops = wp.flops()
+    tflops_rank = flops / (pre_avg * 1e-3) / 1e12
+    value = sum_over_ranks(flops, world) / (pre_avg * 1e-3) / 1e12
+    dec_bytes = wd.algorithmic_bytes(out_bytes_per_elem=4, with_lse=True)
+    dec_gbs_rank = dec_bytes / (dec_avg * 1e-3) / 1e9
+    dec_value = sum_over_ranks(dec_bytes, world) / (dec_avg * 1e-3) / 1e9
+    peak_tf = float(pk["bf16_tflops"])
+    peak_bw = float(pk["hbm_gbs"])
+
+    # ---- end to end through the public API from pinned host buffers
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    hout = torch.empty(outd.shape, dtype=torch.float32).pin_memory()
+    hlse = torch.empty(lsed.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        prefill()
+        hout.copy_(outd, non_blocking=True)
+        hlse.copy_(lsed, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = (q.numel() + k.numel() + v.numel()) * 2
+    d2h = hout.numel() * 4 + hlse.numel() * 4
+
+    # ---- oracle on the host cores (rank 0, N=1 only)
+    cpu = None
+    if world == 1:
+        tf, desc, _ = oracle_prefill_sample(wp, 10.0)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle", "sample": desc}
+        gbs, ddesc, _ = oracle_paged_sample(wd, pq, cache, bt, sl, 8.0)
+        cpu_dec = {"value": gbs, "unit": "GB/s", "cores": cores_used(), "kind": "oracle", "sample": ddesc}
+    else:
+        cpu_dec = None
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{wp.name} + {wd.name}",
+            "prefill": {"B": wp.B, "seq_len": wp.Sq, "heads": wp.Hq, "kv_heads": wp.Hkv, "head_dim": wp.D,
+                        "causal": wp.causal, "out_dtype": "f32", "lse": True},
+            "decode": {"num_seqs": len(wd.seq_lens), "context_tokens": wd.context_tokens(),
+                       "max_seq_len": max_len, "heads": wd.Hq, "kv_heads": wd.Hkv, "head_dim": wd.D,
+                       "block_size": 128, "num_blocks": wd.num_blocks},
+            "l2": "512 MiB buffer rewritten between steps (flush); decode cache 4.4 GB > L2",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "tensor", "kernel": "fmha_fwd_sm103a<128>", "achieved": tflops_rank, "peak": peak_tf,
+            "unit": "TFLOP/s", "frac": tflops_rank / peak_tf, "peak_kind": f"{peak_kind} bf16 burst",
+            "traffic": traffic_for("fmha_fwd_sm103a", "prefill.cu"),
+            "flops_per_launch": flops, "launch_ms": pre_avg,
+        },
+        "paged_decode": {
+            "value": dec_value, "unit": "GB/s", "ms": dec_avg,
+            "roofline": {"bound": "hbm", "kernel": "paged_decode_sm103a + paged_combine", "achieved": dec_gbs_rank,
+                         "peak": peak_bw, "unit": "GB/s", "frac": dec_gbs_rank / peak_bw,
+                         "peak_kind": f"{peak_kind} HBM copy", "bytes_per_call": dec_bytes,
+                         "traffic": traffic_for("paged_decode_sm103a", "decode.cu")},
+            "cpu_baseline": cpu_dec,
+        },
+        "cpu_baseline": cpu,
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * gbattn.h -- C ABI of the GB300 (sm_103a) fused attention forward.
+ *
+ * Every entry point computes, for each query row i of query head h,
+ *
+ *     out[i, h, :] = softmax_j(softmax_scale * q[i, h] . k[j, kv(h)]) @ v[j, kv(h)]
+ *     lse[h, i]    = ln sum_j exp(softmax_scale * q[i, h] . k[j, kv(h)])
+ *
+ * over the keys j that row i may see, with kv(h) = h / (num_heads / num_kv_heads)
+ * (GQA: consecutive query heads share one KV head).  The operation and its
+ * argument set follow the attention backends of vllm-omni flash_attn.py
+ * (FlashAttentionImpl: flash_attn_func / flash_attn_varlen_func routes, the
+ * (out, lse) pair of _unwrap_flash_output) and vllm-ascend attention_v1.py
+ * (AscendAttentionBackendImpl.forward_paged_attention over the paged cache).
+ *
+ * Conventions shared by all calls
+ * -------------------------------
+ *  - Inputs q, k, v and the KV cache are bfloat16, row-major, head_size
+ *    contiguous.  head_size must be one of 64, 96, 128, 192, 256
+ *    (FlashAttentionBackend.get_supported_head_sizes).
+ *  - num_heads % num_kv_heads == 0 (AscendAttentionBackendImpl.__init__).
+ *  - Causal masking is bottom-right aligned per document: key j is visible
+ *    to query i iff j <= i + (Lk - Lq) (FlashAttentionImpl.forward_fa_npu).
+ *    A row that sees no key gets out = 0 and lse = -inf.
+ *  - softmax_scale must be finite and > 0; there is no implicit default.
+ *  - The caller owns every buffer.  The library allocates nothing, never
+ *    synchronises, and launches only on `stream` (a cudaStream_t passed as
+ *    void*; NULL = the legacy default stream).  All pointers named "device"
+ *    must be device-accessible; q, k, v, kv_cache and out must be 16-byte
+ *    aligned.
+ *  - out is written in out_dtype (bf16 or fp32); lse is fp32 and optional
+ *    (NULL = not written).
+ *  - dev_status (optional, device uint32): kernels OR GBATTN_DEV_* bits into
+ *    it when they meet bad indices or a timed-out wait; they never trap.  The
+ *    caller zeroes it and reads it after synchronising.
+ *  - Host-side validation failures return a status before anything is
+ *    launched; GBATTN_ERR_CUDA reports a launch or driver error.
+ *  - Only devices of compute capability 10.3 (GB300) are accepted.
+ */
+#ifndef GBATTN_H
+#define GBATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GBATTN_OK = 0,
+    GBATTN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad scale, Hq % Hkv != 0 */
+    GBATTN_ERR_UNSUPPORTED = 2, /* head size, block size or output dtype not supported */
+    GBATTN_ERR_ALIGNMENT = 3,   /* a tensor pointer is not 16-byte aligned */
+    GBATTN_ERR_WORKSPACE = 4,   /* paged workspace missing or too small */
+    GBATTN_ERR_CUDA = 5,        /* CUDA runtime / driver error (launch, attribute, tensor map) */
+    GBATTN_ERR_DEVICE = 6       /* current device is not compute capability 10.3 */
+} gbattn_status;
+
+typedef enum {
+    GBATTN_OUT_BF16 = 0,
+    GBATTN_OUT_F32 = 1
+} gbattn_dtype;
+
+/* Bits the kernels OR into *dev_status. */
+#define GBATTN_DEV_BAD_INDEX 1u   /* block_table entry outside [0, num_blocks) (token skipped) */
+#define GBATTN_DEV_TIMEOUT 2u     /* a pipeline wait gave up; that tile's output is invalid */
+#define GBATTN_DEV_BAD_SEQLEN 4u  /* cu_seqlens / seq_lens inconsistent or above the stated max */
+
+/*
+ * attn_fwd_dense -- fixed-length batch (the flash_attn_func route of
+ * FlashAttentionImpl.forward_cuda in vllm-omni flash_attn.py).
+ *
+ *   q    device bf16 [B, Sq, Hq, D]
+ *   k, v device bf16 [B, Sk, Hkv, D]
+ *   out  device [B, Sq, Hq, D] in out_dtype
+ *   lse  device fp32 [B, Hq, Sq] or NULL
+ *
+ * Batch b attends only its own keys.  Equivalent to attn_fwd_varlen with
+ * cu_seqlens_q = arange(0, (B+1)*Sq, Sq) and cu_seqlens_k likewise
+ * (FlashAttentionImpl._flash_varlen_wrapper), except for the LSE layout.
+ * B, Sq or Sk equal to 0 is allowed (Sk = 0 writes zeros and -inf; k and v
+ * may then be NULL).
+ */
+gbattn_status attn_fwd_dense(const void* q, const void* k, const void* v,
+                             int B, int Sq, int Sk, int Hq, int Hkv, int D,
+                             float softmax_scale, int causal,
+                             void* out, gbattn_dtype out_dtype, float* lse,
+                             uint32_t* dev_status, void* stream);
+
+/*
+ * attn_fwd_varlen -- packed documents (FlashAttentionImpl._forward_varlen_packed,
+ * flash_attn_varlen_func with cu_seqlens_q/k and max_seqlen_q/k).
+ *
+ *   q              device bf16 [Tq, Hq, D]
+ *   k, v           device bf16 [Tk, Hkv, D]
+ *   cu_seqlens_q/k device int32 [num_docs + 1]: 0 = c[0] <= c[1] <= ... <= c[N] = Tq (Tk)
+ *   max_seqlen_q/k host ints, >= every document's length (they size the grid;
+ *                  no device read happens on the host)
+ *   out            device [Tq, Hq, D] in out_dtype
+ *   lse            device fp32 [Hq, Tq] or NULL
+ *
+ * Document n owns query rows [cu_q[n], cu_q[n+1]) and key rows
+ * [cu_k[n], cu_k[n+1]); no row attends across documents.  Empty documents
+ * are allowed (with Tk = 0, k and v may be NULL).  A document longer than max_seqlen, or cu_seqlens that
+ * decrease or run past Tq/Tk, set GBATTN_DEV_BAD_SEQLEN and that document's
+ * rows are left unwritten.  Keys past a document's end are masked in the
+ * scores and multiplied by zero weight, so every bf16 value in k and v must
+ * be finite.
+ */
+gbattn_status attn_fwd_varlen(const void* q, const void* k, const void* v,
+                              const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                              int num_docs, int Tq, int Tk, int max_seqlen_q, int max_seqlen_k,
+                              int Hq, int Hkv, int D, float softmax_scale, int causal,
+                              void* out, gbattn_dtype out_dtype, float* lse,
+                              uint32_t* dev_status, void* stream);
+
+/*
+ * attn_fwd_paged_workspace_size -- bytes of device workspace attn_fwd_paged
+ * needs for these sizes (split-K partial results).  Pure host arithmetic; the
+ * same arguments always give the same answer, so it can be queried once
+ * before CUDA-graph capture (cf. the workspace query in
+ * AscendAttentionBackendImpl.full_graph_pa).  Returns 0 for invalid sizes.
+ */
+size_t attn_fwd_paged_workspace_size(int num_seqs, int Hq, int Hkv, int D, int max_seq_len);
+
+/*
+ * attn_fwd_paged -- one query token per sequence over a paged KV cache
+ * (AscendAttentionBackendImpl.forward_paged_attention; cache shape from
+ * AscendAttentionBackend.get_kv_cache_shape).
+ *
+ *   q            device bf16 [num_seqs, Hq, D]
+ *   kv_cache     device bf16 [2, num_blocks, block_size, Hkv, D]; [0] = keys, [1] = values
+ *   block_size   must be 128 (AscendAttentionBackend.get_supported_block_size)
+ *   block_table  device int32 [num_seqs, max_blocks_per_seq]; token t of
+ *                sequence s lives in physical block block_table[s, t / 128],
+ *                slot t % 128 (the slot_mapping rule of AscendMetadata).
+ *                Entries past ceil(seq_lens[s] / 128) are never read.
+ *   seq_lens     device int32 [num_seqs], each in [0, max_seq_len] and
+ *                <= 128 * max_blocks_per_seq (context_lens)
+ *   max_seq_len  host int bounding seq_lens (sizes the split-K grid)
+ *   causal       accepted for symmetry; a single query sees its whole
+ *                context under the bottom-right rule, so it has no effect
+ *   out          device [num_seqs, Hq, D] in out_dtype
+ *   lse          device fp32 [num_seqs, Hq] or NULL
+ *   workspace    device buffer of at least
+ *                attn_fwd_paged_workspace_size(num_seqs, Hq, Hkv, D, max_seq_len)
+ *                bytes, 256-byte aligned; contents need no initialisation
+ *
+ * Slots of the last block past seq_len are never used.  A block_table
+ * entry outside [0, num_blocks) sets GBATTN_DEV_BAD_INDEX and its tokens are
+ * skipped; a seq_len above max_seq_len sets GBATTN_DEV_BAD_SEQLEN and is
+ * clamped.  A sequence with seq_len 0 gets out = 0 and lse = -inf.
+ */
+gbattn_status attn_fwd_paged(const void* q, const void* kv_cache, int num_blocks, int block_size,
+                             const int32_t* block_table, int max_blocks_per_seq,
+                             const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                             int Hq, int Hkv, int D, float softmax_scale, int causal,
+                             void* out, gbattn_dtype out_dtype, float* lse,
+                             void* workspace, size_t workspace_bytes,
+                             uint32_t* dev_status, void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* attn_status_string(gbattn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBATTN_H */

@@ -163,19 +163,27 @@ def paged_gather(kv_cache, block_table, seq_lens):
     kv_cache: [2, num_blocks, block_size, Hkv, D]; block_table: [S, max_blocks];
     seq_lens: [S].  Token t of sequence s is slot ``block_table[s, t // bs] *
     bs + t % bs`` (``attention_v1.py``, ``AscendMetadata.slot_mapping``).
+    Only the gathered rows are converted to float64.
     Returns two lists of [L_s, Hkv, D] float64 arrays.
     """
-    cache = _f64(kv_cache)
     bt, sl = _i64(block_table), _i64(seq_lens)
-    _, nb, bs, hkv, d = cache.shape
+    _, nb, bs, hkv, d = kv_cache.shape
     ks, vs = [], []
     for s in range(sl.size):
         t = np.arange(sl[s])
         blocks = bt[s, t // bs]
         if t.size and (blocks.min() < 0 or blocks.max() >= nb):
             raise ValueError(f"block_table row {s} points outside the cache")
-        ks.append(cache[0, blocks, t % bs])
-        vs.append(cache[1, blocks, t % bs])
+        slots = t % bs
+        if hasattr(kv_cache, "detach"):  # torch tensor: index first, then convert
+            import torch
+
+            bi, si = torch.from_numpy(blocks), torch.from_numpy(slots)
+            ks.append(_f64(kv_cache[0][bi, si]))
+            vs.append(_f64(kv_cache[1][bi, si]))
+        else:
+            ks.append(_f64(np.asarray(kv_cache)[0][blocks, slots]))
+            vs.append(_f64(np.asarray(kv_cache)[1][blocks, slots]))
     return ks, vs
 
 

@@ -1,0 +1,123 @@
+"""The C-ABI library builds, loads, exports every declared symbol, and rejects
+bad arguments on the host before touching the GPU (these calls make no CUDA
+call, so they run on a machine without a GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_forward_09_gb300 as gb
+from attention_forward_09_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbattn.h")
+
+OK, INVALID, UNSUPPORTED, ALIGN, WORKSPACE = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return gb.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_functions() == sorted(
+        ["attn_fwd_dense", "attn_fwd_varlen", "attn_fwd_paged", "attn_fwd_paged_workspace_size",
+         "attn_status_string"])
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in gb.SIGNATURES, name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.attn_status_string(code)
+    assert lib.attn_status_string(99) == b"unknown status"
+
+
+# A fake, 16-byte aligned "device" address: validation must fail before any use.
+P = ctypes.c_void_p(0x10000)
+UNALIGNED = ctypes.c_void_p(0x10008)
+
+
+def dense(lib, **kw):
+    a = dict(q=P, k=P, v=P, B=1, Sq=8, Sk=8, Hq=4, Hkv=2, D=128, scale=0.1, causal=0, out=P, odt=1, lse=None)
+    a.update(kw)
+    return lib.attn_fwd_dense(a["q"], a["k"], a["v"], a["B"], a["Sq"], a["Sk"], a["Hq"], a["Hkv"], a["D"],
+                              a["scale"], a["causal"], a["out"], a["odt"], a["lse"], None, None)
+
+
+def test_dense_validation(lib):
+    assert dense(lib, D=80) == UNSUPPORTED
+    assert dense(lib, D=32) == UNSUPPORTED
+    assert dense(lib, Hq=6, Hkv=4) == INVALID
+    assert dense(lib, Hkv=0) == INVALID
+    assert dense(lib, q=None) == INVALID
+    assert dense(lib, out=None) == INVALID
+    assert dense(lib, scale=0.0) == INVALID
+    assert dense(lib, scale=-1.0) == INVALID
+    assert dense(lib, scale=float("nan")) == INVALID
+    assert dense(lib, odt=7) == UNSUPPORTED
+    assert dense(lib, k=UNALIGNED) == ALIGN
+    assert dense(lib, B=-1) == INVALID
+    # empty problems are a no-op success without touching the device
+    assert dense(lib, B=0) == OK
+    assert dense(lib, Sq=0) == OK
+
+
+def varlen(lib, **kw):
+    a = dict(cq=P, ck=P, N=2, Tq=16, Tk=16, mq=8, mk=8, Hq=4, Hkv=4, D=64, out=P)
+    a.update(kw)
+    return lib.attn_fwd_varlen(P, P, P, a["cq"], a["ck"], a["N"], a["Tq"], a["Tk"], a["mq"], a["mk"], a["Hq"],
+                               a["Hkv"], a["D"], 0.125, 0, a["out"], 1, None, None, None)
+
+
+def test_varlen_validation(lib):
+    assert varlen(lib, cq=None) == INVALID
+    assert varlen(lib, ck=None) == INVALID
+    assert varlen(lib, mq=17) == INVALID  # a document cannot be longer than the tensor
+    assert varlen(lib, N=-1) == INVALID
+    assert varlen(lib, D=100) == UNSUPPORTED
+    assert varlen(lib, N=0) == OK
+    assert varlen(lib, Tq=0, mq=0) == OK
+
+
+def paged(lib, **kw):
+    a = dict(nb=16, bs=128, bt=P, maxb=4, sl=P, S=2, maxlen=512, Hq=8, Hkv=2, D=128, ws=P, wsb=1 << 30)
+    a.update(kw)
+    return lib.attn_fwd_paged(P, P, a["nb"], a["bs"], a["bt"], a["maxb"], a["sl"], a["S"], a["maxlen"], a["Hq"],
+                              a["Hkv"], a["D"], 0.1, 1, P, 1, None, a["ws"], a["wsb"], None, None)
+
+
+def test_paged_validation(lib):
+    assert paged(lib, bs=64) == UNSUPPORTED  # AscendAttentionBackend.get_supported_block_size is [128]
+    assert paged(lib, bt=None) == INVALID
+    assert paged(lib, sl=None) == INVALID
+    assert paged(lib, Hq=6, Hkv=4) == INVALID
+    assert paged(lib, D=48) == UNSUPPORTED
+    assert paged(lib, ws=None) == WORKSPACE
+    assert paged(lib, wsb=16) == WORKSPACE
+    assert paged(lib, ws=ctypes.c_void_p(0x10010)) == WORKSPACE  # must be 256-byte aligned
+    assert paged(lib, S=0) == OK
+
+
+def test_workspace_size_is_pure_and_sized_for_the_plan(lib):
+    f = lib.attn_fwd_paged_workspace_size
+    a = f(64, 32, 8, 128, 32768)
+    assert a == f(64, 32, 8, 128, 32768) and a > 0
+    # one partial (D floats + 1 lse float) per (seq, q head, split)
+    assert a >= 64 * 32 * (128 + 1) * 4
+    assert f(64, 32, 8, 80, 32768) == 0 and f(0, 32, 8, 128, 100) == 0 and f(4, 6, 4, 128, 100) == 0
+    assert f(1, 8, 8, 128, 1) > 0

@@ -1,0 +1,350 @@
+"""GPU parity: every entry point of libgbattn.so against the float64 oracle on
+the same seeded bf16 inputs (max |out err| <= 1e-2 with fp32 out, max |lse
+err| <= 1e-3), plus the bit-exact invariants and the device status bits."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attention_forward_09_gb300 as gb
+import oracle
+import workloads
+from _helpers import LSE_TOL, OUT_TOL, assert_close, bf16_half_ulp, dev, max_err, status_word, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from attention_forward_09_gb300 import _build
+
+    _build.build()
+    gb.load_library()
+
+
+def _gen(seed, *shape):
+    return workloads.randn_bf16(torch.Generator().manual_seed(seed), *shape)
+
+
+def _dense_case(B, Sq, Sk, Hq, Hkv, D, causal, seed, scale=None, out_dtype=torch.float32):
+    g = torch.Generator().manual_seed(seed)
+    q = workloads.randn_bf16(g, B, Sq, Hq, D)
+    k = workloads.randn_bf16(g, B, Sk, Hkv, D)
+    v = workloads.randn_bf16(g, B, Sk, Hkv, D)
+    scale = scale or 1.0 / math.sqrt(D)
+    st = status_word()
+    out, lse = gb.attn_fwd_dense(q.to(dev()), k.to(dev()), v.to(dev()), scale, causal, lse=True,
+                                 out_dtype=out_dtype, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return (q, k, v, scale), out, lse
+
+
+def _varlen_case(lens_q, lens_k, Hq, Hkv, D, causal, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = workloads.randn_bf16(g, sum(lens_q), Hq, D)
+    k = workloads.randn_bf16(g, sum(lens_k), Hkv, D)
+    v = workloads.randn_bf16(g, sum(lens_k), Hkv, D)
+    cq, ck = workloads.cu_from_lengths(lens_q), workloads.cu_from_lengths(lens_k)
+    scale = 1.0 / math.sqrt(D)
+    st = status_word()
+    out, lse = gb.attn_fwd_varlen(q.to(dev()), k.to(dev()), v.to(dev()), cq.to(dev()), ck.to(dev()),
+                                  max(lens_q + [0]), max(lens_k + [0]), scale, causal, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return (q, k, v, cq, ck, scale), out, lse
+
+
+# ------------------------------------------------------------------ dense
+
+@pytest.mark.parametrize("D", workloads.HEAD_SIZES)
+@pytest.mark.parametrize("causal", [False, True])
+def test_dense_all_head_sizes(D, causal):
+    (q, k, v, s), out, lse = _dense_case(2, 200, 200, 4, 2, D, causal, seed=D + causal)
+    ro, rl = oracle.attention_dense(q, k, v, s, causal)
+    assert_close(out, lse, ro, rl, what=f"dense D={D} causal={causal}")
+
+
+@pytest.mark.parametrize("Sq,Sk", [(1, 1), (1, 300), (37, 1), (100, 300), (300, 100), (129, 127), (256, 512)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_dense_ragged_and_bottom_right_causal(Sq, Sk, causal):
+    (q, k, v, s), out, lse = _dense_case(1, Sq, Sk, 3, 1, 128, causal, seed=Sq * 7 + Sk)
+    ro, rl = oracle.attention_dense(q, k, v, s, causal)
+    assert_close(out, lse, ro, rl, what=f"dense Sq={Sq} Sk={Sk} causal={causal}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 2), (8, 1), (32, 8)])
+def test_dense_gqa_ratios(Hq, Hkv):
+    (q, k, v, s), out, lse = _dense_case(1, 130, 190, Hq, Hkv, 64, False, seed=Hq + 100 * Hkv)
+    ro, rl = oracle.attention_dense(q, k, v, s, False)
+    assert_close(out, lse, ro, rl, what=f"GQA {Hq}/{Hkv}")
+
+
+def test_dense_bf16_output_within_rounding():
+    (q, k, v, s), out, lse = _dense_case(1, 150, 150, 2, 2, 128, True, seed=3, out_dtype=torch.bfloat16)
+    ro, rl = oracle.attention_dense(q, k, v, s, True)
+    err = np.abs(to_np(out) - ro)
+    assert np.all(err <= OUT_TOL + bf16_half_ulp(ro))
+    assert max_err(to_np(lse), rl) <= LSE_TOL
+
+
+def test_empty_keys_give_zero_and_minus_inf():
+    (q, k, v, s), out, lse = _dense_case(2, 5, 0, 2, 2, 64, False, seed=1)
+    assert torch.all(out == 0) and torch.all(lse == -math.inf)
+
+
+def test_large_logits_rescale_path():
+    """Scores spanning hundreds of log2 units force the O rescale."""
+    (q, k, v, s), out, lse = _dense_case(1, 128, 512, 2, 2, 128, False, seed=9, scale=2.0)
+    ro, rl = oracle.attention_dense(q, k, v, 2.0, False)
+    assert_close(out, lse, ro, rl, lse_tol=5e-3, what="large logits")  # |lse| ~ 100 here
+
+
+# ------------------------------------------------------------------ varlen
+
+def test_tiny_varlen_config():
+    w = workloads.tiny_varlen()
+    (q, k, v, cq, ck, s), out, lse = _varlen_case(w.lens_q, w.lens_k, w.Hq, w.Hkv, w.D, w.causal, w.seed)
+    ro, rl = oracle.attention_varlen(q, k, v, cq, ck, s, False)
+    assert_close(out, lse, ro, rl, what="tiny varlen")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_odd_lengths_and_empty_docs(causal):
+    lens_q = [1, 37, 0, 127, 129, 300]
+    lens_k = [1, 37, 5, 127, 200, 301]
+    (q, k, v, cq, ck, s), out, lse = _varlen_case(lens_q, lens_k, 8, 2, 128, causal, seed=11 + causal)
+    ro, rl = oracle.attention_varlen(q, k, v, cq, ck, s, causal)
+    assert_close(out, lse, ro, rl, what=f"varlen causal={causal}")
+
+
+def test_varlen_pack_equals_documents_alone_bit_exact():
+    lens = [129, 37, 300]
+    (q, k, v, cq, ck, s), out, lse = _varlen_case(lens, lens, 4, 4, 64, True, seed=5)
+    for n, L in enumerate(lens):
+        a, b = int(cq[n]), int(cq[n + 1])
+        o1, l1 = gb.attn_fwd_varlen(q[a:b].contiguous().to(dev()), k[a:b].contiguous().to(dev()),
+                                    v[a:b].contiguous().to(dev()),
+                                    torch.tensor([0, L], dtype=torch.int32, device=dev()),
+                                    torch.tensor([0, L], dtype=torch.int32, device=dev()), L, L, s, True, lse=True)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, out[a:b]) and torch.equal(l1, lse[:, a:b])
+
+
+def test_dense_equals_varlen_with_arange_bit_exact():
+    B, S, H, D = 3, 150, 4, 128
+    (q, k, v, s), out, lse = _dense_case(B, S, S, H, H, D, True, seed=21)
+    cu = torch.arange(0, (B + 1) * S, S, dtype=torch.int32, device=dev())
+    ov, lv = gb.attn_fwd_varlen(q.reshape(B * S, H, D).to(dev()), k.reshape(B * S, H, D).to(dev()),
+                                v.reshape(B * S, H, D).to(dev()), cu, cu, S, S, s, True, lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(ov.reshape(B, S, H, D), out)
+    assert torch.equal(lv.reshape(H, B, S).permute(1, 0, 2), lse)
+
+
+def test_varlen_bad_cu_seqlens_sets_status():
+    q = _gen(1, 64, 2, 64).to(dev())
+    cu = torch.tensor([0, 40, 30, 64], dtype=torch.int32, device=dev())  # decreasing
+    st = status_word()
+    out = torch.full((64, 2, 64), 7.0, device=dev())
+    gb.attn_fwd_varlen(q, q, q, cu, cu, 40, 40, 0.125, False, out=out, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & gb.DEV_BAD_SEQLEN
+    st.zero_()
+    cu2 = torch.tensor([0, 64], dtype=torch.int32, device=dev())
+    gb.attn_fwd_varlen(q, q, q, cu2, cu2, 32, 32, 0.125, False, out=out, dev_status=st)  # max_seqlen too small
+    torch.cuda.synchronize()
+    assert int(st.item()) & gb.DEV_BAD_SEQLEN
+
+
+# ------------------------------------------------------------ invariants
+
+def test_power_of_two_prescale_bit_exact():
+    """vllm-omni flash_attn.py, FlashAttentionImpl._forward_prefix_kv_slice_npu:
+    inputs divided by 2 with the scale times 4, output times 2, is exact."""
+    (q, k, v, s), out, lse = _dense_case(1, 200, 260, 4, 2, 128, True, seed=31)
+    o2, l2 = gb.attn_fwd_dense((q / 2).to(dev()), (k / 2).to(dev()), (v / 2).to(dev()), 4 * s, True, lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o2 * 2, out) and torch.equal(l2, lse)
+
+
+def test_deterministic():
+    (q, k, v, s), out, lse = _dense_case(1, 300, 300, 4, 4, 96, True, seed=41)
+    o2, l2 = gb.attn_fwd_dense(q.to(dev()), k.to(dev()), v.to(dev()), s, True, lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, out) and torch.equal(l2, lse)
+
+
+def test_constant_values_give_constant_output():
+    """Weights sum to one.  The P V product uses P rounded to bf16 while the
+    normaliser sums the fp32 weights, so this holds to 2^-8 relative, not
+    exactly."""
+    q, k = _gen(1, 1, 260, 4, 128), _gen(2, 1, 260, 4, 128)
+    v = torch.ones(1, 260, 4, 128, dtype=torch.bfloat16)
+    out, _ = gb.attn_fwd_dense(q.to(dev()), k.to(dev()), v.to(dev()), 0.09, True)
+    torch.cuda.synchronize()
+    assert float((out - 1).abs().max()) <= 2.0 ** -8
+
+
+def test_causal_last_row_equals_full_single_query():
+    (q, k, v, s), out, lse = _dense_case(1, 77, 333, 2, 2, 128, True, seed=51)
+    o1, l1 = gb.attn_fwd_dense(q[:, -1:].contiguous().to(dev()), k.to(dev()), v.to(dev()), s, False, lse=True)
+    torch.cuda.synchronize()
+    assert float((o1[0, 0] - out[0, -1]).abs().max()) <= 1e-5
+    assert float((l1[0, :, 0] - lse[0, :, -1]).abs().max()) <= 1e-5
+
+
+# ---------------------------------------------------------- full configs
+# Sampled rows at the full sizes the bench times; the oracle evaluates them one by one.
+
+def _sample_rows(n, count, seed):
+    r = np.random.default_rng(seed)
+    rows = set([0, n - 1, min(n - 1, 127), min(n - 1, 128)])
+    rows.update(int(x) for x in r.integers(0, n, count))
+    return sorted(rows)
+
+
+def _check_dense_sampled(w, count=24):
+    q, k, v = w.make()
+    st = status_word()
+    out, lse = gb.attn_fwd_dense(q.to(dev()), k.to(dev()), v.to(dev()), w.scale, w.causal, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rows = _sample_rows(w.Sq, count, 7)
+    for b in range(w.B):
+        ro, rl = oracle.attention_single(q[b], k[b], v[b], w.scale, w.causal, rows=rows)
+        assert_close(out[b, rows], lse[b][:, rows], ro, rl, what=f"{w.name} batch {b}")
+
+
+def test_config_dit_self_attention_sampled():
+    _check_dense_sampled(workloads.dit_self())
+
+
+def test_config_cross_attention_sampled():
+    _check_dense_sampled(workloads.cross_attn())
+
+
+@pytest.mark.parametrize("D", [64, 96, 192, 256])
+def test_config_head_sweep_sampled(D):
+    _check_dense_sampled(workloads.head_sweep(D), count=12)
+
+
+def test_config_varlen_causal_gqa_sampled():
+    w = workloads.varlen_causal_gqa()
+    q, k, v, cq, ck = w.make()
+    st = status_word()
+    out, lse = gb.attn_fwd_varlen(q.to(dev()), k.to(dev()), v.to(dev()), cq.to(dev()), ck.to(dev()),
+                                  max(w.lens_q), max(w.lens_k), w.scale, True, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for n, L in enumerate(w.lens_q):
+        a = int(cq[n])
+        rows = _sample_rows(L, 6, n)
+        ro, rl = oracle.attention_single(q[a:a + L], k[a:a + L], v[a:a + L], w.scale, True, rows=rows)
+        glob = [a + r for r in rows]
+        assert_close(out[glob], lse[:, glob], ro, rl, what=f"doc {n} (L={L})")
+
+
+# ------------------------------------------------------------------ paged
+
+def _paged_run(w, poison=False, bt_override=None, sl_override=None, max_len=None):
+    q, cache, bt, sl = w.make()
+    if bt_override is not None:
+        bt = bt_override
+    if sl_override is not None:
+        sl = sl_override
+    cache_d = cache.to(dev())
+    if poison:  # slots past each sequence's end hold NaN: they must never be read into the result
+        for s, n in enumerate(w.seq_lens):
+            if n % 128:
+                blk = int(bt[s, n // 128])
+                cache_d[:, blk, n % 128:] = float("nan")
+    st = status_word()
+    out, lse = gb.attn_fwd_paged(q.to(dev()), cache_d, bt.to(dev()), sl.to(dev()),
+                                 max_len or max(w.seq_lens), w.scale, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    return (q, cache, bt, sl), out, lse, int(st.item())
+
+
+@pytest.mark.parametrize("D", workloads.HEAD_SIZES)
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4), (16, 2)])
+def test_paged_small(D, Hq, Hkv):
+    w = workloads.Paged("p", [1, 127, 128, 129, 700, 3000], Hq, Hkv, D, seed=D + Hq, extra_blocks=3)
+    (q, cache, bt, sl), out, lse, st = _paged_run(w, poison=True)
+    assert st == 0
+    ro, rl = oracle.attention_paged(q, cache, bt, sl, w.scale)
+    assert_close(out, lse, ro, rl, what=f"paged D={D} {Hq}/{Hkv}")
+
+
+def test_paged_long_context_many_splits():
+    w = workloads.Paged("p", [32768, 5000, 1], 32, 8, 128, seed=77)
+    (q, cache, bt, sl), out, lse, st = _paged_run(w)
+    assert st == 0
+    ro, rl = oracle.attention_paged(q, cache, bt, sl, w.scale)
+    assert_close(out, lse, ro, rl, what="paged long")
+
+
+def test_paged_block_permutation_bit_identical():
+    w = workloads.Paged("p", [900, 2000, 130], 8, 2, 128, seed=5)
+    (q, cache, bt, sl), out, lse, _ = _paged_run(w)
+    # move every block to a new physical place and rewrite the table to match
+    perm = torch.randperm(w.num_blocks, generator=torch.Generator().manual_seed(99))
+    cache2 = torch.empty_like(cache)
+    cache2[:, perm] = cache
+    bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].to(torch.int32), bt)
+    st = status_word()
+    out2, lse2 = gb.attn_fwd_paged(q.to(dev()), cache2.to(dev()), bt2.to(dev()), sl.to(dev()), max(w.seq_lens),
+                                   w.scale, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, out) and torch.equal(lse2, lse)
+
+
+def test_paged_matches_dense_single_query():
+    w = workloads.Paged("p", [1000, 257], 8, 2, 128, seed=15)
+    (q, cache, bt, sl), out, lse, _ = _paged_run(w)
+    ks, vs = oracle.paged_gather(cache, bt, sl)
+    for s, n in enumerate(w.seq_lens):
+        kk = torch.from_numpy(ks[s]).to(torch.bfloat16)[None].contiguous()
+        vv = torch.from_numpy(vs[s]).to(torch.bfloat16)[None].contiguous()
+        o1, l1 = gb.attn_fwd_dense(q[s][None, None].contiguous().to(dev()), kk.to(dev()), vv.to(dev()), w.scale,
+                                   False, lse=True)
+        torch.cuda.synchronize()
+        assert float((o1[0, 0] - out[s]).abs().max()) <= 2e-3
+        assert float((l1[0, :, 0] - lse[s]).abs().max()) <= 1e-4
+
+
+def test_paged_bad_block_and_seq_len_status():
+    w = workloads.Paged("p", [300, 200], 4, 2, 64, seed=3)
+    q, cache, bt, sl = w.make()
+    bt_bad = bt.clone()
+    bt_bad[0, 1] = w.num_blocks + 5
+    (_, _, _, _), out, lse, st = _paged_run(w, bt_override=bt_bad)
+    assert st & gb.DEV_BAD_INDEX
+    # the bad block's tokens are skipped: sequence 0 then equals attention over its other tokens
+    ks, vs = oracle.paged_gather(cache, bt, sl)
+    keep = np.r_[0:128, 256:300]
+    ro, rl = oracle.attention_single(q[0:1], ks[0][keep], vs[0][keep], w.scale, False)
+    assert_close(out[0:1], lse[0:1].T, ro, rl, what="bad block skipped")
+    sl_bad = sl.clone()
+    sl_bad[1] = 5000
+    (_, _, _, _), out, lse, st = _paged_run(w, sl_override=sl_bad, max_len=300)
+    assert st & gb.DEV_BAD_SEQLEN
+
+
+def test_paged_zero_length_sequence():
+    w = workloads.Paged("p", [0, 50], 4, 4, 128, seed=8)
+    (q, cache, bt, sl), out, lse, st = _paged_run(w)
+    assert torch.all(out[0] == 0) and torch.all(lse[0] == -math.inf)
+    ro, rl = oracle.attention_paged(q, cache, bt, sl, w.scale)
+    assert_close(out, lse, ro, rl, what="zero length")
+
+
+def test_config_paged_decode_sampled():
+    w = workloads.paged_decode()
+    (q, cache, bt, sl), out, lse, st = _paged_run(w)
+    assert st == 0
+    pick = sorted({0, int(np.argmax(w.seq_lens)), int(np.argmin(w.seq_lens)), 17, 63})
+    ro, rl = oracle.attention_paged(q[pick], cache, bt[pick], sl[pick], w.scale)
+    assert_close(out[pick], lse[pick], ro, rl, what="paged decode config")
