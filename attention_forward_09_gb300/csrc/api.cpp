@@ -225,7 +225,8 @@ gbattn_status attn_fwd_paged(const void* q, const void* kv_cache, int num_blocks
     gbattn_status s = device_info(&di);
     if (s != GBATTN_OK) return s;
     CUtensorMap tm;
-    if (!encode_rows_heads_d(&tm, kv_cache, 2LL * num_blocks * 128, Hkv, D, 128)) return GBATTN_ERR_CUDA;
+    if (!encode_rows_heads_d(&tm, kv_cache, 2LL * num_blocks * 128, Hkv, D, gbattn::paged_slice_rows(D)))
+        return GBATTN_ERR_CUDA;
     PagedParams p{};
     p.q = q;
     p.block_table = block_table;

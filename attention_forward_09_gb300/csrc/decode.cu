@@ -7,20 +7,30 @@
 // is slot t % 128 of block block_table[s, t / 128], the AscendMetadata
 // slot_mapping rule).
 //
-// The path is HBM-bound (about 4 bytes of K/V per multiply-add), so it runs on
-// the CUDA cores, not the tensor cores:
-//   * work item = (sequence, KV head, split of `blocks_per_split` blocks); a
-//     persistent grid of one CTA per SM walks the items round-robin;
-//   * one producer thread streams each 128-token block's K and V tile
-//     (32 KB each at D = 128) with TMA into a ring of shared-memory slots, the
-//     block id taken from block_table (bounds-checked; a bad id is skipped
-//     and reported);
-//   * 128 consumer threads: thread t scores token t against the GQA group's
-//     query heads (each K byte is read once for the whole group), an online
-//     softmax per head across the block, then O += P V with one thread per
-//     (column pair, token group);
-//   * each item writes a partial (o / l, lse); paged_combine merges the splits
-//     with lse = ln sum_i exp(lse_i), o = sum_i exp(lse_i - lse) o_i.
+// The path is HBM-bound, so it runs on the CUDA cores.  Design:
+//   * work item = (sequence, KV head [, query-head subgroup], split of up to
+//     `blocks_per_split` cache blocks), KV heads varying fastest so that the
+//     CTAs working at one moment read neighbouring 256-byte head rows of the
+//     same cache rows; a persistent grid of one CTA per SM walks the items;
+//   * the K and V of one slice (a whole 128-token block, or 64 tokens at
+//     D >= 192) arrive by TMA as one box per 64 columns into a ring of
+//     shared-memory slots (large boxes: the TMA issue cost per box, not the
+//     bytes, limits small-box streaming);
+//   * all 8 warps consume every slot, each a fixed run of its tokens, so
+//     every mbarrier phase is awaited in order; there is no producer warp:
+//     the last warp to release a slot (a shared-memory counter) refills it
+//     from a look-ahead walk of the same slice sequence;
+//   * inside a warp a group of LPG lanes owns one token at a time, each lane
+//     E = D / LPG columns, with the GQA group's query rows for those columns
+//     in registers: q.k is a packed-fp32 (fma.rn.f32x2) dot product plus a
+//     log2(LPG)-level shuffle reduction, o += p.v reuses the same columns, so
+//     each K and V byte is read from shared memory once for all HG heads;
+//   * each warp keeps its own online softmax; at the end of an item the
+//     groups and warps merge (m, l, o) by the log-sum-exp rule and write the
+//     item's partial (o / l, lse); paged_combine merges the splits:
+//     lse = ln sum_i exp(lse_i), o = sum_i exp(lse_i - lse) o_i.
+// Tokens at or past seq_len are never used, neither in q.k nor in p.v, so
+// whatever the unused cache slots hold cannot reach the result.
 #include <math.h>
 
 #include "kernels.h"
@@ -29,6 +39,7 @@
 namespace gbattn {
 
 constexpr int kBlk = 128;  // tokens per cache block
+constexpr int kWarps = 8;  // all of them consume every slot
 constexpr float kLn2f = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -36,45 +47,52 @@ template <int D_, int HG_>
 struct PagedCfg {
     static constexpr int D = D_;
     static constexpr int HG = HG_;                       // query heads per CTA (divides the GQA group)
+    static constexpr int SLICE = D <= 128 ? 128 : 64;    // tokens per slot
+    // columns per lane: at most 64 / HG (q and o stay in registers), and small
+    // enough that every warp owns at least one token step of a slice
+    static constexpr int E0 = (D % 96 == 0) ? 48 / HG : 64 / HG;
+    static constexpr int EMAX = D * SLICE / (32 * kWarps);
+    static constexpr int E = E0 < EMAX ? E0 : EMAX;
+    static constexpr int LPG = D / E;                    // lanes per token group
+    static constexpr int TPW = 32 / LPG;                 // tokens a warp handles per step
+    static constexpr int NSTEP = SLICE / TPW;            // steps per slot
+    static constexpr int WSTEP = NSTEP / kWarps;         // steps per warp per slot
+    static constexpr int SUBS = WSTEP < 32 / HG ? WSTEP : 32 / HG;  // steps per softmax sub-chunk
     static constexpr int NCH = (D + 63) / 64;
-    static constexpr int SLOT_BYTES = NCH * kBlk * 128;  // K or V of one block for one KV head
-    static constexpr int STAGES = D <= 64 ? 8 : (D <= 128 ? 6 : (D <= 192 ? 4 : 3));
-    static constexpr int DP = D / 2;                     // column pairs
-    static constexpr int TG = DP <= 32 ? 4 : (DP <= 64 ? 2 : 1);  // token groups in P V
-    static constexpr int TPG = kBlk / TG;                // tokens per group
-    static constexpr int PV_THREADS = DP * TG;           // <= 128
-    // shared memory: slots | q[HG][D] f32 | P[128][HG] f32 | red[2][4][HG] | acc[TG][HG][D] | flags | bars
-    static constexpr int OFF_Q = STAGES * SLOT_BYTES;
-    static constexpr int OFF_P = OFF_Q + HG * D * 4;
-    static constexpr int OFF_RED = OFF_P + kBlk * HG * 4;
-    static constexpr int OFF_ACC = OFF_RED + 2 * 4 * HG * 4;
-    static constexpr int OFF_FLAG = OFF_ACC + TG * HG * D * 4;
-    static constexpr int OFF_BAR = (OFF_FLAG + STAGES * 4 + 7) & ~7;
-    static constexpr int SMEM_BYTES = 1024 + OFF_BAR + 2 * STAGES * 8;
-    static_assert(PV_THREADS <= 128, "P V thread map");
-    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static constexpr int HALF_BYTES = NCH * SLICE * 128;  // K (or V) of one slice
+    static constexpr int SLOT_BYTES = 2 * HALF_BYTES;
+    static constexpr int MERGE_BYTES = kWarps * HG * (D + 2) * 4;
+    static constexpr int STAGES_RAW = (230400 - MERGE_BYTES) / SLOT_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    // vector width of one shared-memory load, in bf16 elements
+    static constexpr int U = (E % 8 == 0) ? 8 : ((E % 4 == 0) ? 4 : 2);
+    // shared memory: slots | merge scratch [warps][HG][D + 2] f32 | counters | flags | bars
+    static constexpr int OFF_MERGE = STAGES * SLOT_BYTES;
+    static constexpr int OFF_CNT = OFF_MERGE + MERGE_BYTES;
+    static constexpr int OFF_FLAG = OFF_CNT + STAGES * 4;
+    static constexpr int OFF_USE = OFF_FLAG + STAGES * 4;
+    static constexpr int OFF_BAR = (OFF_USE + STAGES * 4 + 7) & ~7;
+    static constexpr int SMEM_BYTES = 1024 + OFF_BAR + STAGES * 8;
+    static_assert(LPG * E == D && 32 % LPG == 0 && SLICE % TPW == 0 && NSTEP % kWarps == 0 && WSTEP % SUBS == 0,
+                  "lane map");
+    static_assert(STAGES >= 2 && SMEM_BYTES <= 232448, "shared memory budget");
 };
-
-__device__ __forceinline__ void consumer_sync() {  // the 128 consumer threads only
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-}
 
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
 struct ItemCoords {
-    int s, kvh, h0, sp, b0, b1, L;
+    int s, kvh, h0, sp, tok0, tok1;  // tokens [tok0, tok1) of sequence s
 };
 
-// Item `it` -> (sequence, head group, split); sp varies fastest so the splits
-// of one long sequence land on different CTAs.
+// Item `it` -> (sequence, head group, split); the head group varies fastest.
 __device__ __forceinline__ ItemCoords item_coords(const PagedParams& p, int it, int n_hgroups,
                                                   uint32_t* status, bool report) {
     ItemCoords c;
-    c.sp = it % p.max_splits;
-    const int rest = it / p.max_splits;
-    const int hg = rest % n_hgroups;
-    c.s = rest / n_hgroups;
+    const int hg = it % n_hgroups;
+    const int rest = it / n_hgroups;
+    c.sp = rest % p.max_splits;
+    c.s = rest / p.max_splits;
     const int per_kv = p.group / p.heads_per_cta;
     c.kvh = hg / per_kv;
     c.h0 = c.kvh * p.group + (hg % per_kv) * p.heads_per_cta;
@@ -84,260 +102,313 @@ __device__ __forceinline__ ItemCoords item_coords(const PagedParams& p, int it, 
         if (report && status) atomicOr(status, kDevBadSeqlen);
         L = L < 0 ? 0 : cap;
     }
-    c.L = L;
-    const int nblk = (L + kBlk - 1) / kBlk;
-    c.b0 = c.sp * p.blocks_per_split;
-    c.b1 = min(nblk, c.b0 + p.blocks_per_split);
+    c.tok0 = c.sp * p.blocks_per_split * kBlk;
+    c.tok1 = min(L, c.tok0 + p.blocks_per_split * kBlk);
     return c;
 }
 
+// Walks this CTA's slices in order: (item, first token of the slice).
+struct SliceWalk {
+    int it, tok;
+    ItemCoords c;
+    __device__ __forceinline__ void seek(const PagedParams& p, int n_items, int n_hgroups, int start) {
+        for (it = start; it < n_items; it += gridDim.x) {
+            c = item_coords(p, it, n_hgroups, nullptr, false);
+            if (c.tok0 < c.tok1) {
+                tok = c.tok0;
+                return;
+            }
+        }
+        tok = 0;
+    }
+    __device__ __forceinline__ bool done(int n_items) const { return it >= n_items; }
+    template <int SLICE>
+    __device__ __forceinline__ void next(const PagedParams& p, int n_items, int n_hgroups) {
+        tok += SLICE;
+        if (tok >= c.tok1) seek(p, n_items, n_hgroups, it + gridDim.x);
+    }
+};
+
+// E columns [e0, e0 + E) of row `row` of a swizzled slice (64-column chunks
+// of SLICE rows x 128 B, 16-byte piece c of row r stored at c ^ (r % 8)), as
+// E/2 packed words.
 template <class C>
-__global__ void __launch_bounds__(160, 1)
+__device__ __forceinline__ void load_cols(uint32_t base, int row, int e0, uint32_t (&w)[C::E / 2]) {
+#pragma unroll
+    for (int u = 0; u < C::E / C::U; ++u) {
+        const int e = e0 + u * C::U;
+        const uint32_t addr = base + (e >> 6) * (C::SLICE * 128) + row * 128 + ((((e & 63) >> 3) ^ (row & 7)) << 4) +
+                              (e & 7) * 2;
+        if constexpr (C::U == 8) {
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[u * 4]), "=r"(w[u * 4 + 1]), "=r"(w[u * 4 + 2]), "=r"(w[u * 4 + 3])
+                         : "r"(addr));
+        } else if constexpr (C::U == 4) {
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(w[u * 2]), "=r"(w[u * 2 + 1]) : "r"(addr));
+        } else {
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[u]) : "r"(addr));
+        }
+    }
+}
+
+// Issue the TMA copies of one slice into `slot` (one thread).  A block id
+// outside [0, num_blocks) is reported; the slot is then marked bad and its
+// barrier completed without data.
+template <class C>
+__device__ __forceinline__ void fill_slot(const CUtensorMap* tm, const PagedParams& p, uint32_t sSlots, uint32_t bar,
+                                          volatile int* sflag, volatile int* suse, int slot, int use,
+                                          const SliceWalk& w) {
+    const int blk = p.block_table[static_cast<long long>(w.c.s) * p.max_blocks_per_seq + w.tok / kBlk];
+    const bool valid = blk >= 0 && blk < p.num_blocks;
+    sflag[slot] = valid ? 0 : 1;
+    suse[slot] = use;
+    if (!valid) {
+        if (p.status) atomicOr(p.status, kDevBadIndex);
+        mbar_arrive(bar);
+        return;
+    }
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, C::SLOT_BYTES);
+    const int row = blk * kBlk + (w.tok & (kBlk - 1));
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+        for (int ch = 0; ch < C::NCH; ++ch)
+            tma_load_3d(sSlots + slot * C::SLOT_BYTES + kv * C::HALF_BYTES + ch * C::SLICE * 128, tm, bar, ch * 64,
+                        w.c.kvh, row + kv * p.num_blocks * kBlk);
+}
+
+template <class C>
+__global__ void __launch_bounds__(32 * kWarps, 1)
     paged_decode_sm103a(const __grid_constant__ CUtensorMap tmKV, const PagedParams p) {
-    constexpr int D = C::D, HG = C::HG, STAGES = C::STAGES, NCH = C::NCH;
+    constexpr int D = C::D, HG = C::HG, E = C::E, LPG = C::LPG, TPW = C::TPW, STAGES = C::STAGES;
+    constexpr int SLICE = C::SLICE, WSTEP = C::WSTEP, SUBS = C::SUBS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sSlots = smem_u32(smem);
-    float* sq = reinterpret_cast<float*>(smem + C::OFF_Q);    // [HG][D]
-    float* sp_ = reinterpret_cast<float*>(smem + C::OFF_P);   // [128][HG]
-    float* sred = reinterpret_cast<float*>(smem + C::OFF_RED);  // [2][4][HG]
-    float* sacc = reinterpret_cast<float*>(smem + C::OFF_ACC);  // [TG][HG][D]
-    volatile int* sflag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);  // slot holds a bad block
+    float* smerge = reinterpret_cast<float*>(smem + C::OFF_MERGE);  // [warp][HG][D + 2]: o..., m, l
+    int* scnt = reinterpret_cast<int*>(smem + C::OFF_CNT);          // releases per slot, monotonic
+    volatile int* sflag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
+    volatile int* suse = reinterpret_cast<volatile int*>(smem + C::OFF_USE);  // last use issued per slot
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     auto b_full = [&](int s) { return smem_u32(&bars[s]); };
-    auto b_empty = [&](int s) { return smem_u32(&bars[STAGES + s]); };
     __shared__ int abort_flag_storage;
     volatile int* abort_flag = &abort_flag_storage;
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_hgroups = p.Hkv * (p.group / p.heads_per_cta);
     const int n_items = p.num_seqs * n_hgroups * p.max_splits;
 
     if (status_has_timeout(p.status, kDevTimeout)) return;
-    if (tid == 0) {
+    SliceWalk cur, ahead;
+    cur.seek(p, n_items, n_hgroups, blockIdx.x);
+    ahead = cur;
+    if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(b_full(s), 1);
-            mbar_init(b_empty(s), 128);
+            scnt[s] = 0;
+            suse[s] = -1;
         }
         abort_flag_storage = 0;
         fence_mbar_init();
+        tma_prefetch_desc(&tmKV);
     }
     __syncthreads();
+    // prologue: the first STAGES slices; `ahead` ends STAGES slices past `cur`
+    for (int s = 0; s < STAGES; ++s) {
+        if (ahead.done(n_items)) break;
+        if (threadIdx.x == 0) fill_slot<C>(&tmKV, p, sSlots, b_full(s), sflag, suse, s, 0, ahead);
+        ahead.template next<SLICE>(p, n_items, n_hgroups);
+    }
     bool ok = true;
-
-    if (warp == 4) {
-        // --------------------------------------------------------- producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tmKV);
-            int cnt = 0;
-            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-                const ItemCoords c = item_coords(p, it, n_hgroups, p.status, false);
-                for (int b = c.b0; ok && b < c.b1; ++b) {
-                    const int blk = p.block_table[static_cast<long long>(c.s) * p.max_blocks_per_seq + b];
-                    const bool valid = blk >= 0 && blk < p.num_blocks;
-                    if (!valid && p.status) atomicOr(p.status, kDevBadIndex);
-                    for (int kv = 0; kv < 2; ++kv, ++cnt) {
-                        const int slot = cnt % STAGES, u = cnt / STAGES;
-                        if (u > 0 && !(ok = mbar_wait(b_empty(slot), (u - 1) & 1, abort_flag))) {
-                            *abort_flag = 1;
-                            break;
+    const float c2 = p.scale_log2;
+    const int grp = lane / LPG;        // token group within the warp
+    const int e0 = (lane % LPG) * E;   // this lane's first column
+    int g = 0;                         // global slice counter
+    while (!cur.done(n_items)) {
+        const ItemCoords c = item_coords(p, cur.it, n_hgroups, p.status, threadIdx.x == 0);
+        // this lane's columns of the HG query rows, fp32 pairs
+        float2 q[HG][E / 2];
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+            const uint16_t* qh =
+                reinterpret_cast<const uint16_t*>(p.q) + (static_cast<long long>(c.s) * p.Hq + c.h0 + h) * D + e0;
+#pragma unroll
+            for (int x = 0; x < E / 2; ++x)
+                q[h][x] = make_float2(__uint_as_float(static_cast<uint32_t>(qh[2 * x]) << 16),
+                                      __uint_as_float(static_cast<uint32_t>(qh[2 * x + 1]) << 16));
+        }
+        float m[HG], l[HG];
+        float2 o[HG][E / 2];
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+#pragma unroll
+            for (int x = 0; x < E / 2; ++x) o[h][x] = make_float2(0.f, 0.f);
+        }
+        // ---------------------------------------------- slices of this item
+        const int item = cur.it;
+        while (!cur.done(n_items) && cur.it == item) {
+            const int slot = g % STAGES, use = g / STAGES;
+            if (!mbar_wait(b_full(slot), use & 1, abort_flag)) {
+                ok = false;
+                *abort_flag = 1;
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            const int nvalid = (ok && !sflag[slot]) ? min(SLICE, c.tok1 - cur.tok) : 0;
+            const uint32_t kbase = sSlots + slot * C::SLOT_BYTES;
+            const uint32_t vbase = kbase + C::HALF_BYTES;
+#pragma unroll 1
+            for (int sc = 0; sc < WSTEP / SUBS; ++sc) {
+                // ---- scores of SUBS tokens of this group, HG heads
+                float s[SUBS][HG];
+#pragma unroll
+                for (int st = 0; st < SUBS; ++st) {
+                    const int t = (warp * WSTEP + sc * SUBS + st) * TPW + grp;
+                    float dot[HG];
+                    if (t < nvalid) {  // group-uniform
+                        uint32_t w[E / 2];
+                        load_cols<C>(kbase, t, e0, w);
+                        float2 acc[HG];
+#pragma unroll
+                        for (int h = 0; h < HG; ++h) acc[h] = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int x = 0; x < E / 2; ++x) {
+                            const float2 kk = make_float2(bf_lo(w[x]), bf_hi(w[x]));
+#pragma unroll
+                            for (int h = 0; h < HG; ++h) acc[h] = __ffma2_rn(q[h][x], kk, acc[h]);
                         }
-                        sflag[slot] = valid ? 0 : 1;
-                        if (valid) {
-                            mbar_arrive_expect_tx(b_full(slot), C::SLOT_BYTES);
-                            const int row = (kv * p.num_blocks + blk) * kBlk;
-                            for (int ch = 0; ch < NCH; ++ch)
-                                tma_load_3d(sSlots + slot * C::SLOT_BYTES + ch * kBlk * 128, &tmKV, b_full(slot),
-                                            ch * 64, c.kvh, row);
-                        } else {
-                            mbar_arrive(b_full(slot));
+#pragma unroll
+                        for (int h = 0; h < HG; ++h) dot[h] = acc[h].x + acc[h].y;
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < HG; ++h) dot[h] = 0.f;
+                    }
+#pragma unroll
+                    for (int off = 1; off < LPG; off <<= 1)
+#pragma unroll
+                        for (int h = 0; h < HG; ++h) dot[h] += __shfl_xor_sync(0xffffffffu, dot[h], off);
+#pragma unroll
+                    for (int h = 0; h < HG; ++h) s[st][h] = (t < nvalid) ? dot[h] * c2 : -INFINITY;
+                }
+                // ---- online softmax for this group (identical in its LPG lanes)
+#pragma unroll
+                for (int h = 0; h < HG; ++h) {
+                    float cm = s[0][h];
+#pragma unroll
+                    for (int st = 1; st < SUBS; ++st) cm = fmaxf(cm, s[st][h]);
+                    if (cm > m[h] + 8.0f) {  // rescale only when the max grows by more than 2^8
+                        const float a = ex2(m[h] - cm);
+                        const float2 a2 = make_float2(a, a);
+                        l[h] *= a;
+#pragma unroll
+                        for (int x = 0; x < E / 2; ++x) o[h][x] = __fmul2_rn(o[h][x], a2);
+                        m[h] = cm;
+                    }
+                    const float ms = (m[h] == -INFINITY) ? 0.f : m[h];
+#pragma unroll
+                    for (int st = 0; st < SUBS; ++st) {
+                        s[st][h] = ex2(s[st][h] - ms);
+                        l[h] += s[st][h];
+                    }
+                }
+                // ---- o += p v over the same columns
+#pragma unroll
+                for (int st = 0; st < SUBS; ++st) {
+                    const int t = (warp * WSTEP + sc * SUBS + st) * TPW + grp;
+                    if (t < nvalid) {
+                        uint32_t w[E / 2];
+                        load_cols<C>(vbase, t, e0, w);
+#pragma unroll
+                        for (int x = 0; x < E / 2; ++x) {
+                            const float2 vv = make_float2(bf_lo(w[x]), bf_hi(w[x]));
+#pragma unroll
+                            for (int h = 0; h < HG; ++h)
+                                o[h][x] = __ffma2_rn(make_float2(s[st][h], s[st][h]), vv, o[h][x]);
                         }
                     }
                 }
             }
-            if (!ok) {
-                // Drain: wait (bounded) for the copies still in flight.
-                for (int t = (cnt > STAGES ? cnt - STAGES : 0); t < cnt; ++t)
-                    mbar_wait_drain(b_full(t % STAGES), (t / STAGES) & 1);
+            // ---- release the slot; the last warp out refills it with the slice STAGES ahead
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();  // this warp's reads of the slot happen before its release
+                const int prev = atomicAdd(scnt + slot, 1);
+                __threadfence_block();
+                if (prev == use * kWarps + kWarps - 1 && ok && !*abort_flag && !ahead.done(n_items))
+                    fill_slot<C>(&tmKV, p, sSlots, b_full(slot), sflag, suse, slot, use + 1, ahead);
+            }
+            __syncwarp();
+            if (!ahead.done(n_items)) ahead.template next<SLICE>(p, n_items, n_hgroups);
+            cur.template next<SLICE>(p, n_items, n_hgroups);
+            ++g;
+        }
+        // ---- merge the token groups of this warp (same columns, different tokens)
+#pragma unroll
+        for (int off = LPG; off < 32; off <<= 1) {
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+                const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
+                const float lo = __shfl_xor_sync(0xffffffffu, l[h], off);
+                const float mt = fmaxf(m[h], mo);
+                const float a = (m[h] == -INFINITY) ? 0.f : ex2(m[h] - mt);
+                const float b = (mo == -INFINITY) ? 0.f : ex2(mo - mt);
+                l[h] = l[h] * a + lo * b;
+#pragma unroll
+                for (int x = 0; x < E / 2; ++x) {
+                    const float ox = __shfl_xor_sync(0xffffffffu, o[h][x].x, off);
+                    const float oy = __shfl_xor_sync(0xffffffffu, o[h][x].y, off);
+                    o[h][x] = make_float2(o[h][x].x * a + ox * b, o[h][x].y * a + oy * b);
+                }
+                m[h] = mt;
             }
         }
-    } else {
-        // -------------------------------------------------------- consumers
-        const float c2 = p.scale_log2;
-        int cnt = 0;
-        // P V thread map: column pair dp, token group tg.
-        const bool pv_active = tid < C::PV_THREADS;
-        const int dp = tid % C::DP, tg = tid / C::DP;
-        for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-            const ItemCoords c = item_coords(p, it, n_hgroups, p.status, tid == 0);
-            if (c.b0 >= c.b1) continue;
-            // this item's query heads -> shared f32
-            consumer_sync();
-            for (int e = tid; e < HG * D; e += 128) {
-                const int i = e / D, d = e % D;
-                const uint16_t* qh = reinterpret_cast<const uint16_t*>(p.q) +
-                                     (static_cast<long long>(c.s) * p.Hq + c.h0 + i) * D + d;
-                sq[e] = __uint_as_float(static_cast<uint32_t>(*qh) << 16);
-            }
-            consumer_sync();
-            float m[HG], l[HG], acc[HG][2];
+        // ---- merge the warps through shared memory, write the item's partial
+        if (grp == 0) {
 #pragma unroll
-            for (int i = 0; i < HG; ++i) {
-                m[i] = -INFINITY;
-                l[i] = 0.f;
-                acc[i][0] = acc[i][1] = 0.f;
-            }
-            for (int b = c.b0; b < c.b1; ++b) {
-                const int nvalid = min(kBlk, c.L - b * kBlk);
-                // ---------------- K: scores of token `tid` for the HG heads
-                // A failed wait never leaves the loop: the consumers keep
-                // meeting at the named barriers (which cannot time out) and
-                // run through the remaining blocks on garbage, fast, because
-                // every later wait sees the abort flag.
-                int slot = cnt % STAGES;
-                if (!mbar_wait(b_full(slot), (cnt / STAGES) & 1, abort_flag)) {
-                    ok = false;
-                    *abort_flag = 1;
+            for (int h = 0; h < HG; ++h) {
+                float* dst = smerge + (warp * HG + h) * (D + 2);
+#pragma unroll
+                for (int x = 0; x < E / 2; ++x) {
+                    dst[e0 + 2 * x] = o[h][x].x;
+                    dst[e0 + 2 * x + 1] = o[h][x].y;
                 }
-                const bool bad = !ok || sflag[slot] != 0;
-                float sc[HG];
-#pragma unroll
-                for (int i = 0; i < HG; ++i) sc[i] = 0.f;
-                if (!bad && tid < nvalid) {
-                    const uint32_t krow = sSlots + slot * C::SLOT_BYTES + tid * 128;
-#pragma unroll
-                    for (int pc = 0; pc < D / 8; ++pc) {
-                        const uint32_t addr = krow + (pc >> 3) * kBlk * 128 + (((pc & 7) ^ (tid & 7)) << 4);
-                        uint32_t k0, k1, k2, k3;
-                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                     : "=r"(k0), "=r"(k1), "=r"(k2), "=r"(k3)
-                                     : "r"(addr));
-                        const float kf[8] = {bf_lo(k0), bf_hi(k0), bf_lo(k1), bf_hi(k1),
-                                             bf_lo(k2), bf_hi(k2), bf_lo(k3), bf_hi(k3)};
-#pragma unroll
-                        for (int i = 0; i < HG; ++i) {
-                            const float4 qa = *reinterpret_cast<const float4*>(sq + i * D + pc * 8);
-                            const float4 qb = *reinterpret_cast<const float4*>(sq + i * D + pc * 8 + 4);
-                            float a = sc[i];
-                            a = fmaf(qa.x, kf[0], a);
-                            a = fmaf(qa.y, kf[1], a);
-                            a = fmaf(qa.z, kf[2], a);
-                            a = fmaf(qa.w, kf[3], a);
-                            a = fmaf(qb.x, kf[4], a);
-                            a = fmaf(qb.y, kf[5], a);
-                            a = fmaf(qb.z, kf[6], a);
-                            a = fmaf(qb.w, kf[7], a);
-                            sc[i] = a;
-                        }
-                    }
+                if (lane == 0) {
+                    dst[D] = m[h];
+                    dst[D + 1] = l[h];
                 }
-                mbar_arrive(b_empty(slot));
-                ++cnt;
-                const bool live = !bad && tid < nvalid;
-                // ---------------- online softmax across the block, per head
-#pragma unroll
-                for (int i = 0; i < HG; ++i) {
-                    float v = live ? sc[i] * c2 : -INFINITY;
-                    sc[i] = v;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-                    if (lane == 0) sred[warp * HG + i] = v;
-                }
-                consumer_sync();
-                float alpha[HG];
-#pragma unroll
-                for (int i = 0; i < HG; ++i) {
-                    const float bm = fmaxf(fmaxf(sred[i], sred[HG + i]), fmaxf(sred[2 * HG + i], sred[3 * HG + i]));
-                    const float mn = fmaxf(m[i], bm);
-                    alpha[i] = (mn == -INFINITY) ? 1.f : ex2(m[i] - mn);
-                    const float msub = (mn == -INFINITY) ? 0.f : mn;
-                    m[i] = mn;
-                    float pv = ex2(sc[i] - msub);  // 0 for masked tokens
-                    sp_[tid * HG + i] = pv;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) pv += __shfl_xor_sync(0xffffffffu, pv, o);
-                    if (lane == 0) sred[4 * HG + warp * HG + i] = pv;
-                }
-                consumer_sync();
-#pragma unroll
-                for (int i = 0; i < HG; ++i)
-                    l[i] = l[i] * alpha[i] + (sred[4 * HG + i] + sred[5 * HG + i]) + (sred[6 * HG + i] + sred[7 * HG + i]);
-                // ---------------- V: O += P V
-                slot = cnt % STAGES;
-                if (!mbar_wait(b_full(slot), (cnt / STAGES) & 1, abort_flag)) {
-                    ok = false;
-                    *abort_flag = 1;
-                }
-                if (pv_active) {
-#pragma unroll
-                    for (int i = 0; i < HG; ++i) {
-                        acc[i][0] *= alpha[i];
-                        acc[i][1] *= alpha[i];
-                    }
-                    if (!bad && ok) {
-                        const int t0 = tg * C::TPG, t1 = min(t0 + C::TPG, nvalid);
-                        const int d = 2 * dp, ch = d >> 6, byte = (d & 63) * 2;
-                        const uint32_t vbase = sSlots + slot * C::SLOT_BYTES + ch * kBlk * 128 + (byte & 15);
-                        const int piece = byte >> 4;
-                        for (int t = t0; t < t1; ++t) {
-                            uint32_t vv;
-                            asm volatile("ld.shared.b32 %0, [%1];"
-                                         : "=r"(vv)
-                                         : "r"(vbase + t * 128 + ((piece ^ (t & 7)) << 4)));
-                            const float v0 = bf_lo(vv), v1 = bf_hi(vv);
-                            if constexpr (HG % 4 == 0) {
-#pragma unroll
-                                for (int i = 0; i < HG; i += 4) {
-                                    const float4 pp = *reinterpret_cast<const float4*>(sp_ + t * HG + i);
-                                    acc[i][0] = fmaf(pp.x, v0, acc[i][0]);
-                                    acc[i][1] = fmaf(pp.x, v1, acc[i][1]);
-                                    acc[i + 1][0] = fmaf(pp.y, v0, acc[i + 1][0]);
-                                    acc[i + 1][1] = fmaf(pp.y, v1, acc[i + 1][1]);
-                                    acc[i + 2][0] = fmaf(pp.z, v0, acc[i + 2][0]);
-                                    acc[i + 2][1] = fmaf(pp.z, v1, acc[i + 2][1]);
-                                    acc[i + 3][0] = fmaf(pp.w, v0, acc[i + 3][0]);
-                                    acc[i + 3][1] = fmaf(pp.w, v1, acc[i + 3][1]);
-                                }
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < HG; ++i) {
-                                    const float pp = sp_[t * HG + i];
-                                    acc[i][0] = fmaf(pp, v0, acc[i][0]);
-                                    acc[i][1] = fmaf(pp, v1, acc[i][1]);
-                                }
-                            }
-                        }
-                    }
-                }
-                mbar_arrive(b_empty(slot));
-                ++cnt;
-                consumer_sync();  // P and the reduction scratch are rewritten by the next block
-            }
-            // ---------------- partial result of this item
-            if (pv_active) {
-#pragma unroll
-                for (int i = 0; i < HG; ++i) {
-                    sacc[(tg * HG + i) * D + 2 * dp] = acc[i][0];
-                    sacc[(tg * HG + i) * D + 2 * dp + 1] = acc[i][1];
-                }
-            }
-            consumer_sync();
-            for (int e = tid; e < HG * D; e += 128) {
-                const int i = e / D, d = e % D;
-                float a = 0.f;
-#pragma unroll
-                for (int g = 0; g < C::TG; ++g) a += sacc[(g * HG + i) * D + d];
-                const long long row = (static_cast<long long>(c.s) * p.Hq + c.h0 + i) * p.max_splits + c.sp;
-                p.part_o[row * D + d] = l[i] > 0.f ? a / l[i] : 0.f;
-                if (d == 0) p.part_lse[row] = l[i] > 0.f ? (m[i] + __log2f(l[i])) * kLn2f : -INFINITY;
             }
         }
+        __syncthreads();
+        for (int x = threadIdx.x; x < HG * D; x += 32 * kWarps) {
+            const int h = x / D, d = x % D;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) mt = fmaxf(mt, smerge[(w * HG + h) * (D + 2) + D]);
+            float lt = 0.f, ot = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float* src = smerge + (w * HG + h) * (D + 2);
+                const float a = (src[D] == -INFINITY) ? 0.f : ex2(src[D] - mt);
+                lt = fmaf(src[D + 1], a, lt);
+                ot = fmaf(src[d], a, ot);
+            }
+            const long long row = (static_cast<long long>(c.s) * p.Hq + c.h0 + h) * p.max_splits + c.sp;
+            p.part_o[row * D + d] = lt > 0.f ? ot / lt : 0.f;
+            if (d == 0) p.part_lse[row] = lt > 0.f ? (mt + __log2f(lt)) * kLn2f : -INFINITY;
+        }
+        __syncthreads();
     }
     if (!ok) {
         *abort_flag = 1;
         if (p.status) atomicOr(p.status, kDevTimeout);
     }
     __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) {  // let copies still in flight land (bounded) before exit
+        for (int s = 0; s < STAGES; ++s)
+            if (suse[s] >= 0) mbar_wait_drain(b_full(s), suse[s] & 1);
+    }
 }
 
 // Merge the split partials of each (sequence, query head).
@@ -346,8 +417,7 @@ __global__ void __launch_bounds__(128) paged_combine(const PagedParams p, int D)
     int L = p.seq_lens[s];
     const int cap = min(p.max_seq_len, p.max_blocks_per_seq * kBlk);
     L = L < 0 ? 0 : (L > cap ? cap : L);
-    const int nblk = (L + kBlk - 1) / kBlk;
-    const int nsp = (nblk + p.blocks_per_split - 1) / p.blocks_per_split;
+    const int nsp = (L + p.blocks_per_split * kBlk - 1) / (p.blocks_per_split * kBlk);
     const long long row0 = (static_cast<long long>(s) * p.Hq + h) * p.max_splits;
     float mx = -INFINITY;
     for (int i = 0; i < nsp; ++i) mx = fmaxf(mx, p.part_lse[row0 + i]);
@@ -389,6 +459,8 @@ PagedPlan paged_plan(int num_seqs, int Hq, int Hkv, int D, int max_seq_len) {
     return pl;
 }
 
+int paged_slice_rows(int D) { return D <= 128 ? 128 : 64; }
+
 template <class C>
 static cudaError_t launch_paged_cfg(const CUtensorMap& tm, const PagedParams& p, int num_sms, cudaStream_t st) {
     static bool attr_done = false;
@@ -401,7 +473,7 @@ static cudaError_t launch_paged_cfg(const CUtensorMap& tm, const PagedParams& p,
     const int n_hgroups = p.Hkv * (p.group / p.heads_per_cta);
     const long long n_items = static_cast<long long>(p.num_seqs) * n_hgroups * p.max_splits;
     const int grid = static_cast<int>(n_items < num_sms ? n_items : num_sms);
-    paged_decode_sm103a<C><<<grid, 160, C::SMEM_BYTES, st>>>(tm, p);
+    paged_decode_sm103a<C><<<grid, 32 * kWarps, C::SMEM_BYTES, st>>>(tm, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     paged_combine<<<p.num_seqs * p.Hq, 128, 0, st>>>(p, C::D);

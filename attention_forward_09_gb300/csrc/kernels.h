@@ -64,6 +64,8 @@ struct PagedPlan {
 };
 PagedPlan paged_plan(int num_seqs, int Hq, int Hkv, int D, int max_seq_len);
 
+int paged_slice_rows(int D);  // tokens per TMA box of the paged cache map
+
 cudaError_t launch_paged(int D, const CUtensorMap& tmKV, const PagedParams& p, int num_sms,
                          cudaStream_t stream);
 

@@ -164,24 +164,32 @@ def sum_over_ranks(x: float, world: int) -> float:
 
 # ----------------------------------------------------------------- CPU oracle
 
-def oracle_prefill_sample(w: workloads.Dense, budget_s: float):
-    """Time the float64 oracle on whole (batch, head) slices of the dense
-    workload until budget_s has passed; returns (TFLOP/s, description)."""
+def oracle_prefill_sample(w: workloads.Dense, budget_s: float, inputs=None, rows_per_unit: int = 1024):
+    """Time the float64 oracle on the dense workload, unit by unit (one
+    (batch, head) and `rows_per_unit` query rows against all keys), until
+    budget_s has passed; returns (TFLOP/s, description, seconds)."""
     import oracle
 
-    q, k, v = w.make()
-    done = 0
+    q, k, v = inputs if inputs is not None else w.make()
+    g = w.Hq // w.Hkv
+    per_bh = -(-w.Sq // rows_per_unit)
+    done, flops = 0, 0.0
     t0 = time.perf_counter()
     while True:
-        b, h = divmod(done % (w.B * w.Hq), w.Hq)
-        oracle.attention_single(q[b, :, h:h + 1], k[b, :, h // (w.Hq // w.Hkv):h // (w.Hq // w.Hkv) + 1],
-                                v[b, :, h // (w.Hq // w.Hkv):h // (w.Hq // w.Hkv) + 1], w.scale, w.causal)
+        bh, chunk = divmod(done % (w.B * w.Hq * per_bh), per_bh)
+        b, h = divmod(bh, w.Hq)
+        rows = list(range(chunk * rows_per_unit, min(w.Sq, (chunk + 1) * rows_per_unit)))
+        kv = h // g
+        oracle.attention_single(q[b, :, h:h + 1], k[b, :, kv:kv + 1], v[b, :, kv:kv + 1], w.scale, w.causal,
+                                rows=rows)
+        flops += 4.0 * w.D * len(rows) * w.Sk
         done += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    flops = 4.0 * w.D * w.Sq * w.Sk * done
-    return flops / el / 1e12, f"{done} of {w.B * w.Hq} (batch, head) slices of {w.name}, all {w.Sq} query rows", el
+    desc = (f"{done} units of {rows_per_unit} query rows x all {w.Sk} keys, one (batch, head) each, "
+            f"of {w.name} ({w.B * w.Hq * per_bh} units in the full workload)")
+    return flops / el / 1e12, desc, el
 
 
 def oracle_paged_sample(w: workloads.Paged, q, cache, bt, sl, budget_s: float):
@@ -214,10 +222,11 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     w = workloads.dit_self()
+    inputs = w.make()
     steps = []
-    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    per_step = min(2.0, 120.0 / max(1, args.steps + args.warmup))  # whole run ~2 minutes at most
     for i in range(args.warmup + args.steps):
-        tf, desc, el = oracle_prefill_sample(w, per_step)
+        tf, desc, el = oracle_prefill_sample(w, per_step, inputs)
         if i >= args.warmup:
             steps.append((tf, el))
     value = statistics.median(t for t, _ in steps)
@@ -246,29 +255,37 @@ def run_ours(args, world, rank, local):
     pk, peak_kind = peaks()
 
     # ---- inputs (CPU, seeded), then resident in HBM
+    do_pre, do_dec = args.only in ("all", "prefill"), args.only in ("all", "decode")
     wp = workloads.dit_self()
     q, k, v = wp.make()
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    outd = torch.empty(wp.B, wp.Sq, wp.Hq, wp.D, dtype=torch.float32, device=dev)
-    lsed = torch.empty(wp.B, wp.Hq, wp.Sq, dtype=torch.float32, device=dev)
+    if do_pre:
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        outd = torch.empty(wp.B, wp.Sq, wp.Hq, wp.D, dtype=torch.float32, device=dev)
+        lsed = torch.empty(wp.B, wp.Hq, wp.Sq, dtype=torch.float32, device=dev)
     wd = workloads.paged_decode()
-    pq, cache, bt, sl = wd.make(chunk_rows=256)
-    pqd, cached, btd, sld = pq.to(dev), cache.to(dev), bt.to(dev), sl.to(dev)
+    if args.decode_seqs:
+        wd = workloads.Paged(wd.name + f"_first{args.decode_seqs}", wd.seq_lens[:args.decode_seqs], wd.Hq, wd.Hkv,
+                             wd.D, seed=wd.seed, max_blocks_per_seq=wd.max_blocks_per_seq)
     max_len = max(wd.seq_lens)
-    ws = torch.empty(gb.attn_fwd_paged_workspace_size(len(wd.seq_lens), wd.Hq, wd.Hkv, wd.D, max_len),
-                     dtype=torch.uint8, device=dev)
-    pout = torch.empty(len(wd.seq_lens), wd.Hq, wd.D, dtype=torch.float32, device=dev)
-    plse = torch.empty(len(wd.seq_lens), wd.Hq, dtype=torch.float32, device=dev)
+    if do_dec:
+        pq, cache, bt, sl = wd.make(chunk_rows=256)
+        pqd, cached, btd, sld = pq.to(dev), cache.to(dev), bt.to(dev), sl.to(dev)
+        ws = torch.empty(gb.attn_fwd_paged_workspace_size(len(wd.seq_lens), wd.Hq, wd.Hkv, wd.D, max_len),
+                         dtype=torch.uint8, device=dev)
+        pout = torch.empty(len(wd.seq_lens), wd.Hq, wd.D, dtype=torch.float32, device=dev)
+        plse = torch.empty(len(wd.seq_lens), wd.Hq, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def prefill():
-        gb.attn_fwd_dense(qd, kd, vd, wp.scale, wp.causal, out=outd, lse=lsed, dev_status=status, stream=stream)
+        if do_pre:
+            gb.attn_fwd_dense(qd, kd, vd, wp.scale, wp.causal, out=outd, lse=lsed, dev_status=status, stream=stream)
 
     def decode():
-        gb.attn_fwd_paged(pqd, cached, btd, sld, max_len, wd.scale, out=pout, lse=plse, workspace=ws,
-                          dev_status=status, stream=stream)
+        if do_dec:
+            gb.attn_fwd_paged(pqd, cached, btd, sld, max_len, wd.scale, out=pout, lse=plse, workspace=ws,
+                              dev_status=status, stream=stream)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -302,45 +319,49 @@ def run_ours(args, world, rank, local):
     step_ms = max_over_ranks(statistics.mean(p + d for p, d in zip(pre_ms, dec_ms)), world)
 
     flops = wp.flops()
-    tflops_rank = flops / (pre_avg * 1e-3) / 1e12
-    value = sum_over_ranks(flops, world) / (pre_avg * 1e-3) / 1e12
+    tflops_rank = flops / (pre_avg * 1e-3) / 1e12 if do_pre else None
+    value = sum_over_ranks(flops, world) / (pre_avg * 1e-3) / 1e12 if do_pre else None
     dec_bytes = wd.algorithmic_bytes(out_bytes_per_elem=4, with_lse=True)
-    dec_gbs_rank = dec_bytes / (dec_avg * 1e-3) / 1e9
-    dec_value = sum_over_ranks(dec_bytes, world) / (dec_avg * 1e-3) / 1e9
+    dec_gbs_rank = dec_bytes / (dec_avg * 1e-3) / 1e9 if do_dec else None
+    dec_value = sum_over_ranks(dec_bytes, world) / (dec_avg * 1e-3) / 1e9 if do_dec else None
     peak_tf = float(pk["bf16_tflops"])
     peak_bw = float(pk["hbm_gbs"])
 
     # ---- end to end through the public API from pinned host buffers
-    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    hout = torch.empty(outd.shape, dtype=torch.float32).pin_memory()
-    hlse = torch.empty(lsed.shape, dtype=torch.float32).pin_memory()
-    e2e_steps = max(3, min(args.steps, 20))
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        qd.copy_(hq, non_blocking=True)
-        kd.copy_(hk, non_blocking=True)
-        vd.copy_(hv, non_blocking=True)
-        prefill()
-        hout.copy_(outd, non_blocking=True)
-        hlse.copy_(lsed, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
-    h2d = (q.numel() + k.numel() + v.numel()) * 2
-    d2h = hout.numel() * 4 + hlse.numel() * 4
+    e2e = None
+    if do_pre:
+        hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        hout = torch.empty(outd.shape, dtype=torch.float32).pin_memory()
+        hlse = torch.empty(lsed.shape, dtype=torch.float32).pin_memory()
+        e2e_steps = max(3, min(args.steps, 20))
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            prefill()
+            hout.copy_(outd, non_blocking=True)
+            hlse.copy_(lsed, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+        h2d = (q.numel() + k.numel() + v.numel()) * 2
+        d2h = hout.numel() * 4 + hlse.numel() * 4
+        e2e = {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     # ---- oracle on the host cores (rank 0, N=1 only)
-    cpu = None
-    if world == 1:
-        tf, desc, _ = oracle_prefill_sample(wp, 10.0)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle", "sample": desc}
-        gbs, ddesc, _ = oracle_paged_sample(wd, pq, cache, bt, sl, 8.0)
-        cpu_dec = {"value": gbs, "unit": "GB/s", "cores": cores_used(), "kind": "oracle", "sample": ddesc}
-    else:
-        cpu_dec = None
+    cpu, cpu_dec = None, None
+    if world == 1 and not args.no_cpu:
+        if do_pre:
+            tf, desc, _ = oracle_prefill_sample(wp, 10.0, (q, k, v))
+            cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle", "sample": desc}
+        if do_dec:
+            gbs, ddesc, _ = oracle_paged_sample(wd, pq, cache, bt, sl, 8.0)
+            cpu_dec = {"value": gbs, "unit": "GB/s", "cores": cores_used(), "kind": "oracle", "sample": ddesc}
 
     if rank != 0:
         return
@@ -366,25 +387,25 @@ def run_ours(args, world, rank, local):
                        "block_size": 128, "num_blocks": wd.num_blocks},
             "l2": "512 MiB buffer rewritten between steps (flush); decode cache 4.4 GB > L2",
             "parallelism": f"replicas x{world}",
+            "only": args.only,
         },
         "roofline": {
             "bound": "tensor", "kernel": "fmha_fwd_sm103a<128>", "achieved": tflops_rank, "peak": peak_tf,
-            "unit": "TFLOP/s", "frac": tflops_rank / peak_tf, "peak_kind": f"{peak_kind} bf16 burst",
+            "unit": "TFLOP/s", "frac": tflops_rank / peak_tf if do_pre else None, "peak_kind": f"{peak_kind} bf16 burst",
             "traffic": traffic_for("fmha_fwd_sm103a", "prefill.cu"),
             "flops_per_launch": flops, "launch_ms": pre_avg,
         },
         "paged_decode": {
             "value": dec_value, "unit": "GB/s", "ms": dec_avg,
             "roofline": {"bound": "hbm", "kernel": "paged_decode_sm103a + paged_combine", "achieved": dec_gbs_rank,
-                         "peak": peak_bw, "unit": "GB/s", "frac": dec_gbs_rank / peak_bw,
+                         "peak": peak_bw, "unit": "GB/s", "frac": dec_gbs_rank / peak_bw if do_dec else None,
                          "peak_kind": f"{peak_kind} HBM copy", "bytes_per_call": dec_bytes,
                          "traffic": traffic_for("paged_decode_sm103a", "decode.cu")},
             "cpu_baseline": cpu_dec,
         },
         "cpu_baseline": cpu,
-        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
+        "e2e": e2e,
+        "gpu_launches": (int(do_pre) + 2 * int(do_dec)) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": t_wall,
     }
@@ -397,6 +418,11 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="run one part of the step (profiling captures); the default line needs 'all'")
+    ap.add_argument("--decode-seqs", type=int, default=0,
+                    help="use only the first N sequences of the decode workload (profiling captures)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle timing")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     world, rank, local = dist_setup(args.gpus)
