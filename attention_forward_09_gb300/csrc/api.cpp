@@ -234,9 +234,11 @@ gbattn_status attn_fwd_paged(const void* q, const void* kv_cache, int num_blocks
     p.out = out;
     p.lse = lse;
     p.status = dev_status;
-    const size_t rows = static_cast<size_t>(num_seqs) * Hq * plan.max_splits;
-    p.part_o = static_cast<float*>(workspace);
-    p.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * D * 4 + 255) & ~size_t(255)));
+    char* ws = static_cast<char*>(workspace);
+    p.part_o = reinterpret_cast<float*>(ws);
+    p.part_lse = reinterpret_cast<float*>(ws + plan.o_bytes);
+    p.pairs = reinterpret_cast<int4*>(ws + plan.o_bytes + plan.lse_bytes);
+    p.sched = reinterpret_cast<int*>(ws + plan.o_bytes + plan.lse_bytes + plan.pairs_bytes);
     p.num_seqs = num_seqs;
     p.num_blocks = num_blocks;
     p.max_blocks_per_seq = max_blocks_per_seq;

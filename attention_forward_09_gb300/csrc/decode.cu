@@ -8,10 +8,12 @@
 // slot_mapping rule).
 //
 // The path is HBM-bound, so it runs on the CUDA cores.  Design:
-//   * work item = (sequence, KV head [, query-head subgroup], split of up to
-//     `blocks_per_split` cache blocks), KV heads varying fastest so that the
-//     CTAs working at one moment read neighbouring 256-byte head rows of the
-//     same cache rows; a persistent grid of one CTA per SM walks the items;
+//   * work item = (sequence, split of up to `blocks_per_split` cache blocks,
+//     KV head [, query-head subgroup]); paged_schedule (one CTA) lists the
+//     non-empty (sequence, split) pairs longest first, and a persistent grid
+//     of one CTA per SM claims items from a global counter, KV heads varying
+//     fastest so that the CTAs working at one moment read neighbouring
+//     256-byte head rows of the same cache rows;
 //   * the K and V of one slice (a whole 128-token block, or 64 tokens at
 //     D >= 192) arrive by TMA as one box per 64 columns into a ring of
 //     shared-memory slots (large boxes: the TMA issue cost per box, not the
@@ -19,7 +21,8 @@
 //   * all 8 warps consume every slot, each a fixed run of its tokens, so
 //     every mbarrier phase is awaited in order; there is no producer warp:
 //     the last warp to release a slot (a shared-memory counter) refills it
-//     from a look-ahead walk of the same slice sequence;
+//     with the next slice, claiming a new item when the current one is
+//     exhausted, and records the slice's item in the slot's header;
 //   * inside a warp a group of LPG lanes owns one token at a time, each lane
 //     E = D / LPG columns, with the GQA group's query rows for those columns
 //     in registers: q.k is a packed-fp32 (fma.rn.f32x2) dot product plus a
@@ -32,6 +35,8 @@
 // Tokens at or past seq_len are never used, neither in q.k nor in p.v, so
 // whatever the unused cache slots hold cannot reach the result.
 #include <math.h>
+
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -66,79 +71,66 @@ struct PagedCfg {
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
     // vector width of one shared-memory load, in bf16 elements
     static constexpr int U = (E % 8 == 0) ? 8 : ((E % 4 == 0) ? 4 : 2);
-    // shared memory: slots | merge scratch [warps][HG][D + 2] f32 | counters | flags | bars
+    // period (in steps) of a lane's swizzle pattern: rows advance by TPW per step, the swizzle by row % 8
+    static constexpr int P = TPW >= 8 ? 1 : 8 / TPW;
+    // shared memory: slots | merge scratch [warps][HG][D + 2] f32 | counters | slot headers | uses | cursor | bars
     static constexpr int OFF_MERGE = STAGES * SLOT_BYTES;
     static constexpr int OFF_CNT = OFF_MERGE + MERGE_BYTES;
-    static constexpr int OFF_FLAG = OFF_CNT + STAGES * 4;
-    static constexpr int OFF_USE = OFF_FLAG + STAGES * 4;
-    static constexpr int OFF_BAR = (OFF_USE + STAGES * 4 + 7) & ~7;
+    static constexpr int OFF_INFO = OFF_CNT + STAGES * 4;
+    static constexpr int OFF_USE = OFF_INFO + STAGES * 32;
+    static constexpr int OFF_CUR = OFF_USE + STAGES * 4;
+    static constexpr int OFF_BAR = (OFF_CUR + 32 + 7) & ~7;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + STAGES * 8;
     static_assert(LPG * E == D && 32 % LPG == 0 && SLICE % TPW == 0 && NSTEP % kWarps == 0 && WSTEP % SUBS == 0,
                   "lane map");
     static_assert(STAGES >= 2 && SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert((WSTEP * TPW) % 8 == 0, "each warp's rows start 8-aligned");
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
-struct ItemCoords {
-    int s, kvh, h0, sp, tok0, tok1;  // tokens [tok0, tok1) of sequence s
+// Header of one slot, written by the thread that fills it.
+struct SlotInfo {
+    int item;  // -1: end of this CTA's work
+    int s, h0, kvh, sp, tok, tok1;
+    int bad;   // the block id was outside [0, num_blocks): no data, tokens skipped
 };
 
-// Item `it` -> (sequence, head group, split); the head group varies fastest.
-__device__ __forceinline__ ItemCoords item_coords(const PagedParams& p, int it, int n_hgroups,
-                                                  uint32_t* status, bool report) {
-    ItemCoords c;
-    const int hg = it % n_hgroups;
-    const int rest = it / n_hgroups;
-    c.sp = rest % p.max_splits;
-    c.s = rest / p.max_splits;
-    const int per_kv = p.group / p.heads_per_cta;
-    c.kvh = hg / per_kv;
-    c.h0 = c.kvh * p.group + (hg % per_kv) * p.heads_per_cta;
-    int L = p.seq_lens[c.s];
-    const int cap = min(p.max_seq_len, p.max_blocks_per_seq * kBlk);
-    if (L < 0 || L > cap) {
-        if (report && status) atomicOr(status, kDevBadSeqlen);
-        L = L < 0 ? 0 : cap;
+// The refill cursor: the next slice to load.  Only one thread at a time
+// touches it (refills happen in slice order, handed from one releasing warp
+// to the next through the slot counters' acquire/release atomics).
+struct Cursor {
+    int item, s, h0, kvh, sp, tok, tok1;
+};
+
+__device__ __forceinline__ void claim_item(const PagedParams& p, int n_hgroups, int total, Cursor& cu) {
+    const int k = atomicAdd(p.sched, 1);
+    if (k >= total) {
+        cu.item = -1;
+        return;
     }
-    c.tok0 = c.sp * p.blocks_per_split * kBlk;
-    c.tok1 = min(L, c.tok0 + p.blocks_per_split * kBlk);
-    return c;
+    const int4 pr = p.pairs[k / n_hgroups];
+    const int hg = k % n_hgroups;
+    const int per_kv = p.group / p.heads_per_cta;
+    cu.item = k;
+    cu.s = pr.x;
+    cu.sp = pr.y;
+    cu.tok = pr.z;
+    cu.tok1 = pr.w;
+    cu.kvh = hg / per_kv;
+    cu.h0 = cu.kvh * p.group + (hg % per_kv) * p.heads_per_cta;
 }
 
-// Walks this CTA's slices in order: (item, first token of the slice).
-struct SliceWalk {
-    int it, tok;
-    ItemCoords c;
-    __device__ __forceinline__ void seek(const PagedParams& p, int n_items, int n_hgroups, int start) {
-        for (it = start; it < n_items; it += gridDim.x) {
-            c = item_coords(p, it, n_hgroups, nullptr, false);
-            if (c.tok0 < c.tok1) {
-                tok = c.tok0;
-                return;
-            }
-        }
-        tok = 0;
-    }
-    __device__ __forceinline__ bool done(int n_items) const { return it >= n_items; }
-    template <int SLICE>
-    __device__ __forceinline__ void next(const PagedParams& p, int n_items, int n_hgroups) {
-        tok += SLICE;
-        if (tok >= c.tok1) seek(p, n_items, n_hgroups, it + gridDim.x);
-    }
-};
-
-// E columns [e0, e0 + E) of row `row` of a swizzled slice (64-column chunks
-// of SLICE rows x 128 B, 16-byte piece c of row r stored at c ^ (r % 8)), as
-// E/2 packed words.
+// This lane's E columns of one token row as E/2 packed words: `base[u]` is
+// the shared address of the lane's u-th vector for row offset 0 (swizzle
+// already applied), `imm` a compile-time row offset that keeps the swizzle
+// phase (a multiple of 8 rows, plus the K->V distance).
 template <class C>
-__device__ __forceinline__ void load_cols(uint32_t base, int row, int e0, uint32_t (&w)[C::E / 2]) {
+__device__ __forceinline__ void lds_cols(const uint32_t (&base)[C::E / C::U], uint32_t imm, uint32_t (&w)[C::E / 2]) {
 #pragma unroll
     for (int u = 0; u < C::E / C::U; ++u) {
-        const int e = e0 + u * C::U;
-        const uint32_t addr = base + (e >> 6) * (C::SLICE * 128) + row * 128 + ((((e & 63) >> 3) ^ (row & 7)) << 4) +
-                              (e & 7) * 2;
+        const uint32_t addr = base[u] + imm;
         if constexpr (C::U == 8) {
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(w[u * 4]), "=r"(w[u * 4 + 1]), "=r"(w[u * 4 + 2]), "=r"(w[u * 4 + 3])
@@ -151,45 +143,61 @@ __device__ __forceinline__ void load_cols(uint32_t base, int row, int e0, uint32
     }
 }
 
-// Issue the TMA copies of one slice into `slot` (one thread).  A block id
-// outside [0, num_blocks) is reported; the slot is then marked bad and its
-// barrier completed without data.
+// Fill `slot` with the cursor's slice (one thread) and advance the cursor.
+// A block id outside [0, num_blocks) is reported; the slot is then marked bad
+// and its barrier completed without data.  An exhausted cursor writes the
+// end marker.
 template <class C>
 __device__ __forceinline__ void fill_slot(const CUtensorMap* tm, const PagedParams& p, uint32_t sSlots, uint32_t bar,
-                                          volatile int* sflag, volatile int* suse, int slot, int use,
-                                          const SliceWalk& w) {
-    const int blk = p.block_table[static_cast<long long>(w.c.s) * p.max_blocks_per_seq + w.tok / kBlk];
-    const bool valid = blk >= 0 && blk < p.num_blocks;
-    sflag[slot] = valid ? 0 : 1;
+                                          volatile SlotInfo* info, volatile int* suse, int slot, int use,
+                                          Cursor& cu, int n_hgroups, int total) {
+    volatile SlotInfo& si = info[slot];
     suse[slot] = use;
-    if (!valid) {
-        if (p.status) atomicOr(p.status, kDevBadIndex);
+    si.item = cu.item;
+    if (cu.item < 0) {
         mbar_arrive(bar);
         return;
     }
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, C::SLOT_BYTES);
-    const int row = blk * kBlk + (w.tok & (kBlk - 1));
+    si.s = cu.s;
+    si.h0 = cu.h0;
+    si.kvh = cu.kvh;
+    si.sp = cu.sp;
+    si.tok = cu.tok;
+    si.tok1 = cu.tok1;
+    const int blk = p.block_table[static_cast<long long>(cu.s) * p.max_blocks_per_seq + cu.tok / kBlk];
+    const bool valid = blk >= 0 && blk < p.num_blocks;
+    si.bad = valid ? 0 : 1;
+    if (valid) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, C::SLOT_BYTES);
+        const int row = blk * kBlk + (cu.tok & (kBlk - 1));
 #pragma unroll
-    for (int kv = 0; kv < 2; ++kv)
+        for (int kv = 0; kv < 2; ++kv)
 #pragma unroll
-        for (int ch = 0; ch < C::NCH; ++ch)
-            tma_load_3d(sSlots + slot * C::SLOT_BYTES + kv * C::HALF_BYTES + ch * C::SLICE * 128, tm, bar, ch * 64,
-                        w.c.kvh, row + kv * p.num_blocks * kBlk);
+            for (int ch = 0; ch < C::NCH; ++ch)
+                tma_load_3d(sSlots + slot * C::SLOT_BYTES + kv * C::HALF_BYTES + ch * C::SLICE * 128, tm, bar,
+                            ch * 64, cu.kvh, row + kv * p.num_blocks * kBlk);
+    } else {
+        if (p.status) atomicOr(p.status, kDevBadIndex);
+        mbar_arrive(bar);
+    }
+    cu.tok += C::SLICE;
+    if (cu.tok >= cu.tok1) claim_item(p, n_hgroups, total, cu);
 }
 
 template <class C>
 __global__ void __launch_bounds__(32 * kWarps, 1)
     paged_decode_sm103a(const __grid_constant__ CUtensorMap tmKV, const PagedParams p) {
     constexpr int D = C::D, HG = C::HG, E = C::E, LPG = C::LPG, TPW = C::TPW, STAGES = C::STAGES;
-    constexpr int SLICE = C::SLICE, WSTEP = C::WSTEP, SUBS = C::SUBS;
+    constexpr int SLICE = C::SLICE, WSTEP = C::WSTEP, SUBS = C::SUBS, P = C::P, NU = C::E / C::U;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sSlots = smem_u32(smem);
     float* smerge = reinterpret_cast<float*>(smem + C::OFF_MERGE);  // [warp][HG][D + 2]: o..., m, l
     int* scnt = reinterpret_cast<int*>(smem + C::OFF_CNT);          // releases per slot, monotonic
-    volatile int* sflag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
-    volatile int* suse = reinterpret_cast<volatile int*>(smem + C::OFF_USE);  // last use issued per slot
+    volatile SlotInfo* sinfo = reinterpret_cast<volatile SlotInfo*>(smem + C::OFF_INFO);
+    volatile int* suse = reinterpret_cast<volatile int*>(smem + C::OFF_USE);  // last use filled per slot
+    Cursor* scur = reinterpret_cast<Cursor*>(smem + C::OFF_CUR);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     auto b_full = [&](int s) { return smem_u32(&bars[s]); };
     __shared__ int abort_flag_storage;
@@ -197,12 +205,9 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_hgroups = p.Hkv * (p.group / p.heads_per_cta);
-    const int n_items = p.num_seqs * n_hgroups * p.max_splits;
-
     if (status_has_timeout(p.status, kDevTimeout)) return;
-    SliceWalk cur, ahead;
-    cur.seek(p, n_items, n_hgroups, blockIdx.x);
-    ahead = cur;
+    const int total = p.sched[1] * n_hgroups;  // items in this launch
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(b_full(s), 1);
@@ -214,137 +219,34 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
         tma_prefetch_desc(&tmKV);
     }
     __syncthreads();
-    // prologue: the first STAGES slices; `ahead` ends STAGES slices past `cur`
-    for (int s = 0; s < STAGES; ++s) {
-        if (ahead.done(n_items)) break;
-        if (threadIdx.x == 0) fill_slot<C>(&tmKV, p, sSlots, b_full(s), sflag, suse, s, 0, ahead);
-        ahead.template next<SLICE>(p, n_items, n_hgroups);
+    if (threadIdx.x == 0) {  // prologue: the first STAGES slices
+        Cursor cu;
+        claim_item(p, n_hgroups, total, cu);
+        for (int s = 0; s < STAGES; ++s) fill_slot<C>(&tmKV, p, sSlots, b_full(s), sinfo, suse, s, 0, cu, n_hgroups, total);
+        *scur = cu;
     }
     bool ok = true;
     const float c2 = p.scale_log2;
-    const int grp = lane / LPG;        // token group within the warp
-    const int e0 = (lane % LPG) * E;   // this lane's first column
-    int g = 0;                         // global slice counter
-    while (!cur.done(n_items)) {
-        const ItemCoords c = item_coords(p, cur.it, n_hgroups, p.status, threadIdx.x == 0);
-        // this lane's columns of the HG query rows, fp32 pairs
-        float2 q[HG][E / 2];
+    const int grp = lane / LPG;       // token group within the warp
+    const int e0 = (lane % LPG) * E;  // this lane's first column
+    // byte offset of this lane's u-th load of row (j * TPW + grp), j < P
+    uint32_t loff[P][NU];
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
-            const uint16_t* qh =
-                reinterpret_cast<const uint16_t*>(p.q) + (static_cast<long long>(c.s) * p.Hq + c.h0 + h) * D + e0;
+    for (int j = 0; j < P; ++j) {
+        const int row = j * TPW + grp;
 #pragma unroll
-            for (int x = 0; x < E / 2; ++x)
-                q[h][x] = make_float2(__uint_as_float(static_cast<uint32_t>(qh[2 * x]) << 16),
-                                      __uint_as_float(static_cast<uint32_t>(qh[2 * x + 1]) << 16));
+        for (int u = 0; u < NU; ++u) {
+            const int e = e0 + u * C::U;
+            loff[j][u] = (e >> 6) * (SLICE * 128) + row * 128 + ((((e & 63) >> 3) ^ (row & 7)) << 4) + (e & 7) * 2;
         }
-        float m[HG], l[HG];
-        float2 o[HG][E / 2];
-#pragma unroll
-        for (int h = 0; h < HG; ++h) {
-            m[h] = -INFINITY;
-            l[h] = 0.f;
-#pragma unroll
-            for (int x = 0; x < E / 2; ++x) o[h][x] = make_float2(0.f, 0.f);
-        }
-        // ---------------------------------------------- slices of this item
-        const int item = cur.it;
-        while (!cur.done(n_items) && cur.it == item) {
-            const int slot = g % STAGES, use = g / STAGES;
-            if (!mbar_wait(b_full(slot), use & 1, abort_flag)) {
-                ok = false;
-                *abort_flag = 1;
-            }
-            ok = __all_sync(0xffffffffu, ok);
-            const int nvalid = (ok && !sflag[slot]) ? min(SLICE, c.tok1 - cur.tok) : 0;
-            const uint32_t kbase = sSlots + slot * C::SLOT_BYTES;
-            const uint32_t vbase = kbase + C::HALF_BYTES;
-#pragma unroll 1
-            for (int sc = 0; sc < WSTEP / SUBS; ++sc) {
-                // ---- scores of SUBS tokens of this group, HG heads
-                float s[SUBS][HG];
-#pragma unroll
-                for (int st = 0; st < SUBS; ++st) {
-                    const int t = (warp * WSTEP + sc * SUBS + st) * TPW + grp;
-                    float dot[HG];
-                    if (t < nvalid) {  // group-uniform
-                        uint32_t w[E / 2];
-                        load_cols<C>(kbase, t, e0, w);
-                        float2 acc[HG];
-#pragma unroll
-                        for (int h = 0; h < HG; ++h) acc[h] = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int x = 0; x < E / 2; ++x) {
-                            const float2 kk = make_float2(bf_lo(w[x]), bf_hi(w[x]));
-#pragma unroll
-                            for (int h = 0; h < HG; ++h) acc[h] = __ffma2_rn(q[h][x], kk, acc[h]);
-                        }
-#pragma unroll
-                        for (int h = 0; h < HG; ++h) dot[h] = acc[h].x + acc[h].y;
-                    } else {
-#pragma unroll
-                        for (int h = 0; h < HG; ++h) dot[h] = 0.f;
-                    }
-#pragma unroll
-                    for (int off = 1; off < LPG; off <<= 1)
-#pragma unroll
-                        for (int h = 0; h < HG; ++h) dot[h] += __shfl_xor_sync(0xffffffffu, dot[h], off);
-#pragma unroll
-                    for (int h = 0; h < HG; ++h) s[st][h] = (t < nvalid) ? dot[h] * c2 : -INFINITY;
-                }
-                // ---- online softmax for this group (identical in its LPG lanes)
-#pragma unroll
-                for (int h = 0; h < HG; ++h) {
-                    float cm = s[0][h];
-#pragma unroll
-                    for (int st = 1; st < SUBS; ++st) cm = fmaxf(cm, s[st][h]);
-                    if (cm > m[h] + 8.0f) {  // rescale only when the max grows by more than 2^8
-                        const float a = ex2(m[h] - cm);
-                        const float2 a2 = make_float2(a, a);
-                        l[h] *= a;
-#pragma unroll
-                        for (int x = 0; x < E / 2; ++x) o[h][x] = __fmul2_rn(o[h][x], a2);
-                        m[h] = cm;
-                    }
-                    const float ms = (m[h] == -INFINITY) ? 0.f : m[h];
-#pragma unroll
-                    for (int st = 0; st < SUBS; ++st) {
-                        s[st][h] = ex2(s[st][h] - ms);
-                        l[h] += s[st][h];
-                    }
-                }
-                // ---- o += p v over the same columns
-#pragma unroll
-                for (int st = 0; st < SUBS; ++st) {
-                    const int t = (warp * WSTEP + sc * SUBS + st) * TPW + grp;
-                    if (t < nvalid) {
-                        uint32_t w[E / 2];
-                        load_cols<C>(vbase, t, e0, w);
-#pragma unroll
-                        for (int x = 0; x < E / 2; ++x) {
-                            const float2 vv = make_float2(bf_lo(w[x]), bf_hi(w[x]));
-#pragma unroll
-                            for (int h = 0; h < HG; ++h)
-                                o[h][x] = __ffma2_rn(make_float2(s[st][h], s[st][h]), vv, o[h][x]);
-                        }
-                    }
-                }
-            }
-            // ---- release the slot; the last warp out refills it with the slice STAGES ahead
-            __syncwarp();
-            if (lane == 0) {
-                __threadfence_block();  // this warp's reads of the slot happen before its release
-                const int prev = atomicAdd(scnt + slot, 1);
-                __threadfence_block();
-                if (prev == use * kWarps + kWarps - 1 && ok && !*abort_flag && !ahead.done(n_items))
-                    fill_slot<C>(&tmKV, p, sSlots, b_full(slot), sflag, suse, slot, use + 1, ahead);
-            }
-            __syncwarp();
-            if (!ahead.done(n_items)) ahead.template next<SLICE>(p, n_items, n_hgroups);
-            cur.template next<SLICE>(p, n_items, n_hgroups);
-            ++g;
-        }
-        // ---- merge the token groups of this warp (same columns, different tokens)
+    }
+    int cur_item = -1, cur_s = 0, cur_h0 = 0, cur_sp = 0;
+    float2 q[HG][E / 2];
+    float m[HG], l[HG];
+    float2 o[HG][E / 2];
+
+    // Merge the token groups and warps of the finished item, write its partial.
+    auto finish_item = [&]() {
 #pragma unroll
         for (int off = LPG; off < 32; off <<= 1) {
 #pragma unroll
@@ -364,7 +266,6 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
                 m[h] = mt;
             }
         }
-        // ---- merge the warps through shared memory, write the item's partial
         if (grp == 0) {
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
@@ -394,12 +295,147 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
                 lt = fmaf(src[D + 1], a, lt);
                 ot = fmaf(src[d], a, ot);
             }
-            const long long row = (static_cast<long long>(c.s) * p.Hq + c.h0 + h) * p.max_splits + c.sp;
+            const long long row = (static_cast<long long>(cur_s) * p.Hq + cur_h0 + h) * p.max_splits + cur_sp;
             p.part_o[row * D + d] = lt > 0.f ? ot / lt : 0.f;
             if (d == 0) p.part_lse[row] = lt > 0.f ? (mt + __log2f(lt)) * kLn2f : -INFINITY;
         }
         __syncthreads();
+    };
+
+    for (int g = 0;; ++g) {
+        const int slot = g % STAGES, use = g / STAGES;
+        if (!mbar_wait(b_full(slot), use & 1, abort_flag)) {
+            ok = false;
+            *abort_flag = 1;
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        // every warp reads the same header, so every warp leaves at the same slice
+        const int item = ok ? sinfo[slot].item : -1;
+        if (item < 0) break;
+        if (item != cur_item) {
+            if (cur_item >= 0) finish_item();
+            cur_item = item;
+            cur_s = sinfo[slot].s;
+            cur_h0 = sinfo[slot].h0;
+            cur_sp = sinfo[slot].sp;
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+                const uint16_t* qh = reinterpret_cast<const uint16_t*>(p.q) +
+                                     (static_cast<long long>(cur_s) * p.Hq + cur_h0 + h) * D + e0;
+#pragma unroll
+                for (int x = 0; x < E / 2; ++x) {
+                    const uint32_t qq = *reinterpret_cast<const uint32_t*>(qh + 2 * x);
+                    q[h][x] = make_float2(bf_lo(qq), bf_hi(qq));
+                }
+                m[h] = -INFINITY;
+                l[h] = 0.f;
+#pragma unroll
+                for (int x = 0; x < E / 2; ++x) o[h][x] = make_float2(0.f, 0.f);
+            }
+        }
+        const int nvalid = sinfo[slot].bad ? 0 : min(SLICE, sinfo[slot].tok1 - sinfo[slot].tok);
+        // this warp's K rows start 8-aligned, so every lane's swizzled offsets repeat with period P steps
+        uint32_t kl[P][NU];
+#pragma unroll
+        for (int j = 0; j < P; ++j)
+#pragma unroll
+            for (int u = 0; u < NU; ++u) kl[j][u] = sSlots + slot * C::SLOT_BYTES + warp * (WSTEP * TPW * 128) + loff[j][u];
+        auto process = [&](auto full_tag) {
+            constexpr bool FULL = decltype(full_tag)::value;
+#pragma unroll
+            for (int sc = 0; sc < WSTEP / SUBS; ++sc) {
+                // ---- scores of SUBS tokens of this group, HG heads
+                float s[SUBS][HG];
+#pragma unroll
+                for (int st = 0; st < SUBS; ++st) {
+                    const int stg = sc * SUBS + st;
+                    const int t = (warp * WSTEP + stg) * TPW + grp;
+                    const bool live = FULL || t < nvalid;  // group-uniform
+                    float dot[HG];
+                    if (live) {
+                        uint32_t w[E / 2];
+                        lds_cols<C>(kl[stg % P], (stg - stg % P) * TPW * 128, w);
+                        float2 acc[HG];
+#pragma unroll
+                        for (int h = 0; h < HG; ++h) acc[h] = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int x = 0; x < E / 2; ++x) {
+                            const float2 kk = make_float2(bf_lo(w[x]), bf_hi(w[x]));
+#pragma unroll
+                            for (int h = 0; h < HG; ++h) acc[h] = __ffma2_rn(q[h][x], kk, acc[h]);
+                        }
+#pragma unroll
+                        for (int h = 0; h < HG; ++h) dot[h] = acc[h].x + acc[h].y;
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < HG; ++h) dot[h] = 0.f;
+                    }
+#pragma unroll
+                    for (int off = 1; off < LPG; off <<= 1)
+#pragma unroll
+                        for (int h = 0; h < HG; ++h) dot[h] += __shfl_xor_sync(0xffffffffu, dot[h], off);
+#pragma unroll
+                    for (int h = 0; h < HG; ++h) s[st][h] = live ? dot[h] * c2 : -INFINITY;
+                }
+                // ---- online softmax for this group (identical in its LPG lanes)
+#pragma unroll
+                for (int h = 0; h < HG; ++h) {
+                    float cm = s[0][h];
+#pragma unroll
+                    for (int st = 1; st < SUBS; ++st) cm = fmaxf(cm, s[st][h]);
+                    if (cm > m[h] + 8.0f) {  // rescale only when the max grows by more than 2^8
+                        const float a = ex2(m[h] - cm);
+                        const float2 a2 = make_float2(a, a);
+                        l[h] *= a;
+#pragma unroll
+                        for (int x = 0; x < E / 2; ++x) o[h][x] = __fmul2_rn(o[h][x], a2);
+                        m[h] = cm;
+                    }
+                    const float ms = (m[h] == -INFINITY) ? 0.f : m[h];
+#pragma unroll
+                    for (int st = 0; st < SUBS; ++st) {
+                        s[st][h] = ex2(s[st][h] - ms);
+                        l[h] += s[st][h];
+                    }
+                }
+                // ---- o += p v over the same columns
+#pragma unroll
+                for (int st = 0; st < SUBS; ++st) {
+                    const int stg = sc * SUBS + st;
+                    const int t = (warp * WSTEP + stg) * TPW + grp;
+                    if (FULL || t < nvalid) {
+                        uint32_t w[E / 2];
+                        lds_cols<C>(kl[stg % P], (stg - stg % P) * TPW * 128 + C::HALF_BYTES, w);
+#pragma unroll
+                        for (int x = 0; x < E / 2; ++x) {
+                            const float2 vv = make_float2(bf_lo(w[x]), bf_hi(w[x]));
+#pragma unroll
+                            for (int h = 0; h < HG; ++h)
+                                o[h][x] = __ffma2_rn(make_float2(s[st][h], s[st][h]), vv, o[h][x]);
+                        }
+                    }
+                }
+            }
+        };
+        if (nvalid == SLICE)
+            process(std::true_type{});
+        else
+            process(std::false_type{});
+        // ---- release the slot; the last warp out refills it with the next slice
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();  // this warp's reads of the slot happen before its release
+            const int prev = atomicAdd(scnt + slot, 1);
+            __threadfence_block();
+            if (prev == use * kWarps + kWarps - 1 && !*abort_flag) {
+                Cursor cu = *scur;
+                fill_slot<C>(&tmKV, p, sSlots, b_full(slot), sinfo, suse, slot, use + 1, cu, n_hgroups, total);
+                *scur = cu;
+            }
+        }
+        __syncwarp();
     }
+    if (cur_item >= 0) finish_item();
     if (!ok) {
         *abort_flag = 1;
         if (p.status) atomicOr(p.status, kDevTimeout);
@@ -408,6 +444,54 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
     if (threadIdx.x == 0 && *abort_flag) {  // let copies still in flight land (bounded) before exit
         for (int s = 0; s < STAGES; ++s)
             if (suse[s] >= 0) mbar_wait_drain(b_full(s), suse[s] & 1);
+    }
+}
+
+// One CTA: the non-empty (sequence, split) pairs, longest first (a counting
+// sort on the split's block count, so the short last splits of the
+// sequences come at the end), and the work counter reset to 0.  Reports
+// seq_lens outside [0, min(max_seq_len, 128 * max_blocks_per_seq)].
+__global__ void __launch_bounds__(1024) paged_schedule(const PagedParams p) {
+    __shared__ int count[17], offset[17];
+    const int bps = p.blocks_per_split;
+    const int cap = min(p.max_seq_len, p.max_blocks_per_seq * kBlk);
+    if (threadIdx.x <= 16) count[threadIdx.x] = 0;
+    __syncthreads();
+    for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
+        int L = p.seq_lens[s];
+        if (L < 0 || L > cap) {
+            if (p.status) atomicOr(p.status, kDevBadSeqlen);
+            L = L < 0 ? 0 : cap;
+        }
+        const int nblk = (L + kBlk - 1) / kBlk;
+        if (nblk / bps) atomicAdd(&count[bps], nblk / bps);
+        if (nblk % bps) atomicAdd(&count[nblk % bps], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int at = 0;
+        for (int b = 16; b >= 1; --b) {
+            offset[b] = at;
+            at += count[b];
+        }
+        p.sched[0] = 0;
+        p.sched[1] = at;
+    }
+    __syncthreads();
+    for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
+        int L = p.seq_lens[s];
+        L = L < 0 ? 0 : (L > cap ? cap : L);
+        const int nblk = (L + kBlk - 1) / kBlk;
+        const int nfull = nblk / bps;
+        if (nfull) {
+            const int at = atomicAdd(&offset[bps], nfull);
+            for (int i = 0; i < nfull; ++i)
+                p.pairs[at + i] = make_int4(s, i, i * bps * kBlk, min(L, (i + 1) * bps * kBlk));
+        }
+        if (nblk % bps) {
+            const int at = atomicAdd(&offset[nblk % bps], 1);
+            p.pairs[at] = make_int4(s, nfull, nfull * bps * kBlk, L);
+        }
     }
 }
 
@@ -442,7 +526,7 @@ __global__ void __launch_bounds__(128) paged_combine(const PagedParams p, int D)
 
 // ------------------------------------------------------------------ host side
 PagedPlan paged_plan(int num_seqs, int Hq, int Hkv, int D, int max_seq_len) {
-    PagedPlan pl{1, 0, 0};
+    PagedPlan pl{1, 0, 0, 0, 0, 0};
     if (num_seqs <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_seq_len <= 0) return pl;
     const long long maxblk = (max_seq_len + kBlk - 1) / kBlk;
     // Aim for >= ~1200 (sequence, KV head, split) items so a persistent grid
@@ -453,9 +537,10 @@ PagedPlan paged_plan(int num_seqs, int Hq, int Hkv, int D, int max_seq_len) {
     pl.blocks_per_split = static_cast<int>(bps);
     pl.max_splits = static_cast<int>((maxblk + bps - 1) / bps);
     const size_t rows = static_cast<size_t>(num_seqs) * Hq * pl.max_splits;
-    const size_t o_bytes = (rows * D * 4 + 255) & ~size_t(255);
-    const size_t l_bytes = (rows * 4 + 255) & ~size_t(255);
-    pl.workspace_bytes = o_bytes + l_bytes;
+    pl.o_bytes = (rows * D * 4 + 255) & ~size_t(255);
+    pl.lse_bytes = (rows * 4 + 255) & ~size_t(255);
+    pl.pairs_bytes = (static_cast<size_t>(num_seqs) * pl.max_splits * 16 + 255) & ~size_t(255);
+    pl.workspace_bytes = pl.o_bytes + pl.lse_bytes + pl.pairs_bytes + 256;
     return pl;
 }
 
@@ -473,8 +558,11 @@ static cudaError_t launch_paged_cfg(const CUtensorMap& tm, const PagedParams& p,
     const int n_hgroups = p.Hkv * (p.group / p.heads_per_cta);
     const long long n_items = static_cast<long long>(p.num_seqs) * n_hgroups * p.max_splits;
     const int grid = static_cast<int>(n_items < num_sms ? n_items : num_sms);
-    paged_decode_sm103a<C><<<grid, 32 * kWarps, C::SMEM_BYTES, st>>>(tm, p);
+    paged_schedule<<<1, 1024, 0, st>>>(p);
     cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    paged_decode_sm103a<C><<<grid, 32 * kWarps, C::SMEM_BYTES, st>>>(tm, p);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     paged_combine<<<p.num_seqs * p.Hq, 128, 0, st>>>(p, C::D);
     return cudaGetLastError();

@@ -50,6 +50,8 @@ struct PagedParams {
     uint32_t* status;
     float* part_o;          // [S, Hq, max_splits, D]
     float* part_lse;        // [S, Hq, max_splits]
+    int4* pairs;            // [S * max_splits] work list: (sequence, split, tok0, tok1), longest first
+    int* sched;             // [0] work counter, [1] number of pairs (written by paged_schedule)
     int num_seqs, num_blocks, max_blocks_per_seq, max_seq_len;
     int Hq, Hkv, group, heads_per_cta;
     int blocks_per_split, max_splits;
@@ -60,6 +62,7 @@ struct PagedParams {
 struct PagedPlan {
     int blocks_per_split;
     int max_splits;
+    size_t o_bytes, lse_bytes, pairs_bytes;  // workspace sections, each 256-byte aligned
     size_t workspace_bytes;
 };
 PagedPlan paged_plan(int num_seqs, int Hq, int Hkv, int D, int max_seq_len);

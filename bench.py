@@ -397,7 +397,7 @@ def run_ours(args, world, rank, local):
         },
         "paged_decode": {
             "value": dec_value, "unit": "GB/s", "ms": dec_avg,
-            "roofline": {"bound": "hbm", "kernel": "paged_decode_sm103a + paged_combine", "achieved": dec_gbs_rank,
+            "roofline": {"bound": "hbm", "kernel": "paged_schedule + paged_decode_sm103a + paged_combine", "achieved": dec_gbs_rank,
                          "peak": peak_bw, "unit": "GB/s", "frac": dec_gbs_rank / peak_bw if do_dec else None,
                          "peak_kind": f"{peak_kind} HBM copy", "bytes_per_call": dec_bytes,
                          "traffic": traffic_for("paged_decode_sm103a", "decode.cu")},
@@ -405,7 +405,8 @@ def run_ours(args, world, rank, local):
         },
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": (int(do_pre) + 2 * int(do_dec)) * args.steps,
+        # per step: the prefill kernel; the decode schedule, decode and combine kernels
+        "gpu_launches": (int(do_pre) + 3 * int(do_dec)) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": t_wall,
     }
