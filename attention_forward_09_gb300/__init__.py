@@ -27,7 +27,8 @@ LIB_PATH = os.path.join(_PKG, "libgbattn.so")
 OUT_BF16, OUT_F32 = 0, 1
 DEV_BAD_INDEX, DEV_TIMEOUT, DEV_BAD_SEQLEN = 1, 2, 4
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "workspace",
-                5: "cuda", 6: "device"}
+                5: "cuda", 6: "device", 7: "scratch limit"}
+NOALLOC_SCRATCH_BYTES = 32 << 20  # GBATTN_NOALLOC_SCRATCH_BYTES
 
 # (name, restype, argtypes) for every symbol of include/gbattn.h
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -37,6 +38,7 @@ SIGNATURES = {
     "attn_fwd_paged_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "attn_fwd_paged": (_I, [_P, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _Z, _P, _P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
+    "attn_fwd_paged_noalloc": (_I, [_P, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _P]),
 }
 
 _lib = None
@@ -178,4 +180,34 @@ def attn_fwd_paged(q, kv_cache, block_table, seq_lens, max_seq_len, softmax_scal
                                        workspace.numel() * workspace.element_size(), _ptr(dev_status),
                                        _stream_handle(stream))
     _check("attn_fwd_paged", st)
+    return out, lse
+
+
+def attn_fwd_paged_noalloc(q, kv_cache, block_table, seq_lens, max_seq_len, softmax_scale=None, causal=True,
+                           out=None, lse=None, out_dtype=torch.float32, dev_status=None, stream=None):
+    """attn_fwd_paged without a workspace argument, for callers that must not
+    allocate device memory while it runs (e.g. during CUDA-graph capture): the
+    split-K scratch is the library's built-in 32 MiB device array.  Pass
+    preallocated ``out`` (and ``lse``) to allocate nothing here either.  The
+    first call on a device should happen before any stream capture.  Calls
+    that overlap on the GPU share the scratch and race."""
+    _bf16_cuda("q", q)
+    _bf16_cuda("kv_cache", kv_cache)
+    S, Hq, D = q.shape
+    two, nb, bs, Hkv, Dk = kv_cache.shape
+    if two != 2 or Dk != D:
+        raise ValueError("kv_cache must be [2, num_blocks, block_size, Hkv, D]")
+    for n, t in (("block_table", block_table), ("seq_lens", seq_lens)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    if out is None:
+        out = torch.empty(S, Hq, D, dtype=out_dtype, device=q.device)
+    if lse is True:
+        lse = torch.empty(S, Hq, dtype=torch.float32, device=q.device)
+    st = load_library().attn_fwd_paged_noalloc(_ptr(q), _ptr(kv_cache), nb, bs, _ptr(block_table),
+                                               block_table.shape[1], _ptr(seq_lens), S, int(max_seq_len), Hq, Hkv, D,
+                                               scale, int(bool(causal)), _ptr(out), _out_code(out.dtype), _ptr(lse),
+                                               _ptr(dev_status), _stream_handle(stream))
+    _check("attn_fwd_paged_noalloc", st)
     return out, lse

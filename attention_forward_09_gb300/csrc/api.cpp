@@ -123,6 +123,7 @@ const char* attn_status_string(gbattn_status s) {
         case GBATTN_ERR_WORKSPACE: return "workspace missing or too small";
         case GBATTN_ERR_CUDA: return "CUDA error";
         case GBATTN_ERR_DEVICE: return "device is not compute capability 10.3 (GB300)";
+        case GBATTN_ERR_SCRATCH_LIMIT: return "sizes need more scratch than attn_fwd_paged_noalloc has built in";
         default: return "unknown status";
     }
 }

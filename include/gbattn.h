@@ -54,7 +54,8 @@ typedef enum {
     GBATTN_ERR_ALIGNMENT = 3,   /* a tensor pointer is not 16-byte aligned */
     GBATTN_ERR_WORKSPACE = 4,   /* paged workspace missing or too small */
     GBATTN_ERR_CUDA = 5,        /* CUDA runtime / driver error (launch, attribute, tensor map) */
-    GBATTN_ERR_DEVICE = 6       /* current device is not compute capability 10.3 */
+    GBATTN_ERR_DEVICE = 6,      /* current device is not compute capability 10.3 */
+    GBATTN_ERR_SCRATCH_LIMIT = 7 /* attn_fwd_paged_noalloc: sizes need more than its built-in scratch */
 } gbattn_status;
 
 typedef enum {
@@ -159,6 +160,37 @@ gbattn_status attn_fwd_paged(const void* q, const void* kv_cache, int num_blocks
                              void* out, gbattn_dtype out_dtype, float* lse,
                              void* workspace, size_t workspace_bytes,
                              uint32_t* dev_status, void* stream);
+
+/*
+ * attn_fwd_paged_noalloc -- attn_fwd_paged for callers that cannot allocate
+ * device memory when they run the decode (inside a CUDA-graph capture, where
+ * cudaMalloc is not allowed; as a plugin in a framework that owns all device
+ * memory; in a server whose memory budget is fixed at start-up).  The pages
+ * have no counterpart of this call: it is an addition of this library.
+ *
+ * Same arguments and results as attn_fwd_paged, without workspace and
+ * workspace_bytes.  The split-K scratch comes from one device array built
+ * into the library, GBATTN_NOALLOC_SCRATCH_BYTES long, which every GPU that
+ * has loaded the library's code holds until the process exits.
+ *
+ *  - Sizes needing more scratch than that (see attn_fwd_paged_workspace_size)
+ *    are refused with GBATTN_ERR_SCRATCH_LIMIT before any CUDA call.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture on the device.
+ *  - The call itself allocates nothing and frees nothing.
+ *  - Every call on a device shares the same array, and the array keeps the
+ *    previous call's contents (nothing in it needs to start at zero).  Calls
+ *    that can overlap on the GPU (different streams without ordering between
+ *    them) race on it and give wrong results: order them.
+ */
+#define GBATTN_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+gbattn_status attn_fwd_paged_noalloc(const void* q, const void* kv_cache, int num_blocks, int block_size,
+                                     const int32_t* block_table, int max_blocks_per_seq,
+                                     const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                                     int Hq, int Hkv, int D, float softmax_scale, int causal,
+                                     void* out, gbattn_dtype out_dtype, float* lse,
+                                     uint32_t* dev_status, void* stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* attn_status_string(gbattn_status status);

@@ -32,7 +32,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(
         ["attn_fwd_dense", "attn_fwd_varlen", "attn_fwd_paged", "attn_fwd_paged_workspace_size",
-         "attn_status_string"])
+         "attn_status_string", "attn_fwd_paged_noalloc"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         assert lib.attn_status_string(code)
     assert lib.attn_status_string(99) == b"unknown status"
 
@@ -121,3 +121,12 @@ def test_workspace_size_is_pure_and_sized_for_the_plan(lib):
     assert a >= 64 * 32 * (128 + 1) * 4
     assert f(64, 32, 8, 80, 32768) == 0 and f(0, 32, 8, 128, 100) == 0 and f(4, 6, 4, 128, 100) == 0
     assert f(1, 8, 8, 128, 1) > 0
+
+
+def test_noalloc_refuses_sizes_beyond_its_scratch_on_the_host(lib):
+    """The size check comes before any CUDA call, so it runs without a GPU."""
+    S, Hq, Hkv, D, L = 4096, 64, 8, 256, 131072
+    assert lib.attn_fwd_paged_workspace_size(S, Hq, Hkv, D, L) > gb.NOALLOC_SCRATCH_BYTES
+    st = lib.attn_fwd_paged_noalloc(P, P, 1 << 20, 128, P, L // 128, P, S, L, Hq, Hkv, D, 0.1, 1, P, 1, None,
+                                    None, None)
+    assert st == 7
