@@ -94,7 +94,7 @@ gbattn_status check_common(const void* q, const void* k, const void* v, const vo
 }
 
 gbattn_status run_prefill(const void* q, const void* k, const void* v, long long Tq, long long Tk, int D,
-                          PrefillParams& p, int q_tiles, cudaStream_t st) {
+                          PrefillParams& p, cudaStream_t st) {
     DeviceInfo di;
     gbattn_status s = device_info(&di);
     if (s != GBATTN_OK) return s;
@@ -107,7 +107,7 @@ gbattn_status run_prefill(const void* q, const void* k, const void* v, long long
         !encode_rows_heads_d(&tk, no_keys ? q : k, no_keys ? Tq : Tk, no_keys ? p.Hq : p.Hkv, D, bn) ||
         !encode_rows_heads_d(&tv, no_keys ? q : v, no_keys ? Tq : Tk, no_keys ? p.Hq : p.Hkv, D, bn))
         return GBATTN_ERR_CUDA;
-    return gbattn::launch_prefill(D, tq, tk, tv, p, q_tiles, st) == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+    return gbattn::launch_prefill(D, tq, tk, tv, p, st) == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 
 }  // namespace
@@ -158,7 +158,7 @@ gbattn_status attn_fwd_dense(const void* q, const void* k, const void* v, int B,
     p.lse_hstride = Sq;
     p.lse_row_global = 0;
     return run_prefill(q, k, v, static_cast<long long>(B) * Sq, static_cast<long long>(B) * Sk, D, p,
-                       (Sq + 127) / 128, static_cast<cudaStream_t>(stream));
+                       static_cast<cudaStream_t>(stream));
 }
 
 gbattn_status attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
@@ -193,7 +193,7 @@ gbattn_status attn_fwd_varlen(const void* q, const void* k, const void* v, const
     p.lse_bstride = 0;
     p.lse_hstride = Tq;
     p.lse_row_global = 1;
-    return run_prefill(q, k, v, Tq, Tk, D, p, (max_seqlen_q + 127) / 128, static_cast<cudaStream_t>(stream));
+    return run_prefill(q, k, v, Tq, Tk, D, p, static_cast<cudaStream_t>(stream));
 }
 
 size_t attn_fwd_paged_workspace_size(int num_seqs, int Hq, int Hkv, int D, int max_seq_len) {

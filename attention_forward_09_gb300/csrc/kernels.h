@@ -36,9 +36,9 @@ struct PrefillParams {
 
 // Tensor maps are built by the host (see api.cpp) over q [Tq, Hq, D] and
 // k / v [Tk, Hkv, D]; box {64, 1, rows}, 128-byte swizzle.
+// The grid is sized from p.max_seqlen_q (128 or 256 query rows per CTA).
 cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                           const CUtensorMap& tmV, const PrefillParams& p, int num_q_tiles,
-                           cudaStream_t stream);
+                           const CUtensorMap& tmV, const PrefillParams& p, cudaStream_t stream);
 int prefill_block_n(int D);  // keys per KV tile for head size D
 
 struct PagedParams {

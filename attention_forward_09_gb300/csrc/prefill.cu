@@ -343,47 +343,400 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Two query tiles per CTA (D <= 128).
+//
+// The CTA owns 256 query rows of one (document, head): tile A = rows
+// [q0, q0 + 128), tile B = [q0 + 128, q0 + 256).  Each tile has its own
+// softmax warpgroup (warps 0-3: A, warps 4-7: B), so while one warpgroup
+// exponentiates its scores the tensor core runs the other tile's products.
+//   warp 8   TMA producer (Q_A, Q_B once; then K_0 V_0 K_1 V_1 ...)
+//   warp 9   TMEM allocator + MMA issuer, in the order
+//            S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
+//   warps 10-11 idle (they complete the third warpgroup)
+// Registers: launched at 168 per thread; the third warpgroup gives back
+// down to 56 so each softmax thread can hold a whole 128-column S row (224).
+// TMEM: S_A [0,128) S_B [128,256) O_A [256, 256+D) O_B [256+D, 256+2D).
+// P_X (bf16 pairs) is written back over the first 64 columns of S_X and
+// read from there by the P.V product (tcgen05.mma with A in tensor memory),
+// so P never goes through shared memory.  The MMA thread issues every
+// tcgen05.mma in order, so once S_X(j) is complete PV_X(j-1) is complete
+// too: the softmax warps may then rescale O_X and overwrite P_X without a
+// separate wait.
+template <int D_, int STAGES_>
+struct Prefill2Cfg {
+    static constexpr int D = D_;
+    static constexpr int BN = 128;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int BM = 128;  // rows per tile; two tiles per CTA
+    static constexpr int NCH = (D + 63) / 64;
+    static constexpr int QT_BYTES = NCH * BM * 128;  // one Q tile
+    static constexpr int KV_BYTES = NCH * BN * 128;
+    static constexpr int NUM_BARS = 2 * STAGES + 8;
+    static constexpr int SMEM_BYTES = 1024 + 2 * QT_BYTES + STAGES * KV_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int TMEM_S = 0;          // S_X at X * BN
+    static constexpr int TMEM_O = 2 * BN;     // O_X at TMEM_O + X * D
+    static constexpr int TMEM_COLS = 512;
+    static_assert(2 * BN + 2 * D <= 512, "TMEM budget");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <class C>
+__global__ void __launch_bounds__(384, 1)
+    fmha2_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+    constexpr int D = C::D, BN = C::BN, STAGES = C::STAGES, BM = C::BM, NCH = C::NCH;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sQ = smem_u32(smem);  // Q_X at sQ + X * QT_BYTES
+    const uint32_t sKV = sQ + 2 * C::QT_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * C::QT_BYTES + STAGES * C::KV_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t b_q_full = smem_u32(&bars[0]);
+    auto b_kv_full = [&](int s) { return smem_u32(&bars[1 + s]); };
+    auto b_kv_empty = [&](int s) { return smem_u32(&bars[1 + STAGES + s]); };
+    auto b_s_full = [&](int x) { return smem_u32(&bars[1 + 2 * STAGES + x]); };
+    auto b_p_full = [&](int x) { return smem_u32(&bars[3 + 2 * STAGES + x]); };
+    auto b_pv_done = [&](int x) { return smem_u32(&bars[5 + 2 * STAGES + x]); };
+    const uint32_t b_drain = smem_u32(&bars[7 + 2 * STAGES]);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ------------------------------------------------------------ tile coordinates
+    const int tile = p.causal ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;  // heavy causal tiles first
+    const int h = blockIdx.y;
+    const int doc = blockIdx.z;
+    const int kvh = h / p.group;
+    int q_start, Lq, k_start, Lk;
+    if (p.cu_q) {
+        q_start = p.cu_q[doc];
+        k_start = p.cu_k[doc];
+        const int q_end = p.cu_q[doc + 1], k_end = p.cu_k[doc + 1];
+        Lq = q_end - q_start;
+        Lk = k_end - k_start;
+        const bool bad = q_start < 0 || Lq < 0 || q_end > p.Tq || k_start < 0 || Lk < 0 ||
+                         k_end > p.Tk || Lq > p.max_seqlen_q || Lk > p.max_seqlen_k;
+        if (bad) {
+            if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0 && p.status) atomicOr(p.status, kDevBadSeqlen);
+            return;
+        }
+    } else {
+        q_start = doc * p.Sq;
+        Lq = p.Sq;
+        k_start = doc * p.Sk;
+        Lk = p.Sk;
+    }
+    const int q0 = tile * 2 * BM;
+    if (q0 >= Lq) return;  // CTA-uniform, before any barrier or TMEM use
+    if (status_has_timeout(p.status, kDevTimeout)) return;
+    const int diag = Lk - Lq;
+    // KV tiles each query tile needs (0 for a tile with no rows)
+    auto kv_tiles = [&](int first_row) {
+        if (first_row >= Lq) return 0;
+        int kend = Lk;
+        if (p.causal) kend = min(Lk, min(first_row + BM - 1, Lq - 1) + diag + 1);
+        return kend > 0 ? (kend + BN - 1) / BN : 0;
+    };
+    const int nA = kv_tiles(q0), nB = kv_tiles(q0 + BM);
+    const int nmax = max(nA, nB);
+
+    // ------------------------------------------------------------------ setup
+    if (threadIdx.x == 0) {
+        mbar_init(b_q_full, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(b_kv_full(s), 1);
+            mbar_init(b_kv_empty(s), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(b_s_full(x), 1);
+            mbar_init(b_p_full(x), 128);
+            mbar_init(b_pv_done(x), 1);
+        }
+        mbar_init(b_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+    // 3 x 128 threads x 168 launched = 2 x 128 x 224 + 128 x 56
+    if (warp >= 8) {
+      regs_dec<56>();
+      if (warp == 8) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            mbar_arrive_expect_tx(b_q_full, 2 * C::QT_BYTES);
+            for (int x = 0; x < 2; ++x)
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_3d(sQ + x * C::QT_BYTES + c * BM * 128, &tmQ, b_q_full, c * 64, h, q_start + q0 + x * BM);
+            int issued = 0;
+            for (int t = 0; t < 2 * nmax; ++t) {
+                const int s = t % STAGES, u = t / STAGES;
+                if (u > 0 && !mbar_wait(b_kv_empty(s), (u - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const CUtensorMap* m = (t & 1) ? &tmV : &tmK;
+                const int row = k_start + (t >> 1) * BN;
+                mbar_arrive_expect_tx(b_kv_full(s), C::KV_BYTES);
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_3d(sKV + s * C::KV_BYTES + c * BN * 128, m, b_kv_full(s), c * 64, kvh, row);
+                ++issued;
+            }
+            if (!ok || *abort_flag) {
+                // Let every copy this thread started land before the CTA retires.
+                mbar_wait_drain(b_q_full, 0);
+                for (int t = (issued > STAGES ? issued - STAGES : 0); t < issued; ++t)
+                    mbar_wait_drain(b_kv_full(t % STAGES), (t / STAGES) & 1);
+            }
+        }
+    } else if (warp == 9) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc_bf16_f32(BM, BN, false, false);
+            constexpr uint32_t kIdO = idesc_bf16_f32(BM, D, false, true);
+            ok = mbar_wait(b_q_full, 0, abort_flag);
+            auto issue_s = [&](int x, int j) {
+                const int s = (2 * j) % STAGES;
+                const uint32_t kb = sKV + s * C::KV_BYTES;
+                const uint32_t qb = sQ + x * C::QT_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    const uint64_t a = sdesc_sw128(qb + (kk >> 2) * BM * 128 + off, 16, 1024);
+                    const uint64_t b = sdesc_sw128(kb + (kk >> 2) * BN * 128 + off, 16, 1024);
+                    mma_bf16_ss(tmem + C::TMEM_S + x * BN, a, b, kIdS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(b_s_full(x));
+            };
+            auto issue_pv = [&](int x, int j) {
+                const int s = (2 * j + 1) % STAGES;
+                const uint32_t vb = sKV + s * C::KV_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t b = sdesc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
+                    mma_bf16_ts(tmem + C::TMEM_O + x * D, tmem + C::TMEM_S + x * BN + kk * 8, b, kIdO,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(b_pv_done(x));
+            };
+            auto wait_k = [&](int j) {
+                const int t = 2 * j;
+                return mbar_wait(b_kv_full(t % STAGES), (t / STAGES) & 1, abort_flag);
+            };
+            auto wait_v = [&](int j) {
+                const int t = 2 * j + 1;
+                return mbar_wait(b_kv_full(t % STAGES), (t / STAGES) & 1, abort_flag);
+            };
+            if (ok && nmax > 0) {
+                if ((ok = wait_k(0))) {
+                    tc_fence_after();
+                    if (nA > 0) issue_s(0, 0);
+                    if (nB > 0) issue_s(1, 0);
+                    mma_commit(b_kv_empty(0));  // K_0: read by both S products above
+                }
+            }
+            for (int j = 0; ok && j < nmax; ++j) {
+                const bool more = j + 1 < nmax;
+                if (!(ok = wait_v(j))) break;
+                if (more && !(ok = wait_k(j + 1))) break;
+                if (j < nA) {
+                    if (!(ok = mbar_wait(b_p_full(0), j & 1, abort_flag))) break;
+                    tc_fence_after();
+                    issue_pv(0, j);
+                    if (j + 1 < nA) issue_s(0, j + 1);
+                }
+                if (j < nB) {
+                    if (!(ok = mbar_wait(b_p_full(1), j & 1, abort_flag))) break;
+                    tc_fence_after();
+                    issue_pv(1, j);
+                    if (j + 1 < nB) issue_s(1, j + 1);
+                }
+                mma_commit(b_kv_empty((2 * j + 1) % STAGES));      // V_j: last read by PV of this j
+                if (more) mma_commit(b_kv_empty((2 * j + 2) % STAGES));  // K_{j+1}: read by the S issued above
+            }
+            // Everything issued above must finish before TMEM is released.
+            mma_commit(b_drain);
+            mbar_wait_drain(b_drain, 0);
+        }
+      }
+    } else {
+        regs_inc<224>();
+        // ------------------------------------------------------------- softmax
+        const int x = warp >> 2;               // 0: tile A, 1: tile B
+        const int r = threadIdx.x & 127;       // row within the tile == TMEM lane
+        const int row = q0 + x * BM + r;       // row within the document
+        const int n_kv = x ? nB : nA;
+        const int qfirst = q0 + x * BM;
+        const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t tS = tl + C::TMEM_S + x * BN;
+        const uint32_t tO = tl + C::TMEM_O + x * D;
+        const int row_lim = p.causal ? min(Lk, row + diag + 1) : Lk;  // keys [0, row_lim) visible
+        const float c2 = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        for (int j = 0; j < n_kv; ++j) {
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_s_full(x), j & 1, abort_flag)))) break;
+            tc_fence_after();
+            const int kbase = j * BN;
+            const bool edge = (kbase + BN > Lk) || (p.causal && kbase + BN - 1 > qfirst + diag);
+            const int lim = row_lim - kbase;  // columns >= lim are masked (edge tiles only)
+            uint32_t sr[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c)
+                tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+            tmem_wait_ld();
+            if (edge) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c)
+                    if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+            const float m_new = fmaxf(m, mx * c2);
+            const bool need = m_new > m + kRescaleThreshold;
+            const bool warp_need = __any_sync(0xffffffffu, need);
+            float alpha = 1.f;
+            if (warp_need && m_new > m) {
+                alpha = ex2(m - m_new);
+                m = m_new;
+            }
+            l *= alpha;
+            // O_X already holds every PV_X(i < j): S_X(j) was issued after them
+            if (warp_need && j > 0) {
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(tO + c * 32, o);
+                }
+            }
+            // P = 2^(S c - m) as bf16 pairs over the first 64 columns of S
+            const float msub = (m == -INFINITY) ? 0.f : m;
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float p0 = ex2(fmaf(__uint_as_float(sr[c * 32 + e]), c2, -msub));
+                    const float p1 = ex2(fmaf(__uint_as_float(sr[c * 32 + e + 1]), c2, -msub));
+                    rs += p0 + p1;
+                    pk[e >> 1] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tS + c * 16, pk);
+            }
+            l += rs;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(b_p_full(x));
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok && n_kv > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(b_pv_done(x), (n_kv - 1) & 1, abort_flag));
+            tc_fence_after();
+        }
+        // ------------------------------------------------------------ epilogue
+        const bool row_valid = ok && row < Lq;
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const long long orow = static_cast<long long>(q_start + row) * p.Hq + h;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            if (n_kv > 0 && ok) {
+                tmem_ld32(tO + c * 32, o);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = 0u;
+            }
+            if (row_valid) {
+                if (p.out_f32) {
+                    float* dst = reinterpret_cast<float*>(p.out) + orow * D + c * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        st_global_v4(dst + e, __float_as_uint(__uint_as_float(o[e]) * inv_l),
+                                     __float_as_uint(__uint_as_float(o[e + 1]) * inv_l),
+                                     __float_as_uint(__uint_as_float(o[e + 2]) * inv_l),
+                                     __float_as_uint(__uint_as_float(o[e + 3]) * inv_l));
+                } else {
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + orow * D + c * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8)
+                        st_global_v4(dst + e,
+                                     pack_bf16x2(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l),
+                                     pack_bf16x2(__uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l),
+                                     pack_bf16x2(__uint_as_float(o[e + 4]) * inv_l, __uint_as_float(o[e + 5]) * inv_l),
+                                     pack_bf16x2(__uint_as_float(o[e + 6]) * inv_l, __uint_as_float(o[e + 7]) * inv_l));
+                }
+            }
+        }
+        if (row_valid && p.lse) {
+            const long long lrow = p.lse_row_global ? (q_start + row) : row;
+            p.lse[doc * p.lse_bstride + h * p.lse_hstride + lrow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        }
+    }
+
+    // --------------------------------------------------------------- teardown
+    if (!ok) {
+        *abort_flag = 1;
+        if (p.status) atomicOr(p.status, kDevTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
 // ---------------------------------------------------------------- launchers
-using Cfg64 = PrefillCfg<64, 128, 6>;
-using Cfg96 = PrefillCfg<96, 128, 4>;
-using Cfg128 = PrefillCfg<128, 128, 4>;
+// D <= 128: two query tiles per CTA; D = 192, 256: one tile (two O
+// accumulators of that width do not fit next to the S buffers in TMEM).
+using Cfg64 = Prefill2Cfg<64, 8>;
+using Cfg96 = Prefill2Cfg<96, 4>;
+using Cfg128 = Prefill2Cfg<128, 4>;
 using Cfg192 = PrefillCfg<192, 128, 3>;
 using Cfg256 = PrefillCfg<256, 128, 2>;
 
-template <class C>
-static cudaError_t launch_cfg(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                              const PrefillParams& p, int num_q_tiles, cudaStream_t stream) {
-    static bool attr_done = false;  // attribute is per function; setting it twice is harmless
+template <class C, class K>
+static cudaError_t launch_kernel(K kernel, int threads, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                 const CUtensorMap& tmV, const PrefillParams& p, int rows_per_cta,
+                                 cudaStream_t stream) {
+    static bool attr_done = false;  // the attribute is per function
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(fmha_fwd_sm103a<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    dim3 grid(num_q_tiles, p.Hq, p.num_docs);
-    fmha_fwd_sm103a<C><<<grid, 192, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
+    dim3 grid((p.max_seqlen_q + rows_per_cta - 1) / rows_per_cta, p.Hq, p.num_docs);
+    kernel<<<grid, threads, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
 }
 
-int prefill_block_n(int D) {
-    switch (D) {
-        case 64: return Cfg64::BN;
-        case 96: return Cfg96::BN;
-        case 128: return Cfg128::BN;
-        case 192: return Cfg192::BN;
-        case 256: return Cfg256::BN;
-        default: return 0;
-    }
-}
+int prefill_block_n(int D) { return (D == 64 || D == 96 || D == 128 || D == 192 || D == 256) ? 128 : 0; }
 
 cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                           const PrefillParams& p, int num_q_tiles, cudaStream_t stream) {
+                           const PrefillParams& p, cudaStream_t stream) {
     switch (D) {
-        case 64: return launch_cfg<Cfg64>(tmQ, tmK, tmV, p, num_q_tiles, stream);
-        case 96: return launch_cfg<Cfg96>(tmQ, tmK, tmV, p, num_q_tiles, stream);
-        case 128: return launch_cfg<Cfg128>(tmQ, tmK, tmV, p, num_q_tiles, stream);
-        case 192: return launch_cfg<Cfg192>(tmQ, tmK, tmV, p, num_q_tiles, stream);
-        case 256: return launch_cfg<Cfg256>(tmQ, tmK, tmV, p, num_q_tiles, stream);
+        case 64: return launch_kernel<Cfg64>(fmha2_fwd_sm103a<Cfg64>, 384, tmQ, tmK, tmV, p, 256, stream);
+        case 96: return launch_kernel<Cfg96>(fmha2_fwd_sm103a<Cfg96>, 384, tmQ, tmK, tmV, p, 256, stream);
+        case 128: return launch_kernel<Cfg128>(fmha2_fwd_sm103a<Cfg128>, 384, tmQ, tmK, tmV, p, 256, stream);
+        case 192: return launch_kernel<Cfg192>(fmha_fwd_sm103a<Cfg192>, 192, tmQ, tmK, tmV, p, 128, stream);
+        case 256: return launch_kernel<Cfg256>(fmha_fwd_sm103a<Cfg256>, 192, tmQ, tmK, tmV, p, 128, stream);
         default: return cudaErrorInvalidValue;
     }
 }
