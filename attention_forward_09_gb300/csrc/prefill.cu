@@ -232,9 +232,14 @@ __global__ void __launch_bounds__(192, 1)
                 for (int c = 0; c < BN; ++c)
                     if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
             }
-            float mx = -INFINITY;
+            // row max: three-input max into 4 independent chains (16 deep, 2 values per op)
+            float mxp[4];
 #pragma unroll
-            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+            for (int i = 0; i < 4; ++i) mxp[i] = __uint_as_float(sr[i]);
+#pragma unroll
+            for (int c = 4; c < BN; c += 2)
+                mxp[(c >> 1) & 3] = fmax3(mxp[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            const float mx = fmaxf(fmax3(mxp[0], mxp[1], mxp[2]), mxp[3]);
             const float m_new = fmaxf(m, mx * c2);
             const bool need = m_new > m + kRescaleThreshold;
             const bool warp_need = __any_sync(0xffffffffu, need);
@@ -246,15 +251,19 @@ __global__ void __launch_bounds__(192, 1)
             l *= alpha;
             const float msub = (m == -INFINITY) ? 0.f : m;
             uint32_t pk[BN / 2];
-            float rs = 0.f;
+            const float2 c2x2 = make_float2(c2, c2), negm = make_float2(-msub, -msub);
+            float2 rsp[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};  // independent partial row sums, in pairs
 #pragma unroll
             for (int c = 0; c < BN; c += 2) {
-                const float p0 = ex2(fmaf(__uint_as_float(sr[c]), c2, -msub));
-                const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), c2, -msub));
-                rs += p0 + p1;
-                pk[c >> 1] = pack_bf16x2(p0, p1);
+                const float2 t =
+                    __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2x2, negm);
+                const float2 pp = make_float2(ex2(t.x), ex2(t.y));
+                rsp[(c >> 1) & 3] = __fadd2_rn(rsp[(c >> 1) & 3], pp);
+                pk[c >> 1] = pack_bf16x2(pp.x, pp.y);
             }
-            l += rs;
+            const float2 rr = __fadd2_rn(__fadd2_rn(rsp[0], rsp[1]), __fadd2_rn(rsp[2], rsp[3]));
+            l += rr.x + rr.y;
             // PV_{j-1} has to be finished before O is rescaled or P overwritten.
             if (j > 0) {
                 if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_pv_done, (j - 1) & 1, abort_flag)))) break;
@@ -548,20 +557,31 @@ __global__ void __launch_bounds__(384, 1)
             }
             for (int j = 0; ok && j < nmax; ++j) {
                 const bool more = j + 1 < nmax;
+                bool k_ready = false;  // K_{j+1} is waited for only once an S product needs it
                 if (!(ok = wait_v(j))) break;
-                if (more && !(ok = wait_k(j + 1))) break;
                 if (j < nA) {
                     if (!(ok = mbar_wait(b_p_full(0), j & 1, abort_flag))) break;
                     tc_fence_after();
                     issue_pv(0, j);
-                    if (j + 1 < nA) issue_s(0, j + 1);
+                    if (j + 1 < nA) {
+                        if (!(ok = wait_k(j + 1))) break;
+                        k_ready = true;
+                        tc_fence_after();
+                        issue_s(0, j + 1);
+                    }
                 }
                 if (j < nB) {
                     if (!(ok = mbar_wait(b_p_full(1), j & 1, abort_flag))) break;
                     tc_fence_after();
                     issue_pv(1, j);
-                    if (j + 1 < nB) issue_s(1, j + 1);
+                    if (j + 1 < nB) {
+                        if (!k_ready && !(ok = wait_k(j + 1))) break;
+                        k_ready = true;
+                        tc_fence_after();
+                        issue_s(1, j + 1);
+                    }
                 }
+                if (more && !k_ready && !(ok = wait_k(j + 1))) break;  // keep the K_{j+1} phase in step
                 mma_commit(b_kv_empty((2 * j + 1) % STAGES));      // V_j: last read by PV of this j
                 if (more) mma_commit(b_kv_empty((2 * j + 2) % STAGES));  // K_{j+1}: read by the S issued above
             }
@@ -600,9 +620,14 @@ __global__ void __launch_bounds__(384, 1)
                 for (int c = 0; c < BN; ++c)
                     if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
             }
-            float mx = -INFINITY;
+            // row max: three-input max into 4 independent chains (16 deep, 2 values per op)
+            float mxp[4];
 #pragma unroll
-            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+            for (int i = 0; i < 4; ++i) mxp[i] = __uint_as_float(sr[i]);
+#pragma unroll
+            for (int c = 4; c < BN; c += 2)
+                mxp[(c >> 1) & 3] = fmax3(mxp[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            const float mx = fmaxf(fmax3(mxp[0], mxp[1], mxp[2]), mxp[3]);
             const float m_new = fmaxf(m, mx * c2);
             const bool need = m_new > m + kRescaleThreshold;
             const bool warp_need = __any_sync(0xffffffffu, need);
@@ -626,20 +651,24 @@ __global__ void __launch_bounds__(384, 1)
             }
             // P = 2^(S c - m) as bf16 pairs over the first 64 columns of S
             const float msub = (m == -INFINITY) ? 0.f : m;
-            float rs = 0.f;
+            const float2 c2x2 = make_float2(c2, c2), negm = make_float2(-msub, -msub);
+            float2 rsp[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};  // independent partial row sums, in pairs
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sr[c * 32 + e]), c2, -msub));
-                    const float p1 = ex2(fmaf(__uint_as_float(sr[c * 32 + e + 1]), c2, -msub));
-                    rs += p0 + p1;
-                    pk[e >> 1] = pack_bf16x2(p0, p1);
+                    const float2 t = __ffma2_rn(
+                        make_float2(__uint_as_float(sr[c * 32 + e]), __uint_as_float(sr[c * 32 + e + 1])), c2x2, negm);
+                    const float2 pp = make_float2(ex2(t.x), ex2(t.y));
+                    rsp[(e >> 1) & 3] = __fadd2_rn(rsp[(e >> 1) & 3], pp);
+                    pk[e >> 1] = pack_bf16x2(pp.x, pp.y);
                 }
                 tmem_st16(tS + c * 16, pk);
             }
-            l += rs;
+            const float2 rr = __fadd2_rn(__fadd2_rn(rsp[0], rsp[1]), __fadd2_rn(rsp[2], rsp[3]));
+            l += rr.x + rr.y;
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(b_p_full(x));
@@ -706,9 +735,9 @@ __global__ void __launch_bounds__(384, 1)
 // ---------------------------------------------------------------- launchers
 // D <= 128: two query tiles per CTA; D = 192, 256: one tile (two O
 // accumulators of that width do not fit next to the S buffers in TMEM).
-using Cfg64 = Prefill2Cfg<64, 8>;
-using Cfg96 = Prefill2Cfg<96, 4>;
-using Cfg128 = Prefill2Cfg<128, 4>;
+using Cfg64 = Prefill2Cfg<64, 10>;
+using Cfg96 = Prefill2Cfg<96, 5>;
+using Cfg128 = Prefill2Cfg<128, 5>;
 using Cfg192 = PrefillCfg<192, 128, 3>;
 using Cfg256 = PrefillCfg<256, 128, 2>;
 

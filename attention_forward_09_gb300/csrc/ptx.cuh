@@ -249,6 +249,12 @@ __device__ __forceinline__ float ex2(float x) {  // hardware 2^x (MUFU), ftz
     return y;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {  // three-input max
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {  // round to nearest even
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
