@@ -475,9 +475,9 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
-    // 3 x 128 threads x 168 launched = 2 x 128 x 224 + 128 x 56
+    // 3 x 128 threads x 168 launched = 2 x 128 x 216 + 128 x 72
     if (warp >= 8) {
-      regs_dec<56>();
+      regs_dec<72>();
       if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -511,87 +511,110 @@ __global__ void __launch_bounds__(384, 1)
         }
     } else if (warp == 9) {
         // ----------------------------------------------------------------- MMA
-        if (lane == 0) {
-            constexpr uint32_t kIdS = idesc_bf16_f32(BM, BN, false, false);
-            constexpr uint32_t kIdO = idesc_bf16_f32(BM, D, false, true);
-            ok = mbar_wait(b_q_full, 0, abort_flag);
-            auto issue_s = [&](int x, int j) {
-                const int s = (2 * j) % STAGES;
-                const uint32_t kb = sKV + s * C::KV_BYTES;
-                const uint32_t qb = sQ + x * C::QT_BYTES;
+        // The whole warp walks the schedule, so every wait and all descriptor
+        // arithmetic stay warp-uniform; one elected lane issues each tcgen05
+        // instruction.  Shared-memory descriptors are built once and offset by
+        // compile-time constants; the K/V ring position advances by counters.
+        constexpr uint32_t kIdS = idesc_bf16_f32(BM, BN, false, false);
+        constexpr uint32_t kIdO = idesc_bf16_f32(BM, D, false, true);
+        const bool leader = elect_one();
+        const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
+        const uint64_t dK = sdesc_sw128(sKV, 16, 1024);
+        const uint64_t dV = sdesc_sw128(sKV, BN * 128, 1024);
+        auto issue_s = [&](int x, int s) {  // S_X = Q_X K^T, K in stage s
+            if (leader) {
+                const uint64_t a0 = dQ + static_cast<uint64_t>(x * (C::QT_BYTES >> 4));
+                const uint64_t b0 = dK + static_cast<uint64_t>(s * (C::KV_BYTES >> 4));
+                const uint32_t d = tmem + C::TMEM_S + x * BN;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    const uint64_t a = sdesc_sw128(qb + (kk >> 2) * BM * 128 + off, 16, 1024);
-                    const uint64_t b = sdesc_sw128(kb + (kk >> 2) * BN * 128 + off, 16, 1024);
-                    mma_bf16_ss(tmem + C::TMEM_S + x * BN, a, b, kIdS, kk > 0 ? 1u : 0u);
+                    const uint32_t oa = ((kk >> 2) * BM * 128 + (kk & 3) * 32) >> 4;
+                    const uint32_t ob = ((kk >> 2) * BN * 128 + (kk & 3) * 32) >> 4;
+                    mma_bf16_ss(d, a0 + oa, b0 + ob, kIdS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(b_s_full(x));
-            };
-            auto issue_pv = [&](int x, int j) {
-                const int s = (2 * j + 1) % STAGES;
-                const uint32_t vb = sKV + s * C::KV_BYTES;
+            }
+            __syncwarp();
+        };
+        auto issue_pv = [&](int x, int s, bool acc) {  // O_X += P_X V, V in stage s
+            if (leader) {
+                const uint64_t b0 = dV + static_cast<uint64_t>(s * (C::KV_BYTES >> 4));
+                const uint32_t d = tmem + C::TMEM_O + x * D, a = tmem + C::TMEM_S + x * BN;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t b = sdesc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
-                    mma_bf16_ts(tmem + C::TMEM_O + x * D, tmem + C::TMEM_S + x * BN + kk * 8, b, kIdO,
-                                (j > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_bf16_ts(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdO, (acc || kk > 0) ? 1u : 0u);
                 mma_commit(b_pv_done(x));
-            };
-            auto wait_k = [&](int j) {
-                const int t = 2 * j;
-                return mbar_wait(b_kv_full(t % STAGES), (t / STAGES) & 1, abort_flag);
-            };
-            auto wait_v = [&](int j) {
-                const int t = 2 * j + 1;
-                return mbar_wait(b_kv_full(t % STAGES), (t / STAGES) & 1, abort_flag);
-            };
-            if (ok && nmax > 0) {
-                if ((ok = wait_k(0))) {
-                    tc_fence_after();
-                    if (nA > 0) issue_s(0, 0);
-                    if (nB > 0) issue_s(1, 0);
-                    mma_commit(b_kv_empty(0));  // K_0: read by both S products above
-                }
             }
-            for (int j = 0; ok && j < nmax; ++j) {
-                const bool more = j + 1 < nmax;
-                bool k_ready = false;  // K_{j+1} is waited for only once an S product needs it
-                if (!(ok = wait_v(j))) break;
-                if (j < nA) {
-                    if (!(ok = mbar_wait(b_p_full(0), j & 1, abort_flag))) break;
-                    tc_fence_after();
-                    issue_pv(0, j);
-                    if (j + 1 < nA) {
-                        if (!(ok = wait_k(j + 1))) break;
-                        k_ready = true;
-                        tc_fence_after();
-                        issue_s(0, j + 1);
-                    }
-                }
-                if (j < nB) {
-                    if (!(ok = mbar_wait(b_p_full(1), j & 1, abort_flag))) break;
-                    tc_fence_after();
-                    issue_pv(1, j);
-                    if (j + 1 < nB) {
-                        if (!k_ready && !(ok = wait_k(j + 1))) break;
-                        k_ready = true;
-                        tc_fence_after();
-                        issue_s(1, j + 1);
-                    }
-                }
-                if (more && !k_ready && !(ok = wait_k(j + 1))) break;  // keep the K_{j+1} phase in step
-                mma_commit(b_kv_empty((2 * j + 1) % STAGES));      // V_j: last read by PV of this j
-                if (more) mma_commit(b_kv_empty((2 * j + 2) % STAGES));  // K_{j+1}: read by the S issued above
+            __syncwarp();
+        };
+        auto release = [&](int s) {  // stage s is free once the MMAs issued so far finish
+            if (leader) mma_commit(b_kv_empty(s));
+            __syncwarp();
+        };
+        auto wait_all = [&](uint32_t bar, uint32_t ph) {
+            return __all_sync(0xffffffffu, mbar_wait(bar, ph, abort_flag));
+        };
+        // K_j is load 2j of the ring, V_j load 2j + 1 (STAGES >= 2)
+        int ks = 0, vs = 1;
+        uint32_t kph = 0, vph = 0;
+        auto adv = [](int& s, uint32_t& ph) {
+            s += 2;
+            if (s >= STAGES) {
+                s -= STAGES;
+                ph ^= 1u;
             }
-            // Everything issued above must finish before TMEM is released.
-            mma_commit(b_drain);
-            mbar_wait_drain(b_drain, 0);
+        };
+        ok = wait_all(b_q_full, 0);
+        if (ok && nmax > 0) {
+            if ((ok = wait_all(b_kv_full(ks), kph))) {
+                tc_fence_after();
+                if (nA > 0) issue_s(0, ks);
+                if (nB > 0) issue_s(1, ks);
+                release(ks);  // K_0: read by both S products above
+            }
         }
+        adv(ks, kph);
+        for (int j = 0; ok && j < nmax; ++j) {
+            const bool more = j + 1 < nmax;
+            bool k_ready = false;  // K_{j+1} is waited for only once an S product needs it
+            if (!(ok = wait_all(b_kv_full(vs), vph))) break;
+            if (j < nA) {
+                if (!(ok = wait_all(b_p_full(0), j & 1))) break;
+                tc_fence_after();
+                issue_pv(0, vs, j > 0);
+                if (j + 1 < nA) {
+                    if (!(ok = wait_all(b_kv_full(ks), kph))) break;
+                    k_ready = true;
+                    tc_fence_after();
+                    issue_s(0, ks);
+                }
+            }
+            if (j < nB) {
+                if (!(ok = wait_all(b_p_full(1), j & 1))) break;
+                tc_fence_after();
+                issue_pv(1, vs, j > 0);
+            }
+            release(vs);  // V_j: its last reader was issued above
+            if (j + 1 < nB) {
+                if (!k_ready && !(ok = wait_all(b_kv_full(ks), kph))) break;
+                k_ready = true;
+                tc_fence_after();
+                issue_s(1, ks);
+            }
+            if (more) {
+                if (!k_ready && !(ok = wait_all(b_kv_full(ks), kph))) break;  // keep the phase in step
+                release(ks);  // K_{j+1}: read by the S products issued above
+            }
+            adv(ks, kph);
+            adv(vs, vph);
+        }
+        // Everything issued above must finish before TMEM is released.
+        if (leader) mma_commit(b_drain);
+        __syncwarp();
+        mbar_wait_drain(b_drain, 0);
       }
     } else {
-        regs_inc<224>();
+        regs_inc<216>();
         // ------------------------------------------------------------- softmax
         const int x = warp >> 2;               // 0: tile A, 1: tile B
         const int r = threadIdx.x & 127;       // row within the tile == TMEM lane

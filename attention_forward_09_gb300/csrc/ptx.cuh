@@ -242,6 +242,17 @@ __device__ __forceinline__ void regs_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// True in exactly one lane of the (fully converged) warp.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, e;\n\t}"
+        : "=r"(r));
+    return r != 0;
+}
+
 // --------------------------------------------------------------------- ALU
 __device__ __forceinline__ float ex2(float x) {  // hardware 2^x (MUFU), ftz
     float y;
