@@ -107,7 +107,7 @@ gbattn_status run_prefill(const void* q, const void* k, const void* v, long long
         !encode_rows_heads_d(&tk, no_keys ? q : k, no_keys ? Tq : Tk, no_keys ? p.Hq : p.Hkv, D, bn) ||
         !encode_rows_heads_d(&tv, no_keys ? q : v, no_keys ? Tq : Tk, no_keys ? p.Hq : p.Hkv, D, bn))
         return GBATTN_ERR_CUDA;
-    return gbattn::launch_prefill(D, tq, tk, tv, p, st) == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+    return gbattn::launch_prefill(D, tq, tk, tv, p, di.sms, st) == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 
 }  // namespace

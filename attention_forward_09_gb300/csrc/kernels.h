@@ -32,13 +32,20 @@ struct PrefillParams {
     long long lse_bstride;  // lse offset = b*lse_bstride + h*lse_hstride + row
     long long lse_hstride;
     int lse_row_global;     // row counted from the start of the packed tensor (varlen)
+    // Dense batches on the two-tile kernel use a 1D grid of items
+    // (query tile, head, batch), tile fastest; varlen keeps the 3D grid
+    // (tile, head, document).  Set by launch_prefill, not by callers.
+    int linear;     // 1: blockIdx.x counts items from item_base
+    int tiles;      // query tiles (2 x 128 rows) per (batch, head)
+    int item_base;  // first item of this launch
+    int split;      // > 1: each item is shared by a cluster of `split` CTAs, one key range each
 };
 
 // Tensor maps are built by the host (see api.cpp) over q [Tq, Hq, D] and
 // k / v [Tk, Hkv, D]; box {64, 1, rows}, 128-byte swizzle.
 // The grid is sized from p.max_seqlen_q (128 or 256 query rows per CTA).
 cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                           const CUtensorMap& tmV, const PrefillParams& p, cudaStream_t stream);
+                           const CUtensorMap& tmV, const PrefillParams& p, int num_sms, cudaStream_t stream);
 int prefill_block_n(int D);  // keys per KV tile for head size D
 
 struct PagedParams {

@@ -166,48 +166,72 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else if (warp == 5) {
         // ----------------------------------------------------------------- MMA
-        if (lane == 0) {
-            constexpr uint32_t kIdS = idesc_bf16_f32(BM, BN, false, false);
-            constexpr uint32_t kIdO = idesc_bf16_f32(BM, D, false, true);
-            ok = mbar_wait(b_q_full, 0, abort_flag);
-            auto issue_s = [&](int j) -> bool {
-                const int t = 2 * j, s = t % STAGES;
-                if (!mbar_wait(b_kv_full(s), (t / STAGES) & 1, abort_flag)) return false;
-                tc_fence_after();
+        // Whole warp walks the schedule (warp-uniform waits and descriptor
+        // arithmetic); one elected lane issues each tcgen05 instruction.
+        constexpr uint32_t kIdS = idesc_bf16_f32(BM, BN, false, false);
+        constexpr uint32_t kIdO = idesc_bf16_f32(BM, D, false, true);
+        const bool leader = elect_one();
+        const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
+        const uint64_t dP = sdesc_sw128(sP, 16, 1024);
+        const uint64_t dK = sdesc_sw128(sKV, 16, 1024);
+        const uint64_t dV = sdesc_sw128(sKV, BN * 128, 1024);
+        auto wait_all = [&](uint32_t bar, uint32_t ph) {
+            return __all_sync(0xffffffffu, mbar_wait(bar, ph, abort_flag));
+        };
+        // K_j is load 2j of the ring, V_j load 2j + 1 (STAGES >= 2)
+        int ks = 0, vs = 1;
+        uint32_t kph = 0, vph = 0;
+        auto adv = [](int& s, uint32_t& ph) {
+            s += 2;
+            if (s >= STAGES) {
+                s -= STAGES;
+                ph ^= 1u;
+            }
+        };
+        auto issue_s = [&](int j) -> bool {
+            if (!wait_all(b_kv_full(ks), kph)) return false;
+            tc_fence_after();
+            if (leader) {
                 const uint32_t dS = tmem + C::TMEM_S + (j & 1) * BN;
-                const uint32_t kb = sKV + s * C::KV_BYTES;
+                const uint64_t b0 = dK + static_cast<uint64_t>(ks * (C::KV_BYTES >> 4));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;  // 16 bf16 = 32 B step inside a 128-B row
-                    const uint64_t a = sdesc_sw128(sQ + (kk >> 2) * BM * 128 + off, 16, 1024);
-                    const uint64_t b = sdesc_sw128(kb + (kk >> 2) * BN * 128 + off, 16, 1024);
-                    mma_bf16_ss(dS, a, b, kIdS, kk > 0 ? 1u : 0u);
+                    const uint32_t oa = ((kk >> 2) * BM * 128 + (kk & 3) * 32) >> 4;
+                    const uint32_t ob = ((kk >> 2) * BN * 128 + (kk & 3) * 32) >> 4;
+                    mma_bf16_ss(dS, dQ + oa, b0 + ob, kIdS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(b_s_full(j & 1));
-                mma_commit(b_kv_empty(s));
-                return true;
-            };
-            if (ok && n_kv > 0) ok = issue_s(0);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
-                if (!(ok = mbar_wait(b_p_full, j & 1, abort_flag))) break;
-                const int t = 2 * j + 1, s = t % STAGES;
-                if (!(ok = mbar_wait(b_kv_full(s), (t / STAGES) & 1, abort_flag))) break;
-                tc_fence_after();
-                const uint32_t vb = sKV + s * C::KV_BYTES;
+                mma_commit(b_kv_empty(ks));
+            }
+            __syncwarp();
+            adv(ks, kph);
+            return true;
+        };
+        ok = wait_all(b_q_full, 0);
+        if (ok && n_kv > 0) ok = issue_s(0);
+        for (int j = 0; ok && j < n_kv; ++j) {
+            if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
+            if (!(ok = wait_all(b_p_full, j & 1))) break;
+            if (!(ok = wait_all(b_kv_full(vs), vph))) break;
+            tc_fence_after();
+            if (leader) {
+                const uint64_t b0 = dV + static_cast<uint64_t>(vs * (C::KV_BYTES >> 4));
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(sP + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = sdesc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
-                    mma_bf16_ss(tmem + C::TMEM_O, a, b, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+                    const uint32_t oa = ((kk >> 2) * BM * 128 + (kk & 3) * 32) >> 4;
+                    mma_bf16_ss(tmem + C::TMEM_O, dP + oa, b0 + ((kk * 16 * 128) >> 4), kIdO,
+                                (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(b_pv_done);
-                mma_commit(b_kv_empty(s));
+                mma_commit(b_kv_empty(vs));
             }
-            // Everything issued above must finish before TMEM is released.
-            mma_commit(b_drain);
-            mbar_wait_drain(b_drain, 0);
+            __syncwarp();
+            adv(vs, vph);
         }
+        // Everything issued above must finish before TMEM is released.
+        if (leader) mma_commit(b_drain);
+        __syncwarp();
+        mbar_wait_drain(b_drain, 0);
     } else {
         // ------------------------------------------------------------- softmax
         const int r = threadIdx.x;  // row within the tile == TMEM lane
@@ -386,9 +410,119 @@ struct Prefill2Cfg {
     static constexpr int TMEM_S = 0;          // S_X at X * BN
     static constexpr int TMEM_O = 2 * BN;     // O_X at TMEM_O + X * D
     static constexpr int TMEM_COLS = 512;
+    // setmaxnreg split of the 384 x 168 launched registers: softmax warpgroups
+    // / producer + MMA warpgroup (each the smallest share with no spills)
+    static constexpr int REG_SOFTMAX = D == 64 ? 224 : 216;
+    static constexpr int REG_OTHER = D == 64 ? 56 : 72;
+    static_assert(2 * 128 * REG_SOFTMAX + 128 * REG_OTHER <= 384 * 168, "register split");
     static_assert(2 * BN + 2 * D <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(2 * BM * D * 4 <= STAGES * KV_BYTES && 2 * BM * 8 <= 2 * QT_BYTES, "split-merge staging");
 };
+
+// Merge of an item split along the keys over a cluster of p.split CTAs (the
+// softmax threads of every CTA call this; the other warps only pass the same
+// three cluster barriers).  CTA c holds, for the pair's 256 rows, O_c
+// (unnormalised, in TMEM), m_c and l_c over its key range; the partial
+// softmaxes combine as
+//   out = sum_c 2^(m_c - M) O_c / L,   L = sum_c 2^(m_c - M) l_c,   M = max_c m_c,
+//   lse = (M + log2 L) ln 2.
+// Each CTA stages its weighted rows in its own shared memory; CTA c then sums
+// rows [c R, (c + 1) R), R = 256 / p.split, over the cluster through
+// distributed shared memory and writes them.  Called once every MMA of the
+// CTA has completed, so the Q and K/V areas are free.
+template <int D>
+__device__ __forceinline__ void split_merge(uint8_t* smem, uint32_t sO, uint32_t tO, int pr, float m, float l,
+                                            bool have_o, bool ok, int crank, int q0, int Lq, int q_start, int h,
+                                            int doc, const PrefillParams& p) {
+    constexpr int ROWS = 256, CH = D / 4;  // 16-byte chunks per staged fp32 row
+    const int C = p.split;
+    float2* sML = reinterpret_cast<float2*>(smem);  // (m, l) of the 256 rows, over the Q area
+    sML[pr] = make_float2(m, l);
+    cluster_sync();
+    auto merged = [&](int row, float& M, float& L) {
+        float mc[8], lc[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            mc[c] = -INFINITY;
+            lc[c] = 0.f;
+            if (c < C) {
+                const float2 v = ld_cluster_f2(mapa_shared(smem_u32(&sML[row]), c));
+                mc[c] = v.x;
+                lc[c] = v.y;
+            }
+        }
+        M = mc[0];
+#pragma unroll
+        for (int c = 1; c < 8; ++c) M = fmaxf(M, mc[c]);
+        L = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            if (lc[c] > 0.f) L += lc[c] * ex2(mc[c] - M);
+    };
+    float M, L;
+    merged(pr, M, L);
+    const float w = (L > 0.f && l > 0.f) ? ex2(m - M) / L : 0.f;
+    const uint32_t row_base = sO + static_cast<uint32_t>(pr) * (D * 4);
+#pragma unroll 1
+    for (int c32 = 0; c32 < D / 32; ++c32) {
+        uint32_t o[32];
+        if (have_o && ok) {
+            tmem_ld32(tO + c32 * 32, o);
+            tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+            const int slot = (c32 * 8 + e4) ^ (pr & 7);
+            st_shared_v4(row_base + slot * 16, __float_as_uint(__uint_as_float(o[4 * e4]) * w),
+                         __float_as_uint(__uint_as_float(o[4 * e4 + 1]) * w),
+                         __float_as_uint(__uint_as_float(o[4 * e4 + 2]) * w),
+                         __float_as_uint(__uint_as_float(o[4 * e4 + 3]) * w));
+        }
+    }
+    cluster_sync();
+    const int R = ROWS / C;
+    const int t = static_cast<int>(threadIdx.x);  // 0 .. 255
+#pragma unroll 1
+    for (int id = t; id < R * CH; id += ROWS) {
+        const int orow = crank * R + id / CH, ch = id % CH;
+        const uint32_t off = sO + static_cast<uint32_t>(orow) * (D * 4) + static_cast<uint32_t>((ch ^ (orow & 7)) * 16);
+        float4 v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[c] = c < C ? ld_cluster_f4(mapa_shared(off, c)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 acc = v[0];
+#pragma unroll
+        for (int c = 1; c < 8; ++c) {
+            acc.x += v[c].x;
+            acc.y += v[c].y;
+            acc.z += v[c].z;
+            acc.w += v[c].w;
+        }
+        const int qrow = q0 + orow;
+        if (ok && qrow < Lq) {
+            const long long o_off = (static_cast<long long>(q_start + qrow) * p.Hq + h) * D + ch * 4;
+            if (p.out_f32)
+                st_global_v4(reinterpret_cast<float*>(p.out) + o_off, __float_as_uint(acc.x), __float_as_uint(acc.y),
+                             __float_as_uint(acc.z), __float_as_uint(acc.w));
+            else
+                *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) + o_off) =
+                    make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+        }
+    }
+    if (t < R && p.lse) {
+        const int orow = crank * R + t, qrow = q0 + orow;
+        float Mr, Lr;
+        merged(orow, Mr, Lr);
+        if (ok && qrow < Lq) {
+            const long long lrow = p.lse_row_global ? (q_start + qrow) : qrow;
+            p.lse[doc * p.lse_bstride + h * p.lse_hstride + lrow] = Lr > 0.f ? (Mr + __log2f(Lr)) * kLn2 : -INFINITY;
+        }
+    }
+    cluster_sync();  // no CTA leaves while another still reads its shared memory
+}
 
 template <class C>
 __global__ void __launch_bounds__(384, 1)
@@ -413,9 +547,21 @@ __global__ void __launch_bounds__(384, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // ------------------------------------------------------------ tile coordinates
-    const int tile = p.causal ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;  // heavy causal tiles first
-    const int h = blockIdx.y;
-    const int doc = blockIdx.z;
+    const bool split = p.split > 1;  // kernel-uniform
+    int tile, h, doc, crank = 0;
+    if (p.linear) {
+        const int item = p.item_base + static_cast<int>(split ? blockIdx.x / p.split : blockIdx.x);
+        if (split) crank = static_cast<int>(cluster_ctarank());
+        tile = item % p.tiles;
+        const int hb = item / p.tiles;
+        h = hb % p.Hq;
+        doc = hb / p.Hq;
+        if (p.causal) tile = p.tiles - 1 - tile;  // heavy causal tiles first
+    } else {
+        tile = p.causal ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
+        h = blockIdx.y;
+        doc = blockIdx.z;
+    }
     const int kvh = h / p.group;
     int q_start, Lq, k_start, Lk;
     if (p.cu_q) {
@@ -437,8 +583,8 @@ __global__ void __launch_bounds__(384, 1)
         Lk = p.Sk;
     }
     const int q0 = tile * 2 * BM;
-    if (q0 >= Lq) return;  // CTA-uniform, before any barrier or TMEM use
-    if (status_has_timeout(p.status, kDevTimeout)) return;
+    if (q0 >= Lq) return;  // CTA-uniform, before any barrier or TMEM use (never in a split cluster)
+    if (!split && status_has_timeout(p.status, kDevTimeout)) return;
     const int diag = Lk - Lq;
     // KV tiles each query tile needs (0 for a tile with no rows)
     auto kv_tiles = [&](int first_row) {
@@ -447,7 +593,17 @@ __global__ void __launch_bounds__(384, 1)
         if (p.causal) kend = min(Lk, min(first_row + BM - 1, Lq - 1) + diag + 1);
         return kend > 0 ? (kend + BN - 1) / BN : 0;
     };
-    const int nA = kv_tiles(q0), nB = kv_tiles(q0 + BM);
+    int nA = kv_tiles(q0), nB = kv_tiles(q0 + BM);
+    // A split item (non-causal, so both tiles see the same keys) gives CTA
+    // `crank` of its cluster KV tiles [j0, j1); loops below count from j0.
+    int j0 = 0;
+    if (split) {
+        const int n = max(nA, nB);
+        j0 = crank * n / p.split;
+        const int j1 = (crank + 1) * n / p.split;
+        nA = nA > 0 ? j1 - j0 : 0;
+        nB = nB > 0 ? j1 - j0 : 0;
+    }
     const int nmax = max(nA, nB);
 
     // ------------------------------------------------------------------ setup
@@ -475,9 +631,8 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
-    // 3 x 128 threads x 168 launched = 2 x 128 x 216 + 128 x 72
     if (warp >= 8) {
-      regs_dec<72>();
+      regs_dec<C::REG_OTHER>();
       if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -496,7 +651,7 @@ __global__ void __launch_bounds__(384, 1)
                     break;
                 }
                 const CUtensorMap* m = (t & 1) ? &tmV : &tmK;
-                const int row = k_start + (t >> 1) * BN;
+                const int row = k_start + (j0 + (t >> 1)) * BN;
                 mbar_arrive_expect_tx(b_kv_full(s), C::KV_BYTES);
                 for (int c = 0; c < NCH; ++c)
                     tma_load_3d(sKV + s * C::KV_BYTES + c * BN * 128, m, b_kv_full(s), c * 64, kvh, row);
@@ -613,8 +768,14 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
         mbar_wait_drain(b_drain, 0);
       }
+      __syncwarp();
+      if (split) {  // the three cluster barriers of split_merge
+          cluster_sync();
+          cluster_sync();
+          cluster_sync();
+      }
     } else {
-        regs_inc<216>();
+        regs_inc<C::REG_SOFTMAX>();
         // ------------------------------------------------------------- softmax
         const int x = warp >> 2;               // 0: tile A, 1: tile B
         const int r = threadIdx.x & 127;       // row within the tile == TMEM lane
@@ -630,7 +791,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int j = 0; j < n_kv; ++j) {
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_s_full(x), j & 1, abort_flag)))) break;
             tc_fence_after();
-            const int kbase = j * BN;
+            const int kbase = (j0 + j) * BN;
             const bool edge = (kbase + BN > Lk) || (p.causal && kbase + BN - 1 > qfirst + diag);
             const int lim = row_lim - kbase;  // columns >= lim are masked (edge tiles only)
             uint32_t sr[BN];
@@ -702,6 +863,11 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_after();
         }
         // ------------------------------------------------------------ epilogue
+        if (split) {
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_drain, 0, abort_flag));  // all MMAs done
+            tc_fence_after();
+            split_merge<D>(smem, sKV, tO, x * BM + r, m, l, n_kv > 0, ok, crank, q0, Lq, q_start, h, doc, p);
+        } else {
         const bool row_valid = ok && row < Lq;
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         const long long orow = static_cast<long long>(q_start + row) * p.Hq + h;
@@ -740,6 +906,7 @@ __global__ void __launch_bounds__(384, 1)
             const long long lrow = p.lse_row_global ? (q_start + row) : row;
             p.lse[doc * p.lse_bstride + h * p.lse_hstride + lrow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
         }
+        }
     }
 
     // --------------------------------------------------------------- teardown
@@ -764,29 +931,128 @@ using Cfg128 = Prefill2Cfg<128, 5>;
 using Cfg192 = PrefillCfg<192, 128, 3>;
 using Cfg256 = PrefillCfg<256, 128, 2>;
 
+// Sets the dynamic shared-memory limit of `kernel` once per device (one flag
+// set per configuration: the kernels of several configurations share a type).
+template <class C, class K>
+static cudaError_t set_smem_attr(K kernel, int bytes) {
+    static bool done[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    return e;
+}
+
 template <class C, class K>
 static cudaError_t launch_kernel(K kernel, int threads, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const PrefillParams& p, int rows_per_cta,
                                  cudaStream_t stream) {
-    static bool attr_done = false;  // the attribute is per function
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    cudaError_t e = set_smem_attr<C>(kernel, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
     dim3 grid((p.max_seqlen_q + rows_per_cta - 1) / rows_per_cta, p.Hq, p.num_docs);
     kernel<<<grid, threads, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
+    return cudaGetLastError();
+}
+
+// Clusters of `c` CTAs of `kernel` that can be resident at once (cached per
+// device and cluster size; 0 if the query fails).
+template <class C, class K>
+static int resident_clusters(K kernel, int c) {
+    static int cache[64][4];
+    static bool have[64][4];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    const int slot = c == 2 ? 0 : c == 4 ? 1 : 2;
+    if (!have[dev][slot]) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = c;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(c);
+        cfg.blockDim = dim3(384);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        cache[dev][slot] = n;
+        have[dev][slot] = true;
+    }
+    return cache[dev][slot];
+}
+
+// Two-tile kernel.  Varlen: 3D grid (tile, head, document).  Dense: a 1D
+// grid of items (tile, head, batch).  When the last wave of a dense
+// non-causal launch would be less than half full, its items go to a second
+// launch in which a cluster of `split` CTAs shares each item along the keys
+// and merges the partial results on chip, so that the wave lasts about
+// 1/split of an item instead of a whole one.
+template <class C, class K>
+static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                   const PrefillParams& p, int num_sms, cudaStream_t stream) {
+    cudaError_t e = set_smem_attr<C>(kernel, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    PrefillParams q = p;
+    q.split = 0;
+    q.item_base = 0;
+    if (p.cu_q) {
+        q.linear = 0;
+        dim3 grid((p.max_seqlen_q + 255) / 256, p.Hq, p.num_docs);
+        kernel<<<grid, 384, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, q);
+        return cudaGetLastError();
+    }
+    q.linear = 1;
+    q.tiles = (p.Sq + 255) / 256;
+    const long long n_items = static_cast<long long>(q.tiles) * p.Hq * p.num_docs;
+    if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const int n_kv = (p.Sk + C::BN - 1) / C::BN;
+    const int tail = num_sms > 0 ? static_cast<int>(n_items % num_sms) : 0;
+    int split = 0;
+    if (!p.causal && tail > 0 && 2 * tail <= num_sms) {
+        for (int c = 8; c >= 2 && !split; c >>= 1)
+            if (tail * c <= num_sms && n_kv >= 4 * c && resident_clusters<C>(kernel, c) >= tail) split = c;
+    }
+    const long long n_full = split ? n_items - tail : n_items;
+    if (n_full > 0) {
+        kernel<<<static_cast<unsigned>(n_full), 384, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, q);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (split) {
+        q.item_base = static_cast<int>(n_full);
+        q.split = split;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = split;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(tail * split);
+        cfg.blockDim = dim3(384);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = stream;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kernel, tmQ, tmK, tmV, q);
+        if (e != cudaSuccess) return e;
+    }
     return cudaGetLastError();
 }
 
 int prefill_block_n(int D) { return (D == 64 || D == 96 || D == 128 || D == 192 || D == 256) ? 128 : 0; }
 
 cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                           const PrefillParams& p, cudaStream_t stream) {
+                           const PrefillParams& p, int num_sms, cudaStream_t stream) {
     switch (D) {
-        case 64: return launch_kernel<Cfg64>(fmha2_fwd_sm103a<Cfg64>, 384, tmQ, tmK, tmV, p, 256, stream);
-        case 96: return launch_kernel<Cfg96>(fmha2_fwd_sm103a<Cfg96>, 384, tmQ, tmK, tmV, p, 256, stream);
-        case 128: return launch_kernel<Cfg128>(fmha2_fwd_sm103a<Cfg128>, 384, tmQ, tmK, tmV, p, 256, stream);
+        case 64: return launch_two_tile<Cfg64>(fmha2_fwd_sm103a<Cfg64>, tmQ, tmK, tmV, p, num_sms, stream);
+        case 96: return launch_two_tile<Cfg96>(fmha2_fwd_sm103a<Cfg96>, tmQ, tmK, tmV, p, num_sms, stream);
+        case 128: return launch_two_tile<Cfg128>(fmha2_fwd_sm103a<Cfg128>, tmQ, tmK, tmV, p, num_sms, stream);
         case 192: return launch_kernel<Cfg192>(fmha_fwd_sm103a<Cfg192>, 192, tmQ, tmK, tmV, p, 128, stream);
         case 256: return launch_kernel<Cfg256>(fmha_fwd_sm103a<Cfg256>, 192, tmQ, tmK, tmV, p, 128, stream);
         default: return cudaErrorInvalidValue;

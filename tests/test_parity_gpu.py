@@ -102,6 +102,34 @@ def test_large_logits_rescale_path():
     assert_close(out, lse, ro, rl, lse_tol=5e-3, what="large logits")  # |lse| ~ 100 here
 
 
+# Dense non-causal launches whose last wave would be under half full give
+# those items to clusters of 2, 4 or 8 CTAs, each taking a share of the keys,
+# which merge their partial softmaxes on chip.  On a 152-SM GB300 the eight
+# items below split 2-, 4- and 8-way by key length (8, 17 and 33 KV tiles).
+
+@pytest.mark.parametrize("D", [64, 96, 128])
+@pytest.mark.parametrize("Sk", [1024, 2100, 4200])
+def test_dense_split_tail_items(D, Sk):
+    (q, k, v, s), out, lse = _dense_case(1, 300, Sk, 4, 2, D, False, seed=D * 3 + Sk)
+    ro, rl = oracle.attention_dense(q, k, v, s, False)
+    assert_close(out, lse, ro, rl, what=f"split tail D={D} Sk={Sk}")
+
+
+def test_dense_split_after_full_waves():
+    """160 items: one full wave of 152, then 8 items split 2-way."""
+    (q, k, v, s), out, lse = _dense_case(1, 256, 1100, 160, 8, 64, False, seed=77)
+    ro, rl = oracle.attention_dense(q, k, v, s, False)
+    assert_close(out, lse, ro, rl, what="full wave + split tail")
+
+
+def test_dense_split_bf16_output():
+    (q, k, v, s), out, lse = _dense_case(2, 256, 2048, 4, 4, 128, False, seed=78, out_dtype=torch.bfloat16)
+    ro, rl = oracle.attention_dense(q, k, v, s, False)
+    err = np.abs(to_np(out) - ro)
+    assert np.all(err <= OUT_TOL + bf16_half_ulp(ro))
+    assert max_err(to_np(lse), rl) <= LSE_TOL
+
+
 # ------------------------------------------------------------------ varlen
 
 def test_tiny_varlen_config():
