@@ -39,6 +39,7 @@ SIGNATURES = {
     "attn_fwd_paged": (_I, [_P, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _Z, _P, _P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_fwd_paged_noalloc": (_I, [_P, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _P]),
+    "attn_fwd_dense_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
 }
 
 _lib = None
@@ -114,6 +115,15 @@ def attn_fwd_dense(q, k, v, softmax_scale=None, causal=False, out=None, lse=None
                                        _stream_handle(stream))
     _check("attn_fwd_dense", st)
     return out, lse
+
+
+def attn_fwd_dense_plan(B, Sq, Sk, Hq, Hkv, D, causal=False):
+    """(launches, split) attn_fwd_dense makes for these sizes on the current device."""
+    n, sp = ctypes.c_int(0), ctypes.c_int(0)
+    st = load_library().attn_fwd_dense_plan(B, Sq, Sk, Hq, Hkv, D, int(bool(causal)), ctypes.byref(n),
+                                            ctypes.byref(sp))
+    _check("attn_fwd_dense_plan", st)
+    return n.value, sp.value
 
 
 def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, softmax_scale=None,

@@ -161,6 +161,35 @@ gbattn_status attn_fwd_dense(const void* q, const void* k, const void* v, int B,
                        static_cast<cudaStream_t>(stream));
 }
 
+gbattn_status attn_fwd_dense_plan(int B, int Sq, int Sk, int Hq, int Hkv, int D, int causal, int* launches,
+                                  int* split) {
+    if (!launches || !split) return GBATTN_ERR_INVALID_ARG;
+    *launches = 0;
+    *split = 0;
+    if (B < 0 || Sq < 0 || Sk < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
+    if (!head_size_ok(D)) return GBATTN_ERR_UNSUPPORTED;
+    if (B > 65535) return GBATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Sq == 0) return GBATTN_OK;
+    DeviceInfo di;
+    gbattn_status s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    PrefillParams p{};
+    p.num_docs = B;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.max_seqlen_q = Sq;
+    p.max_seqlen_k = Sk;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.group = Hq / Hkv;
+    p.causal = causal ? 1 : 0;
+    gbattn::PrefillPlan pl;
+    if (gbattn::prefill_plan(D, p, di.sms, &pl) != cudaSuccess) return GBATTN_ERR_CUDA;
+    *launches = pl.launches;
+    *split = pl.split;
+    return GBATTN_OK;
+}
+
 gbattn_status attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
                               const int32_t* cu_seqlens_k, int num_docs, int Tq, int Tk, int max_seqlen_q,
                               int max_seqlen_k, int Hq, int Hkv, int D, float softmax_scale, int causal, void* out,

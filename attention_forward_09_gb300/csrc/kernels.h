@@ -48,6 +48,17 @@ cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK
                            const CUtensorMap& tmV, const PrefillParams& p, int num_sms, cudaStream_t stream);
 int prefill_block_n(int D);  // keys per KV tile for head size D
 
+// How launch_prefill runs these sizes: kernel launches, items (CTAs of work),
+// items launched whole, and the key split of the rest (0: none).
+struct PrefillPlan {
+    int launches;
+    int split;
+    int tiles;
+    long long n_items;
+    long long n_full;
+};
+cudaError_t prefill_plan(int D, const PrefillParams& p, int num_sms, PrefillPlan* plan);
+
 struct PagedParams {
     const void* q;          // [S, Hq, D] bf16
     const int32_t* block_table;

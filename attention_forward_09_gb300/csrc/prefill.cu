@@ -988,16 +988,43 @@ static int resident_clusters(K kernel, int c) {
     return cache[dev][slot];
 }
 
-// Two-tile kernel.  Varlen: 3D grid (tile, head, document).  Dense: a 1D
-// grid of items (tile, head, batch).  When the last wave of a dense
-// non-causal launch would be less than half full, its items go to a second
-// launch in which a cluster of `split` CTAs shares each item along the keys
-// and merges the partial results on chip, so that the wave lasts about
-// 1/split of an item instead of a whole one.
+// Launch plan of the two-tile kernel.  Varlen: one launch on a 3D grid
+// (tile, head, document).  Dense: a 1D grid of items (tile, head, batch).
+// When the last wave of a dense non-causal launch would be less than half
+// full, its items go to a second launch in which a cluster of `split` CTAs
+// shares each item along the keys and merges the partial results on chip,
+// so that the wave lasts about 1/split of an item instead of a whole one.
+template <class C, class K>
+static cudaError_t plan_two_tile(K kernel, const PrefillParams& p, int num_sms, PrefillPlan* pl) {
+    *pl = PrefillPlan{};
+    if (p.cu_q) {
+        pl->n_items = pl->n_full = static_cast<long long>((p.max_seqlen_q + 255) / 256) * p.Hq * p.num_docs;
+        pl->launches = pl->n_items > 0 ? 1 : 0;
+        return cudaSuccess;
+    }
+    cudaError_t e = set_smem_attr<C>(kernel, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    pl->tiles = (p.Sq + 255) / 256;
+    pl->n_items = static_cast<long long>(pl->tiles) * p.Hq * p.num_docs;
+    if (pl->n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const int n_kv = (p.Sk + C::BN - 1) / C::BN;
+    const int tail = num_sms > 0 ? static_cast<int>(pl->n_items % num_sms) : 0;
+    if (!p.causal && tail > 0 && 2 * tail <= num_sms) {
+        for (int c = 8; c >= 2 && !pl->split; c >>= 1)
+            if (tail * c <= num_sms && n_kv >= 4 * c && resident_clusters<C>(kernel, c) >= tail) pl->split = c;
+    }
+    pl->n_full = pl->split ? pl->n_items - tail : pl->n_items;
+    pl->launches = (pl->n_full > 0 ? 1 : 0) + (pl->split ? 1 : 0);
+    return cudaSuccess;
+}
+
 template <class C, class K>
 static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                    const PrefillParams& p, int num_sms, cudaStream_t stream) {
-    cudaError_t e = set_smem_attr<C>(kernel, C::SMEM_BYTES);
+    PrefillPlan pl;
+    cudaError_t e = plan_two_tile<C>(kernel, p, num_sms, &pl);
+    if (e != cudaSuccess) return e;
+    e = set_smem_attr<C>(kernel, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     PrefillParams q = p;
     q.split = 0;
@@ -1009,31 +1036,21 @@ static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUten
         return cudaGetLastError();
     }
     q.linear = 1;
-    q.tiles = (p.Sq + 255) / 256;
-    const long long n_items = static_cast<long long>(q.tiles) * p.Hq * p.num_docs;
-    if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const int n_kv = (p.Sk + C::BN - 1) / C::BN;
-    const int tail = num_sms > 0 ? static_cast<int>(n_items % num_sms) : 0;
-    int split = 0;
-    if (!p.causal && tail > 0 && 2 * tail <= num_sms) {
-        for (int c = 8; c >= 2 && !split; c >>= 1)
-            if (tail * c <= num_sms && n_kv >= 4 * c && resident_clusters<C>(kernel, c) >= tail) split = c;
-    }
-    const long long n_full = split ? n_items - tail : n_items;
-    if (n_full > 0) {
-        kernel<<<static_cast<unsigned>(n_full), 384, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, q);
+    q.tiles = pl.tiles;
+    if (pl.n_full > 0) {
+        kernel<<<static_cast<unsigned>(pl.n_full), 384, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, q);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if (split) {
-        q.item_base = static_cast<int>(n_full);
-        q.split = split;
+    if (pl.split) {
+        q.item_base = static_cast<int>(pl.n_full);
+        q.split = pl.split;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute at[1];
         at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = split;
+        at[0].val.clusterDim.x = pl.split;
         at[0].val.clusterDim.y = 1;
         at[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(tail * split);
+        cfg.gridDim = dim3(static_cast<unsigned>((pl.n_items - pl.n_full) * pl.split));
         cfg.blockDim = dim3(384);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = stream;
@@ -1055,6 +1072,22 @@ cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK
         case 128: return launch_two_tile<Cfg128>(fmha2_fwd_sm103a<Cfg128>, tmQ, tmK, tmV, p, num_sms, stream);
         case 192: return launch_kernel<Cfg192>(fmha_fwd_sm103a<Cfg192>, 192, tmQ, tmK, tmV, p, 128, stream);
         case 256: return launch_kernel<Cfg256>(fmha_fwd_sm103a<Cfg256>, 192, tmQ, tmK, tmV, p, 128, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t prefill_plan(int D, const PrefillParams& p, int num_sms, PrefillPlan* pl) {
+    switch (D) {
+        case 64: return plan_two_tile<Cfg64>(fmha2_fwd_sm103a<Cfg64>, p, num_sms, pl);
+        case 96: return plan_two_tile<Cfg96>(fmha2_fwd_sm103a<Cfg96>, p, num_sms, pl);
+        case 128: return plan_two_tile<Cfg128>(fmha2_fwd_sm103a<Cfg128>, p, num_sms, pl);
+        case 192:
+        case 256: {
+            *pl = PrefillPlan{};
+            pl->n_items = pl->n_full = static_cast<long long>((p.max_seqlen_q + 127) / 128) * p.Hq * p.num_docs;
+            pl->launches = pl->n_items > 0 ? 1 : 0;
+            return cudaSuccess;
+        }
         default: return cudaErrorInvalidValue;
     }
 }

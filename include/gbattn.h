@@ -90,6 +90,21 @@ gbattn_status attn_fwd_dense(const void* q, const void* k, const void* v,
                              uint32_t* dev_status, void* stream);
 
 /*
+ * attn_fwd_dense_plan -- how attn_fwd_dense runs these sizes on the current
+ * device, for launch accounting and tests; it launches and allocates nothing
+ * and has no counterpart on the pages.
+ *   launches  out: kernel launches one attn_fwd_dense call makes (0 when
+ *             B or Sq is 0)
+ *   split     out: 0, or 2, 4 or 8 when the items of a partly filled last
+ *             wave (non-causal, head size <= 128) are each shared by a
+ *             cluster of that many CTAs along the keys
+ * Errors: GBATTN_ERR_INVALID_ARG (null outputs, bad sizes),
+ * GBATTN_ERR_UNSUPPORTED (head size), GBATTN_ERR_DEVICE / GBATTN_ERR_CUDA.
+ */
+gbattn_status attn_fwd_dense_plan(int B, int Sq, int Sk, int Hq, int Hkv, int D, int causal, int* launches,
+                                  int* split);
+
+/*
  * attn_fwd_varlen -- packed documents (FlashAttentionImpl._forward_varlen_packed,
  * flash_attn_varlen_func with cu_seqlens_q/k and max_seqlen_q/k).
  *

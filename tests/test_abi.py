@@ -32,7 +32,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(
         ["attn_fwd_dense", "attn_fwd_varlen", "attn_fwd_paged", "attn_fwd_paged_workspace_size",
-         "attn_status_string", "attn_fwd_paged_noalloc"])
+         "attn_status_string", "attn_fwd_paged_noalloc", "attn_fwd_dense_plan"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -130,3 +130,13 @@ def test_noalloc_refuses_sizes_beyond_its_scratch_on_the_host(lib):
     st = lib.attn_fwd_paged_noalloc(P, P, 1 << 20, 128, P, L // 128, P, S, L, Hq, Hkv, D, 0.1, 1, P, 1, None,
                                     None, None)
     assert st == 7
+
+
+def test_dense_plan_validates_before_touching_a_device(lib):
+    n, sp = ctypes.c_int(7), ctypes.c_int(7)
+    assert lib.attn_fwd_dense_plan(1, 8, 8, 4, 3, 128, 0, ctypes.byref(n), ctypes.byref(sp)) == 1  # Hq % Hkv
+    assert (n.value, sp.value) == (0, 0)
+    assert lib.attn_fwd_dense_plan(1, 8, 8, 4, 2, 80, 0, ctypes.byref(n), ctypes.byref(sp)) == 2  # head size
+    assert lib.attn_fwd_dense_plan(1, 8, 8, 4, 2, 128, 0, None, ctypes.byref(sp)) == 1
+    assert lib.attn_fwd_dense_plan(0, 8, 8, 4, 2, 128, 0, ctypes.byref(n), ctypes.byref(sp)) == 0  # nothing to do
+    assert (n.value, sp.value) == (0, 0)

@@ -110,6 +110,9 @@ def test_large_logits_rescale_path():
 @pytest.mark.parametrize("D", [64, 96, 128])
 @pytest.mark.parametrize("Sk", [1024, 2100, 4200])
 def test_dense_split_tail_items(D, Sk):
+    launches, split = gb.attn_fwd_dense_plan(1, 300, Sk, 4, 2, D, False)
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert (launches, split) == (1, {1024: 2, 2100: 4, 4200: 8}[Sk])
     (q, k, v, s), out, lse = _dense_case(1, 300, Sk, 4, 2, D, False, seed=D * 3 + Sk)
     ro, rl = oracle.attention_dense(q, k, v, s, False)
     assert_close(out, lse, ro, rl, what=f"split tail D={D} Sk={Sk}")
@@ -117,6 +120,8 @@ def test_dense_split_tail_items(D, Sk):
 
 def test_dense_split_after_full_waves():
     """160 items: one full wave of 152, then 8 items split 2-way."""
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert gb.attn_fwd_dense_plan(1, 256, 1100, 160, 8, 64, False) == (2, 2)
     (q, k, v, s), out, lse = _dense_case(1, 256, 1100, 160, 8, 64, False, seed=77)
     ro, rl = oracle.attention_dense(q, k, v, s, False)
     assert_close(out, lse, ro, rl, what="full wave + split tail")
