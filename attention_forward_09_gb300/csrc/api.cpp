@@ -64,17 +64,21 @@ gbattn_status device_info(DeviceInfo* out) {
     return out->ok ? GBATTN_OK : GBATTN_ERR_DEVICE;
 }
 
-// bf16 tensor [rows, heads, D] (D contiguous) as a 3-D TMA map with box
-// {64, 1, box_rows} and 128-byte swizzle; out-of-range elements read as zero.
-bool encode_rows_heads_d(CUtensorMap* m, const void* base, long long rows, int heads, int d, int box_rows) {
+// Tensor [rows, heads, D] (D contiguous; bf16, or fp32 when f32) as a 3-D
+// TMA map with box {128 bytes of D, 1, box_rows} and 128-byte swizzle;
+// loads read out-of-range elements as zero, stores skip them.
+bool encode_rows_heads_d(CUtensorMap* m, const void* base, long long rows, int heads, int d, int box_rows,
+                         bool f32 = false) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
+    const cuuint64_t es = f32 ? 4 : 2;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                           static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(heads) * d * 2};
-    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(heads) * d * es};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 1, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -98,16 +102,17 @@ gbattn_status run_prefill(const void* q, const void* k, const void* v, long long
     DeviceInfo di;
     gbattn_status s = device_info(&di);
     if (s != GBATTN_OK) return s;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const int bn = gbattn::prefill_block_n(D);
     // With no keys at all no KV tile is ever loaded; point the K/V maps at q
     // so that they are still well-formed.
     const bool no_keys = Tk == 0;
     if (!encode_rows_heads_d(&tq, q, Tq, p.Hq, D, 128) ||
         !encode_rows_heads_d(&tk, no_keys ? q : k, no_keys ? Tq : Tk, no_keys ? p.Hq : p.Hkv, D, bn) ||
-        !encode_rows_heads_d(&tv, no_keys ? q : v, no_keys ? Tq : Tk, no_keys ? p.Hq : p.Hkv, D, bn))
+        !encode_rows_heads_d(&tv, no_keys ? q : v, no_keys ? Tq : Tk, no_keys ? p.Hq : p.Hkv, D, bn) ||
+        !encode_rows_heads_d(&to, p.out, Tq, p.Hq, D, 128, p.out_f32 != 0))
         return GBATTN_ERR_CUDA;
-    return gbattn::launch_prefill(D, tq, tk, tv, p, di.sms, st) == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+    return gbattn::launch_prefill(D, tq, tk, tv, to, p, di.sms, st) == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 
 }  // namespace

@@ -41,11 +41,11 @@ struct PrefillParams {
     int split;      // > 1: each item is shared by a cluster of `split` CTAs, one key range each
 };
 
-// Tensor maps are built by the host (see api.cpp) over q [Tq, Hq, D] and
-// k / v [Tk, Hkv, D]; box {64, 1, rows}, 128-byte swizzle.
-// The grid is sized from p.max_seqlen_q (128 or 256 query rows per CTA).
-cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                           const CUtensorMap& tmV, const PrefillParams& p, int num_sms, cudaStream_t stream);
+// Tensor maps are built by the host (api.cpp) over q [Tq, Hq, D] and
+// k / v [Tk, Hkv, D] (box {64, 1, rows}) and over out [Tq, Hq, D] (box
+// {128 bytes of columns, 1, 128}), all with 128-byte swizzle.
+cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                           const CUtensorMap& tmO, const PrefillParams& p, int num_sms, cudaStream_t stream);
 int prefill_block_n(int D);  // keys per KV tile for head size D
 
 // How launch_prefill runs these sizes: kernel launches, items (CTAs of work),

@@ -418,6 +418,7 @@ struct Prefill2Cfg {
     static_assert(2 * BN + 2 * D <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(2 * BM * D * 4 <= STAGES * KV_BYTES && 2 * BM * 8 <= 2 * QT_BYTES, "split-merge staging");
+    static_assert(KV_BYTES == NCH * BM * 128 && 2 * ((D + 31) / 32) + NCH <= STAGES * NCH, "output staging slots");
 };
 
 // Merge of an item split along the keys over a cluster of p.split CTAs (the
@@ -527,7 +528,8 @@ __device__ __forceinline__ void split_merge(uint8_t* smem, uint32_t sO, uint32_t
 template <class C>
 __global__ void __launch_bounds__(384, 1)
     fmha2_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                     const PrefillParams p) {
     constexpr int D = C::D, BN = C::BN, STAGES = C::STAGES, BM = C::BM, NCH = C::NCH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -867,6 +869,72 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_drain, 0, abort_flag));  // all MMAs done
             tc_fence_after();
             split_merge<D>(smem, sKV, tO, x * BM + r, m, l, n_kv > 0, ok, crank, q0, Lq, q_start, h, doc, p);
+        } else if (qfirst + BM <= Lq && (x == 1 || nA >= nB)) {
+            // A tile wholly inside its document leaves through shared memory:
+            // its rows are staged in the TMA 128-byte-swizzled box layout
+            // (128 rows x 128 bytes per 16 KB box) in slots of the K/V area
+            // and written by tiled TMA stores.  Once PV_X(last) is complete
+            // the only MMA that may still read the K/V area is PV_B(last),
+            // when tile A finishes with nA == nB: it reads V_{n-1}, whose
+            // stage no slot uses.  (Tile A with nA < nB, causal, stores
+            // directly instead, while tile B computes on.)
+            const bool f32 = p.out_f32 != 0;
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const int boxes = f32 ? D / 32 : (D + 63) / 64, cols = f32 ? 32 : 64;  // 128-byte boxes per row
+            const int v0 = nmax > 0 ? ((2 * nmax - 1) % STAGES) * NCH : STAGES * NCH;  // V_{n-1}'s first slot
+            auto slot_addr = [&](int b) {  // box b of this tile: the (x * boxes + b)-th slot outside V_{n-1}
+                const int i = x * boxes + b;
+                return sKV + static_cast<uint32_t>(i < v0 ? i : i + NCH) * (BM * 128);
+            };
+            const int sw = r & 7;
+            auto load_scaled = [&](int c, uint32_t (&o)[32]) {
+                if (n_kv > 0 && ok) {
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
+            };
+            if (f32) {  // 32 columns = one 128-byte box row, 8 units of 16 bytes
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    load_scaled(c, o);
+                    const uint32_t rb = slot_addr(c) + r * 128;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        st_shared_v4(rb + ((k ^ sw) << 4), o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                }
+            } else {    // 32 columns = half a box row
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    load_scaled(c, o);
+                    const uint32_t rb = slot_addr(c >> 1) + r * 128;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        st_shared_v4(rb + ((((c & 1) * 4 + k) ^ sw) << 4),
+                                     pack_bf16x2(__uint_as_float(o[8 * k]), __uint_as_float(o[8 * k + 1])),
+                                     pack_bf16x2(__uint_as_float(o[8 * k + 2]), __uint_as_float(o[8 * k + 3])),
+                                     pack_bf16x2(__uint_as_float(o[8 * k + 4]), __uint_as_float(o[8 * k + 5])),
+                                     pack_bf16x2(__uint_as_float(o[8 * k + 6]), __uint_as_float(o[8 * k + 7])));
+                }
+            }
+            fence_proxy_async_smem();  // generic-proxy writes -> the TMA engine
+            named_bar_sync(1 + x, 128);
+            if (r == 0) {
+                for (int b = 0; b < boxes; ++b) tma_store_3d(&tmO, slot_addr(b), b * cols, h, q_start + qfirst);
+                bulk_commit();
+                bulk_wait_read0();  // the staging area must outlive the reads
+            }
+            if (ok && p.lse) {
+                const long long lrow = p.lse_row_global ? (q_start + row) : row;
+                p.lse[doc * p.lse_bstride + h * p.lse_hstride + lrow] =
+                    l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+            }
         } else {
         const bool row_valid = ok && row < Lq;
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -1020,7 +1088,7 @@ static cudaError_t plan_two_tile(K kernel, const PrefillParams& p, int num_sms, 
 
 template <class C, class K>
 static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                   const PrefillParams& p, int num_sms, cudaStream_t stream) {
+                                   const CUtensorMap& tmO, const PrefillParams& p, int num_sms, cudaStream_t stream) {
     PrefillPlan pl;
     cudaError_t e = plan_two_tile<C>(kernel, p, num_sms, &pl);
     if (e != cudaSuccess) return e;
@@ -1032,13 +1100,13 @@ static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUten
     if (p.cu_q) {
         q.linear = 0;
         dim3 grid((p.max_seqlen_q + 255) / 256, p.Hq, p.num_docs);
-        kernel<<<grid, 384, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, q);
+        kernel<<<grid, 384, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, q);
         return cudaGetLastError();
     }
     q.linear = 1;
     q.tiles = pl.tiles;
     if (pl.n_full > 0) {
-        kernel<<<static_cast<unsigned>(pl.n_full), 384, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, q);
+        kernel<<<static_cast<unsigned>(pl.n_full), 384, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, q);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (pl.split) {
@@ -1056,7 +1124,7 @@ static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUten
         cfg.stream = stream;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kernel, tmQ, tmK, tmV, q);
+        e = cudaLaunchKernelEx(&cfg, kernel, tmQ, tmK, tmV, tmO, q);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
@@ -1065,11 +1133,11 @@ static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUten
 int prefill_block_n(int D) { return (D == 64 || D == 96 || D == 128 || D == 192 || D == 256) ? 128 : 0; }
 
 cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                           const PrefillParams& p, int num_sms, cudaStream_t stream) {
+                           const CUtensorMap& tmO, const PrefillParams& p, int num_sms, cudaStream_t stream) {
     switch (D) {
-        case 64: return launch_two_tile<Cfg64>(fmha2_fwd_sm103a<Cfg64>, tmQ, tmK, tmV, p, num_sms, stream);
-        case 96: return launch_two_tile<Cfg96>(fmha2_fwd_sm103a<Cfg96>, tmQ, tmK, tmV, p, num_sms, stream);
-        case 128: return launch_two_tile<Cfg128>(fmha2_fwd_sm103a<Cfg128>, tmQ, tmK, tmV, p, num_sms, stream);
+        case 64: return launch_two_tile<Cfg64>(fmha2_fwd_sm103a<Cfg64>, tmQ, tmK, tmV, tmO, p, num_sms, stream);
+        case 96: return launch_two_tile<Cfg96>(fmha2_fwd_sm103a<Cfg96>, tmQ, tmK, tmV, tmO, p, num_sms, stream);
+        case 128: return launch_two_tile<Cfg128>(fmha2_fwd_sm103a<Cfg128>, tmQ, tmK, tmV, tmO, p, num_sms, stream);
         case 192: return launch_kernel<Cfg192>(fmha_fwd_sm103a<Cfg192>, 192, tmQ, tmK, tmV, p, 128, stream);
         case 256: return launch_kernel<Cfg256>(fmha_fwd_sm103a<Cfg256>, 192, tmQ, tmK, tmV, p, 128, stream);
         default: return cudaErrorInvalidValue;
