@@ -406,6 +406,9 @@ struct Prefill2Cfg {
     static constexpr int QT_BYTES = NCH * BM * 128;  // one Q tile
     static constexpr int KV_BYTES = NCH * BN * 128;
     static constexpr int NUM_BARS = 2 * STAGES + 8;
+    // Full output tiles of D >= 96 leave through TMA stores; D = 64 ones
+    // (256 bytes of fp32 per row) by direct stores, which measured faster.
+    static constexpr bool TMA_OUT = D >= 96;
     static constexpr int SMEM_BYTES = 1024 + 2 * QT_BYTES + STAGES * KV_BYTES + NUM_BARS * 8 + 16;
     static constexpr int TMEM_S = 0;          // S_X at X * BN
     static constexpr int TMEM_O = 2 * BN;     // O_X at TMEM_O + X * D
@@ -869,7 +872,7 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_drain, 0, abort_flag));  // all MMAs done
             tc_fence_after();
             split_merge<D>(smem, sKV, tO, x * BM + r, m, l, n_kv > 0, ok, crank, q0, Lq, q_start, h, doc, p);
-        } else if (qfirst + BM <= Lq && (x == 1 || nA >= nB)) {
+        } else if (C::TMA_OUT && qfirst + BM <= Lq && (x == 1 || nA >= nB)) {
             // A tile wholly inside its document leaves through shared memory:
             // its rows are staged in the TMA 128-byte-swizzled box layout
             // (128 rows x 128 bytes per 16 KB box) in slots of the K/V area

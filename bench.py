@@ -18,6 +18,7 @@ same workload on this machine's host cores (there is no other reference
 implementation of this path).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--only all|prefill|decode] [--prefill WORKLOAD] [--no-cpu]
 """
 
 from __future__ import annotations
@@ -41,6 +42,16 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 METRIC = "attn fwd TFLOP/s & % bf16 TC peak; paged-decode HBM GB/s & % of HBM peak"
+# Prefill workloads the step can run (--prefill); the default is the headline one.
+PREFILL_WORKLOADS = {
+    "dit_self": workloads.dit_self,
+    "cross_attn": workloads.cross_attn,
+    "varlen_causal_gqa": workloads.varlen_causal_gqa,
+    "self_d64": lambda: workloads.head_sweep(64),
+    "self_d96": lambda: workloads.head_sweep(96),
+    "self_d192": lambda: workloads.head_sweep(192),
+    "self_d256": lambda: workloads.head_sweep(256),
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -53,14 +64,15 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def traffic_for(kernel: str, source_file: str):
-    """DRAM bytes per launch from a committed ncu summary, only while the
-    kernel source still matches the one the counters were taken on."""
+def traffic_for(key: str, source_file: str):
+    """DRAM bytes per call from a committed ncu summary (key "kernel@workload"),
+    only while the kernel source still matches the one the counters were
+    taken on."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        d = json.load(f).get(kernel)
+        d = json.load(f).get(key)
     if not d:
         return None
     with open(os.path.join(ROOT, "attention_forward_09_gb300", "csrc", source_file), "rb") as f:
@@ -256,12 +268,21 @@ def run_ours(args, world, rank, local):
 
     # ---- inputs (CPU, seeded), then resident in HBM
     do_pre, do_dec = args.only in ("all", "prefill"), args.only in ("all", "decode")
-    wp = workloads.dit_self()
-    q, k, v = wp.make()
+    wp = PREFILL_WORKLOADS[args.prefill]()
+    varlen = isinstance(wp, workloads.Varlen)
+    if varlen:
+        q, k, v, cq, ck = wp.make()
+    else:
+        q, k, v = wp.make()
     if do_pre:
         qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-        outd = torch.empty(wp.B, wp.Sq, wp.Hq, wp.D, dtype=torch.float32, device=dev)
-        lsed = torch.empty(wp.B, wp.Hq, wp.Sq, dtype=torch.float32, device=dev)
+        if varlen:
+            cqd, ckd = cq.to(dev), ck.to(dev)
+            outd = torch.empty(wp.Tq, wp.Hq, wp.D, dtype=torch.float32, device=dev)
+            lsed = torch.empty(wp.Hq, wp.Tq, dtype=torch.float32, device=dev)
+        else:
+            outd = torch.empty(wp.B, wp.Sq, wp.Hq, wp.D, dtype=torch.float32, device=dev)
+            lsed = torch.empty(wp.B, wp.Hq, wp.Sq, dtype=torch.float32, device=dev)
     wd = workloads.paged_decode()
     if args.decode_seqs:
         wd = workloads.Paged(wd.name + f"_first{args.decode_seqs}", wd.seq_lens[:args.decode_seqs], wd.Hq, wd.Hkv,
@@ -278,10 +299,18 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    pre_launches = gb.attn_fwd_dense_plan(wp.B, wp.Sq, wp.Sk, wp.Hq, wp.Hkv, wp.D, wp.causal)[0] if do_pre else 0
+    if not do_pre:
+        pre_launches = 0
+    elif varlen:
+        pre_launches = 1
+    else:
+        pre_launches = gb.attn_fwd_dense_plan(wp.B, wp.Sq, wp.Sk, wp.Hq, wp.Hkv, wp.D, wp.causal)[0]
 
     def prefill():
-        if do_pre:
+        if do_pre and varlen:
+            gb.attn_fwd_varlen(qd, kd, vd, cqd, ckd, max(wp.lens_q), max(wp.lens_k), wp.scale, wp.causal, out=outd,
+                               lse=lsed, dev_status=status, stream=stream)
+        elif do_pre:
             gb.attn_fwd_dense(qd, kd, vd, wp.scale, wp.causal, out=outd, lse=lsed, dev_status=status, stream=stream)
 
     def decode():
@@ -333,6 +362,8 @@ def run_ours(args, world, rank, local):
     e2e = None
     if do_pre:
         hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        if varlen:  # the cu_seqlens travel too
+            hcq, hck = cq.pin_memory(), ck.pin_memory()
         hout = torch.empty(outd.shape, dtype=torch.float32).pin_memory()
         hlse = torch.empty(lsed.shape, dtype=torch.float32).pin_memory()
         e2e_steps = max(3, min(args.steps, 20))
@@ -344,13 +375,16 @@ def run_ours(args, world, rank, local):
             qd.copy_(hq, non_blocking=True)
             kd.copy_(hk, non_blocking=True)
             vd.copy_(hv, non_blocking=True)
+            if varlen:
+                cqd.copy_(hcq, non_blocking=True)
+                ckd.copy_(hck, non_blocking=True)
             prefill()
             hout.copy_(outd, non_blocking=True)
             hlse.copy_(lsed, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
-        h2d = (q.numel() + k.numel() + v.numel()) * 2
+        h2d = (q.numel() + k.numel() + v.numel()) * 2 + (8 * (len(wp.lens_q) + 1) if varlen else 0)
         d2h = hout.numel() * 4 + hlse.numel() * 4
         e2e = {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
@@ -358,7 +392,7 @@ def run_ours(args, world, rank, local):
     # ---- oracle on the host cores (rank 0, N=1 only)
     cpu, cpu_dec = None, None
     if world == 1 and not args.no_cpu:
-        if do_pre:
+        if do_pre and not varlen:
             tf, desc, _ = oracle_prefill_sample(wp, 10.0, (q, k, v))
             cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle", "sample": desc}
         if do_dec:
@@ -367,6 +401,7 @@ def run_ours(args, world, rank, local):
 
     if rank != 0:
         return
+    pre_kernel = (f"fmha2_fwd_sm103a<Prefill2Cfg<{wp.D}>>" if wp.D <= 128 else f"fmha_fwd_sm103a<PrefillCfg<{wp.D}>>")
     line = {
         "metric": METRIC,
         "value": value,
@@ -382,8 +417,11 @@ def run_ours(args, world, rank, local):
         "data": "synthetic",
         "config": {
             "workload": f"{wp.name} + {wd.name}",
-            "prefill": {"B": wp.B, "seq_len": wp.Sq, "heads": wp.Hq, "kv_heads": wp.Hkv, "head_dim": wp.D,
-                        "causal": wp.causal, "out_dtype": "f32", "lse": True},
+            "prefill": ({"docs": len(wp.lens_q), "tokens": wp.Tq, "max_doc": max(wp.lens_q), "heads": wp.Hq,
+                         "kv_heads": wp.Hkv, "head_dim": wp.D, "causal": wp.causal, "out_dtype": "f32", "lse": True}
+                        if varlen else
+                        {"B": wp.B, "seq_len": wp.Sq, "kv_len": wp.Sk, "heads": wp.Hq, "kv_heads": wp.Hkv,
+                         "head_dim": wp.D, "causal": wp.causal, "out_dtype": "f32", "lse": True}),
             "decode": {"num_seqs": len(wd.seq_lens), "context_tokens": wd.context_tokens(),
                        "max_seq_len": max_len, "heads": wd.Hq, "kv_heads": wd.Hkv, "head_dim": wd.D,
                        "block_size": 128, "num_blocks": wd.num_blocks},
@@ -392,10 +430,10 @@ def run_ours(args, world, rank, local):
             "only": args.only,
         },
         "roofline": {
-            "bound": "tensor", "kernel": "fmha2_fwd_sm103a<Prefill2Cfg<128,5>>", "launches_per_call": pre_launches,
+            "bound": "tensor", "kernel": pre_kernel, "launches_per_call": pre_launches,
             "achieved": tflops_rank, "peak": peak_tf,
             "unit": "TFLOP/s", "frac": tflops_rank / peak_tf if do_pre else None, "peak_kind": f"{peak_kind} bf16 burst",
-            "traffic": traffic_for("fmha2_fwd_sm103a", "prefill.cu"),
+            "traffic": traffic_for(f"{pre_kernel.split('<')[0]}@{wp.name}", "prefill.cu"),
             "flops_per_launch": flops, "launch_ms": pre_avg,
         },
         "paged_decode": {
@@ -403,7 +441,7 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "kernel": "paged_schedule + paged_decode_sm103a + paged_combine", "achieved": dec_gbs_rank,
                          "peak": peak_bw, "unit": "GB/s", "frac": dec_gbs_rank / peak_bw if do_dec else None,
                          "peak_kind": f"{peak_kind} HBM copy", "bytes_per_call": dec_bytes,
-                         "traffic": traffic_for("paged_decode_sm103a", "decode.cu")},
+                         "traffic": traffic_for(f"paged_decode_sm103a@{wd.name}", "decode.cu")},
             "cpu_baseline": cpu_dec,
         },
         "cpu_baseline": cpu,
@@ -422,6 +460,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--prefill", choices=sorted(PREFILL_WORKLOADS), default="dit_self",
+                    help="prefill workload of the step (default: the headline DiT self-attention)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
                     help="run one part of the step (profiling captures); the default line needs 'all'")
