@@ -548,12 +548,14 @@ int paged_slice_rows(int D) { return D <= 128 ? 128 : 64; }
 
 template <class C>
 static cudaError_t launch_paged_cfg(const CUtensorMap& tm, const PagedParams& p, int num_sms, cudaStream_t st) {
-    static bool attr_done = false;
-    if (!attr_done) {
+    static bool attr_done[64];  // the attribute is per function and device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
         cudaError_t e = cudaFuncSetAttribute(paged_decode_sm103a<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_done = true;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     const int n_hgroups = p.Hkv * (p.group / p.heads_per_cta);
     const long long n_items = static_cast<long long>(p.num_seqs) * n_hgroups * p.max_splits;

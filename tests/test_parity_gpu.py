@@ -102,6 +102,33 @@ def test_large_logits_rescale_path():
     assert_close(out, lse, ro, rl, lse_tol=5e-3, what="large logits")  # |lse| ~ 100 here
 
 
+# Query tiles wholly inside their document (D >= 96) leave through shared
+# memory and TMA tiled stores; at D = 96 a bf16 row is one and a half
+# 128-byte boxes, so the second box is half outside the tensor and clipped.
+# Causal: tile A, with fewer KV tiles than tile B, stores directly.
+
+@pytest.mark.parametrize("D", [96, 128])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_dense_tma_store_epilogue(D, out_dtype, causal):
+    g = torch.Generator().manual_seed(D + 7 * causal)
+    q, k, v = (workloads.randn_bf16(g, 2, n, 2, D) for n in (512, 300, 300))
+    s = 1.0 / math.sqrt(D)
+    out = torch.full((2, 512, 2, D), float("nan"), dtype=out_dtype, device=dev())  # unwritten stays NaN
+    st = status_word()
+    out, lse = gb.attn_fwd_dense(q.to(dev()), k.to(dev()), v.to(dev()), s, causal, out=out, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ro, rl = oracle.attention_dense(q, k, v, s, causal)
+    if out_dtype == torch.float32:
+        assert_close(out, lse, ro, rl, what=f"TMA-store epilogue D={D} causal={causal}")
+    else:
+        err = np.abs(to_np(out) - ro)
+        assert np.all(err <= OUT_TOL + bf16_half_ulp(ro))
+        assert max_err(to_np(lse), rl) <= LSE_TOL
+    assert torch.isfinite(out.float()).all()
+
+
 # Dense non-causal launches whose last wave would be under half full give
 # those items to clusters of 2, 4 or 8 CTAs, each taking a share of the keys,
 # which merge their partial softmaxes on chip.  On a 152-SM GB300 the eight
