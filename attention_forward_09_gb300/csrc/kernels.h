@@ -39,6 +39,8 @@ struct PrefillParams {
     int tiles;      // query tiles (2 x 128 rows) per (batch, head)
     int item_base;  // first item of this launch
     int split;      // > 1: each item is shared by a cluster of `split` CTAs, one key range each
+    int persist;    // 1: CTA b walks items item_base + b + i * gridDim.x < item_end
+    int item_end;
 };
 
 // Tensor maps are built by the host (api.cpp) over q [Tq, Hq, D] and
@@ -53,6 +55,7 @@ int prefill_block_n(int D);  // keys per KV tile for head size D
 struct PrefillPlan {
     int launches;
     int split;
+    int persist;  // the full-wave launch is persistent (one CTA per SM)
     int tiles;
     long long n_items;
     long long n_full;

@@ -26,6 +26,7 @@
 // K-major operands; V is the MN-major B operand of P V; P is written by the
 // softmax threads in the same K-major layout as Q.
 #include <math.h>
+#include <algorithm>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -379,16 +380,20 @@ __global__ void __launch_bounds__(192, 1)
 // ---------------------------------------------------------------------------
 // Two query tiles per CTA (D <= 128).
 //
-// The CTA owns 256 query rows of one (document, head): tile A = rows
+// An item is 256 query rows of one (document, head): tile A = rows
 // [q0, q0 + 128), tile B = [q0 + 128, q0 + 256).  Each tile has its own
 // softmax warpgroup (warps 0-3: A, warps 4-7: B), so while one warpgroup
 // exponentiates its scores the tensor core runs the other tile's products.
-//   warp 8   TMA producer (Q_A, Q_B once; then K_0 V_0 K_1 V_1 ...)
+//   warp 8   TMA producer (per item Q_A, Q_B; then K_0 V_0 K_1 V_1 ...)
 //   warp 9   TMEM allocator + MMA issuer, in the order
 //            S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
 //   warps 10-11 idle (they complete the third warpgroup)
+// A CTA runs one item, or (persistent launches) several in turn: the ring
+// of K/V stages, the mbarrier phases and the Q buffers carry on from item
+// to item; Q of the next item is loaded once the current item's last S
+// products are done, its K_0 while the current epilogue runs.
 // Registers: launched at 168 per thread; the third warpgroup gives back
-// down to 56 so each softmax thread can hold a whole 128-column S row (224).
+// down to 72 so each softmax thread can hold a whole 128-column S row (216).
 // TMEM: S_A [0,128) S_B [128,256) O_A [256, 256+D) O_B [256+D, 256+2D).
 // P_X (bf16 pairs) is written back over the first 64 columns of S_X and
 // read from there by the P.V product (tcgen05.mma with A in tensor memory),
@@ -405,7 +410,7 @@ struct Prefill2Cfg {
     static constexpr int NCH = (D + 63) / 64;
     static constexpr int QT_BYTES = NCH * BM * 128;  // one Q tile
     static constexpr int KV_BYTES = NCH * BN * 128;
-    static constexpr int NUM_BARS = 2 * STAGES + 8;
+    static constexpr int NUM_BARS = 2 * STAGES + 10;
     // Full output tiles of D >= 96 leave through TMA stores; D = 64 ones
     // (256 bytes of fp32 per row) by direct stores, which measured faster.
     static constexpr bool TMA_OUT = D >= 96;
@@ -414,14 +419,15 @@ struct Prefill2Cfg {
     static constexpr int TMEM_O = 2 * BN;     // O_X at TMEM_O + X * D
     static constexpr int TMEM_COLS = 512;
     // setmaxnreg split of the 384 x 168 launched registers: softmax warpgroups
-    // / producer + MMA warpgroup (each the smallest share with no spills)
-    static constexpr int REG_SOFTMAX = D == 64 ? 224 : 216;
-    static constexpr int REG_OTHER = D == 64 ? 56 : 72;
+    // / producer + MMA warpgroup (the MMA warp needs more than 56)
+    static constexpr int REG_SOFTMAX = 216;
+    static constexpr int REG_OTHER = 72;
     static_assert(2 * 128 * REG_SOFTMAX + 128 * REG_OTHER <= 384 * 168, "register split");
     static_assert(2 * BN + 2 * D <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(2 * BM * D * 4 <= STAGES * KV_BYTES && 2 * BM * 8 <= 2 * QT_BYTES, "split-merge staging");
-    static_assert(KV_BYTES == NCH * BM * 128 && 2 * ((D + 31) / 32) + NCH <= STAGES * NCH, "output staging slots");
+    static_assert(KV_BYTES == NCH * BM * 128 && 2 * ((D + 31) / 32) <= (STAGES - 1) * NCH &&
+                      (D + 31) / 32 <= (STAGES - 2) * NCH, "output staging slots");
 };
 
 // Merge of an item split along the keys over a cluster of p.split CTAs (the
@@ -548,68 +554,99 @@ __global__ void __launch_bounds__(384, 1)
     auto b_p_full = [&](int x) { return smem_u32(&bars[3 + 2 * STAGES + x]); };
     auto b_pv_done = [&](int x) { return smem_u32(&bars[5 + 2 * STAGES + x]); };
     const uint32_t b_drain = smem_u32(&bars[7 + 2 * STAGES]);
+    const uint32_t b_q_empty = smem_u32(&bars[8 + 2 * STAGES]);  // Q tiles read by every S of an item
+    const uint32_t b_staged = smem_u32(&bars[9 + 2 * STAGES]);   // persistent: both tiles' output staging read
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ------------------------------------------------------------ tile coordinates
+    // ------------------------------------------------------------ work items
+    // An item is one pair of query tiles of one (head, document).  Varlen:
+    // the CTA's grid cell (tile, head, document).  Dense: item item_base +
+    // blockIdx.x (of blockIdx.x / split in a split cluster), or, persistent,
+    // items item_base + blockIdx.x + i * gridDim.x below item_end, one after
+    // the other: the next item's Q and K/V loads and first S products then
+    // overlap the current item's softmax tail and epilogue.
     const bool split = p.split > 1;  // kernel-uniform
-    int tile, h, doc, crank = 0;
-    if (p.linear) {
-        const int item = p.item_base + static_cast<int>(split ? blockIdx.x / p.split : blockIdx.x);
-        if (split) crank = static_cast<int>(cluster_ctarank());
-        tile = item % p.tiles;
-        const int hb = item / p.tiles;
-        h = hb % p.Hq;
-        doc = hb / p.Hq;
-        if (p.causal) tile = p.tiles - 1 - tile;  // heavy causal tiles first
-    } else {
-        tile = p.causal ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
-        h = blockIdx.y;
-        doc = blockIdx.z;
-    }
-    const int kvh = h / p.group;
-    int q_start, Lq, k_start, Lk;
-    if (p.cu_q) {
-        q_start = p.cu_q[doc];
-        k_start = p.cu_k[doc];
-        const int q_end = p.cu_q[doc + 1], k_end = p.cu_k[doc + 1];
-        Lq = q_end - q_start;
-        Lk = k_end - k_start;
-        const bool bad = q_start < 0 || Lq < 0 || q_end > p.Tq || k_start < 0 || Lk < 0 ||
-                         k_end > p.Tk || Lq > p.max_seqlen_q || Lk > p.max_seqlen_k;
-        if (bad) {
-            if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0 && p.status) atomicOr(p.status, kDevBadSeqlen);
-            return;
-        }
-    } else {
-        q_start = doc * p.Sq;
-        Lq = p.Sq;
-        k_start = doc * p.Sk;
-        Lk = p.Sk;
-    }
-    const int q0 = tile * 2 * BM;
-    if (q0 >= Lq) return;  // CTA-uniform, before any barrier or TMEM use (never in a split cluster)
-    if (!split && status_has_timeout(p.status, kDevTimeout)) return;
-    const int diag = Lk - Lq;
-    // KV tiles each query tile needs (0 for a tile with no rows)
-    auto kv_tiles = [&](int first_row) {
-        if (first_row >= Lq) return 0;
-        int kend = Lk;
-        if (p.causal) kend = min(Lk, min(first_row + BM - 1, Lq - 1) + diag + 1);
-        return kend > 0 ? (kend + BN - 1) / BN : 0;
+    // Only configurations with the TMA-store epilogue run persistent; for the
+    // others every item loop below has one iteration, known at compile time.
+    constexpr int kMaxItems = C::TMA_OUT ? 0x7fffffff : 1;
+    const bool persist = C::TMA_OUT && p.persist != 0;
+    const int crank = split ? static_cast<int>(cluster_ctarank()) : 0;
+    struct Item {
+        int h, doc, kvh, q_start, Lq, k_start, Lk, q0, diag, nA, nB, nmax, j0;
+        bool valid;  // false: no such item, or one with nothing to do (CTA-uniform)
     };
-    int nA = kv_tiles(q0), nB = kv_tiles(q0 + BM);
-    // A split item (non-causal, so both tiles see the same keys) gives CTA
-    // `crank` of its cluster KV tiles [j0, j1); loops below count from j0.
-    int j0 = 0;
-    if (split) {
-        const int n = max(nA, nB);
-        j0 = crank * n / p.split;
-        const int j1 = (crank + 1) * n / p.split;
-        nA = nA > 0 ? j1 - j0 : 0;
-        nB = nB > 0 ? j1 - j0 : 0;
-    }
-    const int nmax = max(nA, nB);
+    auto item_at = [&](int i) -> Item {
+        Item I{};
+        I.valid = false;
+        int tile;
+        if (p.linear) {
+            long long item;
+            if (persist)
+                item = p.item_base + static_cast<long long>(blockIdx.x) + static_cast<long long>(i) * gridDim.x;
+            else
+                item = i == 0 ? p.item_base + static_cast<long long>(split ? blockIdx.x / p.split : blockIdx.x) : -1;
+            if (item < 0 || (persist && item >= p.item_end)) return I;
+            tile = static_cast<int>(item % p.tiles);
+            const int hb = static_cast<int>(item / p.tiles);
+            I.h = hb % p.Hq;
+            I.doc = hb / p.Hq;
+            if (p.causal) tile = p.tiles - 1 - tile;  // heavy causal tiles first
+        } else {
+            if (i > 0) return I;
+            tile = p.causal ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
+            I.h = blockIdx.y;
+            I.doc = blockIdx.z;
+        }
+        I.kvh = I.h / p.group;
+        if (p.cu_q) {
+            I.q_start = p.cu_q[I.doc];
+            I.k_start = p.cu_k[I.doc];
+            const int q_end = p.cu_q[I.doc + 1], k_end = p.cu_k[I.doc + 1];
+            I.Lq = q_end - I.q_start;
+            I.Lk = k_end - I.k_start;
+            const bool bad = I.q_start < 0 || I.Lq < 0 || q_end > p.Tq || I.k_start < 0 || I.Lk < 0 ||
+                             k_end > p.Tk || I.Lq > p.max_seqlen_q || I.Lk > p.max_seqlen_k;
+            if (bad) {
+                if (threadIdx.x == 0 && blockIdx.x == 0 && I.h == 0 && p.status) atomicOr(p.status, kDevBadSeqlen);
+                return I;
+            }
+        } else {
+            I.q_start = I.doc * p.Sq;
+            I.Lq = p.Sq;
+            I.k_start = I.doc * p.Sk;
+            I.Lk = p.Sk;
+        }
+        I.q0 = tile * 2 * BM;
+        if (I.q0 >= I.Lq) return I;
+        I.diag = I.Lk - I.Lq;
+        // KV tiles each query tile needs (0 for a tile with no rows)
+        auto kv_tiles = [&](int first_row) {
+            if (first_row >= I.Lq) return 0;
+            int kend = I.Lk;
+            if (p.causal) kend = min(I.Lk, min(first_row + BM - 1, I.Lq - 1) + I.diag + 1);
+            return kend > 0 ? (kend + BN - 1) / BN : 0;
+        };
+        I.nA = kv_tiles(I.q0);
+        I.nB = kv_tiles(I.q0 + BM);
+        // A split item (non-causal, so both tiles see the same keys) gives CTA
+        // `crank` of its cluster KV tiles [j0, j1); loops below count from j0.
+        I.j0 = 0;
+        if (split) {
+            const int n = max(I.nA, I.nB);
+            I.j0 = crank * n / p.split;
+            const int j1 = (crank + 1) * n / p.split;
+            I.nA = I.nA > 0 ? j1 - I.j0 : 0;
+            I.nB = I.nB > 0 ? j1 - I.j0 : 0;
+        }
+        I.nmax = max(I.nA, I.nB);
+        I.valid = true;
+        return I;
+    };
+    // Before any barrier or TMEM use; never taken by a split cluster, and a
+    // persistent CTA always has a first item.
+    if (!item_at(0).valid) return;
+    if (!split && status_has_timeout(p.status, kDevTimeout)) return;
 
     // ------------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
@@ -624,6 +661,8 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(b_pv_done(x), 1);
         }
         mbar_init(b_drain, 1);
+        mbar_init(b_q_empty, 1);
+        mbar_init(b_staged, 2);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -644,29 +683,45 @@ __global__ void __launch_bounds__(384, 1)
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            mbar_arrive_expect_tx(b_q_full, 2 * C::QT_BYTES);
-            for (int x = 0; x < 2; ++x)
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_3d(sQ + x * C::QT_BYTES + c * BM * 128, &tmQ, b_q_full, c * 64, h, q_start + q0 + x * BM);
-            int issued = 0;
-            for (int t = 0; t < 2 * nmax; ++t) {
-                const int s = t % STAGES, u = t / STAGES;
-                if (u > 0 && !mbar_wait(b_kv_empty(s), (u - 1) & 1, abort_flag)) {
+            int t = 0, nq = 0;  // K/V loads and Q loads issued, over all items
+            for (int i = 0; ok && i < kMaxItems; ++i) {
+                const Item I = item_at(i);
+                if (!I.valid) break;
+                // Q_A, Q_B of item i replace item i-1's once its S products are done
+                if (i > 0 && !mbar_wait(b_q_empty, (i - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const CUtensorMap* m = (t & 1) ? &tmV : &tmK;
-                const int row = k_start + (j0 + (t >> 1)) * BN;
-                mbar_arrive_expect_tx(b_kv_full(s), C::KV_BYTES);
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_3d(sKV + s * C::KV_BYTES + c * BN * 128, m, b_kv_full(s), c * 64, kvh, row);
-                ++issued;
+                mbar_arrive_expect_tx(b_q_full, 2 * C::QT_BYTES);
+                for (int x = 0; x < 2; ++x)
+                    for (int c = 0; c < NCH; ++c)
+                        tma_load_3d(sQ + x * C::QT_BYTES + c * BM * 128, &tmQ, b_q_full, c * 64, I.h,
+                                    I.q_start + I.q0 + x * BM);
+                ++nq;
+                for (int tt = 0; tt < 2 * I.nmax; ++tt, ++t) {
+                    // The previous item's output may be staged in every K/V stage but
+                    // the one K_0 goes to, until its stores have read it.
+                    if (tt == 1 && i > 0 && !mbar_wait(b_staged, (i - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const int s = t % STAGES, u = t / STAGES;
+                    if (u > 0 && !mbar_wait(b_kv_empty(s), (u - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const CUtensorMap* m = (tt & 1) ? &tmV : &tmK;
+                    const int row = I.k_start + (I.j0 + (tt >> 1)) * BN;
+                    mbar_arrive_expect_tx(b_kv_full(s), C::KV_BYTES);
+                    for (int c = 0; c < NCH; ++c)
+                        tma_load_3d(sKV + s * C::KV_BYTES + c * BN * 128, m, b_kv_full(s), c * 64, I.kvh, row);
+                }
             }
             if (!ok || *abort_flag) {
                 // Let every copy this thread started land before the CTA retires.
-                mbar_wait_drain(b_q_full, 0);
-                for (int t = (issued > STAGES ? issued - STAGES : 0); t < issued; ++t)
-                    mbar_wait_drain(b_kv_full(t % STAGES), (t / STAGES) & 1);
+                if (nq > 0) mbar_wait_drain(b_q_full, (nq - 1) & 1);
+                for (int tt = (t > STAGES ? t - STAGES : 0); tt < t; ++tt)
+                    mbar_wait_drain(b_kv_full(tt % STAGES), (tt / STAGES) & 1);
             }
         }
     } else if (warp == 9) {
@@ -714,9 +769,6 @@ __global__ void __launch_bounds__(384, 1)
         auto wait_all = [&](uint32_t bar, uint32_t ph) {
             return __all_sync(0xffffffffu, mbar_wait(bar, ph, abort_flag));
         };
-        // K_j is load 2j of the ring, V_j load 2j + 1 (STAGES >= 2)
-        int ks = 0, vs = 1;
-        uint32_t kph = 0, vph = 0;
         auto adv = [](int& s, uint32_t& ph) {
             s += 2;
             if (s >= STAGES) {
@@ -724,49 +776,68 @@ __global__ void __launch_bounds__(384, 1)
                 ph ^= 1u;
             }
         };
-        ok = wait_all(b_q_full, 0);
-        if (ok && nmax > 0) {
-            if ((ok = wait_all(b_kv_full(ks), kph))) {
-                tc_fence_after();
-                if (nA > 0) issue_s(0, ks);
-                if (nB > 0) issue_s(1, ks);
-                release(ks);  // K_0: read by both S products above
-            }
-        }
-        adv(ks, kph);
-        for (int j = 0; ok && j < nmax; ++j) {
-            const bool more = j + 1 < nmax;
-            bool k_ready = false;  // K_{j+1} is waited for only once an S product needs it
-            if (!(ok = wait_all(b_kv_full(vs), vph))) break;
-            if (j < nA) {
-                if (!(ok = wait_all(b_p_full(0), j & 1))) break;
-                tc_fence_after();
-                issue_pv(0, vs, j > 0);
-                if (j + 1 < nA) {
-                    if (!(ok = wait_all(b_kv_full(ks), kph))) break;
-                    k_ready = true;
+        int tbase = 0;             // ring index of the current item's K_0 (K_j: tbase + 2j, V_j: + 1)
+        uint32_t pa = 0, pb = 0;   // softmax steps of tiles A and B in earlier items
+        for (int i = 0; ok && i < kMaxItems; ++i) {
+            const Item I = item_at(i);
+            if (!I.valid) break;
+            const int nA = I.nA, nB = I.nB, nmax = I.nmax;
+            int ks = tbase % STAGES, vs = (tbase + 1) % STAGES;
+            uint32_t kph = (tbase / STAGES) & 1, vph = ((tbase + 1) / STAGES) & 1;
+            if (!(ok = wait_all(b_q_full, i & 1))) break;
+            if (nmax > 0) {
+                if ((ok = wait_all(b_kv_full(ks), kph))) {
                     tc_fence_after();
-                    issue_s(0, ks);
+                    if (nA > 0) issue_s(0, ks);
+                    if (nB > 0) issue_s(1, ks);
+                    release(ks);  // K_0: read by both S products above
                 }
             }
-            if (j < nB) {
-                if (!(ok = wait_all(b_p_full(1), j & 1))) break;
-                tc_fence_after();
-                issue_pv(1, vs, j > 0);
-            }
-            release(vs);  // V_j: its last reader was issued above
-            if (j + 1 < nB) {
-                if (!k_ready && !(ok = wait_all(b_kv_full(ks), kph))) break;
-                k_ready = true;
-                tc_fence_after();
-                issue_s(1, ks);
-            }
-            if (more) {
-                if (!k_ready && !(ok = wait_all(b_kv_full(ks), kph))) break;  // keep the phase in step
-                release(ks);  // K_{j+1}: read by the S products issued above
-            }
+            // Q_A and Q_B are free for the next item once the item's last S product completes
+            auto release_q = [&]() {
+                if (leader) mma_commit(b_q_empty);
+                __syncwarp();
+            };
+            if (nmax <= 1) release_q();
             adv(ks, kph);
-            adv(vs, vph);
+            for (int j = 0; ok && j < nmax; ++j) {
+                const bool more = j + 1 < nmax;
+                bool k_ready = false;  // K_{j+1} is waited for only once an S product needs it
+                if (!(ok = wait_all(b_kv_full(vs), vph))) break;
+                if (j < nA) {
+                    if (!(ok = wait_all(b_p_full(0), (pa + j) & 1))) break;
+                    tc_fence_after();
+                    issue_pv(0, vs, j > 0);
+                    if (j + 1 < nA) {
+                        if (!(ok = wait_all(b_kv_full(ks), kph))) break;
+                        k_ready = true;
+                        tc_fence_after();
+                        issue_s(0, ks);
+                    }
+                }
+                if (j < nB) {
+                    if (!(ok = wait_all(b_p_full(1), (pb + j) & 1))) break;
+                    tc_fence_after();
+                    issue_pv(1, vs, j > 0);
+                }
+                release(vs);  // V_j: its last reader was issued above
+                if (j + 1 < nB) {
+                    if (!k_ready && !(ok = wait_all(b_kv_full(ks), kph))) break;
+                    k_ready = true;
+                    tc_fence_after();
+                    issue_s(1, ks);
+                }
+                if (j + 2 == nmax) release_q();  // S_X(nmax - 1) were the item's last S products
+                if (more) {
+                    if (!k_ready && !(ok = wait_all(b_kv_full(ks), kph))) break;  // keep the phase in step
+                    release(ks);  // K_{j+1}: read by the S products issued above
+                }
+                adv(ks, kph);
+                adv(vs, vph);
+            }
+            tbase += 2 * nmax;
+            pa += nA;
+            pb += nB;
         }
         // Everything issued above must finish before TMEM is released.
         if (leader) mma_commit(b_drain);
@@ -784,17 +855,24 @@ __global__ void __launch_bounds__(384, 1)
         // ------------------------------------------------------------- softmax
         const int x = warp >> 2;               // 0: tile A, 1: tile B
         const int r = threadIdx.x & 127;       // row within the tile == TMEM lane
-        const int row = q0 + x * BM + r;       // row within the document
-        const int n_kv = x ? nB : nA;
-        const int qfirst = q0 + x * BM;
         const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const uint32_t tS = tl + C::TMEM_S + x * BN;
         const uint32_t tO = tl + C::TMEM_O + x * D;
-        const int row_lim = p.causal ? min(Lk, row + diag + 1) : Lk;  // keys [0, row_lim) visible
         const float c2 = p.scale_log2;
+        uint32_t sdone = 0;  // S_X products of earlier items (phase count of s_full and pv_done)
+        int tbase = 0;       // ring index of the item's K_0 (as the producer and MMA warps count)
+        for (int i = 0; ok && i < kMaxItems; ++i) {
+        const Item I = item_at(i);
+        if (!I.valid) break;
+        const int h = I.h, doc = I.doc, q_start = I.q_start, Lq = I.Lq, Lk = I.Lk, q0 = I.q0, diag = I.diag;
+        const int nA = I.nA, nB = I.nB, nmax = I.nmax, j0 = I.j0;
+        const int row = q0 + x * BM + r;       // row within the document
+        const int n_kv = x ? nB : nA;
+        const int qfirst = q0 + x * BM;
+        const int row_lim = p.causal ? min(Lk, row + diag + 1) : Lk;  // keys [0, row_lim) visible
         float m = -INFINITY, l = 0.f;
         for (int j = 0; j < n_kv; ++j) {
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_s_full(x), j & 1, abort_flag)))) break;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_s_full(x), (sdone + j) & 1, abort_flag)))) break;
             tc_fence_after();
             const int kbase = (j0 + j) * BN;
             const bool edge = (kbase + BN > Lk) || (p.causal && kbase + BN - 1 > qfirst + diag);
@@ -864,9 +942,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         ok = __all_sync(0xffffffffu, ok);
         if (ok && n_kv > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(b_pv_done(x), (n_kv - 1) & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(b_pv_done(x), (sdone + n_kv - 1) & 1, abort_flag));
             tc_fence_after();
         }
+        sdone += n_kv;
         // ------------------------------------------------------------ epilogue
         if (split) {
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_drain, 0, abort_flag));  // all MMAs done
@@ -884,10 +963,19 @@ __global__ void __launch_bounds__(384, 1)
             const bool f32 = p.out_f32 != 0;
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             const int boxes = f32 ? D / 32 : (D + 63) / 64, cols = f32 ? 32 : 64;  // 128-byte boxes per row
-            const int v0 = nmax > 0 ? ((2 * nmax - 1) % STAGES) * NCH : STAGES * NCH;  // V_{n-1}'s first slot
-            auto slot_addr = [&](int b) {  // box b of this tile: the (x * boxes + b)-th slot outside V_{n-1}
-                const int i = x * boxes + b;
-                return sKV + static_cast<uint32_t>(i < v0 ? i : i + NCH) * (BM * 128);
+            // Stages for the boxes: never the next item's K_0 stage (sk, loaded
+            // while this epilogue runs); tile A never V_{n-1}'s (sv), which
+            // PV_B(last) may still read: the stages other than sv and sk come
+            // first, sv last, and tile A's boxes fit in the first ones.
+            const int sv = (tbase + 2 * nmax - 1 + STAGES) % STAGES, sk = (tbase + 2 * nmax) % STAGES;
+            const int lo = min(sv, sk), hi = max(sv, sk);
+            auto slot_addr = [&](int b) {  // box b of this tile: the (x * boxes + b)-th usable 16 KB slot
+                const int i = x * boxes + b, k = i / NCH;
+                int st = k;
+                if (st >= lo) ++st;
+                if (st >= hi) ++st;
+                if (k == STAGES - 2) st = sv;
+                return sKV + static_cast<uint32_t>(st * NCH + i % NCH) * (BM * 128);
             };
             const int sw = r & 7;
             auto load_scaled = [&](int c, uint32_t (&o)[32]) {
@@ -932,6 +1020,7 @@ __global__ void __launch_bounds__(384, 1)
                 for (int b = 0; b < boxes; ++b) tma_store_3d(&tmO, slot_addr(b), b * cols, h, q_start + qfirst);
                 bulk_commit();
                 bulk_wait_read0();  // the staging area must outlive the reads
+                if (persist) mbar_arrive(b_staged);
             }
             if (ok && p.lse) {
                 const long long lrow = p.lse_row_global ? (q_start + row) : row;
@@ -939,6 +1028,7 @@ __global__ void __launch_bounds__(384, 1)
                     l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
             }
         } else {
+        if (persist && r == 0) mbar_arrive(b_staged);  // nothing staged
         const bool row_valid = ok && row < Lq;
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         const long long orow = static_cast<long long>(q_start + row) * p.Hq + h;
@@ -978,6 +1068,8 @@ __global__ void __launch_bounds__(384, 1)
             p.lse[doc * p.lse_bstride + h * p.lse_hstride + lrow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
         }
         }
+        tbase += 2 * nmax;
+        }  // items
     }
 
     // --------------------------------------------------------------- teardown
@@ -1086,6 +1178,12 @@ static cudaError_t plan_two_tile(K kernel, const PrefillParams& p, int num_sms, 
     }
     pl->n_full = pl->split ? pl->n_items - tail : pl->n_items;
     pl->launches = (pl->n_full > 0 ? 1 : 0) + (pl->split ? 1 : 0);
+    // More than one wave (non-causal, equal items, TMA-store epilogue): one
+    // CTA per SM walks the full-wave items in turn, so that launch, set-up
+    // and the next item's Q and K_0 loads and first S products overlap the
+    // current item's work.  (D = 64, with direct output stores, measured
+    // faster without.)
+    pl->persist = C::TMA_OUT && !p.causal && num_sms > 0 && pl->n_full > num_sms;
     return cudaSuccess;
 }
 
@@ -1109,8 +1207,12 @@ static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUten
     q.linear = 1;
     q.tiles = pl.tiles;
     if (pl.n_full > 0) {
-        kernel<<<static_cast<unsigned>(pl.n_full), 384, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, q);
+        q.persist = pl.persist;
+        q.item_end = static_cast<int>(pl.n_full);
+        const long long grid = pl.persist ? std::min<long long>(pl.n_full, num_sms) : pl.n_full;
+        kernel<<<static_cast<unsigned>(grid), 384, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, q);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        q.persist = 0;
     }
     if (pl.split) {
         q.item_base = static_cast<int>(pl.n_full);

@@ -129,6 +129,31 @@ def test_dense_tma_store_epilogue(D, out_dtype, causal):
     assert torch.isfinite(out.float()).all()
 
 
+# Dense non-causal launches of more than one wave (D >= 96) run one CTA per
+# SM that walks its items in turn (on 152 SMs: 320 items = 2 or 3 per CTA),
+# loading the next item's Q and K_0 during the current epilogue.
+
+@pytest.mark.parametrize("D,out_dtype", [(128, torch.float32), (96, torch.bfloat16), (96, torch.float32)])
+def test_dense_persistent_items(D, out_dtype):
+    (q, k, v, s), out, lse = _dense_case(1, 512, 300, 160, 8, D, False, seed=D + 91, out_dtype=out_dtype)
+    ro, rl = oracle.attention_dense(q, k, v, s, False)
+    if out_dtype == torch.float32:
+        assert_close(out, lse, ro, rl, what=f"persistent D={D}")
+    else:
+        err = np.abs(to_np(out) - ro)
+        assert np.all(err <= OUT_TOL + bf16_half_ulp(ro))
+        assert max_err(to_np(lse), rl) <= LSE_TOL
+
+
+def test_dense_persistent_then_split_tail():
+    """328 items, 9 KV tiles: 304 on a persistent grid, then 24 split 2-way."""
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert gb.attn_fwd_dense_plan(1, 512, 1100, 164, 4, 128, False) == (2, 2)
+    (q, k, v, s), out, lse = _dense_case(1, 512, 1100, 164, 4, 128, False, seed=92)
+    ro, rl = oracle.attention_dense(q, k, v, s, False)
+    assert_close(out, lse, ro, rl, what="persistent + split tail")
+
+
 # Dense non-causal launches whose last wave would be under half full give
 # those items to clusters of 2, 4 or 8 CTAs, each taking a share of the keys,
 # which merge their partial softmaxes on chip.  On a 152-SM GB300 the eight
