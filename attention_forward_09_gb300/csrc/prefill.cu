@@ -411,9 +411,6 @@ struct Prefill2Cfg {
     static constexpr int QT_BYTES = NCH * BM * 128;  // one Q tile
     static constexpr int KV_BYTES = NCH * BN * 128;
     static constexpr int NUM_BARS = 2 * STAGES + 10;
-    // Full output tiles of D >= 96 leave through TMA stores; D = 64 ones
-    // (256 bytes of fp32 per row) by direct stores, which measured faster.
-    static constexpr bool TMA_OUT = D >= 96;
     static constexpr int SMEM_BYTES = 1024 + 2 * QT_BYTES + STAGES * KV_BYTES + NUM_BARS * 8 + 16;
     static constexpr int TMEM_S = 0;          // S_X at X * BN
     static constexpr int TMEM_O = 2 * BN;     // O_X at TMEM_O + X * D
@@ -567,10 +564,7 @@ __global__ void __launch_bounds__(384, 1)
     // the other: the next item's Q and K/V loads and first S products then
     // overlap the current item's softmax tail and epilogue.
     const bool split = p.split > 1;  // kernel-uniform
-    // Only configurations with the TMA-store epilogue run persistent; for the
-    // others every item loop below has one iteration, known at compile time.
-    constexpr int kMaxItems = C::TMA_OUT ? 0x7fffffff : 1;
-    const bool persist = C::TMA_OUT && p.persist != 0;
+    const bool persist = p.persist != 0;
     const int crank = split ? static_cast<int>(cluster_ctarank()) : 0;
     struct Item {
         int h, doc, kvh, q_start, Lq, k_start, Lk, q0, diag, nA, nB, nmax, j0;
@@ -684,7 +678,7 @@ __global__ void __launch_bounds__(384, 1)
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             int t = 0, nq = 0;  // K/V loads and Q loads issued, over all items
-            for (int i = 0; ok && i < kMaxItems; ++i) {
+            for (int i = 0; ok; ++i) {
                 const Item I = item_at(i);
                 if (!I.valid) break;
                 // Q_A, Q_B of item i replace item i-1's once its S products are done
@@ -778,7 +772,7 @@ __global__ void __launch_bounds__(384, 1)
         };
         int tbase = 0;             // ring index of the current item's K_0 (K_j: tbase + 2j, V_j: + 1)
         uint32_t pa = 0, pb = 0;   // softmax steps of tiles A and B in earlier items
-        for (int i = 0; ok && i < kMaxItems; ++i) {
+        for (int i = 0; ok; ++i) {
             const Item I = item_at(i);
             if (!I.valid) break;
             const int nA = I.nA, nB = I.nB, nmax = I.nmax;
@@ -861,7 +855,7 @@ __global__ void __launch_bounds__(384, 1)
         const float c2 = p.scale_log2;
         uint32_t sdone = 0;  // S_X products of earlier items (phase count of s_full and pv_done)
         int tbase = 0;       // ring index of the item's K_0 (as the producer and MMA warps count)
-        for (int i = 0; ok && i < kMaxItems; ++i) {
+        for (int i = 0; ok; ++i) {
         const Item I = item_at(i);
         if (!I.valid) break;
         const int h = I.h, doc = I.doc, q_start = I.q_start, Lq = I.Lq, Lk = I.Lk, q0 = I.q0, diag = I.diag;
@@ -951,7 +945,7 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_drain, 0, abort_flag));  // all MMAs done
             tc_fence_after();
             split_merge<D>(smem, sKV, tO, x * BM + r, m, l, n_kv > 0, ok, crank, q0, Lq, q_start, h, doc, p);
-        } else if (C::TMA_OUT && qfirst + BM <= Lq && (x == 1 || nA >= nB)) {
+        } else if (qfirst + BM <= Lq && (x == 1 || nA >= nB)) {
             // A tile wholly inside its document leaves through shared memory:
             // its rows are staged in the TMA 128-byte-swizzled box layout
             // (128 rows x 128 bytes per 16 KB box) in slots of the K/V area
@@ -1178,12 +1172,10 @@ static cudaError_t plan_two_tile(K kernel, const PrefillParams& p, int num_sms, 
     }
     pl->n_full = pl->split ? pl->n_items - tail : pl->n_items;
     pl->launches = (pl->n_full > 0 ? 1 : 0) + (pl->split ? 1 : 0);
-    // More than one wave (non-causal, equal items, TMA-store epilogue): one
-    // CTA per SM walks the full-wave items in turn, so that launch, set-up
-    // and the next item's Q and K_0 loads and first S products overlap the
-    // current item's work.  (D = 64, with direct output stores, measured
-    // faster without.)
-    pl->persist = C::TMA_OUT && !p.causal && num_sms > 0 && pl->n_full > num_sms;
+    // More than one wave (non-causal, so equal items): one CTA per SM walks
+    // the full-wave items in turn, so that launch, set-up and the next item's
+    // Q and K_0 loads and first S products overlap the current item's work.
+    pl->persist = !p.causal && num_sms > 0 && pl->n_full > num_sms;
     return cudaSuccess;
 }
 

@@ -102,12 +102,12 @@ def test_large_logits_rescale_path():
     assert_close(out, lse, ro, rl, lse_tol=5e-3, what="large logits")  # |lse| ~ 100 here
 
 
-# Query tiles wholly inside their document (D >= 96) leave through shared
+# Query tiles wholly inside their document (D <= 128) leave through shared
 # memory and TMA tiled stores; at D = 96 a bf16 row is one and a half
 # 128-byte boxes, so the second box is half outside the tensor and clipped.
 # Causal: tile A, with fewer KV tiles than tile B, stores directly.
 
-@pytest.mark.parametrize("D", [96, 128])
+@pytest.mark.parametrize("D", [64, 96, 128])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("causal", [False, True])
 def test_dense_tma_store_epilogue(D, out_dtype, causal):
@@ -129,11 +129,12 @@ def test_dense_tma_store_epilogue(D, out_dtype, causal):
     assert torch.isfinite(out.float()).all()
 
 
-# Dense non-causal launches of more than one wave (D >= 96) run one CTA per
+# Dense non-causal launches of more than one wave (D <= 128) run one CTA per
 # SM that walks its items in turn (on 152 SMs: 320 items = 2 or 3 per CTA),
 # loading the next item's Q and K_0 during the current epilogue.
 
-@pytest.mark.parametrize("D,out_dtype", [(128, torch.float32), (96, torch.bfloat16), (96, torch.float32)])
+@pytest.mark.parametrize("D,out_dtype", [(128, torch.float32), (96, torch.bfloat16), (96, torch.float32),
+                                         (64, torch.float32), (64, torch.bfloat16)])
 def test_dense_persistent_items(D, out_dtype):
     (q, k, v, s), out, lse = _dense_case(1, 512, 300, 160, 8, D, False, seed=D + 91, out_dtype=out_dtype)
     ro, rl = oracle.attention_dense(q, k, v, s, False)
