@@ -51,6 +51,9 @@ struct PrefillCfg {
     static_assert(2 * BN + D <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(D % 32 == 0 && BN % 64 == 0, "tile shape");
+    static_assert(D % 64 == 0 && (D / 32) * BM * 128 <= STAGES * KV_BYTES, "output staging in the K/V area");
+    // TMA-store epilogue for full tiles: measured +1.5% at D = 192, -0.8% at D = 256
+    static constexpr bool TMA_OUT = D < 256;
 };
 
 constexpr float kLn2 = 0.6931471805599453f;
@@ -59,7 +62,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: tolerate P up to 2^8 b
 template <class C>
 __global__ void __launch_bounds__(192, 1)
     fmha_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const PrefillParams p) {
     constexpr int D = C::D, BN = C::BN, STAGES = C::STAGES, BM = C::BM, NCH = C::NCH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -324,6 +328,55 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_after();
         }
         // ------------------------------------------------------------ epilogue
+        if (C::TMA_OUT && q0 + BM <= Lq) {
+            // A tile wholly inside its document leaves through shared memory:
+            // rows staged in the TMA 128-byte-swizzled box layout in 16 KB
+            // slots of the K/V area (free: PV of the last KV tile was the last
+            // MMA) and written by tiled TMA stores.
+            const bool f32 = p.out_f32 != 0;
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const int boxes = f32 ? D / 32 : D / 64, cols = f32 ? 32 : 64;  // 128-byte boxes per row
+            const int sw = r & 7;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                if (n_kv > 0 && ok) {
+                    tmem_ld32(tl + C::TMEM_O + c * 32, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
+                if (f32) {  // 32 columns = one 128-byte box row
+                    const uint32_t rb = sKV + c * (BM * 128) + r * 128;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        st_shared_v4(rb + ((k ^ sw) << 4), o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                } else {    // 32 columns = half a box row
+                    const uint32_t rb = sKV + (c >> 1) * (BM * 128) + r * 128;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        st_shared_v4(rb + ((((c & 1) * 4 + k) ^ sw) << 4),
+                                     pack_bf16x2(__uint_as_float(o[8 * k]), __uint_as_float(o[8 * k + 1])),
+                                     pack_bf16x2(__uint_as_float(o[8 * k + 2]), __uint_as_float(o[8 * k + 3])),
+                                     pack_bf16x2(__uint_as_float(o[8 * k + 4]), __uint_as_float(o[8 * k + 5])),
+                                     pack_bf16x2(__uint_as_float(o[8 * k + 6]), __uint_as_float(o[8 * k + 7])));
+                }
+            }
+            fence_proxy_async_smem();  // generic-proxy writes -> the TMA engine
+            named_bar_sync(1, 128);
+            if (r == 0) {
+                for (int b = 0; b < boxes; ++b) tma_store_3d(&tmO, sKV + b * (BM * 128), b * cols, h, q_start + q0);
+                bulk_commit();
+                bulk_wait_read0();  // the staging area must outlive the reads
+            }
+            if (ok && p.lse) {
+                const long long lrow = p.lse_row_global ? (q_start + row) : row;
+                p.lse[doc * p.lse_bstride + h * p.lse_hstride + lrow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+            }
+        } else {
         const bool row_valid = ok && row < Lq;
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         const long long orow = static_cast<long long>(q_start + row) * p.Hq + h;
@@ -361,6 +414,7 @@ __global__ void __launch_bounds__(192, 1)
         if (row_valid && p.lse) {
             const long long lrow = p.lse_row_global ? (q_start + row) : row;
             p.lse[doc * p.lse_bstride + h * p.lse_hstride + lrow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        }
         }
     }
 
@@ -1104,12 +1158,12 @@ static cudaError_t set_smem_attr(K kernel, int bytes) {
 
 template <class C, class K>
 static cudaError_t launch_kernel(K kernel, int threads, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                                 const CUtensorMap& tmV, const PrefillParams& p, int rows_per_cta,
-                                 cudaStream_t stream) {
+                                 const CUtensorMap& tmV, const CUtensorMap& tmO, const PrefillParams& p,
+                                 int rows_per_cta, cudaStream_t stream) {
     cudaError_t e = set_smem_attr<C>(kernel, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid((p.max_seqlen_q + rows_per_cta - 1) / rows_per_cta, p.Hq, p.num_docs);
-    kernel<<<grid, threads, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
+    kernel<<<grid, threads, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, p);
     return cudaGetLastError();
 }
 
@@ -1235,8 +1289,8 @@ cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK
         case 64: return launch_two_tile<Cfg64>(fmha2_fwd_sm103a<Cfg64>, tmQ, tmK, tmV, tmO, p, num_sms, stream);
         case 96: return launch_two_tile<Cfg96>(fmha2_fwd_sm103a<Cfg96>, tmQ, tmK, tmV, tmO, p, num_sms, stream);
         case 128: return launch_two_tile<Cfg128>(fmha2_fwd_sm103a<Cfg128>, tmQ, tmK, tmV, tmO, p, num_sms, stream);
-        case 192: return launch_kernel<Cfg192>(fmha_fwd_sm103a<Cfg192>, 192, tmQ, tmK, tmV, p, 128, stream);
-        case 256: return launch_kernel<Cfg256>(fmha_fwd_sm103a<Cfg256>, 192, tmQ, tmK, tmV, p, 128, stream);
+        case 192: return launch_kernel<Cfg192>(fmha_fwd_sm103a<Cfg192>, 192, tmQ, tmK, tmV, tmO, p, 128, stream);
+        case 256: return launch_kernel<Cfg256>(fmha_fwd_sm103a<Cfg256>, 192, tmQ, tmK, tmV, tmO, p, 128, stream);
         default: return cudaErrorInvalidValue;
     }
 }

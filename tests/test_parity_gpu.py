@@ -102,12 +102,12 @@ def test_large_logits_rescale_path():
     assert_close(out, lse, ro, rl, lse_tol=5e-3, what="large logits")  # |lse| ~ 100 here
 
 
-# Query tiles wholly inside their document (D <= 128) leave through shared
-# memory and TMA tiled stores; at D = 96 a bf16 row is one and a half
-# 128-byte boxes, so the second box is half outside the tensor and clipped.
-# Causal: tile A, with fewer KV tiles than tile B, stores directly.
+# Query tiles wholly inside their document leave through shared memory and
+# TMA tiled stores; at D = 96 a bf16 row is one and a half 128-byte boxes,
+# so the second box is half outside the tensor and clipped.  Causal (two-tile
+# kernel): tile A, with fewer KV tiles than tile B, stores directly.
 
-@pytest.mark.parametrize("D", [64, 96, 128])
+@pytest.mark.parametrize("D", [64, 96, 128, 192, 256])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("causal", [False, True])
 def test_dense_tma_store_epilogue(D, out_dtype, causal):
