@@ -197,7 +197,7 @@ def oracle_prefill_sample(w: workloads.Dense, budget_s: float, inputs=None, rows
         flops += 4.0 * w.D * len(rows) * w.Sk
         done += 1
         el = time.perf_counter() - t0
-        if el >= budget_s:
+        if el >= budget_s or done >= w.B * w.Hq * per_bh:  # never past the whole workload
             break
     desc = (f"{done} units of {rows_per_unit} query rows x all {w.Sk} keys, one (batch, head) each, "
             f"of {w.name} ({w.B * w.Hq * per_bh} units in the full workload)")
