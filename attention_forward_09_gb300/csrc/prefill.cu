@@ -1,20 +1,29 @@
 // prefill.cu -- fused attention forward for sm_103a (dense and packed varlen).
 //
-// One CTA computes one 128-row query tile of one (document, query head):
-//   S_j = Q K_j^T          tcgen05.mma, bf16 x bf16 -> fp32 in TMEM (double-buffered)
+// For each query tile (128 rows of one document and query head):
+//   S_j = Q K_j^T          tcgen05.mma, bf16 x bf16 -> fp32 in TMEM
 //   P_j = exp2(S_j*c - m)  softmax warps, one thread per query row (TMEM lane)
-//   O  += P_j V_j          tcgen05.mma, P staged in shared memory as bf16
+//   O  += P_j V_j          tcgen05.mma, O accumulated in TMEM
 //   out = O / l, lse = (m + log2 l) ln 2
 // This is the online-softmax form of the plain definition (vllm-omni
 // flash_attn.py, FlashAttentionImpl: flash_attn_func / flash_attn_varlen_func
 // with softmax_scale and causal; the (out, lse) pair of _unwrap_flash_output).
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax + O correction + epilogue; warp w owns TMEM lanes 32w..32w+31
-//   warp 4     TMA producer: Q once, then K_0 V_0 K_1 V_1 ... into a ring of slots
-//   warp 5     TMEM allocator and (lane 0) MMA issuer
-// The MMA warp issues S_{j+1} before PV_j, so the tensor core works on the
-// next scores while the softmax warps exponentiate the current ones.
+// Two kernels:
+//   fmha2_fwd_sm103a (D = 64, 96, 128): two query tiles per CTA that share
+//     every K/V tile, two softmax warpgroups taking turns with the tensor
+//     cores, P written back into TMEM and read by the P.V product from there,
+//     TMA-store epilogue, a persistent grid for dense launches of more than
+//     one wave, and the partly filled last wave split along the keys over
+//     thread-block clusters that merge on chip (see the comments there);
+//   fmha_fwd_sm103a (D = 192, 256): one tile per CTA (two O accumulators of
+//     that width do not fit in TMEM next to the S buffers), 192 threads:
+//       warps 0-3  softmax + O correction + epilogue; warp w owns TMEM lanes 32w..32w+31
+//       warp 4     TMA producer: Q once, then K_0 V_0 K_1 V_1 ... into a ring of slots
+//       warp 5     TMEM allocator and MMA issuer (one elected lane)
+//     S double-buffered in TMEM (S_{j+1} is issued before PV_j, so the tensor
+//     core works on the next scores while the softmax warps exponentiate the
+//     current ones) and P staged in shared memory as bf16.
 //
 // Causal masking is bottom-right aligned (FlashAttentionImpl.forward_fa_npu:
 // key kp is blocked for query qp iff kp > qp + Sk - Sq); KV tiles past the
@@ -23,8 +32,9 @@
 // Shared-memory operand layout: every operand is a stack of 64-column
 // chunks, each chunk [rows x 128 B] with the 128-byte swizzle that TMA
 // writes (16-byte piece c of row r at position c ^ (r % 8)).  Q and K are
-// K-major operands; V is the MN-major B operand of P V; P is written by the
-// softmax threads in the same K-major layout as Q.
+// K-major operands; V is the MN-major B operand of P V; P (one-tile kernel)
+// is written by the softmax threads in the same K-major layout as Q.  Output
+// staged for TMA stores uses the same swizzle, 128-byte boxes of columns.
 #include <math.h>
 #include <algorithm>
 
