@@ -10,6 +10,7 @@ from .attention import (  # noqa: F401
     attention_single,
     attention_varlen,
     check_cu_seqlens,
+    kv_cache_write,
     paged_gather,
     softmax_weights,
     visible_mask,

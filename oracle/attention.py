@@ -187,6 +187,37 @@ def paged_gather(kv_cache, block_table, seq_lens):
     return ks, vs
 
 
+def kv_cache_write(key, value, slot_mapping, kv_cache):
+    """The cache after writing each token's K and V at its slot
+    (vllm-ascend ``attention_v1.py``, ``AscendAttentionBackendImpl.reshape_and_cache``;
+    the slot rule is the ``AscendMetadata.slot_mapping`` comment: slot
+    ``block * block_size + offset``).
+
+    key, value: [T, Hkv, D]; slot_mapping: [T] ints; kv_cache:
+    [2, num_blocks, block_size, Hkv, D].  Token t goes to
+    ``cache[0 / 1, slot // block_size, slot % block_size]``.  A negative slot
+    stores nothing (the padding-token convention); a slot past the cache is an
+    error.  Tokens are written in order, so a repeated slot keeps the last
+    token.  A pure copy: the result holds the input bits, in the cache's dtype.
+    Returns a new tensor / array; the input cache is not modified.
+    """
+    _, nb, bs, hkv, d = kv_cache.shape
+    slots = _i64(slot_mapping)
+    if key.shape[0] != slots.size or value.shape[0] != slots.size:
+        raise ValueError("key, value and slot_mapping disagree on the token count")
+    out = kv_cache.clone() if hasattr(kv_cache, "clone") else np.array(kv_cache, copy=True)
+    for t in range(slots.size):
+        slot = int(slots[t])
+        if slot < 0:
+            continue
+        if slot >= nb * bs:
+            raise ValueError(f"slot {slot} of token {t} is past the cache ({nb} blocks of {bs})")
+        block, offset = divmod(slot, bs)
+        out[0, block, offset] = key[t]
+        out[1, block, offset] = value[t]
+    return out
+
+
 def attention_paged(q, kv_cache, block_table, seq_lens, scale: float):
     """Decode over a paged cache (``attention_v1.py``, ``forward_paged_attention``).
 

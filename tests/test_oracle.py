@@ -15,6 +15,7 @@ from decimal import Decimal, getcontext
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 import workloads
@@ -328,3 +329,57 @@ def test_workload_shapes_and_index_structures():
     assert q.shape == (128, 4, 64) and cq.tolist() == [0, 37, 128]
     assert abs(w1.flops() - 4 * 64 * 4 * (37 ** 2 + 91 ** 2)) < 1
     assert abs(workloads.dit_self().flops() - 412.3e9) / 412.3e9 < 1e-3
+
+
+# ------------------------------------------------------------- KV cache write
+
+def test_kv_cache_write_pages_example():
+    """slot_mapping [35, 2, 17] with blocks of 16 (the AscendMetadata comment)."""
+    g = json.load(open(os.path.join(GOLDEN, "slot_mapping_example.json")))
+    bs, slots = g["block_size"], g["slot_mapping"]
+    cache = torch.zeros(2, 4, bs, 1, 32, dtype=torch.bfloat16)
+    k = torch.arange(1, 4, dtype=torch.float32).view(3, 1, 1).expand(3, 1, 32).to(torch.bfloat16)
+    new = oracle.kv_cache_write(k, -k, torch.tensor(slots), cache)
+    for t, (b, o) in enumerate(g["block_offset"]):
+        assert torch.equal(new[0, b, o], k[t]) and torch.equal(new[1, b, o], -k[t])
+    assert int((new != 0).any(dim=-1).sum()) == 2 * len(slots)  # nothing else written
+    assert torch.equal(cache, torch.zeros_like(cache))          # the input is left alone
+
+
+def test_kv_cache_write_then_paged_gather_is_identity():
+    """Writing every token of every sequence at block_table[s, t // bs] * bs + t % bs
+    and reading the cache back through paged_gather returns the tokens bit for bit."""
+    gen = torch.Generator().manual_seed(5)
+    lens, bs, hkv, d = [5, 33, 16, 1], 16, 2, 32
+    nb = sum(-(-n // bs) for n in lens) + 3
+    perm = torch.randperm(nb, generator=gen)
+    bt = torch.full((len(lens), 4), -1, dtype=torch.int32)
+    at = 0
+    for s, n in enumerate(lens):
+        m = -(-n // bs)
+        bt[s, :m] = perm[at:at + m]
+        at += m
+    k = torch.randn(sum(lens), hkv, d, generator=gen).to(torch.bfloat16)
+    v = torch.randn(sum(lens), hkv, d, generator=gen).to(torch.bfloat16)
+    slots, off = [], 0
+    for s, n in enumerate(lens):
+        slots += [int(bt[s, t // bs]) * bs + t % bs for t in range(n)]
+    cache = torch.randn(2, nb, bs, hkv, d, generator=gen).to(torch.bfloat16)
+    new = oracle.kv_cache_write(k, v, torch.tensor(slots), cache)
+    ks, vs = oracle.paged_gather(new, bt, torch.tensor(lens))
+    for s, n in enumerate(lens):
+        assert np.array_equal(ks[s], k[off:off + n].double().numpy())
+        assert np.array_equal(vs[s], v[off:off + n].double().numpy())
+        off += n
+
+
+def test_kv_cache_write_padding_slots_and_errors():
+    cache = torch.randn(2, 3, 8, 1, 32, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    k = torch.ones(3, 1, 32, dtype=torch.bfloat16)
+    new = oracle.kv_cache_write(k, k, torch.tensor([-1, 9, -1]), cache)
+    changed = (new != cache).any(dim=-1).any(dim=-1)
+    assert changed.sum() == 2 and changed[0, 1, 1] and changed[1, 1, 1]  # only slot 9 = block 1, offset 1
+    dup = oracle.kv_cache_write(torch.stack([k[0], 2 * k[0]]), torch.stack([k[0], 2 * k[0]]), torch.tensor([4, 4]), cache)
+    assert torch.equal(dup[0, 0, 4], 2 * k[0])  # tokens in order: the last one stays
+    with pytest.raises(ValueError):
+        oracle.kv_cache_write(k, k, torch.tensor([0, 24, 1]), cache)  # 3 blocks of 8 = slots 0..23
