@@ -40,6 +40,7 @@ SIGNATURES = {
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_fwd_paged_noalloc": (_I, [_P, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _P]),
     "attn_fwd_dense_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
+    "attn_kv_cache_write": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P]),
 }
 
 _lib = None
@@ -221,3 +222,22 @@ def attn_fwd_paged_noalloc(q, kv_cache, block_table, seq_lens, max_seq_len, soft
                                                _ptr(dev_status), _stream_handle(stream))
     _check("attn_fwd_paged_noalloc", st)
     return out, lse
+
+
+def attn_kv_cache_write(key, value, slot_mapping, kv_cache, dev_status=None, stream=None):
+    """Store key / value [T, Hkv, D] (bf16) into kv_cache [2, nb, bs, Hkv, D]
+    in place at slot_mapping [T] (int32 CUDA): token t goes to block
+    slot // bs, offset slot % bs; negative slots store nothing."""
+    for n, t in (("key", key), ("value", value), ("kv_cache", kv_cache)):
+        _bf16_cuda(n, t)
+    T, Hkv, D = key.shape
+    two, nb, bs, Hc, Dc = kv_cache.shape
+    if value.shape != key.shape or two != 2 or (Hc, Dc) != (Hkv, D):
+        raise ValueError("key/value must be [T, Hkv, D] and kv_cache [2, num_blocks, block_size, Hkv, D]")
+    if slot_mapping.dtype != torch.int32 or not slot_mapping.is_cuda or not slot_mapping.is_contiguous() or \
+            slot_mapping.numel() != T:
+        raise ValueError("slot_mapping must be a contiguous int32 CUDA tensor of T entries")
+    st = load_library().attn_kv_cache_write(_ptr(key), _ptr(value), _ptr(slot_mapping), T, _ptr(kv_cache), nb, bs,
+                                            Hkv, D, _ptr(dev_status), _stream_handle(stream))
+    _check("attn_kv_cache_write", st)
+    return kv_cache

@@ -230,6 +230,31 @@ gbattn_status attn_fwd_varlen(const void* q, const void* k, const void* v, const
     return run_prefill(q, k, v, Tq, Tk, D, p, static_cast<cudaStream_t>(stream));
 }
 
+gbattn_status attn_kv_cache_write(const void* key, const void* value, const int32_t* slot_mapping, int num_tokens,
+                                  void* kv_cache, int num_blocks, int block_size, int Hkv, int D,
+                                  uint32_t* dev_status, void* stream) {
+    if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || Hkv <= 0) return GBATTN_ERR_INVALID_ARG;
+    if (!head_size_ok(D)) return GBATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return GBATTN_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return GBATTN_OK;
+    if (!key || !value || !slot_mapping || !kv_cache) return GBATTN_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(kv_cache)) return GBATTN_ERR_ALIGNMENT;
+    DeviceInfo di;
+    gbattn_status s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    gbattn::CacheWriteParams p{};
+    p.key = static_cast<const uint4*>(key);
+    p.value = static_cast<const uint4*>(value);
+    p.slot_mapping = slot_mapping;
+    p.cache = static_cast<uint4*>(kv_cache);
+    p.num_tokens = num_tokens;
+    p.num_slots = static_cast<long long>(num_blocks) * block_size;
+    p.row_vec = Hkv * D * 2 / 16;
+    p.status = dev_status;
+    return gbattn::launch_cache_write(p, di.sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GBATTN_OK
+                                                                                          : GBATTN_ERR_CUDA;
+}
+
 size_t attn_fwd_paged_workspace_size(int num_seqs, int Hq, int Hkv, int D, int max_seq_len) {
     if (Hkv <= 0 || Hq % Hkv != 0 || !head_size_ok(D)) return 0;
     return gbattn::paged_plan(num_seqs, Hq, Hkv, D, max_seq_len).workspace_bytes;

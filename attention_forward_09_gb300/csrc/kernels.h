@@ -93,4 +93,18 @@ int paged_slice_rows(int D);  // tokens per TMA box of the paged cache map
 cudaError_t launch_paged(int D, const CUtensorMap& tmKV, const PagedParams& p, int num_sms,
                          cudaStream_t stream);
 
+// KV cache write (cache_write.cu): key / value [T, Hkv, D] bf16 rows into the
+// cache [2, num_blocks, block_size, Hkv, D] at slot_mapping[t].
+struct CacheWriteParams {
+    const uint4* key;
+    const uint4* value;
+    const int32_t* slot_mapping;
+    uint4* cache;
+    long long num_tokens;
+    long long num_slots;  // num_blocks * block_size
+    int row_vec;          // Hkv * D * 2 / 16: 16-byte vectors per token row
+    uint32_t* status;
+};
+cudaError_t launch_cache_write(const CacheWriteParams& p, int num_sms, cudaStream_t stream);
+
 }  // namespace gbattn

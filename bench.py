@@ -18,7 +18,7 @@ same workload on this machine's host cores (there is no other reference
 implementation of this path).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--only all|prefill|decode] [--prefill WORKLOAD] [--no-cpu]
+                       [--only all|prefill|decode|kv_write] [--prefill WORKLOAD] [--no-cpu]
 """
 
 from __future__ import annotations
@@ -514,6 +514,107 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_kv_write(args, world, rank, local):
+    """`--only kv_write`: the KV cache write of a prefill step (the packed
+    causal GQA workload's K/V stored through slot_mapping), HBM GB/s."""
+    import attention_forward_09_gb300 as gb
+    from attention_forward_09_gb300 import _build
+
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier(world)
+    gb.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk, peak_kind = peaks()
+    w = workloads.prefill_kv_write()
+    k, v, slots, shape = w.make()
+    kd, vd, sd = k.to(dev), v.to(dev), slots.to(dev)
+    cache = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def write(kk, vv, ss):
+        gb.attn_kv_cache_write(kk, vv, ss, cache, dev_status=status, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        write(kd, vd, sd)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            write(kd, vd, sd)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world)
+    nbytes = w.algorithmic_bytes()
+    gbs_rank = nbytes / (ms * 1e-3) / 1e9
+    value = sum_over_ranks(nbytes, world) / (ms * 1e-3) / 1e9
+
+    # end to end: K, V and slots up from pinned host memory, the status word back
+    hk, hv, hs = k.pin_memory(), v.pin_memory(), slots.pin_memory()
+    hst = torch.empty(1, dtype=torch.int32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        sd.copy_(hs, non_blocking=True)
+        write(kd, vd, sd)
+        hst.copy_(status, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = (k.numel() + v.numel()) * 2 + slots.numel() * 4
+
+    cpu = None
+    if world == 1 and not args.no_cpu:  # the oracle on one whole call (about a second)
+        import oracle
+
+        base = torch.zeros(shape, dtype=torch.bfloat16)
+        t0 = time.perf_counter()
+        ref = oracle.kv_cache_write(k, v, slots, base)
+        el = time.perf_counter() - t0
+        cpu = {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": cores_used(), "kind": "oracle",
+               "sample": f"one whole call: {w.tokens} tokens of {w.name}",
+               "matches": bool(torch.equal(ref.view(torch.int16), cache.cpu().view(torch.int16)))}
+    if rank != 0:
+        return
+    line = {
+        "metric": "kv cache write HBM GB/s & % of HBM peak", "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.tokens, "kv_heads": w.Hkv, "head_dim": w.D,
+                   "block_size": w.block_size, "num_blocks": w.num_blocks,
+                   "l2": "512 MiB buffer rewritten between steps (flush)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "kv_cache_write_sm103a", "achieved": gbs_rank,
+                     "peak": float(pk["hbm_gbs"]), "unit": "GB/s", "frac": gbs_rank / float(pk["hbm_gbs"]),
+                     "peak_kind": f"{peak_kind} HBM copy", "bytes_per_call": nbytes,
+                     "traffic": traffic_for(f"kv_cache_write_sm103a@{w.name}", "cache_write.cu")},
+        "cpu_baseline": cpu,
+        "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -522,8 +623,9 @@ def main():
     ap.add_argument("--prefill", choices=sorted(PREFILL_WORKLOADS), default="dit_self",
                     help="prefill workload of the step (default: the headline DiT self-attention)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
-                    help="run one part of the step (profiling captures); the default line needs 'all'")
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "kv_write"], default="all",
+                    help="run one part of the step (profiling captures), or the KV cache write alone; "
+                         "the default line needs 'all'")
     ap.add_argument("--decode-seqs", type=int, default=0,
                     help="use only the first N sequences of the decode workload (profiling captures)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle timing")
@@ -532,6 +634,8 @@ def main():
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.only == "kv_write":
+        run_kv_write(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -64,7 +64,7 @@ typedef enum {
 } gbattn_dtype;
 
 /* Bits the kernels OR into *dev_status. */
-#define GBATTN_DEV_BAD_INDEX 1u   /* block_table entry outside [0, num_blocks) (token skipped) */
+#define GBATTN_DEV_BAD_INDEX 1u   /* block_table entry or slot outside the cache (token skipped) */
 #define GBATTN_DEV_TIMEOUT 2u     /* a pipeline wait gave up; that tile's output is invalid */
 #define GBATTN_DEV_BAD_SEQLEN 4u  /* cu_seqlens / seq_lens inconsistent or above the stated max */
 
@@ -130,6 +130,29 @@ gbattn_status attn_fwd_varlen(const void* q, const void* k, const void* v,
                               int Hq, int Hkv, int D, float softmax_scale, int causal,
                               void* out, gbattn_dtype out_dtype, float* lse,
                               uint32_t* dev_status, void* stream);
+
+/*
+ * attn_kv_cache_write -- store new tokens' keys and values into the paged
+ * cache (vllm-ascend attention_v1.py, AscendAttentionBackendImpl.
+ * reshape_and_cache; slot = block * block_size + offset, the AscendMetadata
+ * slot_mapping comment).
+ *   key, value    device bf16 [num_tokens, Hkv, D], row-major
+ *   slot_mapping  device int32 [num_tokens]; token t goes to
+ *                 kv_cache[0 (key) / 1 (value), slot / block_size,
+ *                 slot % block_size, :, :]; a negative slot (padding token)
+ *                 stores nothing
+ *   kv_cache      device bf16 [2, num_blocks, block_size, Hkv, D], written in
+ *                 place; only the slots named are touched
+ *   block_size    any positive size (attn_fwd_paged reads 128)
+ * Two tokens with the same slot: one of them is stored, which one is not
+ * defined.  A slot >= num_blocks * block_size is skipped and sets
+ * GBATTN_DEV_BAD_INDEX in dev_status.  Errors: GBATTN_ERR_INVALID_ARG,
+ * GBATTN_ERR_UNSUPPORTED (head size), GBATTN_ERR_ALIGNMENT (key, value,
+ * kv_cache not 16-byte aligned), GBATTN_ERR_DEVICE / GBATTN_ERR_CUDA.
+ */
+gbattn_status attn_kv_cache_write(const void* key, const void* value, const int32_t* slot_mapping, int num_tokens,
+                                  void* kv_cache, int num_blocks, int block_size, int Hkv, int D,
+                                  uint32_t* dev_status, void* stream);
 
 /*
  * attn_fwd_paged_workspace_size -- bytes of device workspace attn_fwd_paged

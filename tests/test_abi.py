@@ -32,7 +32,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(
         ["attn_fwd_dense", "attn_fwd_varlen", "attn_fwd_paged", "attn_fwd_paged_workspace_size",
-         "attn_status_string", "attn_fwd_paged_noalloc", "attn_fwd_dense_plan"])
+         "attn_status_string", "attn_fwd_paged_noalloc", "attn_fwd_dense_plan", "attn_kv_cache_write"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -140,3 +140,14 @@ def test_dense_plan_validates_before_touching_a_device(lib):
     assert lib.attn_fwd_dense_plan(1, 8, 8, 4, 2, 128, 0, None, ctypes.byref(sp)) == 1
     assert lib.attn_fwd_dense_plan(0, 8, 8, 4, 2, 128, 0, ctypes.byref(n), ctypes.byref(sp)) == 0  # nothing to do
     assert (n.value, sp.value) == (0, 0)
+
+
+def test_kv_cache_write_validates_before_touching_a_device(lib):
+    w = lib.attn_kv_cache_write
+    assert w(P, P, P, -1, P, 8, 128, 8, 128, None, None) == 1          # negative token count
+    assert w(P, P, P, 4, P, 0, 128, 8, 128, None, None) == 1           # no blocks
+    assert w(P, P, P, 4, P, 8, 0, 8, 128, None, None) == 1             # block size
+    assert w(P, P, P, 4, P, 8, 128, 8, 80, None, None) == 2            # head size
+    assert w(None, P, P, 4, P, 8, 128, 8, 128, None, None) == 1        # null key
+    assert w(UNALIGNED, P, P, 4, P, 8, 128, 8, 128, None, None) == 3   # alignment
+    assert w(P, P, P, 0, P, 8, 128, 8, 128, None, None) == 0           # nothing to write

@@ -471,3 +471,65 @@ def test_dense_repeated_launches_stable():
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     assert torch.equal(out, ref[0]) and torch.equal(lse, ref[1])
+
+
+# ------------------------------------------------------------- KV cache write
+# attn_kv_cache_write against the oracle's kv_cache_write: a copy, so bit-exact.
+
+def _cache_write_case(seed, T, nb, bs, hkv, d, pad_every=0):
+    g = torch.Generator().manual_seed(seed)
+    k = workloads.randn_bf16(g, T, hkv, d)
+    v = workloads.randn_bf16(g, T, hkv, d)
+    cache = workloads.randn_bf16(g, 2, nb, bs, hkv, d)
+    slots = torch.randperm(nb * bs, generator=g)[:T].to(torch.int32)
+    if pad_every:
+        slots[::pad_every] = -1  # padding tokens
+    return k, v, slots, cache
+
+
+@pytest.mark.parametrize("T,nb,bs,hkv,d", [(1000, 16, 128, 8, 128), (77, 9, 16, 2, 64), (300, 4, 128, 1, 256),
+                                            (129, 3, 128, 4, 96), (500, 8, 128, 2, 192)])
+def test_kv_cache_write_bit_exact(T, nb, bs, hkv, d):
+    k, v, slots, cache = _cache_write_case(T + d, T, nb, bs, hkv, d, pad_every=7)
+    ref = oracle.kv_cache_write(k, v, slots, cache)
+    cd = cache.to(dev())
+    st = status_word()
+    gb.attn_kv_cache_write(k.to(dev()), v.to(dev()), slots.to(dev()), cd, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(cd.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+def test_kv_cache_write_slot_past_cache_sets_status():
+    k, v, slots, cache = _cache_write_case(3, 40, 4, 16, 2, 64)
+    slots[5] = 4 * 16  # one past the last slot
+    cd = cache.to(dev())
+    st = status_word()
+    gb.attn_kv_cache_write(k.to(dev()), v.to(dev()), slots.to(dev()), cd, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & gb.DEV_BAD_INDEX
+    keep = slots.clone()
+    keep[5] = -1  # the oracle refuses such a slot; the kernel skips it
+    assert torch.equal(cd.cpu().view(torch.int16), oracle.kv_cache_write(k, v, keep, cache).view(torch.int16))
+
+
+def test_kv_cache_write_then_paged_decode():
+    """New tokens written through slot_mapping = block_table[s, t // 128] * 128 + t % 128
+    are what attn_fwd_paged then reads: its output equals the oracle on contiguous K/V."""
+    w = workloads.Paged("write_then_decode", [300, 1, 1000, 129], 8, 2, 128, seed=31, extra_blocks=2)
+    q, cache, bt, sl = w.make()
+    g = torch.Generator().manual_seed(32)
+    ks = [workloads.randn_bf16(g, n, w.Hkv, w.D) for n in w.seq_lens]
+    vs = [workloads.randn_bf16(g, n, w.Hkv, w.D) for n in w.seq_lens]
+    slots = torch.tensor([int(bt[s, t // 128]) * 128 + t % 128 for s, n in enumerate(w.seq_lens) for t in range(n)],
+                         dtype=torch.int32)
+    cd = torch.zeros_like(cache).to(dev())
+    gb.attn_kv_cache_write(torch.cat(ks).to(dev()), torch.cat(vs).to(dev()), slots.to(dev()), cd)
+    st = status_word()
+    out, lse = gb.attn_fwd_paged(q.to(dev()), cd, bt.to(dev()), sl.to(dev()), max(w.seq_lens), w.scale, lse=True,
+                                 dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for s in range(len(w.seq_lens)):
+        ro, rl = oracle.attention_single(q[s:s + 1], ks[s], vs[s], w.scale, False)
+        assert_close(out[s:s + 1], lse[s:s + 1].T, ro, rl, what=f"sequence {s}")

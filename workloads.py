@@ -206,6 +206,54 @@ class Paged:
         return 4.0 * self.D * self.Hq * self.context_tokens()
 
 
+@dataclass
+class CacheWrite:
+    """New tokens' K/V [T, Hkv, D] bf16 written into a paged cache
+    [2, nb, block_size, Hkv, D] through slot_mapping [T] int32.  Each
+    document's tokens take consecutive slots of its blocks; the physical
+    blocks are a seeded random permutation (as in ``Paged``)."""
+    name: str
+    lens: list
+    Hkv: int
+    D: int
+    seed: int
+    block_size: int = BLOCK_SIZE
+
+    @property
+    def tokens(self) -> int:
+        return int(sum(self.lens))
+
+    @property
+    def num_blocks(self) -> int:
+        return sum(-(-n // self.block_size) for n in self.lens)
+
+    def make(self, chunk_rows: int = 256):
+        """Returns key, value, slot_mapping (CPU tensors) and the cache shape."""
+        g = torch.Generator().manual_seed(self.seed)
+        perm = torch.randperm(self.num_blocks, generator=g)
+        slots, at = [], 0
+        for n in self.lens:
+            nblk = -(-n // self.block_size)
+            blocks = perm[at:at + nblk]
+            t = torch.arange(n)
+            slots.append(blocks[t // self.block_size] * self.block_size + t % self.block_size)
+            at += nblk
+        key = randn_bf16_chunked(g, (self.tokens, self.Hkv, self.D), chunk_rows)
+        value = randn_bf16_chunked(g, (self.tokens, self.Hkv, self.D), chunk_rows)
+        return key, value, torch.cat(slots).to(torch.int32), (2, self.num_blocks, self.block_size, self.Hkv, self.D)
+
+    def algorithmic_bytes(self) -> int:
+        """K and V read once and written once, plus the slot list."""
+        return 2 * 2 * self.tokens * self.Hkv * self.D * 2 + 4 * self.tokens
+
+
+def prefill_kv_write() -> CacheWrite:
+    """The K/V of the packed causal GQA workload (8 documents, 8 KV heads,
+    D=128) stored into a paged cache, as a prefill step does before decode."""
+    lens = doc_lengths_capped(2, 8, 512, 8192, 32768)
+    return CacheWrite("kv_write_8docs_kv8_d128", lens, 8, 128, seed=13)
+
+
 def _uniform_int(gen: torch.Generator, lo: int, hi: int, n: int) -> list:
     """n integers uniform in [lo, hi] (inclusive)."""
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=gen)]
