@@ -237,6 +237,32 @@ def attention_paged(q, kv_cache, block_table, seq_lens, scale: float):
     return out, lse
 
 
+def attention_paged_prefill(q, kv_cache, block_table, seq_lens, cu_seqlens_q, scale: float, causal: bool):
+    """Several query tokens per sequence over the paged cache: chunked
+    prefill and speculative decode (vllm-ascend ``attention_v1.py``,
+    ``AscendAttentionState`` PrefillCacheHit / ChunkedPrefill / SpecDecoding,
+    served from the cache through ``block_table``).
+
+    q: [Tq, Hq, D] packed by cu_seqlens_q [S + 1]; the q_len_s queries of
+    sequence s are the last q_len_s of its seq_lens[s] context tokens, all
+    already in the cache.  Causal is bottom-right: query i sees keys
+    j <= i + seq_len - q_len.  Returns out [Tq, Hq, D], lse [Hq, Tq].
+    """
+    cq, sl = _i64(cu_seqlens_q), _i64(seq_lens)
+    check_cu_seqlens(cq, q.shape[0])
+    ks, vs = paged_gather(kv_cache, block_table, seq_lens)
+    tq, hq, d = q.shape
+    out = np.zeros((tq, hq, d))
+    lse = np.full((hq, tq), -np.inf)
+    for s in range(sl.size):
+        a, b = int(cq[s]), int(cq[s + 1])
+        if b > a:
+            o, l = attention_single(q[a:b], ks[s], vs[s], scale, causal)
+            out[a:b] = o
+            lse[:, a:b] = l
+    return out, lse
+
+
 def softmax_weights(q, k, scale: float, causal: bool, head: int):
     """The attention weights of one head, [Lq, Lk] (for invariant checks)."""
     q, k = _f64(q), _f64(k)

@@ -383,3 +383,59 @@ def test_kv_cache_write_padding_slots_and_errors():
     assert torch.equal(dup[0, 0, 4], 2 * k[0])  # tokens in order: the last one stays
     with pytest.raises(ValueError):
         oracle.kv_cache_write(k, k, torch.tensor([0, 24, 1]), cache)  # 3 blocks of 8 = slots 0..23
+
+
+# -------------------------------------------------------- paged prefill (f2)
+
+def _paged_ctx(seed, lens, hq, hkv, d, bs=16):
+    """A paged cache holding each sequence's contiguous K/V at a random block permutation."""
+    gen = torch.Generator().manual_seed(seed)
+    nb = sum(-(-n // bs) for n in lens) + 2
+    perm = torch.randperm(nb, generator=gen)
+    mb = max(-(-n // bs) for n in lens)
+    bt = torch.full((len(lens), mb), -1, dtype=torch.int32)
+    at = 0
+    for s, n in enumerate(lens):
+        m = -(-n // bs)
+        bt[s, :m] = perm[at:at + m]
+        at += m
+    ks = [torch.randn(n, hkv, d, generator=gen).to(torch.bfloat16) for n in lens]
+    vs = [torch.randn(n, hkv, d, generator=gen).to(torch.bfloat16) for n in lens]
+    cache = torch.full((2, nb, bs, hkv, d), float("nan"), dtype=torch.bfloat16)  # unused slots poisoned
+    slots = [int(bt[s, t // bs]) * bs + t % bs for s, n in enumerate(lens) for t in range(n)]
+    cache = oracle.kv_cache_write(torch.cat(ks), torch.cat(vs), torch.tensor(slots), cache)
+    return ks, vs, cache, bt, torch.tensor(lens, dtype=torch.int32)
+
+
+def test_paged_prefill_single_query_equals_decode():
+    """q_len = 1 with the bottom-right causal rule sees the whole context: the decode."""
+    lens = [1, 17, 40]
+    ks, vs, cache, bt, sl = _paged_ctx(1, lens, 4, 2, 32)
+    q = torch.randn(3, 4, 32, generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
+    cu = torch.tensor([0, 1, 2, 3])
+    o1, l1 = oracle.attention_paged_prefill(q, cache, bt, sl, cu, 0.2, True)
+    o2, l2 = oracle.attention_paged(q, cache, bt, sl, 0.2)
+    assert np.allclose(o1, o2, rtol=0, atol=1e-12) and np.allclose(l1.T, l2, rtol=0, atol=1e-12)
+
+
+def test_paged_prefill_whole_context_equals_varlen_causal():
+    lens = [5, 33, 16]
+    ks, vs, cache, bt, sl = _paged_ctx(3, lens, 4, 1, 32)
+    q = torch.randn(sum(lens), 4, 32, generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    cu = workloads.cu_from_lengths(lens)
+    o1, l1 = oracle.attention_paged_prefill(q, cache, bt, sl, cu, 0.3, True)
+    o2, l2 = oracle.attention_varlen(q, torch.cat(ks), torch.cat(vs), cu, cu, 0.3, True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_paged_prefill_second_chunk_equals_tail_of_full_causal():
+    """Chunked prefill: the last L - c queries over a context of L tokens give the
+    last L - c rows of causal attention over the whole sequence."""
+    L, c = 45, 19
+    ks, vs, cache, bt, sl = _paged_ctx(5, [L], 2, 2, 32)
+    qf = torch.randn(L, 2, 32, generator=torch.Generator().manual_seed(6)).to(torch.bfloat16)
+    o1, l1 = oracle.attention_paged_prefill(qf[c:], cache, bt, sl, torch.tensor([0, L - c]), 0.25, True)
+    o2, l2 = oracle.attention_single(qf, ks[0], vs[0], 0.25, True)
+    assert np.allclose(o1, o2[c:], rtol=0, atol=1e-12) and np.allclose(l1, l2[:, c:], rtol=0, atol=1e-12)
+    with pytest.raises(ValueError):
+        oracle.attention_paged_prefill(qf[c:], cache, bt, sl, torch.tensor([0, L]), 0.25, True)  # cu past Tq
