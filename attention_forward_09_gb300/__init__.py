@@ -41,6 +41,8 @@ SIGNATURES = {
     "attn_fwd_paged_noalloc": (_I, [_P, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _P]),
     "attn_fwd_dense_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "attn_kv_cache_write": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P]),
+    "attn_fwd_paged_prefill": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P,
+                                    _P, _P]),
 }
 
 _lib = None
@@ -241,3 +243,34 @@ def attn_kv_cache_write(key, value, slot_mapping, kv_cache, dev_status=None, str
                                             Hkv, D, _ptr(dev_status), _stream_handle(stream))
     _check("attn_kv_cache_write", st)
     return kv_cache
+
+
+def attn_fwd_paged_prefill(q, kv_cache, block_table, seq_lens, cu_seqlens_q, max_seqlen_q, max_seq_len,
+                           softmax_scale=None, causal=True, out=None, lse=None, out_dtype=torch.float32,
+                           dev_status=None, stream=None):
+    """Several query tokens per sequence (packed by cu_seqlens_q, the last
+    tokens of each context) against the paged cache.  Returns
+    (out [Tq, Hq, D], lse [Hq, Tq] or None); max_seqlen_q / max_seq_len are
+    host ints."""
+    _bf16_cuda("q", q)
+    _bf16_cuda("kv_cache", kv_cache)
+    Tq, Hq, D = q.shape
+    two, nb, bs, Hkv, Dk = kv_cache.shape
+    if two != 2 or Dk != D:
+        raise ValueError("kv_cache must be [2, num_blocks, block_size, Hkv, D]")
+    for n, t in (("block_table", block_table), ("seq_lens", seq_lens), ("cu_seqlens_q", cu_seqlens_q)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    if out is None:
+        out = torch.empty(Tq, Hq, D, dtype=out_dtype, device=q.device)
+    if lse is True:
+        lse = torch.empty(Hq, Tq, dtype=torch.float32, device=q.device)
+    S = cu_seqlens_q.numel() - 1
+    st = load_library().attn_fwd_paged_prefill(_ptr(q), _ptr(kv_cache), nb, bs, _ptr(block_table),
+                                               block_table.shape[1], _ptr(seq_lens), _ptr(cu_seqlens_q), S, Tq,
+                                               int(max_seqlen_q), int(max_seq_len), Hq, Hkv, D, scale,
+                                               int(bool(causal)), _ptr(out), _out_code(out.dtype), _ptr(lse),
+                                               _ptr(dev_status), _stream_handle(stream))
+    _check("attn_fwd_paged_prefill", st)
+    return out, lse

@@ -255,6 +255,58 @@ gbattn_status attn_kv_cache_write(const void* key, const void* value, const int3
                                                                                           : GBATTN_ERR_CUDA;
 }
 
+gbattn_status attn_fwd_paged_prefill(const void* q, const void* kv_cache, int num_blocks, int block_size,
+                                     const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                                     const int32_t* cu_seqlens_q, int num_seqs, int Tq, int max_seqlen_q,
+                                     int max_seq_len, int Hq, int Hkv, int D, float softmax_scale, int causal,
+                                     void* out, gbattn_dtype out_dtype, float* lse, uint32_t* dev_status,
+                                     void* stream) {
+    gbattn_status s = check_common(q, kv_cache, kv_cache, out, Hq, Hkv, D, softmax_scale, out_dtype, true);
+    if (s != GBATTN_OK) return s;
+    if (!block_table || !seq_lens || !cu_seqlens_q) return GBATTN_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || max_blocks_per_seq <= 0 || num_seqs < 0 || Tq < 0 || max_seqlen_q < 0 ||
+        max_seq_len < 0 || max_seqlen_q > Tq)
+        return GBATTN_ERR_INVALID_ARG;
+    if (block_size != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (num_seqs > 65535) return GBATTN_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || Tq == 0 || max_seqlen_q == 0) return GBATTN_OK;
+    DeviceInfo di;
+    s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    PrefillParams p{};
+    p.out = out;
+    p.lse = lse;
+    p.status = dev_status;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = nullptr;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.num_docs = num_seqs;
+    p.Tq = Tq;
+    p.Tk = 0;
+    p.max_seqlen_q = max_seqlen_q;
+    p.max_seqlen_k = max_seq_len;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.group = Hq / Hkv;
+    p.scale_log2 = softmax_scale * kLog2e;
+    p.causal = causal ? 1 : 0;
+    p.out_f32 = out_dtype == GBATTN_OUT_F32;
+    p.lse_bstride = 0;
+    p.lse_hstride = Tq;
+    p.lse_row_global = 1;
+    CUtensorMap tq, tkv, to;
+    const long long cache_rows = 2LL * num_blocks * 128;
+    if (!encode_rows_heads_d(&tq, q, Tq, Hq, D, 128) || !encode_rows_heads_d(&tkv, kv_cache, cache_rows, Hkv, D, 128) ||
+        !encode_rows_heads_d(&to, out, Tq, Hq, D, 128, p.out_f32 != 0))
+        return GBATTN_ERR_CUDA;
+    return gbattn::launch_prefill(D, tq, tkv, tkv, to, p, di.sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GBATTN_OK
+               : GBATTN_ERR_CUDA;
+}
+
 size_t attn_fwd_paged_workspace_size(int num_seqs, int Hq, int Hkv, int D, int max_seq_len) {
     if (Hkv <= 0 || Hq % Hkv != 0 || !head_size_ok(D)) return 0;
     return gbattn::paged_plan(num_seqs, Hq, Hkv, D, max_seq_len).workspace_bytes;

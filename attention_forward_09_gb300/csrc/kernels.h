@@ -41,6 +41,15 @@ struct PrefillParams {
     int split;      // > 1: each item is shared by a cluster of `split` CTAs, one key range each
     int persist;    // 1: CTA b walks items item_base + b + i * gridDim.x < item_end
     int item_end;
+    // Prefill over the paged cache (block_table != nullptr; queries packed by
+    // cu_q): K/V tile j of document s is cache block block_table[s *
+    // max_blocks + j] (block size = BN = 128), Lk = seq_lens[s]; the K and V
+    // maps both view the cache as {D, Hkv, 2 * num_blocks * 128}, V rows
+    // num_blocks * 128 on.
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    int max_blocks;
+    int num_blocks;
 };
 
 // Tensor maps are built by the host (api.cpp) over q [Tq, Hq, D] and

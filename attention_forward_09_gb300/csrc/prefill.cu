@@ -99,7 +99,19 @@ __global__ void __launch_bounds__(192, 1)
     const int doc = blockIdx.z;
     const int kvh = h / p.group;
     int q_start, Lq, k_start, Lk;
-    if (p.cu_q) {
+    if (p.block_table) {  // queries packed by cu_q, keys in the paged cache
+        q_start = p.cu_q[doc];
+        const int q_end = p.cu_q[doc + 1];
+        Lq = q_end - q_start;
+        k_start = 0;
+        Lk = p.seq_lens[doc];
+        const bool bad = q_start < 0 || Lq < 0 || q_end > p.Tq || Lq > p.max_seqlen_q || Lk < 0 ||
+                         Lk > p.max_seqlen_k || Lk > p.max_blocks * BN;
+        if (bad) {
+            if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0 && p.status) atomicOr(p.status, kDevBadSeqlen);
+            return;
+        }
+    } else if (p.cu_q) {
         q_start = p.cu_q[doc];
         k_start = p.cu_k[doc];
         const int q_end = p.cu_q[doc + 1], k_end = p.cu_k[doc + 1];
@@ -166,7 +178,15 @@ __global__ void __launch_bounds__(192, 1)
                     break;
                 }
                 const CUtensorMap* m = (t & 1) ? &tmV : &tmK;
-                const int row = k_start + (t >> 1) * BN;
+                int row = k_start + (t >> 1) * BN;
+                if (p.block_table) {  // cache block of KV tile j; a bad entry is flagged, block 0 read
+                    int blk = p.block_table[static_cast<long long>(doc) * p.max_blocks + (t >> 1)];
+                    if (blk < 0 || blk >= p.num_blocks) {
+                        if (p.status) atomicOr(p.status, kDevBadIndex);
+                        blk = 0;
+                    }
+                    row = ((t & 1) ? p.num_blocks + blk : blk) * BN;
+                }
                 mbar_arrive_expect_tx(b_kv_full(s), C::KV_BYTES);
                 for (int c = 0; c < NCH; ++c)
                     tma_load_3d(sKV + s * C::KV_BYTES + c * BN * 128, m, b_kv_full(s), c * 64, kvh, row);
@@ -228,6 +248,20 @@ __global__ void __launch_bounds__(192, 1)
             if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
             if (!(ok = wait_all(b_p_full, j & 1))) break;
             if (!(ok = wait_all(b_kv_full(vs), vph))) break;
+            if (p.block_table) {
+                // Cache slots past seq_len may hold anything, NaN included; P is 0
+                // there but 0 * NaN is not, so those V rows are zeroed first.
+                const int lim = Lk - j * BN;
+                if (lim < BN) {
+                    const uint32_t vb = sKV + vs * C::KV_BYTES;
+                    for (int idx = lane; idx < (BN - lim) * NCH * 8; idx += 32) {
+                        const int u = idx & 7, rc = idx >> 3, c = rc % NCH, rr = lim + rc / NCH;
+                        st_shared_v4(vb + c * BN * 128 + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+            }
             tc_fence_after();
             if (leader) {
                 const uint64_t b0 = dV + static_cast<uint64_t>(vs * (C::KV_BYTES >> 4));
@@ -657,7 +691,19 @@ __global__ void __launch_bounds__(384, 1)
             I.doc = blockIdx.z;
         }
         I.kvh = I.h / p.group;
-        if (p.cu_q) {
+        if (p.block_table) {  // queries packed by cu_q, keys in the paged cache
+            I.q_start = p.cu_q[I.doc];
+            const int q_end = p.cu_q[I.doc + 1];
+            I.Lq = q_end - I.q_start;
+            I.k_start = 0;
+            I.Lk = p.seq_lens[I.doc];
+            const bool bad = I.q_start < 0 || I.Lq < 0 || q_end > p.Tq || I.Lq > p.max_seqlen_q || I.Lk < 0 ||
+                             I.Lk > p.max_seqlen_k || I.Lk > p.max_blocks * BN;
+            if (bad) {
+                if (threadIdx.x == 0 && blockIdx.x == 0 && I.h == 0 && p.status) atomicOr(p.status, kDevBadSeqlen);
+                return I;
+            }
+        } else if (p.cu_q) {
             I.q_start = p.cu_q[I.doc];
             I.k_start = p.cu_k[I.doc];
             const int q_end = p.cu_q[I.doc + 1], k_end = p.cu_k[I.doc + 1];
@@ -769,7 +815,15 @@ __global__ void __launch_bounds__(384, 1)
                         break;
                     }
                     const CUtensorMap* m = (tt & 1) ? &tmV : &tmK;
-                    const int row = I.k_start + (I.j0 + (tt >> 1)) * BN;
+                    int row = I.k_start + (I.j0 + (tt >> 1)) * BN;
+                    if (p.block_table) {  // cache block of KV tile j; a bad entry is flagged, block 0 read
+                        int blk = p.block_table[static_cast<long long>(I.doc) * p.max_blocks + I.j0 + (tt >> 1)];
+                        if (blk < 0 || blk >= p.num_blocks) {
+                            if (p.status) atomicOr(p.status, kDevBadIndex);
+                            blk = 0;
+                        }
+                        row = ((tt & 1) ? p.num_blocks + blk : blk) * BN;
+                    }
                     mbar_arrive_expect_tx(b_kv_full(s), C::KV_BYTES);
                     for (int c = 0; c < NCH; ++c)
                         tma_load_3d(sKV + s * C::KV_BYTES + c * BN * 128, m, b_kv_full(s), c * 64, I.kvh, row);
@@ -862,6 +916,20 @@ __global__ void __launch_bounds__(384, 1)
                 const bool more = j + 1 < nmax;
                 bool k_ready = false;  // K_{j+1} is waited for only once an S product needs it
                 if (!(ok = wait_all(b_kv_full(vs), vph))) break;
+                if (p.block_table) {
+                    // Cache slots past seq_len may hold anything, NaN included; P is 0
+                    // there but 0 * NaN is not, so those V rows are zeroed first.
+                    const int lim = I.Lk - (I.j0 + j) * BN;
+                    if (lim < BN) {
+                        const uint32_t vb = sKV + vs * C::KV_BYTES;
+                        for (int idx = lane; idx < (BN - lim) * NCH * 8; idx += 32) {
+                            const int u = idx & 7, rc = idx >> 3, c = rc % NCH, rr = lim + rc / NCH;
+                            st_shared_v4(vb + c * BN * 128 + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                }
                 if (j < nA) {
                     if (!(ok = wait_all(b_p_full(0), (pa + j) & 1))) break;
                     tc_fence_after();

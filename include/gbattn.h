@@ -132,6 +132,39 @@ gbattn_status attn_fwd_varlen(const void* q, const void* k, const void* v,
                               uint32_t* dev_status, void* stream);
 
 /*
+ * attn_fwd_paged_prefill -- several query tokens per sequence against the
+ * paged cache: chunked prefill, prefill with a cache hit, speculative decode
+ * (vllm-ascend attention_v1.py, AscendAttentionState PrefillCacheHit /
+ * ChunkedPrefill / SpecDecoding, with the context read through block_table).
+ *   q             device bf16 [Tq, Hq, D], sequences packed by cu_seqlens_q
+ *   cu_seqlens_q  device int32 [num_seqs + 1]; sequence s owns query rows
+ *                 [cu_seqlens_q[s], cu_seqlens_q[s + 1]), its last q_len_s
+ *                 context tokens
+ *   kv_cache, num_blocks, block_size (= 128), block_table,
+ *   max_blocks_per_seq, seq_lens
+ *                 as for attn_fwd_paged; seq_lens[s] counts the whole
+ *                 context including the q_len_s new tokens, whose K/V must
+ *                 already be in the cache (attn_kv_cache_write)
+ *   max_seqlen_q  host int >= every q_len_s; max_seq_len host int >= every
+ *                 seq_lens[s]
+ *   causal        bottom-right: query i of sequence s sees keys
+ *                 j <= i + seq_lens[s] - q_len_s
+ *   out           device [Tq, Hq, D] in out_dtype; lse fp32 [Hq, Tq] or NULL
+ * Cache slots past seq_lens[s] are never used, whatever they hold.  A
+ * block_table entry outside [0, num_blocks) sets GBATTN_DEV_BAD_INDEX (the
+ * sequence's result is then undefined); inconsistent cu_seqlens_q or
+ * seq_lens set GBATTN_DEV_BAD_SEQLEN and the sequence is skipped.  Host
+ * errors as for attn_fwd_varlen, plus GBATTN_ERR_UNSUPPORTED for
+ * block_size != 128.
+ */
+gbattn_status attn_fwd_paged_prefill(const void* q, const void* kv_cache, int num_blocks, int block_size,
+                                     const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                                     const int32_t* cu_seqlens_q, int num_seqs, int Tq, int max_seqlen_q,
+                                     int max_seq_len, int Hq, int Hkv, int D, float softmax_scale, int causal,
+                                     void* out, gbattn_dtype out_dtype, float* lse, uint32_t* dev_status,
+                                     void* stream);
+
+/*
  * attn_kv_cache_write -- store new tokens' keys and values into the paged
  * cache (vllm-ascend attention_v1.py, AscendAttentionBackendImpl.
  * reshape_and_cache; slot = block * block_size + offset, the AscendMetadata

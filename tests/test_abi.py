@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(
         ["attn_fwd_dense", "attn_fwd_varlen", "attn_fwd_paged", "attn_fwd_paged_workspace_size",
-         "attn_status_string", "attn_fwd_paged_noalloc", "attn_fwd_dense_plan", "attn_kv_cache_write"])
+         "attn_status_string", "attn_fwd_paged_noalloc", "attn_fwd_dense_plan", "attn_kv_cache_write",
+         "attn_fwd_paged_prefill"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -151,3 +152,20 @@ def test_kv_cache_write_validates_before_touching_a_device(lib):
     assert w(None, P, P, 4, P, 8, 128, 8, 128, None, None) == 1        # null key
     assert w(UNALIGNED, P, P, 4, P, 8, 128, 8, 128, None, None) == 3   # alignment
     assert w(P, P, P, 0, P, 8, 128, 8, 128, None, None) == 0           # nothing to write
+
+
+def test_paged_prefill_validates_before_touching_a_device(lib):
+    def call(**kw):
+        a = dict(q=P, c=P, nb=8, bs=128, bt=P, mb=4, sl=P, cu=P, S=2, Tq=10, mq=5, ml=300, Hq=4, Hkv=2, D=128,
+                 scale=0.1, causal=1, out=P, odt=1, lse=None)
+        a.update(kw)
+        return lib.attn_fwd_paged_prefill(a["q"], a["c"], a["nb"], a["bs"], a["bt"], a["mb"], a["sl"], a["cu"],
+                                          a["S"], a["Tq"], a["mq"], a["ml"], a["Hq"], a["Hkv"], a["D"], a["scale"],
+                                          a["causal"], a["out"], a["odt"], a["lse"], None, None)
+    assert call(bs=64) == 2           # block size
+    assert call(D=80) == 2            # head size
+    assert call(Hkv=3) == 1           # Hq % Hkv
+    assert call(cu=None) == 1         # missing cu_seqlens_q
+    assert call(mq=11) == 1           # max_seqlen_q > Tq
+    assert call(q=UNALIGNED) == 3     # alignment
+    assert call(S=0) == 0             # nothing to compute

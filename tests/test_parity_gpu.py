@@ -533,3 +533,49 @@ def test_kv_cache_write_then_paged_decode():
     for s in range(len(w.seq_lens)):
         ro, rl = oracle.attention_single(q[s:s + 1], ks[s], vs[s], w.scale, False)
         assert_close(out[s:s + 1], lse[s:s + 1].T, ro, rl, what=f"sequence {s}")
+
+
+# ------------------------------------------- prefill over the paged cache (f2)
+# Several query tokens per sequence (the last q_len of its context) read their
+# keys through the block table; cache slots past each seq_len hold NaN.
+
+def _paged_prefill_run(seed, ctx, qlens, hq, hkv, d, causal, bt_override=None):
+    w = workloads.Paged(f"paged_prefill_{seed}", ctx, hq, hkv, d, seed=seed, extra_blocks=2)
+    _, cache, bt, sl = w.make()
+    if bt_override is not None:
+        bt = bt_override(bt)
+    cache_d = cache.to(dev())
+    for s, n in enumerate(ctx):
+        if n % 128:
+            cache_d[:, int(bt[s, n // 128]), n % 128:] = float("nan")
+    q = workloads.randn_bf16(torch.Generator().manual_seed(seed + 7), sum(qlens), hq, d)
+    cu = workloads.cu_from_lengths(qlens)
+    st = status_word()
+    out, lse = gb.attn_fwd_paged_prefill(q.to(dev()), cache_d, bt.to(dev()), sl.to(dev()), cu.to(dev()), max(qlens),
+                                         max(ctx), w.scale, causal, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    return (q, cache, bt, sl, cu, w.scale), out, lse, int(st.item())
+
+
+@pytest.mark.parametrize("D,hq,hkv,causal,ctx,qlens", [
+    (128, 8, 2, True, [300, 1, 1000, 129], [16, 1, 200, 129]),   # spec decode, decode, chunk, whole context
+    (64, 4, 4, True, [2000, 37], [300, 5]),
+    (96, 4, 2, False, [500, 700], [3, 16]),
+    (192, 4, 4, True, [400, 130], [130, 7]),
+    (256, 2, 1, True, [260], [260]),
+    (128, 4, 4, True, [50], [80]),                                # more queries than keys: leading rows see none
+])
+def test_paged_prefill_matches_oracle(D, hq, hkv, causal, ctx, qlens):
+    (q, cache, bt, sl, cu, s), out, lse, st = _paged_prefill_run(D + len(ctx), ctx, qlens, hq, hkv, D, causal)
+    assert st == 0
+    ro, rl = oracle.attention_paged_prefill(q, cache, bt, sl, cu, s, causal)
+    assert_close(out, lse, ro, rl, what=f"paged prefill D={D}")
+
+
+def test_paged_prefill_bad_block_sets_status():
+    def corrupt(bt):
+        bt = bt.clone()
+        bt[0, 1] = 10 ** 6
+        return bt
+    _, _, _, st = _paged_prefill_run(5, [300, 200], [20, 200], 4, 4, 128, True, bt_override=corrupt)
+    assert st & gb.DEV_BAD_INDEX
