@@ -18,7 +18,8 @@ same workload on this machine's host cores (there is no other reference
 implementation of this path).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--only all|prefill|decode|kv_write] [--prefill WORKLOAD] [--no-cpu]
+                       [--only all|prefill|decode|kv_write|paged_prefill] [--prefill WORKLOAD]
+                       [--paged-prefill chunked_prefill|spec_decode] [--no-cpu]
 """
 
 from __future__ import annotations
@@ -615,6 +616,124 @@ def run_kv_write(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+PAGED_PREFILL_WORKLOADS = {"chunked_prefill": workloads.chunked_prefill, "spec_decode": workloads.spec_decode}
+
+
+def run_paged_prefill(args, world, rank, local):
+    """`--only paged_prefill`: several query tokens per sequence over the
+    paged cache (`--paged-prefill chunked_prefill|spec_decode`), TFLOP/s."""
+    import attention_forward_09_gb300 as gb
+    from attention_forward_09_gb300 import _build
+
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier(world)
+    gb.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk, peak_kind = peaks()
+    w = PAGED_PREFILL_WORKLOADS[args.paged_prefill]()
+    q, cache, bt, sl, cu = w.make()
+    qd, cached, btd, sld, cud = q.to(dev), cache.to(dev), bt.to(dev), sl.to(dev), cu.to(dev)
+    Tq = q.shape[0]
+    outd = torch.empty(Tq, w.Hq, w.D, dtype=torch.float32, device=dev)
+    lsed = torch.empty(w.Hq, Tq, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    mq, ml = max(w.q_lens), max(w.seq_lens)
+
+    def run():
+        gb.attn_fwd_paged_prefill(qd, cached, btd, sld, cud, mq, ml, w.scale, w.causal, out=outd, lse=lsed,
+                                  dev_status=status, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        run()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            run()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world)
+    flops = w.flops()
+    tf_rank = flops / (ms * 1e-3) / 1e12
+    value = sum_over_ranks(flops, world) / (ms * 1e-3) / 1e12
+    kv_bytes = 2 * sum(w.seq_lens) * w.Hkv * w.D * 2
+
+    # end to end: the step's new queries and metadata up (the cache is resident), out and lse back
+    hq, hcu, hbt, hsl = q.pin_memory(), cu.pin_memory(), bt.pin_memory(), sl.pin_memory()
+    hout, hlse = torch.empty(outd.shape).pin_memory(), torch.empty(lsed.shape).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for d_, h_ in ((qd, hq), (cud, hcu), (btd, hbt), (sld, hsl)):
+            d_.copy_(h_, non_blocking=True)
+        run()
+        hout.copy_(outd, non_blocking=True)
+        hlse.copy_(lsed, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = q.numel() * 2 + (cu.numel() + bt.numel() + sl.numel()) * 4
+
+    cpu = None
+    if world == 1 and not args.no_cpu:  # the oracle on the shortest sequences, about 10 s
+        import oracle
+
+        t0, done, fl = time.perf_counter(), 0, 0.0
+        order = sorted(range(len(w.seq_lens)), key=lambda s: w.seq_lens[s])
+        for s in order:
+            a, b = int(cu[s]), int(cu[s + 1])
+            oracle.attention_paged_prefill(q[a:b], cache, bt[s:s + 1], sl[s:s + 1], torch.tensor([0, b - a]),
+                                           w.scale, w.causal)
+            fl += 4.0 * w.D * w.Hq * sum(max(0, min(w.seq_lens[s], i + w.seq_lens[s] - (b - a) + 1))
+                                           for i in range(b - a))
+            done += 1
+            if time.perf_counter() - t0 > 10.0:
+                break
+        el = time.perf_counter() - t0
+        cpu = {"value": fl / el / 1e12, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+               "sample": f"{done} of {len(order)} sequences of {w.name} (shortest first)"}
+    if rank != 0:
+        return
+    peak_tf = float(pk["bf16_tflops"])
+    line = {
+        "metric": "paged prefill TFLOP/s & % bf16 TC peak", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "num_seqs": len(w.seq_lens), "q_len": mq, "context_tokens": sum(w.seq_lens),
+                   "heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D, "causal": w.causal, "block_size": 128,
+                   "l2": "512 MiB buffer rewritten between steps (flush)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": f"fmha2_fwd_sm103a<Prefill2Cfg<{w.D}>> (paged)",
+                     "achieved": tf_rank, "peak": peak_tf, "unit": "TFLOP/s", "frac": tf_rank / peak_tf,
+                     "peak_kind": f"{peak_kind} bf16 burst", "flops_per_launch": flops, "traffic": None},
+        "kv_read": {"bytes": kv_bytes, "GB/s": kv_bytes / (ms * 1e-3) / 1e9,
+                    "frac_of_hbm": kv_bytes / (ms * 1e-3) / 1e9 / float(pk["hbm_gbs"])},
+        "cpu_baseline": cpu,
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hout.numel() * 4 + hlse.numel() * 4},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -623,7 +742,9 @@ def main():
     ap.add_argument("--prefill", choices=sorted(PREFILL_WORKLOADS), default="dit_self",
                     help="prefill workload of the step (default: the headline DiT self-attention)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "kv_write"], default="all",
+    ap.add_argument("--paged-prefill", choices=sorted(PAGED_PREFILL_WORKLOADS), default="chunked_prefill",
+                    help="workload of --only paged_prefill")
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "kv_write", "paged_prefill"], default="all",
                     help="run one part of the step (profiling captures), or the KV cache write alone; "
                          "the default line needs 'all'")
     ap.add_argument("--decode-seqs", type=int, default=0,
@@ -636,6 +757,8 @@ def main():
         run_reference(args, world, rank)
     elif args.only == "kv_write":
         run_kv_write(args, world, rank, local)
+    elif args.only == "paged_prefill":
+        run_paged_prefill(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

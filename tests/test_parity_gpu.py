@@ -579,3 +579,23 @@ def test_paged_prefill_bad_block_sets_status():
         return bt
     _, _, _, st = _paged_prefill_run(5, [300, 200], [20, 200], 4, 4, 128, True, bt_override=corrupt)
     assert st & gb.DEV_BAD_INDEX
+
+
+def test_config_chunked_prefill_sampled():
+    """The bench's chunked-prefill workload at full size, sampled rows of the
+    shortest and the longest sequence against the oracle."""
+    w = workloads.chunked_prefill()
+    q, cache, bt, sl, cu = w.make()
+    st = status_word()
+    out, lse = gb.attn_fwd_paged_prefill(q.to(dev()), cache.to(dev()), bt.to(dev()), sl.to(dev()), cu.to(dev()),
+                                         max(w.q_lens), max(w.seq_lens), w.scale, True, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for s in (min(range(len(w.seq_lens)), key=lambda i: w.seq_lens[i]),
+              max(range(len(w.seq_lens)), key=lambda i: w.seq_lens[i])):
+        a, b = int(cu[s]), int(cu[s + 1])
+        ks, vs = oracle.paged_gather(cache, bt[s:s + 1], sl[s:s + 1])
+        rows = _sample_rows(b - a, 6, s)
+        ro, rl = oracle.attention_single(q[a:b], ks[0], vs[0], w.scale, True, rows=rows)
+        glob = [a + r for r in rows]
+        assert_close(out[glob], lse[:, glob], ro, rl, what=f"chunked prefill sequence {s}")

@@ -254,6 +254,62 @@ def prefill_kv_write() -> CacheWrite:
     return CacheWrite("kv_write_8docs_kv8_d128", lens, 8, 128, seed=13)
 
 
+@dataclass
+class PagedPrefill:
+    """q_len new query tokens per sequence (the last of its context) against
+    a paged cache: the context (cache, block table) is the ``Paged`` one of
+    the same sizes and seed; q [sum q_len, Hq, D] packed by cu_seqlens_q."""
+    name: str
+    seq_lens: list
+    q_lens: list
+    Hq: int
+    Hkv: int
+    D: int
+    seed: int
+    causal: bool = True
+
+    def paged(self) -> Paged:
+        return Paged(self.name, self.seq_lens, self.Hq, self.Hkv, self.D, seed=self.seed)
+
+    @property
+    def scale(self) -> float:
+        return default_scale(self.D)
+
+    def make(self, chunk_rows: int = 256):
+        """Returns q, kv_cache, block_table, seq_lens, cu_seqlens_q (CPU tensors)."""
+        _, cache, bt, sl = self.paged().make(chunk_rows)
+        q = randn_bf16(torch.Generator().manual_seed(self.seed + 2000), sum(self.q_lens), self.Hq, self.D)
+        return q, cache, bt, sl, cu_from_lengths(self.q_lens)
+
+    def visible_pairs(self) -> int:
+        total = 0
+        for lk, lq in zip(self.seq_lens, self.q_lens):
+            if not self.causal:
+                total += lq * lk
+            else:  # query i sees keys j <= i + lk - lq
+                total += sum(max(0, min(lk, i + lk - lq + 1)) for i in range(lq))
+        return total
+
+    def flops(self) -> float:
+        return 4.0 * self.D * self.Hq * self.visible_pairs()
+
+
+def chunked_prefill() -> PagedPrefill:
+    """16 sequences with contexts U[2048, 32768] (seed 14) whose last 512
+    tokens are a new prefill chunk, 32 query / 8 KV heads, D=128, causal."""
+    g = torch.Generator().manual_seed(14)
+    lens = _uniform_int(g, 2048, 32768, 16)
+    return PagedPrefill("chunked_prefill_16seq_q512_h32kv8_d128", lens, [512] * 16, 32, 8, 128, seed=14)
+
+
+def spec_decode() -> PagedPrefill:
+    """64 sequences with contexts U[1024, 32768] (seed 3, as the decode
+    workload) verifying 16 draft tokens each, 32 query / 8 KV heads, D=128."""
+    g = torch.Generator().manual_seed(3)
+    lens = _uniform_int(g, 1024, 32768, 64)
+    return PagedPrefill("spec_decode_64seq_q16_h32kv8_d128", lens, [16] * 64, 32, 8, 128, seed=3)
+
+
 def _uniform_int(gen: torch.Generator, lo: int, hi: int, n: int) -> list:
     """n integers uniform in [lo, hi] (inclusive)."""
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=gen)]
