@@ -6,6 +6,7 @@ reference legs may import this package.  The library never does.
 
 from .attention import (  # noqa: F401
     attention_dense,
+    attention_masked,
     attention_paged,
     attention_paged_prefill,
     attention_single,

@@ -263,6 +263,31 @@ def attention_paged_prefill(q, kv_cache, block_table, seq_lens, cu_seqlens_q, sc
     return out, lse
 
 
+def attention_masked(q, k, v, mask, scale: float, causal: bool, cross: bool = False):
+    """Padded batch with a [B, S] padding mask (vllm-omni ``flash_attn.py``,
+    ``FlashAttentionImpl._forward_varlen_masked``): the masked-in tokens of
+    each batch row are packed in order, varlen attention runs on the packed
+    documents, and the output goes back to the padded positions, zeros at
+    the padding.  ``cross``: the mask covers the keys only and every query
+    row is kept (the cross-attention branch there).
+
+    q: [B, Sq, Hq, D]; k, v: [B, Sk, Hkv, D]; mask: [B, Sk] (nonzero = token).
+    Returns out [B, Sq, Hq, D] and lse [B, Hq, Sq] (-inf at padded rows).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    m = np.asarray(mask.cpu() if hasattr(mask, "cpu") else mask) != 0
+    b, sq, hq, d = q.shape
+    out = np.zeros((b, sq, hq, d))
+    lse = np.full((b, hq, sq), -np.inf)
+    for i in range(b):
+        keys = np.nonzero(m[i])[0]  # packed order = position order
+        rows = np.arange(sq) if cross else keys
+        o, l = attention_single(q[i, rows], k[i, keys], v[i, keys], scale, causal)
+        out[i, rows] = o
+        lse[i][:, rows] = l
+    return out, lse
+
+
 def softmax_weights(q, k, scale: float, causal: bool, head: int):
     """The attention weights of one head, [Lq, Lk] (for invariant checks)."""
     q, k = _f64(q), _f64(k)

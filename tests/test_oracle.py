@@ -439,3 +439,59 @@ def test_paged_prefill_second_chunk_equals_tail_of_full_causal():
     assert np.allclose(o1, o2[c:], rtol=0, atol=1e-12) and np.allclose(l1, l2[:, c:], rtol=0, atol=1e-12)
     with pytest.raises(ValueError):
         oracle.attention_paged_prefill(qf[c:], cache, bt, sl, torch.tensor([0, L]), 0.25, True)  # cu past Tq
+
+
+# ------------------------------------------------ padding mask -> varlen (f3)
+
+def _masked_case(seed, b, s, hq, hkv, d):
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(b, s, hq, d, generator=gen).to(torch.bfloat16)
+    k = torch.randn(b, s, hkv, d, generator=gen).to(torch.bfloat16)
+    v = torch.randn(b, s, hkv, d, generator=gen).to(torch.bfloat16)
+    return q, k, v
+
+
+def test_masked_prefix_mask_equals_dense_on_the_valid_prefix():
+    """A mask that keeps a prefix of each row is attention over that prefix,
+    zeros and -inf at the padding."""
+    q, k, v = _masked_case(1, 2, 20, 2, 1, 32)
+    n = [13, 20]
+    mask = torch.zeros(2, 20, dtype=torch.uint8)
+    for i, L in enumerate(n):
+        mask[i, :L] = 1
+    for causal in (False, True):
+        o, l = oracle.attention_masked(q, k, v, mask, 0.3, causal)
+        for i, L in enumerate(n):
+            r_o, r_l = oracle.attention_single(q[i, :L], k[i, :L], v[i, :L], 0.3, causal)
+            assert np.array_equal(o[i, :L], r_o) and np.array_equal(l[i][:, :L], r_l)
+            assert np.all(o[i, L:] == 0) and np.all(l[i][:, L:] == -np.inf)
+
+
+def test_masked_scattered_mask_is_the_packed_varlen_of_the_kept_tokens():
+    q, k, v = _masked_case(2, 2, 24, 4, 2, 32)
+    g = torch.Generator().manual_seed(3)
+    mask = (torch.rand(2, 24, generator=g) < 0.6).to(torch.uint8)
+    keep = [torch.nonzero(mask[i]).flatten() for i in range(2)]
+    lens = [len(x) for x in keep]
+    qp = torch.cat([q[i, keep[i]] for i in range(2)])
+    kp = torch.cat([k[i, keep[i]] for i in range(2)])
+    vp = torch.cat([v[i, keep[i]] for i in range(2)])
+    cu = workloads.cu_from_lengths(lens)
+    rv, rl = oracle.attention_varlen(qp, kp, vp, cu, cu, 0.2, True)
+    o, l = oracle.attention_masked(q, k, v, mask, 0.2, True)
+    for i in range(2):
+        a = int(cu[i])
+        assert np.array_equal(o[i, keep[i].numpy()], rv[a:a + lens[i]])
+        assert np.array_equal(l[i][:, keep[i].numpy()], rl[:, a:a + lens[i]])
+    assert np.all(o[mask.numpy() == 0] == 0)
+
+
+def test_masked_cross_keeps_every_query():
+    """Cross-attention: masked-out keys get no weight, every query row is computed."""
+    q, k, v = _masked_case(4, 1, 16, 2, 2, 32)
+    mask = torch.zeros(1, 16, dtype=torch.uint8)
+    mask[0, [1, 4, 5, 11]] = 1
+    o, l = oracle.attention_masked(q, k, v, mask, 0.25, False, cross=True)
+    idx = [1, 4, 5, 11]
+    r_o, r_l = oracle.attention_single(q[0], k[0, idx], v[0, idx], 0.25, False)
+    assert np.array_equal(o[0], r_o) and np.array_equal(l[0], r_l)
