@@ -43,6 +43,10 @@ SIGNATURES = {
     "attn_kv_cache_write": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P]),
     "attn_fwd_paged_prefill": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P,
                                     _P, _P]),
+    "attn_mask_to_varlen": (_I, [_P, _I, _I, _P, _P, _P]),
+    "attn_pack_rows": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "attn_unpack_rows": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "attn_unpack_lse": (_I, [_P, _P, _I, _I, _I, _P, _P]),
 }
 
 _lib = None
@@ -274,3 +278,76 @@ def attn_fwd_paged_prefill(q, kv_cache, block_table, seq_lens, cu_seqlens_q, max
                                                _ptr(dev_status), _stream_handle(stream))
     _check("attn_fwd_paged_prefill", st)
     return out, lse
+
+
+def attn_mask_to_varlen(mask, stream=None):
+    """mask [B, S] (bool or uint8 CUDA, nonzero = token) -> (cu_seqlens [B+1], packed_pos [B*S]) int32."""
+    if mask.dim() != 2 or not mask.is_cuda or mask.element_size() != 1:
+        raise ValueError("mask must be a [B, S] bool / uint8 CUDA tensor")
+    mask = mask.contiguous()
+    B, S = mask.shape
+    cu = torch.empty(B + 1, dtype=torch.int32, device=mask.device)
+    pos = torch.empty(B * S, dtype=torch.int32, device=mask.device)
+    st = load_library().attn_mask_to_varlen(_ptr(mask), B, S, _ptr(cu), _ptr(pos), _stream_handle(stream))
+    _check("attn_mask_to_varlen", st)
+    return cu, pos
+
+
+def attn_pack_rows(x, packed_pos, cu_seqlens, stream=None):
+    """x [B, S, ...] contiguous CUDA -> packed [B*S, ...]: the masked-in rows in order, then zero rows."""
+    B, S = x.shape[:2]
+    packed = torch.empty((B * S,) + tuple(x.shape[2:]), dtype=x.dtype, device=x.device)
+    rb = x[0, 0].numel() * x.element_size()
+    st = load_library().attn_pack_rows(_ptr(x), _ptr(packed_pos), _ptr(cu_seqlens), B, S, rb, _ptr(packed),
+                                       _stream_handle(stream))
+    _check("attn_pack_rows", st)
+    return packed
+
+
+def attn_unpack_rows(packed, packed_pos, B, S, stream=None):
+    """packed [B*S, ...] -> [B, S, ...] with zeros at the padding."""
+    out = torch.empty((B, S) + tuple(packed.shape[1:]), dtype=packed.dtype, device=packed.device)
+    rb = packed[0].numel() * packed.element_size()
+    st = load_library().attn_unpack_rows(_ptr(packed), _ptr(packed_pos), B, S, rb, _ptr(out), _stream_handle(stream))
+    _check("attn_unpack_rows", st)
+    return out
+
+
+def attn_unpack_lse(lse_packed, packed_pos, B, S, stream=None):
+    """lse_packed [H, B*S] -> [B, H, S], -inf at the padding."""
+    H = lse_packed.shape[0]
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=lse_packed.device)
+    st = load_library().attn_unpack_lse(_ptr(lse_packed), _ptr(packed_pos), B, H, S, _ptr(lse), _stream_handle(stream))
+    _check("attn_unpack_lse", st)
+    return lse
+
+
+def attn_fwd_masked(q, k, v, mask, softmax_scale=None, causal=False, cross=False, lse=False, out_dtype=torch.float32,
+                    dev_status=None, stream=None):
+    """Padded batch q [B, Sq, Hq, D], k/v [B, Sk, Hkv, D] with a [B, Sk]
+    padding mask: the masked-in tokens are packed, attended as varlen
+    documents and put back (zeros, lse -inf at the padding).  cross=True:
+    the mask covers the keys only and every query row is kept.  Returns
+    (out [B, Sq, Hq, D], lse [B, Hq, Sq] or None)."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _bf16_cuda(n, t)
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    if not cross and Sq != Sk:
+        raise ValueError("self-attention needs Sq == Sk (use cross=True for a key-only mask)")
+    cu_k, pos_k = attn_mask_to_varlen(mask, stream)
+    kp, vp = attn_pack_rows(k, pos_k, cu_k, stream), attn_pack_rows(v, pos_k, cu_k, stream)
+    if cross:
+        qp = q.view(B * Sq, Hq, D)
+        cu_q = torch.arange(0, (B + 1) * Sq, Sq, dtype=torch.int32, device=q.device)
+    else:
+        qp, cu_q = attn_pack_rows(q, pos_k, cu_k, stream), cu_k
+    out_p, lse_p = attn_fwd_varlen(qp, kp, vp, cu_q, cu_k, Sq, Sk, softmax_scale, causal, lse=True if lse else None,
+                                   out_dtype=out_dtype, dev_status=dev_status, stream=stream)
+    if cross:
+        out = out_p.view(B, Sq, Hq, D)
+        lse_out = lse_p.view(Hq, B, Sq).permute(1, 0, 2) if lse else None
+    else:
+        out = attn_unpack_rows(out_p, pos_k, B, Sq, stream)
+        lse_out = attn_unpack_lse(lse_p, pos_k, B, Sq, stream) if lse else None
+    return out, lse_out

@@ -307,6 +307,68 @@ gbattn_status attn_fwd_paged_prefill(const void* q, const void* kv_cache, int nu
                : GBATTN_ERR_CUDA;
 }
 
+gbattn_status attn_mask_to_varlen(const uint8_t* mask, int B, int S, int32_t* cu_seqlens, int32_t* packed_pos,
+                                  void* stream) {
+    if (B < 0 || S < 0) return GBATTN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * S > 0x7fffffffLL || B > 0x7fffffff / 2) return GBATTN_ERR_UNSUPPORTED;
+    if (B == 0) return GBATTN_OK;
+    if (!mask || !cu_seqlens || (S > 0 && !packed_pos)) return GBATTN_ERR_INVALID_ARG;
+    DeviceInfo di;
+    gbattn_status s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    return gbattn::launch_mask_to_varlen(mask, B, S, cu_seqlens, packed_pos, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? GBATTN_OK
+               : GBATTN_ERR_CUDA;
+}
+
+gbattn_status attn_pack_rows(const void* x, const int32_t* packed_pos, const int32_t* cu_seqlens, int B, int S,
+                             int row_bytes, void* packed, void* stream) {
+    if (B < 0 || S < 0 || row_bytes <= 0 || row_bytes % 16 != 0) return GBATTN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * S > 0x7fffffffLL) return GBATTN_ERR_UNSUPPORTED;
+    if (B == 0 || S == 0) return GBATTN_OK;
+    if (!x || !packed_pos || !cu_seqlens || !packed) return GBATTN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(packed)) return GBATTN_ERR_ALIGNMENT;
+    DeviceInfo di;
+    gbattn_status s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    return gbattn::launch_pack_rows(x, packed_pos, cu_seqlens, B, static_cast<long long>(B) * S, row_bytes, packed,
+                                    di.sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GBATTN_OK
+               : GBATTN_ERR_CUDA;
+}
+
+gbattn_status attn_unpack_rows(const void* packed, const int32_t* packed_pos, int B, int S, int row_bytes, void* out,
+                               void* stream) {
+    if (B < 0 || S < 0 || row_bytes <= 0 || row_bytes % 16 != 0) return GBATTN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * S > 0x7fffffffLL) return GBATTN_ERR_UNSUPPORTED;
+    if (B == 0 || S == 0) return GBATTN_OK;
+    if (!packed || !packed_pos || !out) return GBATTN_ERR_INVALID_ARG;
+    if (!aligned16(packed) || !aligned16(out)) return GBATTN_ERR_ALIGNMENT;
+    DeviceInfo di;
+    gbattn_status s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    return gbattn::launch_unpack_rows(packed, packed_pos, static_cast<long long>(B) * S, row_bytes, out, di.sms,
+                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GBATTN_OK
+               : GBATTN_ERR_CUDA;
+}
+
+gbattn_status attn_unpack_lse(const float* lse_packed, const int32_t* packed_pos, int B, int H, int S, float* lse,
+                              void* stream) {
+    if (B < 0 || S < 0 || H <= 0) return GBATTN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * S > 0x7fffffffLL) return GBATTN_ERR_UNSUPPORTED;
+    if (B == 0 || S == 0) return GBATTN_OK;
+    if (!lse_packed || !packed_pos || !lse) return GBATTN_ERR_INVALID_ARG;
+    DeviceInfo di;
+    gbattn_status s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    return gbattn::launch_unpack_lse(lse_packed, static_cast<long long>(B) * S, packed_pos, B, H, S, lse, di.sms,
+                                     static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GBATTN_OK
+               : GBATTN_ERR_CUDA;
+}
+
 size_t attn_fwd_paged_workspace_size(int num_seqs, int Hq, int Hkv, int D, int max_seq_len) {
     if (Hkv <= 0 || Hq % Hkv != 0 || !head_size_ok(D)) return 0;
     return gbattn::paged_plan(num_seqs, Hq, Hkv, D, max_seq_len).workspace_bytes;

@@ -116,4 +116,18 @@ struct CacheWriteParams {
 };
 cudaError_t launch_cache_write(const CacheWriteParams& p, int num_sms, cudaStream_t stream);
 
+// Padding mask <-> packed varlen (masks.cu).  mask [B, S] bytes (nonzero =
+// token); cu_seqlens [B + 1]; packed_pos [B * S]: the token's packed row or -1.
+cudaError_t launch_mask_to_varlen(const uint8_t* mask, int B, int S, int32_t* cu_seqlens, int32_t* packed_pos,
+                                  cudaStream_t st);
+// x [rows, row_bytes] -> packed [rows, row_bytes]; rows past cu_seqlens[B] zeroed
+cudaError_t launch_pack_rows(const void* x, const int32_t* packed_pos, const int32_t* cu_seqlens, int B, long long rows,
+                             int row_bytes, void* packed, int num_sms, cudaStream_t st);
+// packed [rows, row_bytes] -> out [rows, row_bytes], zero rows where packed_pos < 0
+cudaError_t launch_unpack_rows(const void* packed, const int32_t* packed_pos, long long rows, int row_bytes, void* out,
+                               int num_sms, cudaStream_t st);
+// lse_packed [H, hstride] -> lse [B, H, S], -inf where packed_pos < 0
+cudaError_t launch_unpack_lse(const float* lse_packed, long long hstride, const int32_t* packed_pos, int B, int H,
+                              int S, float* lse, int num_sms, cudaStream_t st);
+
 }  // namespace gbattn

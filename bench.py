@@ -18,7 +18,7 @@ same workload on this machine's host cores (there is no other reference
 implementation of this path).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--only all|prefill|decode|kv_write|paged_prefill] [--prefill WORKLOAD]
+                       [--only all|prefill|decode|kv_write|paged_prefill|masked] [--prefill WORKLOAD]
                        [--paged-prefill chunked_prefill|spec_decode] [--no-cpu]
 """
 
@@ -734,6 +734,94 @@ def run_paged_prefill(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_masked(args, world, rank, local):
+    """`--only masked`: a padded batch through attn_fwd_masked (mask ->
+    cu_seqlens, pack, varlen attention, unpack), TFLOP/s on the kept tokens."""
+    import attention_forward_09_gb300 as gb
+    from attention_forward_09_gb300 import _build
+
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier(world)
+    gb.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk, peak_kind = peaks()
+    w = workloads.masked_dit()
+    q, k, v, mask = w.make()
+    qd, kd, vd, md = q.to(dev), k.to(dev), v.to(dev), mask.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def run():
+        return gb.attn_fwd_masked(qd, kd, vd, md, w.scale, w.causal, lse=True, dev_status=status, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        run()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            run()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world)
+    flops = w.flops()
+    tf_rank = flops / (ms * 1e-3) / 1e12
+    value = sum_over_ranks(flops, world) / (ms * 1e-3) / 1e12
+
+    hq_, hk_, hv_, hm_ = q.pin_memory(), k.pin_memory(), v.pin_memory(), mask.pin_memory()
+    out0, lse0 = run()
+    hout, hlse = torch.empty(out0.shape).pin_memory(), torch.empty(lse0.shape).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for d_, h_ in ((qd, hq_), (kd, hk_), (vd, hv_), (md, hm_)):
+            d_.copy_(h_, non_blocking=True)
+        o, l = run()
+        hout.copy_(o, non_blocking=True)
+        hlse.copy_(l, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    if rank != 0:
+        return
+    peak_tf = float(pk["bf16_tflops"])
+    line = {
+        "metric": "masked attention TFLOP/s & % bf16 TC peak", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "seq_len": w.S, "kept": w.lens, "heads": w.Hq, "head_dim": w.D,
+                   "causal": w.causal, "l2": "512 MiB buffer rewritten between steps (flush)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "mask_to_varlen + 3 x pack_rows + fmha2 + unpack_rows + unpack_lse",
+                     "achieved": tf_rank, "peak": peak_tf, "unit": "TFLOP/s", "frac": tf_rank / peak_tf,
+                     "peak_kind": f"{peak_kind} bf16 burst", "flops_per_launch": flops, "traffic": None},
+        "cpu_baseline": None,
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2 + mask.numel(),
+                "d2h_bytes_per_step": hout.numel() * 4 + hlse.numel() * 4},
+        "gpu_launches": 7 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -744,7 +832,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--paged-prefill", choices=sorted(PAGED_PREFILL_WORKLOADS), default="chunked_prefill",
                     help="workload of --only paged_prefill")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "kv_write", "paged_prefill"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "kv_write", "paged_prefill", "masked"], default="all",
                     help="run one part of the step (profiling captures), or the KV cache write alone; "
                          "the default line needs 'all'")
     ap.add_argument("--decode-seqs", type=int, default=0,
@@ -759,6 +847,8 @@ def main():
         run_kv_write(args, world, rank, local)
     elif args.only == "paged_prefill":
         run_paged_prefill(args, world, rank, local)
+    elif args.only == "masked":
+        run_masked(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -165,6 +165,42 @@ gbattn_status attn_fwd_paged_prefill(const void* q, const void* kv_cache, int nu
                                      void* stream);
 
 /*
+ * Padding mask <-> packed documents, for padded batches (vllm-omni
+ * flash_attn.py, FlashAttentionImpl._forward_varlen_masked: the masked-in
+ * tokens of each row are packed in order, attended as varlen documents, and
+ * the output goes back to their positions with zeros at the padding).  With
+ * these helpers the whole path runs on the device with no host round trip:
+ * attn_fwd_varlen is called with Tq = Tk = B * S rows and max_seqlen = S.
+ *
+ * attn_mask_to_varlen -- mask: device bytes [B, S], nonzero = token.
+ *   cu_seqlens  out, device int32 [B + 1]: the packed document boundaries
+ *   packed_pos  out, device int32 [B * S]: packed row of token (b, s), or -1
+ *
+ * attn_pack_rows -- x: device [B * S, row_bytes] (one token row each, e.g.
+ *   Hkv * D bf16), packed: device [B * S, row_bytes].  Token (b, s) goes to
+ *   packed row packed_pos[b * S + s]; rows at or past cu_seqlens[B] are
+ *   zeroed, so that attention reads no uninitialised row.
+ *
+ * attn_unpack_rows -- packed [B * S, row_bytes] -> out [B * S, row_bytes]:
+ *   the packed row of each token, zeros at the padding.
+ *
+ * attn_unpack_lse -- lse_packed fp32 [H, B * S] (attn_fwd_varlen's layout)
+ *   -> lse fp32 [B, H, S], -inf at the padding.
+ *
+ * row_bytes must be a positive multiple of 16 and x, packed, out 16-byte
+ * aligned.  Errors: GBATTN_ERR_INVALID_ARG, GBATTN_ERR_ALIGNMENT,
+ * GBATTN_ERR_UNSUPPORTED (B * S >= 2^31), GBATTN_ERR_DEVICE / _CUDA.
+ */
+gbattn_status attn_mask_to_varlen(const uint8_t* mask, int B, int S, int32_t* cu_seqlens, int32_t* packed_pos,
+                                  void* stream);
+gbattn_status attn_pack_rows(const void* x, const int32_t* packed_pos, const int32_t* cu_seqlens, int B, int S,
+                             int row_bytes, void* packed, void* stream);
+gbattn_status attn_unpack_rows(const void* packed, const int32_t* packed_pos, int B, int S, int row_bytes, void* out,
+                               void* stream);
+gbattn_status attn_unpack_lse(const float* lse_packed, const int32_t* packed_pos, int B, int H, int S, float* lse,
+                              void* stream);
+
+/*
  * attn_kv_cache_write -- store new tokens' keys and values into the paged
  * cache (vllm-ascend attention_v1.py, AscendAttentionBackendImpl.
  * reshape_and_cache; slot = block * block_size + offset, the AscendMetadata

@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted(
         ["attn_fwd_dense", "attn_fwd_varlen", "attn_fwd_paged", "attn_fwd_paged_workspace_size",
          "attn_status_string", "attn_fwd_paged_noalloc", "attn_fwd_dense_plan", "attn_kv_cache_write",
-         "attn_fwd_paged_prefill"])
+         "attn_fwd_paged_prefill", "attn_mask_to_varlen", "attn_pack_rows", "attn_unpack_rows",
+         "attn_unpack_lse"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -169,3 +170,14 @@ def test_paged_prefill_validates_before_touching_a_device(lib):
     assert call(mq=11) == 1           # max_seqlen_q > Tq
     assert call(q=UNALIGNED) == 3     # alignment
     assert call(S=0) == 0             # nothing to compute
+
+
+def test_mask_helpers_validate_before_touching_a_device(lib):
+    assert lib.attn_mask_to_varlen(P, -1, 8, P, P, None) == 1
+    assert lib.attn_mask_to_varlen(None, 2, 8, P, P, None) == 1
+    assert lib.attn_mask_to_varlen(P, 0, 8, P, P, None) == 0
+    assert lib.attn_pack_rows(P, P, P, 2, 8, 24, P, None) == 1          # row bytes not a multiple of 16
+    assert lib.attn_pack_rows(UNALIGNED, P, P, 2, 8, 256, P, None) == 3
+    assert lib.attn_unpack_rows(P, P, 2, 8, 256, UNALIGNED, None) == 3
+    assert lib.attn_unpack_lse(P, P, 2, 0, 8, P, None) == 1             # no heads
+    assert lib.attn_pack_rows(P, P, P, 1 << 16, 1 << 16, 256, P, None) == 2  # B * S >= 2^31

@@ -599,3 +599,75 @@ def test_config_chunked_prefill_sampled():
         ro, rl = oracle.attention_single(q[a:b], ks[0], vs[0], w.scale, True, rows=rows)
         glob = [a + r for r in rows]
         assert_close(out[glob], lse[:, glob], ro, rl, what=f"chunked prefill sequence {s}")
+
+
+# ----------------------------------------------- padding mask -> varlen (f3)
+
+def test_mask_to_varlen_indices_bit_exact():
+    g = torch.Generator().manual_seed(8)
+    mask = (torch.rand(5, 3000, generator=g) < 0.55).to(torch.uint8)
+    mask[2] = 0  # a row with no token at all
+    cu, pos = gb.attn_mask_to_varlen(mask.to(dev()))
+    torch.cuda.synchronize()
+    counts = mask.sum(dim=1)
+    ref_cu = torch.zeros(6, dtype=torch.int64)
+    ref_cu[1:] = torch.cumsum(counts, 0)
+    flat = mask.flatten().to(torch.int64)
+    ref_pos = torch.where(flat != 0, torch.cumsum(flat, 0) - 1, torch.full_like(flat, -1))
+    assert torch.equal(cu.cpu().to(torch.int64), ref_cu) and torch.equal(pos.cpu().to(torch.int64), ref_pos)
+
+
+def test_pack_rows_zeroes_the_tail_and_round_trips():
+    g = torch.Generator().manual_seed(9)
+    B, S = 3, 500
+    x = workloads.randn_bf16(g, B, S, 2, 64)
+    mask = (torch.rand(B, S, generator=g) < 0.4).to(torch.uint8)
+    xd = x.to(dev())
+    xd[mask.to(dev()) == 0] = float("nan")  # padding rows must never be copied
+    cu, pos = gb.attn_mask_to_varlen(mask.to(dev()))
+    packed = gb.attn_pack_rows(xd, pos, cu)
+    back = gb.attn_unpack_rows(packed, pos, B, S)
+    torch.cuda.synchronize()
+    total = int(mask.sum())
+    keep = mask.flatten() != 0
+    assert torch.equal(packed[:total].cpu().view(torch.int16), x.flatten(0, 1)[keep].view(torch.int16))
+    assert torch.all(packed[total:].cpu() == 0)
+    ref = torch.where(mask[..., None, None] != 0, x, torch.zeros_like(x))
+    assert torch.equal(back.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("kind,causal,D,hq,hkv,S", [
+    ("scattered", False, 128, 4, 2, 300), ("scattered", True, 64, 4, 4, 257), ("prefix", True, 128, 2, 1, 400),
+    ("empty_row", False, 96, 2, 2, 200), ("cross", False, 128, 4, 4, 77)])
+def test_masked_matches_oracle(kind, causal, D, hq, hkv, S):
+    g = torch.Generator().manual_seed(D + S)
+    B, Sq = 3, (200 if kind == "cross" else S)
+    q = workloads.randn_bf16(g, B, Sq, hq, D)
+    k = workloads.randn_bf16(g, B, S, hkv, D)
+    v = workloads.randn_bf16(g, B, S, hkv, D)
+    if kind == "prefix":
+        mask = torch.zeros(B, S, dtype=torch.uint8)
+        for i, n in enumerate([S, S // 2, 13]):
+            mask[i, :n] = 1
+    else:
+        mask = (torch.rand(B, S, generator=g) < 0.65).to(torch.uint8)
+        if kind == "empty_row":
+            mask[1] = 0
+    st = status_word()
+    out, lse = gb.attn_fwd_masked(q.to(dev()), k.to(dev()), v.to(dev()), mask.to(dev()), 1.0 / math.sqrt(D), causal,
+                                  cross=(kind == "cross"), lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ro, rl = oracle.attention_masked(q, k, v, mask, 1.0 / math.sqrt(D), causal, cross=(kind == "cross"))
+    assert_close(out, lse, ro, rl, what=f"masked {kind}")
+
+
+def test_masked_bf16_output():
+    g = torch.Generator().manual_seed(10)
+    q, k, v = (workloads.randn_bf16(g, 2, 256, 2, 128) for _ in range(3))
+    mask = (torch.rand(2, 256, generator=g) < 0.5).to(torch.uint8)
+    out, _ = gb.attn_fwd_masked(q.to(dev()), k.to(dev()), v.to(dev()), mask.to(dev()), 0.088, False,
+                                out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    ro, _ = oracle.attention_masked(q, k, v, mask, 0.088, False)
+    assert np.all(np.abs(to_np(out) - ro) <= OUT_TOL + bf16_half_ulp(ro))

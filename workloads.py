@@ -310,6 +310,49 @@ def spec_decode() -> PagedPrefill:
     return PagedPrefill("spec_decode_64seq_q16_h32kv8_d128", lens, [16] * 64, 32, 8, 128, seed=3)
 
 
+@dataclass
+class Masked:
+    """Padded batch q/k/v [B, S, H, D] with a [B, S] padding mask keeping the
+    first lens[b] tokens of row b (the structural padding at the end of a
+    packed video-latent batch)."""
+    name: str
+    lens: list
+    S: int
+    Hq: int
+    Hkv: int
+    D: int
+    causal: bool
+    seed: int
+
+    @property
+    def B(self) -> int:
+        return len(self.lens)
+
+    @property
+    def scale(self) -> float:
+        return default_scale(self.D)
+
+    def make(self):
+        g = torch.Generator().manual_seed(self.seed)
+        q = randn_bf16(g, self.B, self.S, self.Hq, self.D)
+        k = randn_bf16(g, self.B, self.S, self.Hkv, self.D)
+        v = randn_bf16(g, self.B, self.S, self.Hkv, self.D)
+        mask = torch.zeros(self.B, self.S, dtype=torch.uint8)
+        for b, n in enumerate(self.lens):
+            mask[b, :n] = 1
+        return q, k, v, mask
+
+    def flops(self) -> float:
+        pairs = sum((n * (n + 1)) // 2 if self.causal else n * n for n in self.lens)
+        return 4.0 * self.D * self.Hq * pairs
+
+
+def masked_dit() -> Masked:
+    """The DiT self-attention shape, B=2, S=4096, 24 heads, D=128, with the
+    second row padded after 3072 tokens."""
+    return Masked("masked_dit_b2_s4096_h24_d128_len4096_3072", [4096, 3072], 4096, 24, 24, 128, False, seed=15)
+
+
 def _uniform_int(gen: torch.Generator, lo: int, hi: int, n: int) -> list:
     """n integers uniform in [lo, hi] (inclusive)."""
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=gen)]
