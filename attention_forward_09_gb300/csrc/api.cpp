@@ -68,14 +68,15 @@ gbattn_status device_info(DeviceInfo* out) {
 // TMA map with box {128 bytes of D, 1, box_rows} and 128-byte swizzle;
 // loads read out-of-range elements as zero, stores skip them.
 bool encode_rows_heads_d(CUtensorMap* m, const void* base, long long rows, int heads, int d, int box_rows,
-                         bool f32 = false) {
+                         bool f32 = false, int box_heads = 1) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t es = f32 ? 4 : 2;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                           static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(heads) * d * es};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 1, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(box_heads),
+                         static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                     const_cast<void*>(base), dims, strides, box, estr,
@@ -297,10 +298,17 @@ gbattn_status attn_fwd_paged_prefill(const void* q, const void* kv_cache, int nu
     p.lse_bstride = 0;
     p.lse_hstride = Tq;
     p.lse_row_global = 1;
+    // D <= 128 with a GQA group dividing 128: one CTA per KV head, a tile's
+    // rows are 128 / group tokens x the group's heads (each KV byte read once
+    // per group; short query chunks fill the tile group times better).
+    const int g = Hq / Hkv;
+    p.gqa_pack = (D <= 128 && g >= 2 && 128 % g == 0) ? 1 : 0;
+    const int box_heads = p.gqa_pack ? g : 1, box_rows = 128 / box_heads;
     CUtensorMap tq, tkv, to;
     const long long cache_rows = 2LL * num_blocks * 128;
-    if (!encode_rows_heads_d(&tq, q, Tq, Hq, D, 128) || !encode_rows_heads_d(&tkv, kv_cache, cache_rows, Hkv, D, 128) ||
-        !encode_rows_heads_d(&to, out, Tq, Hq, D, 128, p.out_f32 != 0))
+    if (!encode_rows_heads_d(&tq, q, Tq, Hq, D, box_rows, false, box_heads) ||
+        !encode_rows_heads_d(&tkv, kv_cache, cache_rows, Hkv, D, 128) ||
+        !encode_rows_heads_d(&to, out, Tq, Hq, D, box_rows, p.out_f32 != 0, box_heads))
         return GBATTN_ERR_CUDA;
     return gbattn::launch_prefill(D, tq, tkv, tkv, to, p, di.sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? GBATTN_OK

@@ -50,6 +50,10 @@ struct PrefillParams {
     const int32_t* seq_lens;
     int max_blocks;
     int num_blocks;
+    // GQA packing (cu_q modes, D <= 128): a CTA serves one KV head; a tile's
+    // 128 rows are 128 / group tokens x the group's query heads (the Q and
+    // out maps then have boxes {64 or 128 B, group, 128 / group}).
+    int gqa_pack;
 };
 
 // Tensor maps are built by the host (api.cpp) over q [Tq, Hq, D] and

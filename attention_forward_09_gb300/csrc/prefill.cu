@@ -662,6 +662,10 @@ __global__ void __launch_bounds__(384, 1)
     // the other: the next item's Q and K/V loads and first S products then
     // overlap the current item's softmax tail and epilogue.
     const bool split = p.split > 1;  // kernel-uniform
+    // GQA packing (paged prefill): a tile's 128 rows are TPT tokens x the
+    // group's query heads, row r = token r / group, head r % group.
+    const int gq = p.gqa_pack ? p.group : 1;
+    const int TPT = BM / gq;
     const bool persist = p.persist != 0;
     const int crank = split ? static_cast<int>(cluster_ctarank()) : 0;
     struct Item {
@@ -687,7 +691,7 @@ __global__ void __launch_bounds__(384, 1)
         } else {
             if (i > 0) return I;
             tile = p.causal ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
-            I.h = blockIdx.y;
+            I.h = blockIdx.y * gq;  // with GQA packing blockIdx.y is the KV head
             I.doc = blockIdx.z;
         }
         I.kvh = I.h / p.group;
@@ -721,18 +725,18 @@ __global__ void __launch_bounds__(384, 1)
             I.k_start = I.doc * p.Sk;
             I.Lk = p.Sk;
         }
-        I.q0 = tile * 2 * BM;
+        I.q0 = tile * 2 * TPT;
         if (I.q0 >= I.Lq) return I;
         I.diag = I.Lk - I.Lq;
         // KV tiles each query tile needs (0 for a tile with no rows)
         auto kv_tiles = [&](int first_row) {
             if (first_row >= I.Lq) return 0;
             int kend = I.Lk;
-            if (p.causal) kend = min(I.Lk, min(first_row + BM - 1, I.Lq - 1) + I.diag + 1);
+            if (p.causal) kend = min(I.Lk, min(first_row + TPT - 1, I.Lq - 1) + I.diag + 1);
             return kend > 0 ? (kend + BN - 1) / BN : 0;
         };
         I.nA = kv_tiles(I.q0);
-        I.nB = kv_tiles(I.q0 + BM);
+        I.nB = kv_tiles(I.q0 + TPT);
         // A split item (non-causal, so both tiles see the same keys) gives CTA
         // `crank` of its cluster KV tiles [j0, j1); loops below count from j0.
         I.j0 = 0;
@@ -800,7 +804,7 @@ __global__ void __launch_bounds__(384, 1)
                 for (int x = 0; x < 2; ++x)
                     for (int c = 0; c < NCH; ++c)
                         tma_load_3d(sQ + x * C::QT_BYTES + c * BM * 128, &tmQ, b_q_full, c * 64, I.h,
-                                    I.q_start + I.q0 + x * BM);
+                                    I.q_start + I.q0 + x * TPT);
                 ++nq;
                 for (int tt = 0; tt < 2 * I.nmax; ++tt, ++t) {
                     // The previous item's output may be staged in every K/V stage but
@@ -992,9 +996,10 @@ __global__ void __launch_bounds__(384, 1)
         if (!I.valid) break;
         const int h = I.h, doc = I.doc, q_start = I.q_start, Lq = I.Lq, Lk = I.Lk, q0 = I.q0, diag = I.diag;
         const int nA = I.nA, nB = I.nB, nmax = I.nmax, j0 = I.j0;
-        const int row = q0 + x * BM + r;       // row within the document
+        const int row = q0 + x * TPT + r / gq;  // token within the document
+        const int hh = h + r % gq;              // query head of this row
         const int n_kv = x ? nB : nA;
-        const int qfirst = q0 + x * BM;
+        const int qfirst = q0 + x * TPT;
         const int row_lim = p.causal ? min(Lk, row + diag + 1) : Lk;  // keys [0, row_lim) visible
         float m = -INFINITY, l = 0.f;
         for (int j = 0; j < n_kv; ++j) {
@@ -1077,7 +1082,7 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_drain, 0, abort_flag));  // all MMAs done
             tc_fence_after();
             split_merge<D>(smem, sKV, tO, x * BM + r, m, l, n_kv > 0, ok, crank, q0, Lq, q_start, h, doc, p);
-        } else if (qfirst + BM <= Lq && (x == 1 || nA >= nB)) {
+        } else if (qfirst + TPT <= Lq && (x == 1 || nA >= nB)) {
             // A tile wholly inside its document leaves through shared memory:
             // its rows are staged in the TMA 128-byte-swizzled box layout
             // (128 rows x 128 bytes per 16 KB box) in slots of the K/V area
@@ -1150,14 +1155,14 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (ok && p.lse) {
                 const long long lrow = p.lse_row_global ? (q_start + row) : row;
-                p.lse[doc * p.lse_bstride + h * p.lse_hstride + lrow] =
+                p.lse[doc * p.lse_bstride + hh * p.lse_hstride + lrow] =
                     l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
             }
         } else {
         if (persist && r == 0) mbar_arrive(b_staged);  // nothing staged
         const bool row_valid = ok && row < Lq;
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        const long long orow = static_cast<long long>(q_start + row) * p.Hq + h;
+        const long long orow = static_cast<long long>(q_start + row) * p.Hq + hh;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -1191,7 +1196,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (row_valid && p.lse) {
             const long long lrow = p.lse_row_global ? (q_start + row) : row;
-            p.lse[doc * p.lse_bstride + h * p.lse_hstride + lrow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+            p.lse[doc * p.lse_bstride + hh * p.lse_hstride + lrow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
         }
         }
         tbase += 2 * nmax;
@@ -1287,7 +1292,9 @@ template <class C, class K>
 static cudaError_t plan_two_tile(K kernel, const PrefillParams& p, int num_sms, PrefillPlan* pl) {
     *pl = PrefillPlan{};
     if (p.cu_q) {
-        pl->n_items = pl->n_full = static_cast<long long>((p.max_seqlen_q + 255) / 256) * p.Hq * p.num_docs;
+        const int tpt = p.gqa_pack ? 128 / p.group : 128;
+        pl->n_items = pl->n_full =
+            static_cast<long long>((p.max_seqlen_q + 2 * tpt - 1) / (2 * tpt)) * (p.gqa_pack ? p.Hkv : p.Hq) * p.num_docs;
         pl->launches = pl->n_items > 0 ? 1 : 0;
         return cudaSuccess;
     }
@@ -1324,7 +1331,8 @@ static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUten
     q.item_base = 0;
     if (p.cu_q) {
         q.linear = 0;
-        dim3 grid((p.max_seqlen_q + 255) / 256, p.Hq, p.num_docs);
+        const int tpt = p.gqa_pack ? 128 / p.group : 128;  // tokens per tile
+        dim3 grid((p.max_seqlen_q + 2 * tpt - 1) / (2 * tpt), p.gqa_pack ? p.Hkv : p.Hq, p.num_docs);
         kernel<<<grid, 384, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, q);
         return cudaGetLastError();
     }

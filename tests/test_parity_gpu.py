@@ -564,6 +564,8 @@ def _paged_prefill_run(seed, ctx, qlens, hq, hkv, d, causal, bt_override=None):
     (192, 4, 4, True, [400, 130], [130, 7]),
     (256, 2, 1, True, [260], [260]),
     (128, 4, 4, True, [50], [80]),                                # more queries than keys: leading rows see none
+    (128, 8, 1, True, [700, 3000, 129], [16, 16, 5]),             # GQA packing, 16 tokens x 8 heads per tile
+    (64, 16, 2, False, [900, 260], [300, 40]),                    # GQA packing, 16 x 8, several tile pairs
 ])
 def test_paged_prefill_matches_oracle(D, hq, hkv, causal, ctx, qlens):
     (q, cache, bt, sl, cu, s), out, lse, st = _paged_prefill_run(D + len(ctx), ctx, qlens, hq, hkv, D, causal)
@@ -671,3 +673,20 @@ def test_masked_bf16_output():
     torch.cuda.synchronize()
     ro, _ = oracle.attention_masked(q, k, v, mask, 0.088, False)
     assert np.all(np.abs(to_np(out) - ro) <= OUT_TOL + bf16_half_ulp(ro))
+
+
+def test_config_spec_decode_sampled():
+    """The bench's speculative-decode workload at full size (GQA-packed tiles):
+    every row of three sequences against the oracle."""
+    w = workloads.spec_decode()
+    q, cache, bt, sl, cu = w.make()
+    st = status_word()
+    out, lse = gb.attn_fwd_paged_prefill(q.to(dev()), cache.to(dev()), bt.to(dev()), sl.to(dev()), cu.to(dev()),
+                                         max(w.q_lens), max(w.seq_lens), w.scale, True, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for s in (0, 17, len(w.seq_lens) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        ks, vs = oracle.paged_gather(cache, bt[s:s + 1], sl[s:s + 1])
+        ro, rl = oracle.attention_single(q[a:b], ks[0], vs[0], w.scale, True)
+        assert_close(out[a:b], lse[:, a:b], ro, rl, what=f"spec decode sequence {s}")
