@@ -69,7 +69,7 @@ struct PrefillCfg {
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: tolerate P up to 2^8 before rescaling O
 
-template <class C>
+template <class C, bool PAGED>
 __global__ void __launch_bounds__(192, 1)
     fmha_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(192, 1)
     const int doc = blockIdx.z;
     const int kvh = h / p.group;
     int q_start, Lq, k_start, Lk;
-    if (p.block_table) {  // queries packed by cu_q, keys in the paged cache
+    if (PAGED) {  // queries packed by cu_q, keys in the paged cache
         q_start = p.cu_q[doc];
         const int q_end = p.cu_q[doc + 1];
         Lq = q_end - q_start;
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 const CUtensorMap* m = (t & 1) ? &tmV : &tmK;
                 int row = k_start + (t >> 1) * BN;
-                if (p.block_table) {  // cache block of KV tile j; a bad entry is flagged, block 0 read
+                if (PAGED) {  // cache block of KV tile j; a bad entry is flagged, block 0 read
                     int blk = p.block_table[static_cast<long long>(doc) * p.max_blocks + (t >> 1)];
                     if (blk < 0 || blk >= p.num_blocks) {
                         if (p.status) atomicOr(p.status, kDevBadIndex);
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(192, 1)
             if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
             if (!(ok = wait_all(b_p_full, j & 1))) break;
             if (!(ok = wait_all(b_kv_full(vs), vph))) break;
-            if (p.block_table) {
+            if (PAGED) {
                 // Cache slots past seq_len may hold anything, NaN included; P is 0
                 // there but 0 * NaN is not, so those V rows are zeroed first.
                 const int lim = Lk - j * BN;
@@ -629,7 +629,7 @@ __device__ __forceinline__ void split_merge(uint8_t* smem, uint32_t sO, uint32_t
     cluster_sync();  // no CTA leaves while another still reads its shared memory
 }
 
-template <class C>
+template <class C, bool PAGED>
 __global__ void __launch_bounds__(384, 1)
     fmha2_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(384, 1)
     const bool split = p.split > 1;  // kernel-uniform
     // GQA packing (paged prefill): a tile's 128 rows are TPT tokens x the
     // group's query heads, row r = token r / group, head r % group.
-    const int gq = p.gqa_pack ? p.group : 1;
+    const int gq = (PAGED && p.gqa_pack) ? p.group : 1;
     const int TPT = BM / gq;
     const bool persist = p.persist != 0;
     const int crank = split ? static_cast<int>(cluster_ctarank()) : 0;
@@ -695,7 +695,7 @@ __global__ void __launch_bounds__(384, 1)
             I.doc = blockIdx.z;
         }
         I.kvh = I.h / p.group;
-        if (p.block_table) {  // queries packed by cu_q, keys in the paged cache
+        if (PAGED) {  // queries packed by cu_q, keys in the paged cache
             I.q_start = p.cu_q[I.doc];
             const int q_end = p.cu_q[I.doc + 1];
             I.Lq = q_end - I.q_start;
@@ -820,7 +820,7 @@ __global__ void __launch_bounds__(384, 1)
                     }
                     const CUtensorMap* m = (tt & 1) ? &tmV : &tmK;
                     int row = I.k_start + (I.j0 + (tt >> 1)) * BN;
-                    if (p.block_table) {  // cache block of KV tile j; a bad entry is flagged, block 0 read
+                    if (PAGED) {  // cache block of KV tile j; a bad entry is flagged, block 0 read
                         int blk = p.block_table[static_cast<long long>(I.doc) * p.max_blocks + I.j0 + (tt >> 1)];
                         if (blk < 0 || blk >= p.num_blocks) {
                             if (p.status) atomicOr(p.status, kDevBadIndex);
@@ -920,7 +920,7 @@ __global__ void __launch_bounds__(384, 1)
                 const bool more = j + 1 < nmax;
                 bool k_ready = false;  // K_{j+1} is waited for only once an S product needs it
                 if (!(ok = wait_all(b_kv_full(vs), vph))) break;
-                if (p.block_table) {
+                if (PAGED) {
                     // Cache slots past seq_len may hold anything, NaN included; P is 0
                     // there but 0 * NaN is not, so those V rows are zeroed first.
                     const int lim = I.Lk - (I.j0 + j) * BN;
@@ -1227,7 +1227,7 @@ using Cfg256 = PrefillCfg<256, 128, 2>;
 
 // Sets the dynamic shared-memory limit of `kernel` once per device (one flag
 // set per configuration: the kernels of several configurations share a type).
-template <class C, class K>
+template <class C, bool PAGED, class K>
 static cudaError_t set_smem_attr(K kernel, int bytes) {
     static bool done[64];
     int dev = 0;
@@ -1239,11 +1239,11 @@ static cudaError_t set_smem_attr(K kernel, int bytes) {
     return e;
 }
 
-template <class C, class K>
+template <class C, bool PAGED, class K>
 static cudaError_t launch_kernel(K kernel, int threads, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmO, const PrefillParams& p,
                                  int rows_per_cta, cudaStream_t stream) {
-    cudaError_t e = set_smem_attr<C>(kernel, C::SMEM_BYTES);
+    cudaError_t e = set_smem_attr<C, PAGED>(kernel, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid((p.max_seqlen_q + rows_per_cta - 1) / rows_per_cta, p.Hq, p.num_docs);
     kernel<<<grid, threads, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, p);
@@ -1288,7 +1288,7 @@ static int resident_clusters(K kernel, int c) {
 // full, its items go to a second launch in which a cluster of `split` CTAs
 // shares each item along the keys and merges the partial results on chip,
 // so that the wave lasts about 1/split of an item instead of a whole one.
-template <class C, class K>
+template <class C, bool PAGED, class K>
 static cudaError_t plan_two_tile(K kernel, const PrefillParams& p, int num_sms, PrefillPlan* pl) {
     *pl = PrefillPlan{};
     if (p.cu_q) {
@@ -1298,7 +1298,7 @@ static cudaError_t plan_two_tile(K kernel, const PrefillParams& p, int num_sms, 
         pl->launches = pl->n_items > 0 ? 1 : 0;
         return cudaSuccess;
     }
-    cudaError_t e = set_smem_attr<C>(kernel, C::SMEM_BYTES);
+    cudaError_t e = set_smem_attr<C, PAGED>(kernel, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     pl->tiles = (p.Sq + 255) / 256;
     pl->n_items = static_cast<long long>(pl->tiles) * p.Hq * p.num_docs;
@@ -1318,13 +1318,13 @@ static cudaError_t plan_two_tile(K kernel, const PrefillParams& p, int num_sms, 
     return cudaSuccess;
 }
 
-template <class C, class K>
+template <class C, bool PAGED, class K>
 static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                    const CUtensorMap& tmO, const PrefillParams& p, int num_sms, cudaStream_t stream) {
     PrefillPlan pl;
-    cudaError_t e = plan_two_tile<C>(kernel, p, num_sms, &pl);
+    cudaError_t e = plan_two_tile<C, PAGED>(kernel, p, num_sms, &pl);
     if (e != cudaSuccess) return e;
-    e = set_smem_attr<C>(kernel, C::SMEM_BYTES);
+    e = set_smem_attr<C, PAGED>(kernel, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     PrefillParams q = p;
     q.split = 0;
@@ -1367,25 +1367,48 @@ static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUten
     return cudaGetLastError();
 }
 
+// The paged mode (K/V through block_table) is a separate instantiation, so
+// that the dense and varlen kernels carry none of its code.
+template <class C>
+static cudaError_t two_tile(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                            const CUtensorMap& tmO, const PrefillParams& p, int num_sms, cudaStream_t stream) {
+    return p.block_table ? launch_two_tile<C, true>(fmha2_fwd_sm103a<C, true>, tmQ, tmK, tmV, tmO, p, num_sms, stream)
+                         : launch_two_tile<C, false>(fmha2_fwd_sm103a<C, false>, tmQ, tmK, tmV, tmO, p, num_sms,
+                                                     stream);
+}
+
+template <class C>
+static cudaError_t one_tile(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                            const CUtensorMap& tmO, const PrefillParams& p, cudaStream_t stream) {
+    return p.block_table ? launch_kernel<C, true>(fmha_fwd_sm103a<C, true>, 192, tmQ, tmK, tmV, tmO, p, 128, stream)
+                         : launch_kernel<C, false>(fmha_fwd_sm103a<C, false>, 192, tmQ, tmK, tmV, tmO, p, 128, stream);
+}
+
+template <class C>
+static cudaError_t plan_for(const PrefillParams& p, int num_sms, PrefillPlan* pl) {
+    return p.block_table ? plan_two_tile<C, true>(fmha2_fwd_sm103a<C, true>, p, num_sms, pl)
+                         : plan_two_tile<C, false>(fmha2_fwd_sm103a<C, false>, p, num_sms, pl);
+}
+
 int prefill_block_n(int D) { return (D == 64 || D == 96 || D == 128 || D == 192 || D == 256) ? 128 : 0; }
 
 cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            const CUtensorMap& tmO, const PrefillParams& p, int num_sms, cudaStream_t stream) {
     switch (D) {
-        case 64: return launch_two_tile<Cfg64>(fmha2_fwd_sm103a<Cfg64>, tmQ, tmK, tmV, tmO, p, num_sms, stream);
-        case 96: return launch_two_tile<Cfg96>(fmha2_fwd_sm103a<Cfg96>, tmQ, tmK, tmV, tmO, p, num_sms, stream);
-        case 128: return launch_two_tile<Cfg128>(fmha2_fwd_sm103a<Cfg128>, tmQ, tmK, tmV, tmO, p, num_sms, stream);
-        case 192: return launch_kernel<Cfg192>(fmha_fwd_sm103a<Cfg192>, 192, tmQ, tmK, tmV, tmO, p, 128, stream);
-        case 256: return launch_kernel<Cfg256>(fmha_fwd_sm103a<Cfg256>, 192, tmQ, tmK, tmV, tmO, p, 128, stream);
+        case 64: return two_tile<Cfg64>(tmQ, tmK, tmV, tmO, p, num_sms, stream);
+        case 96: return two_tile<Cfg96>(tmQ, tmK, tmV, tmO, p, num_sms, stream);
+        case 128: return two_tile<Cfg128>(tmQ, tmK, tmV, tmO, p, num_sms, stream);
+        case 192: return one_tile<Cfg192>(tmQ, tmK, tmV, tmO, p, stream);
+        case 256: return one_tile<Cfg256>(tmQ, tmK, tmV, tmO, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t prefill_plan(int D, const PrefillParams& p, int num_sms, PrefillPlan* pl) {
     switch (D) {
-        case 64: return plan_two_tile<Cfg64>(fmha2_fwd_sm103a<Cfg64>, p, num_sms, pl);
-        case 96: return plan_two_tile<Cfg96>(fmha2_fwd_sm103a<Cfg96>, p, num_sms, pl);
-        case 128: return plan_two_tile<Cfg128>(fmha2_fwd_sm103a<Cfg128>, p, num_sms, pl);
+        case 64: return plan_for<Cfg64>(p, num_sms, pl);
+        case 96: return plan_for<Cfg96>(p, num_sms, pl);
+        case 128: return plan_for<Cfg128>(p, num_sms, pl);
         case 192:
         case 256: {
             *pl = PrefillPlan{};
