@@ -10,10 +10,13 @@ from .attention import (  # noqa: F401
     attention_paged,
     attention_paged_prefill,
     attention_single,
+    attention_block_sparse,
     attention_varlen,
     check_cu_seqlens,
     kv_cache_write,
     paged_gather,
     softmax_weights,
     visible_mask,
+    vsa_block_map,
+    vsa_blocks,
 )

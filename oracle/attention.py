@@ -288,6 +288,87 @@ def attention_masked(q, k, v, mask, scale: float, causal: bool, cross: bool = Fa
     return out, lse
 
 
+def vsa_blocks(prefix_segments, video_shape, tile=(4, 4, 4), block=64):
+    """Token blocks of block-sparse video attention (vllm-omni
+    ``fastvideo_vsa.py``, ``_get_h3_tile_metadata``): each prefix segment
+    cut into chunks of ``block`` tokens, then the (T, H, W) video grid, whose
+    tokens follow the prefix in T, H, W order, cut into ``tile`` boxes taken
+    in T, H, W order (boxes at the grid's far edges are smaller).
+
+    Returns (blocks, n_prefix_blocks): blocks is a list of int arrays of
+    token indices, each a block in the order the method lays them out.
+    """
+    blocks, at = [], 0
+    for seg in prefix_segments:
+        for c0 in range(0, seg, block):
+            blocks.append(np.arange(at + c0, at + min(seg, c0 + block)))
+        at += seg
+    n_prefix = len(blocks)
+    t, h, w = video_shape
+    grid = np.arange(t * h * w).reshape(t, h, w) + at
+    for i in range(0, t, tile[0]):
+        for j in range(0, h, tile[1]):
+            for k in range(0, w, tile[2]):
+                blocks.append(grid[i:i + tile[0], j:j + tile[1], k:k + tile[2]].flatten())
+    return blocks, n_prefix
+
+
+def vsa_block_map(q, k, blocks, n_prefix, topk: int, scale: float):
+    """Block selection (``fastvideo_vsa.py``, ``_pool_h3_tiles`` and
+    ``_build_h3_block_map``): the mean query and key of every block, block
+    scores scale * mean_q . mean_k per head, then for each query block the
+    ``topk`` best video key blocks (ties to the lower block index), plus
+    every prefix key block; prefix query blocks keep every key block.
+
+    q, k: [S, Hq, D] / [S, Hkv, D] (one sequence).  Returns bool [Hq, NB, NB].
+    """
+    q, k = _f64(q), _f64(k)
+    hq, hkv = q.shape[1], k.shape[1]
+    g = hq // hkv
+    nb = len(blocks)
+    mq = np.stack([q[b].mean(axis=0) for b in blocks])  # [NB, Hq, D]
+    mk = np.stack([k[b].mean(axis=0) for b in blocks])  # [NB, Hkv, D]
+    n_video = nb - n_prefix
+    keep = min(topk, n_video)
+    bm = np.zeros((hq, nb, nb), dtype=bool)
+    for h in range(hq):
+        sc = scale * (mq[:, h, :] @ mk[:, h // g, :].T)  # [NB, NB]
+        for i in range(nb):
+            if i < n_prefix or keep == n_video:
+                bm[h, i, :] = True
+                continue
+            order = np.argsort(-sc[i, n_prefix:], kind="stable")[:keep] + n_prefix
+            bm[h, i, order] = True
+            bm[h, i, :n_prefix] = True
+    return bm
+
+
+def attention_block_sparse(q, k, v, blocks, block_map, scale: float):
+    """Each query token attends the tokens of the key blocks its block keeps
+    (``fastvideo_vsa.py``, the block-sparse forward behind ``_forward_h3``,
+    without the trained gate branch), in token order.
+
+    q: [S, Hq, D]; k, v: [S, Hkv, D]; block_map bool [Hq, NB, NB].
+    Returns out [S, Hq, D], lse [Hq, S].
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    s_len, hq, d = q.shape
+    g = hq // k.shape[1]
+    out = np.zeros((s_len, hq, d))
+    lse = np.full((hq, s_len), -np.inf)
+    for h in range(hq):
+        kv = h // g
+        for i, rows in enumerate(blocks):
+            keys = np.concatenate([blocks[j] for j in np.nonzero(block_map[h, i])[0]])
+            sc = scale * (q[rows, h, :] @ k[keys, kv, :].T)
+            m = sc.max(axis=1)
+            p = np.exp(sc - m[:, None])
+            l = p.sum(axis=1)
+            out[rows, h, :] = (p @ v[keys, kv, :]) / l[:, None]
+            lse[h, rows] = m + np.log(l)
+    return out, lse
+
+
 def softmax_weights(q, k, scale: float, causal: bool, head: int):
     """The attention weights of one head, [Lq, Lk] (for invariant checks)."""
     q, k = _f64(q), _f64(k)

@@ -495,3 +495,85 @@ def test_masked_cross_keeps_every_query():
     idx = [1, 4, 5, 11]
     r_o, r_l = oracle.attention_single(q[0], k[0, idx], v[0, idx], 0.25, False)
     assert np.array_equal(o[0], r_o) and np.array_equal(l[0], r_l)
+
+
+# --------------------------------------------- block-sparse video attention (f4)
+
+def test_vsa_blocks_partition_the_sequence_into_boxes():
+    prefix, shape = [70, 5], (5, 6, 7)
+    blocks, n_prefix = oracle.vsa_blocks(prefix, shape)
+    allidx = np.concatenate(blocks)
+    assert np.array_equal(np.sort(allidx), np.arange(75 + 5 * 6 * 7))  # every token exactly once
+    assert [len(b) for b in blocks[:n_prefix]] == [64, 6, 5]
+    # video block sizes: per-axis sizes 4,...,4,remainder multiplied out in T, H, W order
+    per_axis = [[min(4, n - i) for i in range(0, n, 4)] for n in shape]
+    expect = [a * b * c for a in per_axis[0] for b in per_axis[1] for c in per_axis[2]]
+    assert [len(b) for b in blocks[n_prefix:]] == expect
+    for b in blocks[n_prefix:]:  # each block is an axis-aligned box of the grid
+        t, h, w = np.unravel_index(b - 75, shape)
+        for axis in (t, h, w):
+            lo, hi = axis.min(), axis.max()
+            assert lo % 4 == 0 and hi - lo < 4 and set(axis) == set(range(lo, hi + 1))
+        assert len(b) == len(set(t)) * len(set(h)) * len(set(w))
+
+
+def _vsa_inputs(seed, prefix, shape, hq, hkv, d):
+    n = sum(prefix) + int(np.prod(shape))
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(n, hq, d, generator=g).to(torch.bfloat16), torch.randn(n, hkv, d, generator=g).to(torch.bfloat16),
+            torch.randn(n, hkv, d, generator=g).to(torch.bfloat16))
+
+
+def test_vsa_keeping_every_block_is_dense_attention():
+    q, k, v = _vsa_inputs(1, [20], (4, 5, 6), 4, 2, 32)
+    blocks, npre = oracle.vsa_blocks([20], (4, 5, 6))
+    bm = oracle.vsa_block_map(q, k, blocks, npre, topk=100, scale=0.2)
+    assert bm.all()
+    o, l = oracle.attention_block_sparse(q, k, v, blocks, bm, 0.2)
+    r_o, r_l = oracle.attention_single(q, k, v, 0.2, False)
+    assert np.allclose(o, r_o, rtol=0, atol=1e-12) and np.allclose(l, r_l, rtol=0, atol=1e-12)
+
+
+def test_vsa_top1_follows_planted_routing_and_attends_only_there():
+    """Query block i's mean points at key block pi(i): top-1 keeps pi(i) (plus
+    the prefix), and its rows equal attention over those keys alone."""
+    prefix, shape, d = [10], (4, 8, 8), 32
+    blocks, npre = oracle.vsa_blocks(prefix, shape)
+    nb, nv = len(blocks), len(blocks) - npre
+    n = sum(prefix) + int(np.prod(shape))
+    rng = np.random.default_rng(3)
+    pi = rng.permutation(nv) + npre
+    q = torch.zeros(n, 1, d)
+    k = torch.zeros(n, 1, d)
+    for i in range(npre, nb):
+        q[blocks[i], 0, pi[i - npre] % d] = 1.0
+        k[blocks[i], 0, i % d] = 1.0
+    q = (q + 0.01 * torch.randn(n, 1, d, generator=torch.Generator().manual_seed(4))).to(torch.bfloat16)
+    k, v = k.to(torch.bfloat16), torch.randn(n, 1, d, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    bm = oracle.vsa_block_map(q, k, blocks, npre, topk=1, scale=1.0)
+    for i in range(npre, nb):
+        assert set(np.nonzero(bm[0, i])[0]) == set(range(npre)) | {int(pi[i - npre])}
+    assert bm[0, :npre].all()  # prefix queries stay dense
+    o, l = oracle.attention_block_sparse(q, k, v, blocks, bm, 1.0)
+    for i in (npre, nb - 1):
+        keys = np.concatenate([blocks[j] for j in range(npre)] + [blocks[pi[i - npre]]])
+        r_o, r_l = oracle.attention_single(q[blocks[i]], k[keys], v[keys], 1.0, False)
+        assert np.allclose(o[blocks[i]], r_o, rtol=0, atol=1e-12)
+        assert np.allclose(l[:, blocks[i]], r_l, rtol=0, atol=1e-12)
+    r_o, _ = oracle.attention_single(q[blocks[0]], k, v, 1.0, False)
+    assert np.allclose(o[blocks[0]], r_o, rtol=0, atol=1e-12)
+
+
+def test_vsa_pooling_divides_by_the_true_block_size():
+    """A small edge block whose keys match best must win top-1: pooling that
+    divided by 64 instead of the block's size would shrink its mean."""
+    blocks, npre = oracle.vsa_blocks([], (4, 4, 6))  # blocks of 64 and 32 tokens
+    assert [len(b) for b in blocks] == [64, 32]
+    n, d = 96, 32
+    q = torch.zeros(n, 1, d)
+    q[:, 0, 0] = 1.0
+    k = torch.zeros(n, 1, d)
+    k[blocks[0], 0, 0] = 0.9
+    k[blocks[1], 0, 0] = 1.0
+    bm = oracle.vsa_block_map(q.to(torch.bfloat16), k.to(torch.bfloat16), blocks, npre, topk=1, scale=1.0)
+    assert bm[0, :, 1].all() and not bm[0, :, 0].any()
