@@ -141,6 +141,8 @@ gbattn_status attn_fwd_dense(const void* q, const void* k, const void* v, int B,
     if (s != GBATTN_OK) return s;
     if (B < 0 || Sq < 0 || Sk < 0) return GBATTN_ERR_INVALID_ARG;
     if (B > 65535) return GBATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * Sq > 0x7fffffffLL || static_cast<long long>(B) * Sk > 0x7fffffffLL)
+        return GBATTN_ERR_UNSUPPORTED;  // row counts are 32-bit on the device
     if (B == 0 || Sq == 0) return GBATTN_OK;
     PrefillParams p{};
     p.out = out;

@@ -36,6 +36,7 @@
 // whatever the unused cache slots hold cannot reach the result.
 #include <math.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "kernels.h"
@@ -549,8 +550,10 @@ int paged_slice_rows(int D) { return D <= 128 ? 128 : 64; }
 template <class C>
 static cudaError_t launch_paged_cfg(const CUtensorMap& tm, const PagedParams& p, int num_sms, cudaStream_t st) {
     static bool attr_done[64];  // the attribute is per function and device
+    static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
         cudaError_t e = cudaFuncSetAttribute(paged_decode_sm103a<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);

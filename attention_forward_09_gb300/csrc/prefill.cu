@@ -37,6 +37,7 @@
 // staged for TMA stores uses the same swizzle, 128-byte boxes of columns.
 #include <math.h>
 #include <algorithm>
+#include <mutex>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -1230,9 +1231,11 @@ using Cfg256 = PrefillCfg<256, 128, 2>;
 template <class C, bool PAGED, class K>
 static cudaError_t set_smem_attr(K kernel, int bytes) {
     static bool done[64];
+    static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
@@ -1256,9 +1259,11 @@ template <class C, class K>
 static int resident_clusters(K kernel, int c) {
     static int cache[64][4];
     static bool have[64][4];
+    static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     const int slot = c == 2 ? 0 : c == 4 ? 1 : 2;
+    std::lock_guard<std::mutex> lock(mu);
     if (!have[dev][slot]) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute at[1];
