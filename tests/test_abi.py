@@ -181,3 +181,8 @@ def test_mask_helpers_validate_before_touching_a_device(lib):
     assert lib.attn_unpack_rows(P, P, 2, 8, 256, UNALIGNED, None) == 3
     assert lib.attn_unpack_lse(P, P, 2, 0, 8, P, None) == 1             # no heads
     assert lib.attn_pack_rows(P, P, P, 1 << 16, 1 << 16, 256, P, None) == 2  # B * S >= 2^31
+
+
+def test_dense_refuses_row_counts_past_32_bits(lib):
+    assert dense(lib, B=65535, Sq=40000) == 2
+    assert dense(lib, B=65535, Sq=8, Sk=40000) == 2
