@@ -47,6 +47,8 @@ SIGNATURES = {
     "attn_pack_rows": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "attn_unpack_rows": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "attn_unpack_lse": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "attn_vsa_layout": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.POINTER(ctypes.c_int),
+                             ctypes.POINTER(ctypes.c_int)]),
 }
 
 _lib = None
@@ -351,3 +353,19 @@ def attn_fwd_masked(q, k, v, mask, softmax_scale=None, causal=False, cross=False
         out = attn_unpack_rows(out_p, pos_k, B, Sq, stream)
         lse_out = attn_unpack_lse(lse_p, pos_k, B, Sq, stream) if lse else None
     return out, lse_out
+
+
+def attn_vsa_layout(prefix_segments, video_shape, tile=(4, 4, 4), block=64):
+    """Token blocks of block-sparse video attention (host computation).
+    Returns (order int32 [tokens], block_start int32 [NB + 1], n_prefix_blocks)."""
+    lib = load_library()
+    seg = (ctypes.c_int32 * max(1, len(prefix_segments)))(*[int(x) for x in prefix_segments])
+    nb, npre = ctypes.c_int(0), ctypes.c_int(0)
+    t, h, w = (int(x) for x in video_shape)
+    args = (seg, len(prefix_segments), t, h, w, int(tile[0]), int(tile[1]), int(tile[2]), int(block))
+    _check("attn_vsa_layout", lib.attn_vsa_layout(*args, None, None, ctypes.byref(nb), ctypes.byref(npre)))
+    order = torch.empty(sum(int(x) for x in prefix_segments) + t * h * w, dtype=torch.int32)
+    start = torch.empty(nb.value + 1, dtype=torch.int32)
+    _check("attn_vsa_layout", lib.attn_vsa_layout(*args, _ptr(order), _ptr(start), ctypes.byref(nb),
+                                                  ctypes.byref(npre)))
+    return order, start, npre.value

@@ -201,6 +201,26 @@ gbattn_status attn_unpack_lse(const float* lse_packed, const int32_t* packed_pos
                               void* stream);
 
 /*
+ * attn_vsa_layout -- host function (no device work): the token blocks of
+ * block-sparse video attention (vllm-omni fastvideo_vsa.py,
+ * _get_h3_tile_metadata).  The sequence is prefix_segments[0..num_segments)
+ * tokens, each segment cut into chunks of `block` tokens, followed by a
+ * T x H x W video grid (tokens in T, H, W order) cut into tile_t x tile_h x
+ * tile_w boxes taken in T, H, W order, smaller at the grid's far edges
+ * (the page: 4 x 4 x 4 boxes, blocks of 64).
+ *   order        out, host int32 [total tokens]: token indices block by block
+ *   block_start  out, host int32 [num_blocks + 1]: block b is
+ *                order[block_start[b] .. block_start[b + 1])
+ *   num_blocks, num_prefix_blocks  out
+ * With order or block_start NULL only the counts are written (to size the
+ * arrays).  Errors: GBATTN_ERR_INVALID_ARG (negative sizes, a box larger
+ * than a block), GBATTN_ERR_UNSUPPORTED (more than 2^31 tokens).
+ */
+gbattn_status attn_vsa_layout(const int32_t* prefix_segments, int num_segments, int T, int H, int W, int tile_t,
+                              int tile_h, int tile_w, int block, int32_t* order, int32_t* block_start,
+                              int* num_blocks, int* num_prefix_blocks);
+
+/*
  * attn_kv_cache_write -- store new tokens' keys and values into the paged
  * cache (vllm-ascend attention_v1.py, AscendAttentionBackendImpl.
  * reshape_and_cache; slot = block * block_size + offset, the AscendMetadata

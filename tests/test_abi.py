@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
         ["attn_fwd_dense", "attn_fwd_varlen", "attn_fwd_paged", "attn_fwd_paged_workspace_size",
          "attn_status_string", "attn_fwd_paged_noalloc", "attn_fwd_dense_plan", "attn_kv_cache_write",
          "attn_fwd_paged_prefill", "attn_mask_to_varlen", "attn_pack_rows", "attn_unpack_rows",
-         "attn_unpack_lse"])
+         "attn_unpack_lse", "attn_vsa_layout"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -186,3 +186,21 @@ def test_mask_helpers_validate_before_touching_a_device(lib):
 def test_dense_refuses_row_counts_past_32_bits(lib):
     assert dense(lib, B=65535, Sq=40000) == 2
     assert dense(lib, B=65535, Sq=8, Sk=40000) == 2
+
+
+@pytest.mark.parametrize("prefix,shape", [([70, 5], (5, 6, 7)), ([], (4, 4, 6)), ([128], (1, 1, 1)), ([3], (9, 2, 13))])
+def test_vsa_layout_equals_the_oracle_blocks(lib, prefix, shape):
+    """A host computation: runs without a GPU, bit-exact against the oracle."""
+    import oracle
+    order, start, npre = gb.attn_vsa_layout(prefix, shape)
+    blocks, n_prefix = oracle.vsa_blocks(prefix, shape)
+    assert npre == n_prefix and start.numel() == len(blocks) + 1
+    for b, ref in enumerate(blocks):
+        assert order[int(start[b]):int(start[b + 1])].tolist() == ref.tolist()
+
+
+def test_vsa_layout_validation(lib):
+    nb, npre = ctypes.c_int(), ctypes.c_int()
+    seg = (ctypes.c_int32 * 1)(-1)
+    assert lib.attn_vsa_layout(seg, 1, 4, 4, 4, 4, 4, 4, 64, None, None, ctypes.byref(nb), ctypes.byref(npre)) == 1
+    assert lib.attn_vsa_layout(None, 0, 4, 4, 4, 8, 4, 4, 64, None, None, ctypes.byref(nb), ctypes.byref(npre)) == 1
