@@ -25,6 +25,12 @@
 //     core works on the next scores while the softmax warps exponentiate the
 //     current ones) and P staged in shared memory as bf16.
 //
+// Both kernels have a paged instantiation (PAGED): K/V tiles come from the
+// paged cache through block_table (vllm-ascend attention_v1.py, chunked
+// prefill and speculative decode over the cache), V rows past seq_len are
+// zeroed before P.V, and the two-tile kernel can pack a GQA group into a
+// tile (128 / group tokens x group heads per 128 rows).
+//
 // Causal masking is bottom-right aligned (FlashAttentionImpl.forward_fa_npu:
 // key kp is blocked for query qp iff kp > qp + Sk - Sq); KV tiles past the
 // last visible key of the tile's last row are never loaded.
