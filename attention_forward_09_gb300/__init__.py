@@ -11,6 +11,12 @@ Entry points (same names as the C ABI):
     attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, ...)
     attn_fwd_paged(q, kv_cache, block_table, seq_lens, max_seq_len, ...)
     attn_fwd_paged_workspace_size(num_seqs, Hq, Hkv, D, max_seq_len)
+    attn_kv_cache_write, attn_fwd_paged_prefill, attn_mask_to_varlen, attn_pack_rows,
+    attn_unpack_rows, attn_unpack_lse, attn_fwd_dense_plan, attn_fwd_paged_noalloc
+    attn_vsa_layout, attn_vsa_tile_map, attn_gather_rows, attn_vsa_pool, attn_vsa_list_size,
+    attn_vsa_block_map, attn_fwd_vsa
+Compositions of those calls: attn_fwd_masked (padding mask), attn_vsa (block-sparse
+video attention, with VsaPlan holding one geometry's layout on the device).
 """
 
 from __future__ import annotations
@@ -31,7 +37,7 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment"
 NOALLOC_SCRATCH_BYTES = 32 << 20  # GBATTN_NOALLOC_SCRATCH_BYTES
 
 # (name, restype, argtypes) for every symbol of include/gbattn.h
-_P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_P, _I, _F, _Z, _L = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_longlong
 SIGNATURES = {
     "attn_fwd_dense": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _P]),
     "attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _P]),
@@ -49,6 +55,13 @@ SIGNATURES = {
     "attn_unpack_lse": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "attn_vsa_layout": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.POINTER(ctypes.c_int),
                              ctypes.POINTER(ctypes.c_int)]),
+    "attn_vsa_tile_map": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.POINTER(ctypes.c_int),
+                               ctypes.POINTER(ctypes.c_int)]),
+    "attn_gather_rows": (_I, [_P, _L, _P, _L, _I, _P, _P, _P]),
+    "attn_vsa_pool": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
+    "attn_vsa_list_size": (_I, [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_longlong)]),
+    "attn_vsa_block_map": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
+    "attn_fwd_vsa": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _L, _I, _I, _I, _F, _P, _I, _P, _P, _P]),
 }
 
 _lib = None
@@ -369,3 +382,140 @@ def attn_vsa_layout(prefix_segments, video_shape, tile=(4, 4, 4), block=64):
     _check("attn_vsa_layout", lib.attn_vsa_layout(*args, _ptr(order), _ptr(start), ctypes.byref(nb),
                                                   ctypes.byref(npre)))
     return order, start, npre.value
+
+
+def attn_vsa_tile_map(prefix_segments, video_shape, tile=(4, 4, 4)):
+    """Tiled layout of block-sparse video attention (host computation, 64-token
+    blocks).  Returns (tile_index int32 [nbp * 64], block_sizes int32 [nb],
+    n_prefix_blocks), host tensors."""
+    lib = load_library()
+    seg = (ctypes.c_int32 * max(1, len(prefix_segments)))(*[int(x) for x in prefix_segments])
+    nb, npre = ctypes.c_int(0), ctypes.c_int(0)
+    t, h, w = (int(x) for x in video_shape)
+    args = (seg, len(prefix_segments), t, h, w, int(tile[0]), int(tile[1]), int(tile[2]))
+    _check("attn_vsa_tile_map", lib.attn_vsa_tile_map(*args, None, None, ctypes.byref(nb), ctypes.byref(npre)))
+    index = torch.empty((nb.value + nb.value % 2) * 64, dtype=torch.int32)
+    sizes = torch.empty(nb.value, dtype=torch.int32)
+    _check("attn_vsa_tile_map", lib.attn_vsa_tile_map(*args, _ptr(index), _ptr(sizes), ctypes.byref(nb),
+                                                      ctypes.byref(npre)))
+    return index, sizes, npre.value
+
+
+def attn_gather_rows(src, index, dev_status=None, stream=None):
+    """src [N, ...] contiguous CUDA, index int32 CUDA [M] -> dst [M, ...]:
+    dst[w] = src[index[w]], zero rows where index[w] < 0."""
+    if not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous CUDA tensor")
+    if index.dtype != torch.int32 or not index.is_cuda or not index.is_contiguous():
+        raise ValueError("index must be a contiguous int32 CUDA tensor")
+    M = index.numel()
+    dst = torch.empty((M,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+    rb = src[0].numel() * src.element_size() if src.shape[0] > 0 else dst[0].numel() * dst.element_size()
+    st = load_library().attn_gather_rows(_ptr(src), src.shape[0], _ptr(index), M, rb, _ptr(dst), _ptr(dev_status),
+                                         _stream_handle(stream))
+    _check("attn_gather_rows", st)
+    return dst
+
+
+def attn_vsa_pool(x_tiled, block_sizes, dev_status=None, stream=None):
+    """x_tiled [rows >= nb * 64, H, D] bf16 CUDA, block_sizes int32 CUDA [nb]
+    -> pooled [H, nb, D] fp32 block means."""
+    _bf16_cuda("x_tiled", x_tiled)
+    nb = block_sizes.numel()
+    _, H, D = x_tiled.shape
+    if x_tiled.shape[0] < nb * 64:
+        raise ValueError("x_tiled has fewer than 64 rows per block")
+    pooled = torch.empty(H, nb, D, dtype=torch.float32, device=x_tiled.device)
+    st = load_library().attn_vsa_pool(_ptr(x_tiled), nb, H, D, _ptr(block_sizes), _ptr(pooled), _ptr(dev_status),
+                                      _stream_handle(stream))
+    _check("attn_vsa_pool", st)
+    return pooled
+
+
+def attn_vsa_list_size(num_blocks, num_prefix_blocks, topk, Hq) -> int:
+    n = ctypes.c_longlong(0)
+    _check("attn_vsa_list_size", load_library().attn_vsa_list_size(num_blocks, num_prefix_blocks, topk, Hq,
+                                                                   ctypes.byref(n)))
+    return n.value
+
+
+def attn_vsa_block_map(pooled_q, pooled_k, block_sizes, num_prefix_blocks, topk, softmax_scale, dev_status=None,
+                       stream=None):
+    """pooled_q [Hq, nb, D], pooled_k [Hkv, nb, D] fp32 CUDA -> (kv_list, kv_num)
+    int32: per head and tile (query blocks 2t, 2t+1), the union of the key
+    blocks they keep, entries (block << 9) | (size << 2) | bits."""
+    Hq, nb, D = pooled_q.shape
+    Hkv = pooled_k.shape[0]
+    n = attn_vsa_list_size(nb, num_prefix_blocks, topk, Hq)
+    kv_list = torch.empty(max(n, 1), dtype=torch.int32, device=pooled_q.device)
+    kv_num = torch.empty(Hq, (nb + 1) // 2, dtype=torch.int32, device=pooled_q.device)
+    st = load_library().attn_vsa_block_map(_ptr(pooled_q), _ptr(pooled_k), nb, num_prefix_blocks, Hq, Hkv, D, topk,
+                                           float(softmax_scale), _ptr(block_sizes), _ptr(kv_list), _ptr(kv_num),
+                                           _ptr(dev_status), _stream_handle(stream))
+    _check("attn_vsa_block_map", st)
+    return kv_list, kv_num
+
+
+def attn_fwd_vsa(q_tiled, k_tiled, v_tiled, kv_list, kv_num, num_blocks, num_prefix_blocks, topk, out_index=None,
+                 out_rows=None, softmax_scale=None, lse=None, out_dtype=torch.float32, out=None, dev_status=None,
+                 stream=None):
+    """Block-sparse attention over tiled q [nbp*64, Hq, D], k/v [nbp*64, Hkv, D]
+    (bf16 CUDA) and the lists of attn_vsa_block_map.  Row r of the tiled layout
+    goes to out row out_index[r] (None: out stays tiled).  Returns (out
+    [out_rows, Hq, D], lse [Hq, out_rows] or None)."""
+    for n_, t in (("q_tiled", q_tiled), ("k_tiled", k_tiled), ("v_tiled", v_tiled)):
+        _bf16_cuda(n_, t)
+    rows, Hq, D = q_tiled.shape
+    Hkv = k_tiled.shape[1]
+    if out_rows is None:
+        out_rows = rows
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty(out_rows, Hq, D, dtype=out_dtype, device=q_tiled.device)
+    if lse is True:
+        lse = torch.empty(Hq, out_rows, dtype=torch.float32, device=q_tiled.device)
+    st = load_library().attn_fwd_vsa(_ptr(q_tiled), _ptr(k_tiled), _ptr(v_tiled), num_blocks, num_prefix_blocks, topk,
+                                     _ptr(kv_list), _ptr(kv_num), _ptr(out_index), out_rows, Hq, Hkv, D,
+                                     float(softmax_scale), _ptr(out), _out_code(out.dtype), _ptr(lse),
+                                     _ptr(dev_status), _stream_handle(stream))
+    _check("attn_fwd_vsa", st)
+    return out, lse
+
+
+class VsaPlan:
+    """One geometry's tiled layout, computed on the host once and kept on the
+    device (the page caches the same metadata per geometry)."""
+
+    def __init__(self, prefix_segments, video_shape, device, tile=(4, 4, 4)):
+        index, sizes, npre = attn_vsa_tile_map(prefix_segments, video_shape, tile)
+        self.tokens = sum(int(x) for x in prefix_segments) + math.prod(int(x) for x in video_shape)
+        self.num_blocks = sizes.numel()
+        self.num_prefix_blocks = npre
+        self.rows = index.numel()
+        self.tile_index = index.to(device)
+        self.block_sizes = sizes.to(device)
+
+
+def attn_vsa(q, k, v, plan: VsaPlan, topk=64, softmax_scale=None, lse=False, out_dtype=torch.float32,
+             dev_status=None, stream=None):
+    """Block-sparse video attention of one sequence: q [S, Hq, D], k/v [S, Hkv, D]
+    bf16 CUDA, S = plan.tokens.  Tiles q, k, v, pools q and k, builds the block
+    map and attends it; returns (out [S, Hq, D], lse [Hq, S] or None)."""
+    for n_, t in (("q", q), ("k", k), ("v", v)):
+        _bf16_cuda(n_, t)
+    S, Hq, D = q.shape
+    if S != plan.tokens or k.shape[0] != S or v.shape[0] != S:
+        raise ValueError(f"the plan's geometry has {plan.tokens} tokens, q/k/v have {S}")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    qt = attn_gather_rows(q, plan.tile_index, dev_status, stream)
+    kt = attn_gather_rows(k, plan.tile_index, dev_status, stream)
+    vt = attn_gather_rows(v, plan.tile_index, dev_status, stream)
+    pq = attn_vsa_pool(qt, plan.block_sizes, dev_status, stream)
+    pk = attn_vsa_pool(kt, plan.block_sizes, dev_status, stream)
+    kv_list, kv_num = attn_vsa_block_map(pq, pk, plan.block_sizes, plan.num_prefix_blocks, topk, softmax_scale,
+                                         dev_status, stream)
+    return attn_fwd_vsa(qt, kt, vt, kv_list, kv_num, plan.num_blocks, plan.num_prefix_blocks, topk,
+                        out_index=plan.tile_index, out_rows=S, softmax_scale=softmax_scale,
+                        lse=True if lse else None, out_dtype=out_dtype, dev_status=dev_status, stream=stream)

@@ -18,7 +18,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgbattn.so")
-SOURCES = ["api.cpp", "prefill.cu", "decode.cu", "noalloc.cu", "cache_write.cu", "masks.cu", "vsa_layout.cpp"]
+SOURCES = ["api.cpp", "prefill.cu", "decode.cu", "noalloc.cu", "cache_write.cu", "masks.cu", "vsa_layout.cpp", "vsa.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

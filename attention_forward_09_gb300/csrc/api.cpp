@@ -440,4 +440,109 @@ gbattn_status attn_fwd_paged(const void* q, const void* kv_cache, int num_blocks
                : GBATTN_ERR_CUDA;
 }
 
+
+// ---------------------------------------------------------------- block-sparse video attention
+gbattn_status attn_gather_rows(const void* src, long long src_rows, const int32_t* index, long long dst_rows,
+                               int row_bytes, void* dst, uint32_t* dev_status, void* stream) {
+    if (src_rows < 0 || dst_rows < 0 || row_bytes <= 0 || row_bytes % 16 != 0) return GBATTN_ERR_INVALID_ARG;
+    if (dst_rows == 0) return GBATTN_OK;
+    if (!index || !dst || (src_rows > 0 && !src)) return GBATTN_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return GBATTN_ERR_ALIGNMENT;
+    DeviceInfo di;
+    gbattn_status s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    return gbattn::launch_gather_rows(src, src_rows, index, dst_rows, row_bytes, dst, dev_status, di.sms,
+                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GBATTN_OK
+               : GBATTN_ERR_CUDA;
+}
+
+gbattn_status attn_vsa_pool(const void* x_tiled, int num_blocks, int H, int D, const int32_t* block_sizes,
+                            float* pooled, uint32_t* dev_status, void* stream) {
+    if (num_blocks < 0 || H <= 0) return GBATTN_ERR_INVALID_ARG;
+    if (!head_size_ok(D)) return GBATTN_ERR_UNSUPPORTED;
+    if (num_blocks == 0) return GBATTN_OK;
+    if (!x_tiled || !block_sizes || !pooled) return GBATTN_ERR_INVALID_ARG;
+    if (!aligned16(x_tiled) || !aligned16(pooled)) return GBATTN_ERR_ALIGNMENT;
+    DeviceInfo di;
+    gbattn_status s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    return gbattn::launch_vsa_pool(x_tiled, block_sizes, num_blocks, H, D, pooled, dev_status, di.sms,
+                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GBATTN_OK
+               : GBATTN_ERR_CUDA;
+}
+
+gbattn_status attn_vsa_list_size(int num_blocks, int num_prefix_blocks, int topk, int Hq, long long* entries) {
+    if (!entries || num_blocks < 0 || num_prefix_blocks < 0 || num_prefix_blocks > num_blocks || topk < 1 || Hq <= 0)
+        return GBATTN_ERR_INVALID_ARG;
+    if (num_blocks >= (1 << 22)) return GBATTN_ERR_UNSUPPORTED;  // block index field of a list entry
+    *entries = static_cast<long long>(Hq) * gbattn::VsaGeom::make(num_blocks, num_prefix_blocks, topk).per_head();
+    return GBATTN_OK;
+}
+
+gbattn_status attn_vsa_block_map(const float* pooled_q, const float* pooled_k, int num_blocks, int num_prefix_blocks,
+                                 int Hq, int Hkv, int D, int topk, float softmax_scale, const int32_t* block_sizes,
+                                 int32_t* kv_list, int32_t* kv_num, uint32_t* dev_status, void* stream) {
+    if (num_blocks < 0 || num_prefix_blocks < 0 || num_prefix_blocks > num_blocks || topk < 1)
+        return GBATTN_ERR_INVALID_ARG;
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || !scale_ok(softmax_scale)) return GBATTN_ERR_INVALID_ARG;
+    if (!head_size_ok(D)) return GBATTN_ERR_UNSUPPORTED;
+    if (num_blocks >= (1 << 22) || Hq > 65535) return GBATTN_ERR_UNSUPPORTED;
+    if (num_blocks == 0) return GBATTN_OK;
+    if (!pooled_q || !pooled_k || !block_sizes || !kv_list || !kv_num) return GBATTN_ERR_INVALID_ARG;
+    if (gbattn::vsa_map_smem_bytes(num_blocks, D, 2) < 0) return GBATTN_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    gbattn_status s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    const gbattn::VsaGeom g = gbattn::VsaGeom::make(num_blocks, num_prefix_blocks, topk);
+    return gbattn::launch_vsa_block_map(pooled_q, pooled_k, block_sizes, g, Hq, Hq / Hkv, D, softmax_scale, kv_list,
+                                        kv_num, dev_status, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GBATTN_OK
+               : GBATTN_ERR_CUDA;
+}
+
+gbattn_status attn_fwd_vsa(const void* q_tiled, const void* k_tiled, const void* v_tiled, int num_blocks,
+                           int num_prefix_blocks, int topk, const int32_t* kv_list, const int32_t* kv_num,
+                           const int32_t* out_index, long long out_rows, int Hq, int Hkv, int D, float softmax_scale,
+                           void* out, gbattn_dtype out_dtype, float* lse, uint32_t* dev_status, void* stream) {
+    if (num_blocks < 0 || num_prefix_blocks < 0 || num_prefix_blocks > num_blocks || topk < 1 || out_rows < 0)
+        return GBATTN_ERR_INVALID_ARG;
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || !scale_ok(softmax_scale)) return GBATTN_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (out_dtype != GBATTN_OUT_BF16 && out_dtype != GBATTN_OUT_F32) return GBATTN_ERR_UNSUPPORTED;
+    const long long nbp = num_blocks + (num_blocks & 1);
+    const long long rows = nbp * gbattn::kVsaBlock;
+    if (num_blocks >= (1 << 22) || nbp / 2 > 65535 || Hq > 65535) return GBATTN_ERR_UNSUPPORTED;
+    if (!out_index && out_rows != rows) return GBATTN_ERR_INVALID_ARG;
+    if (num_blocks == 0) return GBATTN_OK;
+    if (!q_tiled || !k_tiled || !v_tiled || !kv_list || !kv_num || !out) return GBATTN_ERR_INVALID_ARG;
+    if (!aligned16(q_tiled) || !aligned16(k_tiled) || !aligned16(v_tiled) || !aligned16(out))
+        return GBATTN_ERR_ALIGNMENT;
+    DeviceInfo di;
+    gbattn_status s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    CUtensorMap tq, tk, tv;
+    if (!encode_rows_heads_d(&tq, q_tiled, rows, Hq, D, 128) ||
+        !encode_rows_heads_d(&tk, k_tiled, rows, Hkv, D, gbattn::kVsaBlock) ||
+        !encode_rows_heads_d(&tv, v_tiled, rows, Hkv, D, gbattn::kVsaBlock))
+        return GBATTN_ERR_CUDA;
+    gbattn::VsaFwdParams p{};
+    p.out = out;
+    p.lse = lse;
+    p.status = dev_status;
+    p.kv_list = kv_list;
+    p.kv_num = kv_num;
+    p.out_index = out_index;
+    p.out_rows = out_rows;
+    p.g = gbattn::VsaGeom::make(num_blocks, num_prefix_blocks, topk);
+    p.Hq = Hq;
+    p.group = Hq / Hkv;
+    p.scale_log2 = softmax_scale * kLog2e;
+    p.out_f32 = out_dtype == GBATTN_OUT_F32;
+    return gbattn::launch_vsa_fwd(D, tq, tk, tv, p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GBATTN_OK
+               : GBATTN_ERR_CUDA;
+}
+
 }  // extern "C"

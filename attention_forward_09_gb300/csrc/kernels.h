@@ -134,4 +134,74 @@ cudaError_t launch_unpack_rows(const void* packed, const int32_t* packed_pos, lo
 cudaError_t launch_unpack_lse(const float* lse_packed, long long hstride, const int32_t* packed_pos, int B, int H,
                               int S, float* lse, int num_sms, cudaStream_t st);
 
+
+// Block-sparse video attention (vsa.cu).  The tiled layout holds block b of
+// the sequence at rows [64 b, 64 b + 64), its first sizes[b] rows real, for
+// nbp = nb rounded up to even blocks: tile t (128 rows) is query blocks 2 t
+// and 2 t + 1, the second an empty partner when nb is odd.
+constexpr int kVsaBlock = 64;
+
+// A key-block entry of a tile's list: (block << 9) | (its token count << 2)
+// | bits, bit 0 set when query block 2 t keeps the block, bit 1 when 2 t + 1
+// does.  Lists are in ascending block order.
+__host__ __device__ inline int vsa_entry(int blk, int size, int bits) { return (blk << 9) | (size << 2) | bits; }
+
+// Sizes of the per-head list array: tile t holds up to capacity(t) entries
+// from offset(t) on.  Tiles with a prefix query block (or every tile, when
+// topk keeps every video block) list every block; the others at most the
+// prefix blocks plus topk video blocks from each of their two query blocks.
+struct VsaGeom {
+    int nb, nt, n_prefix, keep, td, c2;
+    __host__ __device__ static VsaGeom make(int nb_, int n_prefix_, int topk) {
+        VsaGeom g;
+        g.nb = nb_;
+        g.nt = (nb_ + 1) / 2;
+        g.n_prefix = n_prefix_;
+        const int n_video = nb_ - n_prefix_;
+        g.keep = topk < 0 ? 0 : (topk < n_video ? topk : n_video);
+        const int dense_tiles = (n_prefix_ + 1) / 2;
+        g.td = g.keep == n_video ? g.nt : (dense_tiles < g.nt ? dense_tiles : g.nt);
+        const long long c2 = static_cast<long long>(n_prefix_) + 2LL * g.keep;
+        g.c2 = c2 < nb_ ? static_cast<int>(c2) : nb_;
+        return g;
+    }
+    __host__ __device__ int capacity(int t) const { return t < td ? nb : c2; }
+    __host__ __device__ long long offset(int t) const {
+        return t < td ? static_cast<long long>(t) * nb
+                      : static_cast<long long>(td) * nb + static_cast<long long>(t - td) * c2;
+    }
+    __host__ __device__ long long per_head() const { return offset(nt); }
+};
+
+struct VsaFwdParams {
+    void* out;                 // [out_rows, Hq, D]
+    float* lse;                // [Hq, out_rows] or null
+    uint32_t* status;
+    const int32_t* kv_list;    // [Hq, g.per_head()]
+    const int32_t* kv_num;     // [Hq, g.nt]
+    const int32_t* out_index;  // [nbp * 64]: out row of each tiled row, -1 = none; null = identity
+    long long out_rows;
+    VsaGeom g;
+    int Hq, group;
+    float scale_log2;
+    int out_f32;
+};
+
+// dst[w] = src[index[w]] for 0 <= index[w] < src_rows, zeros for a negative
+// index; a larger one is flagged (kDevBadIndex) and zeroed.  row_bytes % 16 == 0.
+cudaError_t launch_gather_rows(const void* src, long long src_rows, const int32_t* index, long long dst_rows,
+                               int row_bytes, void* dst, uint32_t* status, int num_sms, cudaStream_t st);
+// pooled [H, nb, D] fp32 = block means of the tiled x [nb * 64, H, D] bf16.
+cudaError_t launch_vsa_pool(const void* x, const int32_t* sizes, int nb, int H, int D, float* pooled,
+                            uint32_t* status, int num_sms, cudaStream_t st);
+// Shared memory of the block-map kernel for qb query blocks per CTA, or -1 if over the limit.
+int vsa_map_smem_bytes(int nb, int D, int qb);
+cudaError_t launch_vsa_block_map(const float* pq, const float* pk, const int32_t* sizes, const VsaGeom& g, int Hq,
+                                 int group, int D, float scale, int32_t* kv_list, int32_t* kv_num, uint32_t* status,
+                                 cudaStream_t st);
+// Tensor maps over the tiled q [nbp * 64, Hq, D] (box rows 128) and k / v
+// [nbp * 64, Hkv, D] (box rows 64), box {64 columns, 1, rows}, 128-byte swizzle.
+cudaError_t launch_vsa_fwd(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                           const VsaFwdParams& p, cudaStream_t st);
+
 }  // namespace gbattn

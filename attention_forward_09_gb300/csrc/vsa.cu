@@ -1,0 +1,732 @@
+// vsa.cu -- block-sparse video attention for sm_103a.
+//
+// Operation: vllm-omni fastvideo_vsa.py, _forward_h3 without the trained gate
+// branch.  The sequence (a prefix, then a T x H x W video latent grid) is cut
+// into blocks of at most 64 tokens (_get_h3_tile_metadata); q, k and v are
+// reordered into a block-padded "tiled" layout, block b at rows [64 b, 64 b +
+// 64) with its first sizes[b] rows real; every block is mean-pooled
+// (_pool_h3_tiles); pooled block scores scale * mean_q . mean_k pick, for each
+// video query block, its topk best video key blocks plus every prefix key
+// block, while prefix query blocks keep everything (_build_h3_block_map); and
+// each query token attends the tokens of the key blocks its block keeps.
+//
+//   gather_rows      warp per destination row: dst[w] = src[index[w]] or zeros;
+//   vsa_pool         thread per (block, head, 8 columns): fp32 block means;
+//   vsa_block_map    CTA per (head, 8 / 4 / 2 query blocks): the pooled scores
+//                    of those query blocks against every key block in shared
+//                    memory, a 4-pass radix select of the topk-th score per
+//                    query block (ties to the lower block index), and, per
+//                    pair of query blocks, the union of their key blocks;
+//   vsa_fwd          CTA per (head, pair of query blocks = one 128-row tile):
+//                    Q tile by TMA, K/V tiles of two 64-row key blocks taken
+//                    from the pair's union list, S = Q K^T and O += P V by
+//                    tcgen05.mma with accumulators in TMEM, online softmax
+//                    where each row masks the key blocks its own query block
+//                    does not keep and the padding rows of every key block.
+//
+// The pair layout follows the page's note that the Blackwell kernel serves two
+// 64-row query blocks per CTA (hence an even block count, the last block of an
+// odd count being an empty partner).
+#include <math.h>
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gbattn {
+
+// ------------------------------------------------------------------ gather
+__global__ void __launch_bounds__(256) gather_rows_sm103a(const uint4* src, long long src_rows, const int32_t* index,
+                                                          long long dst_rows, int vec, uint4* dst, uint32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < dst_rows; w += nw) {
+        long long i = index[w];
+        if (i >= src_rows) {
+            if (lane == 0 && status) atomicOr(status, kDevBadIndex);
+            i = -1;
+        }
+        uint4* d = dst + w * vec;
+        if (i >= 0) {
+            const uint4* s = src + i * vec;
+            for (int c = lane; c < vec; c += 32) d[c] = s[c];
+        } else {
+            for (int c = lane; c < vec; c += 32) d[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+}
+
+// Token count of block b, clamped to [0, 64]; an out-of-range count is flagged.
+__device__ __forceinline__ int block_size_at(const int32_t* sizes, int b, uint32_t* status) {
+    int s = sizes[b];
+    if (s < 0 || s > kVsaBlock) {
+        if (status) atomicOr(status, kDevBadIndex);
+        s = s < 0 ? 0 : kVsaBlock;
+    }
+    return s;
+}
+
+// -------------------------------------------------------------------- pool
+// pooled[h][b][d] = (sum of rows r < sizes[b] of x[64 b + r][h][d]) / max(sizes[b], 1).
+// Consecutive threads take consecutive 16-byte pieces of one token row.
+__global__ void __launch_bounds__(256) vsa_pool_sm103a(const uint4* x, const int32_t* sizes, int nb, int H, int D,
+                                                       float* pooled, uint32_t* status) {
+    const int G = D / 8;
+    const long long row_vec = static_cast<long long>(H) * G;
+    const long long n = static_cast<long long>(nb) * row_vec;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int g = static_cast<int>(i % G);
+        const long long bh = i / G;
+        const int h = static_cast<int>(bh % H), b = static_cast<int>(bh / H);
+        const int sz = block_size_at(sizes, b, g == 0 ? status : nullptr);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const uint4* src = x + static_cast<long long>(b) * kVsaBlock * row_vec + static_cast<long long>(h) * G + g;
+#pragma unroll 4
+        for (int r = 0; r < sz; ++r) {
+            const uint4 v = src[r * row_vec];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[2 * e] += __uint_as_float(w[e] << 16);
+                acc[2 * e + 1] += __uint_as_float(w[e] & 0xffff0000u);
+            }
+        }
+        const float den = static_cast<float>(sz > 1 ? sz : 1);
+        float4* dst = reinterpret_cast<float4*>(pooled + (static_cast<long long>(h) * nb + b) * D + g * 8);
+        dst[0] = make_float4(acc[0] / den, acc[1] / den, acc[2] / den, acc[3] / den);
+        dst[1] = make_float4(acc[4] / den, acc[5] / den, acc[6] / den, acc[7] / den);
+    }
+}
+
+// --------------------------------------------------------------- block map
+// Monotone map of a float onto uint32 (larger float, larger key); -0 counts as +0.
+__device__ __forceinline__ uint32_t order_key(float s) {
+    const uint32_t u = __float_as_uint(s == 0.f ? 0.f : s);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+struct VsaMapParams {
+    const float* pq;  // [Hq, nb, D]
+    const float* pk;  // [Hkv, nb, D]
+    const int32_t* sizes;
+    int32_t* kv_list;
+    int32_t* kv_num;
+    uint32_t* status;
+    VsaGeom g;
+    int group, D, qb;
+    float scale;
+};
+
+constexpr int kMapWarps = 8;
+
+__global__ void __launch_bounds__(kMapWarps * 32) vsa_block_map_sm103a(const VsaMapParams p) {
+    extern __shared__ float4 map_smem[];
+    const int QB = p.qb, D = p.D, nb = p.g.nb, n_prefix = p.g.n_prefix, keep = p.g.keep;
+    const int words = (nb + 31) >> 5;
+    float* pq_s = reinterpret_cast<float*>(map_smem);                  // [QB][D]
+    float* sc = pq_s + QB * D;                                         // [QB][nb]
+    uint32_t* sel = reinterpret_cast<uint32_t*>(sc + QB * nb);         // [QB][words] kept key blocks
+    int* hist = reinterpret_cast<int*>(sel + QB * words);              // [kMapWarps][256]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y, kvh = h / p.group;
+    const int i0 = blockIdx.x * QB;
+
+    for (int x = threadIdx.x; x < QB * D; x += blockDim.x) {
+        const int i = x / D;
+        pq_s[x] = (i0 + i < nb) ? p.pq[(static_cast<long long>(h) * nb + i0 + i) * D + x % D] : 0.f;
+    }
+    __syncthreads();
+
+    // scores of the QB query blocks against key block j (warp per key block)
+    const float* pkh = p.pk + static_cast<long long>(kvh) * nb * D;
+    for (int j = warp; j < nb; j += kMapWarps) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int d = lane; d < D; d += 32) {
+            const float kv = pkh[static_cast<long long>(j) * D + d];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < QB) acc[i] = fmaf(pq_s[i * D + d], kv, acc[i]);
+        }
+        float mine = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float a = acc[i];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if (lane == i) mine = a;
+        }
+        if (lane < QB) sc[lane * nb + j] = p.scale * mine;
+    }
+    __syncthreads();
+
+    // kept key blocks of each query block (warp per query block)
+    if (warp < QB) {
+        const int qi = i0 + warp;
+        uint32_t* srow = sel + warp * words;
+        const float* row = sc + warp * nb;
+        if (qi >= nb) {
+            for (int w = lane; w < words; w += 32) srow[w] = 0u;
+        } else if (qi < n_prefix || keep == nb - n_prefix) {  // dense rows
+            for (int w = lane; w < words; w += 32) {
+                const int left = nb - w * 32;
+                srow[w] = left >= 32 ? 0xffffffffu : ((1u << left) - 1u);
+            }
+        } else {
+            // T = the keep-th largest key among the video key blocks, found
+            // 8 bits at a time; need_eq = how many blocks with key T are kept.
+            uint32_t T = 0xffffffffu;
+            int need_eq = 0;
+            if (keep > 0) {
+                int* hs = hist + warp * 256;
+                uint32_t prefix = 0u, pmask = 0u;
+                int rem = keep;
+                for (int shift = 24; shift >= 0; shift -= 8) {
+                    for (int b = lane; b < 256; b += 32) hs[b] = 0;
+                    __syncwarp();
+                    for (int j = n_prefix + lane; j < nb; j += 32) {
+                        const uint32_t k = order_key(row[j]);
+                        if ((k & pmask) == prefix) atomicAdd(&hs[(k >> shift) & 255u], 1);
+                    }
+                    __syncwarp();
+                    int c[8], s = 0;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {  // lane l holds bins 255 - 8 l down to 248 - 8 l
+                        c[e] = hs[255 - 8 * lane - e];
+                        s += c[e];
+                    }
+                    int incl = s;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += v;
+                    }
+                    const uint32_t bal = __ballot_sync(0xffffffffu, incl >= rem);
+                    const int L = bal ? __ffs(bal) - 1 : 31;
+                    int bin = 0, above = 0;
+                    if (lane == L) {
+                        int acc = incl - s;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            if (acc + c[e] >= rem) {
+                                bin = 255 - 8 * lane - e;
+                                above = acc;
+                                break;
+                            }
+                            acc += c[e];
+                        }
+                    }
+                    bin = __shfl_sync(0xffffffffu, bin, L);
+                    above = __shfl_sync(0xffffffffu, above, L);
+                    rem -= above;
+                    prefix |= static_cast<uint32_t>(bin) << shift;
+                    pmask |= 0xffu << shift;
+                    __syncwarp();
+                }
+                T = prefix;
+                need_eq = rem;
+            }
+            int eq_before = 0;
+            for (int base = 0; base < nb; base += 32) {
+                const int j = base + lane;
+                bool take = false, eq = false;
+                if (j < nb) {
+                    if (j < n_prefix) {
+                        take = true;
+                    } else if (keep > 0) {
+                        const uint32_t k = order_key(row[j]);
+                        take = k > T;
+                        eq = k == T;
+                    }
+                }
+                const uint32_t eqb = __ballot_sync(0xffffffffu, eq);
+                if (eq) take = eq_before + __popc(eqb & ((1u << lane) - 1u)) < need_eq;
+                eq_before += __popc(eqb);
+                const uint32_t tb = __ballot_sync(0xffffffffu, take);
+                if (lane == 0) srow[base >> 5] = tb;
+            }
+        }
+    }
+    __syncthreads();
+
+    // union list of each pair of query blocks (warp per pair)
+    if (warp < QB / 2) {
+        const int t = (i0 >> 1) + warp;
+        if (t < p.g.nt) {
+            const uint32_t* s0 = sel + (2 * warp) * words;
+            const uint32_t* s1 = s0 + words;
+            int32_t* dst = p.kv_list + static_cast<long long>(h) * p.g.per_head() + p.g.offset(t);
+            const int cap = p.g.capacity(t);
+            int cnt = 0;
+            for (int w = 0; w < words; ++w) {
+                const int j = w * 32 + lane;
+                const uint32_t bits = ((s0[w] >> lane) & 1u) | (((s1[w] >> lane) & 1u) << 1);
+                const uint32_t any = __ballot_sync(0xffffffffu, bits != 0u);
+                if (bits) {
+                    const int at = cnt + __popc(any & ((1u << lane) - 1u));
+                    const int sz = block_size_at(p.sizes, j, p.status);
+                    if (at < cap) dst[at] = vsa_entry(j, sz, static_cast<int>(bits));
+                }
+                cnt += __popc(any);
+            }
+            if (lane == 0) {
+                if (cnt > cap && p.status) atomicOr(p.status, kDevBadIndex);
+                p.kv_num[static_cast<long long>(h) * p.g.nt + t] = cnt < cap ? cnt : cap;
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------------- attention
+template <int D_, int STAGES_>
+struct VsaCfg {
+    static constexpr int D = D_;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int BM = 128;                  // two query blocks
+    static constexpr int BN = 128;                  // two key blocks
+    static constexpr int NCH = D / 64;              // 64-column chunks per row
+    static constexpr int Q_BYTES = NCH * BM * 128;
+    static constexpr int KV_BYTES = NCH * BN * 128;
+    static constexpr int P_BYTES = (BN / 64) * BM * 128;
+    static constexpr int NUM_BARS = 2 * STAGES + 6;
+    static constexpr int SMEM_BYTES = 1024 + Q_BYTES + STAGES * KV_BYTES + P_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int TMEM_S = 0;       // S buffers at [0, BN) and [BN, 2 BN)
+    static constexpr int TMEM_O = 2 * BN;  // O at [2 BN, 2 BN + D)
+    static constexpr int TMEM_COLS = 512;
+    static_assert(D % 64 == 0 && 2 * BN + D <= TMEM_COLS, "tile shape");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(SMEM_BYTES > 232448 / 2, "one CTA per SM: the TMEM allocation is 512 columns");
+};
+
+constexpr float kVsaLn2 = 0.6931471805599453f;
+constexpr float kVsaRescale = 8.0f;  // log2 units: tolerate P up to 2^8 before rescaling O
+
+// Visible keys of a 64-row key block for the rows of query block qb (0 or 1)
+// of the tile: its token count if that query block keeps it, else 0.
+__device__ __forceinline__ int entry_keys(int e, int qb, int nb) {
+    if (e < 0) return 0;
+    const int blk = e >> 9;
+    if (blk >= nb || !((e >> qb) & 1)) return 0;
+    const int s = (e >> 2) & 127;
+    return s < kVsaBlock ? s : kVsaBlock;
+}
+
+template <class C>
+__global__ void __launch_bounds__(192, 1)
+    vsa_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const VsaFwdParams p) {
+    constexpr int D = C::D, BN = C::BN, STAGES = C::STAGES, BM = C::BM, NCH = C::NCH;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sQ = smem_u32(smem);
+    const uint32_t sKV = sQ + C::Q_BYTES;
+    const uint32_t sP = sKV + STAGES * C::KV_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Q_BYTES + STAGES * C::KV_BYTES + C::P_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t b_q_full = smem_u32(&bars[0]);
+    auto b_kv_full = [&](int s) { return smem_u32(&bars[1 + s]); };
+    auto b_kv_empty = [&](int s) { return smem_u32(&bars[1 + STAGES + s]); };
+    auto b_s_full = [&](int b) { return smem_u32(&bars[1 + 2 * STAGES + b]); };
+    const uint32_t b_p_full = smem_u32(&bars[3 + 2 * STAGES]);
+    const uint32_t b_pv_done = smem_u32(&bars[4 + 2 * STAGES]);
+    const uint32_t b_drain = smem_u32(&bars[5 + 2 * STAGES]);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ------------------------------------------------------------ tile coordinates
+    const int h = blockIdx.x;  // heads fastest: the dense prefix tiles of every head start first
+    const int t = blockIdx.y;
+    const int kvh = h / p.group;
+    const int nb = p.g.nb;
+    const int cap = p.g.capacity(t);
+    const int32_t* list = p.kv_list + static_cast<long long>(h) * p.g.per_head() + p.g.offset(t);
+    int n = p.kv_num[static_cast<long long>(h) * p.g.nt + t];
+    if (n < 0 || n > cap) {
+        if (threadIdx.x == 0 && p.status) atomicOr(p.status, kDevBadIndex);
+        n = n < 0 ? 0 : cap;
+    }
+    const int n_kv = (n + 1) >> 1;  // KV tile j = entries 2 j and 2 j + 1
+    if (status_has_timeout(p.status, kDevTimeout)) return;
+
+    // ------------------------------------------------------------------ setup
+    if (threadIdx.x == 0) {
+        mbar_init(b_q_full, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(b_kv_full(s), 1);
+            mbar_init(b_kv_empty(s), 1);
+        }
+        mbar_init(b_s_full(0), 1);
+        mbar_init(b_s_full(1), 1);
+        mbar_init(b_p_full, 128);
+        mbar_init(b_pv_done, 1);
+        mbar_init(b_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            mbar_arrive_expect_tx(b_q_full, C::Q_BYTES);
+            for (int c = 0; c < NCH; ++c) tma_load_3d(sQ + c * BM * 128, &tmQ, b_q_full, c * 64, h, t * BM);
+            int e0 = n > 0 ? list[0] : 0, e1 = n > 1 ? list[1] : -1;
+            int issued = 0;
+            for (int j = 0; ok && j < n_kv; ++j) {
+                int f0 = 0, f1 = -1;  // entries of tile j + 1, read ahead of this tile's waits
+                if (j + 1 < n_kv) {
+                    f0 = list[2 * j + 2];
+                    f1 = 2 * j + 3 < n ? list[2 * j + 3] : -1;
+                }
+                // A missing second entry repeats the first block (masked for
+                // every row); a bad entry is flagged and block 0 read instead.
+                int b0 = e0 >> 9, b1 = e1 < 0 ? b0 : (e1 >> 9);
+                if (b0 < 0 || b0 >= nb || b1 < 0 || b1 >= nb) {
+                    if (p.status) atomicOr(p.status, kDevBadIndex);
+                    b0 = (b0 < 0 || b0 >= nb) ? 0 : b0;
+                    b1 = (b1 < 0 || b1 >= nb) ? 0 : b1;
+                }
+                for (int kv = 0; kv < 2; ++kv) {
+                    const int u_ = 2 * j + kv, s = u_ % STAGES, u = u_ / STAGES;
+                    if (u > 0 && !mbar_wait(b_kv_empty(s), (u - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const CUtensorMap* m = kv ? &tmV : &tmK;
+                    const uint32_t dst = sKV + s * C::KV_BYTES;
+                    mbar_arrive_expect_tx(b_kv_full(s), C::KV_BYTES);
+                    for (int c = 0; c < NCH; ++c) {
+                        tma_load_3d(dst + c * BN * 128, m, b_kv_full(s), c * 64, kvh, b0 * kVsaBlock);
+                        tma_load_3d(dst + c * BN * 128 + kVsaBlock * 128, m, b_kv_full(s), c * 64, kvh,
+                                    b1 * kVsaBlock);
+                    }
+                    ++issued;
+                }
+                e0 = f0;
+                e1 = f1;
+            }
+            if (!ok || *abort_flag) {
+                // Let every copy this thread started land before the CTA retires.
+                mbar_wait_drain(b_q_full, 0);
+                for (int u_ = (issued > STAGES ? issued - STAGES : 0); u_ < issued; ++u_)
+                    mbar_wait_drain(b_kv_full(u_ % STAGES), (u_ / STAGES) & 1);
+            }
+        }
+    } else if (warp == 5) {
+        // ----------------------------------------------------------------- MMA
+        // The whole warp walks the schedule; one elected lane issues.
+        constexpr uint32_t kIdS = idesc_bf16_f32(BM, BN, false, false);
+        constexpr uint32_t kIdO = idesc_bf16_f32(BM, D, false, true);
+        const bool leader = elect_one();
+        const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
+        const uint64_t dP = sdesc_sw128(sP, 16, 1024);
+        const uint64_t dK = sdesc_sw128(sKV, 16, 1024);
+        const uint64_t dV = sdesc_sw128(sKV, BN * 128, 1024);
+        auto wait_all = [&](uint32_t bar, uint32_t ph) {
+            return __all_sync(0xffffffffu, mbar_wait(bar, ph, abort_flag));
+        };
+        int ks = 0, vs = 1;  // K_j is load 2 j of the ring, V_j load 2 j + 1
+        uint32_t kph = 0, vph = 0;
+        auto adv = [](int& s, uint32_t& ph) {
+            s += 2;
+            if (s >= STAGES) {
+                s -= STAGES;
+                ph ^= 1u;
+            }
+        };
+        auto issue_s = [&](int j) -> bool {
+            if (!wait_all(b_kv_full(ks), kph)) return false;
+            tc_fence_after();
+            if (leader) {
+                const uint32_t dS = tmem + C::TMEM_S + (j & 1) * BN;
+                const uint64_t b0 = dK + static_cast<uint64_t>(ks * (C::KV_BYTES >> 4));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t oa = ((kk >> 2) * BM * 128 + (kk & 3) * 32) >> 4;
+                    const uint32_t ob = ((kk >> 2) * BN * 128 + (kk & 3) * 32) >> 4;
+                    mma_bf16_ss(dS, dQ + oa, b0 + ob, kIdS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(b_s_full(j & 1));
+                mma_commit(b_kv_empty(ks));
+            }
+            __syncwarp();
+            adv(ks, kph);
+            return true;
+        };
+        ok = wait_all(b_q_full, 0);
+        if (ok && n_kv > 0) ok = issue_s(0);
+        for (int j = 0; ok && j < n_kv; ++j) {
+            if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
+            if (!(ok = wait_all(b_p_full, j & 1))) break;
+            if (!(ok = wait_all(b_kv_full(vs), vph))) break;
+            tc_fence_after();
+            if (leader) {
+                const uint64_t b0 = dV + static_cast<uint64_t>(vs * (C::KV_BYTES >> 4));
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint32_t oa = ((kk >> 2) * BM * 128 + (kk & 3) * 32) >> 4;
+                    mma_bf16_ss(tmem + C::TMEM_O, dP + oa, b0 + ((kk * 16 * 128) >> 4), kIdO,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(b_pv_done);
+                mma_commit(b_kv_empty(vs));
+            }
+            __syncwarp();
+            adv(vs, vph);
+        }
+        if (leader) mma_commit(b_drain);  // all of the above finishes before TMEM is released
+        __syncwarp();
+        mbar_wait_drain(b_drain, 0);
+    } else {
+        // ------------------------------------------------------------- softmax
+        const int r = threadIdx.x;  // row within the tile == TMEM lane
+        const int qb = r >> 6;      // query block of the row within the pair (warp-uniform)
+        const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const float c2 = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        int e0 = n > 0 ? list[0] : 0, e1 = n > 1 ? list[1] : -1;
+        for (int j = 0; j < n_kv; ++j) {
+            int f0 = 0, f1 = -1;
+            if (j + 1 < n_kv) {
+                f0 = list[2 * j + 2];
+                f1 = 2 * j + 3 < n ? list[2 * j + 3] : -1;
+            }
+            const int la = entry_keys(e0, qb, nb), lb = entry_keys(e1, qb, nb);
+            e0 = f0;
+            e1 = f1;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_s_full(j & 1), (j >> 1) & 1, abort_flag)))) break;
+            tc_fence_after();
+            uint32_t pk[BN / 2];
+            bool warp_need = false;
+            float alpha = 1.f;
+            if (la > 0 || lb > 0) {
+                uint32_t sr[BN];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+                    tmem_ld32(tl + C::TMEM_S + (j & 1) * BN + c * 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+                tmem_wait_ld();
+                if (la < kVsaBlock || lb < kVsaBlock) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c)
+                        if (c < kVsaBlock ? c >= la : c - kVsaBlock >= lb) sr[c] = __float_as_uint(-INFINITY);
+                }
+                float mxp[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) mxp[i] = __uint_as_float(sr[i]);
+#pragma unroll
+                for (int c = 4; c < BN; c += 2)
+                    mxp[(c >> 1) & 3] = fmax3(mxp[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                const float mx = fmaxf(fmax3(mxp[0], mxp[1], mxp[2]), mxp[3]);
+                const float m_new = fmaxf(m, mx * c2);
+                warp_need = __any_sync(0xffffffffu, m_new > m + kVsaRescale);
+                if (warp_need && m_new > m) {
+                    alpha = ex2(m - m_new);
+                    m = m_new;
+                }
+                l *= alpha;
+                const float msub = (m == -INFINITY) ? 0.f : m;
+                const float2 c2x2 = make_float2(c2, c2), negm = make_float2(-msub, -msub);
+                float2 rsp[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
+#pragma unroll
+                for (int c = 0; c < BN; c += 2) {
+                    const float2 x =
+                        __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2x2, negm);
+                    const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+                    rsp[(c >> 1) & 3] = __fadd2_rn(rsp[(c >> 1) & 3], pp);
+                    pk[c >> 1] = pack_bf16x2(pp.x, pp.y);
+                }
+                const float2 rr = __fadd2_rn(__fadd2_rn(rsp[0], rsp[1]), __fadd2_rn(rsp[2], rsp[3]));
+                l += rr.x + rr.y;
+            } else {  // this query block keeps neither key block: P = 0, m and l unchanged
+#pragma unroll
+                for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;
+            }
+            // PV_{j-1} has to be finished before O is rescaled or P overwritten.
+            if (j > 0) {
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_pv_done, (j - 1) & 1, abort_flag)))) break;
+                tc_fence_after();
+                if (warp_need) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tl + C::TMEM_O + c * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(tl + C::TMEM_O + c * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < BN / 64; ++a) {
+                const uint32_t rowp = sP + a * BM * 128 + r * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_shared_v4(rowp + ((q ^ (r & 7)) << 4), pk[a * 32 + q * 4 + 0], pk[a * 32 + q * 4 + 1],
+                                 pk[a * 32 + q * 4 + 2], pk[a * 32 + q * 4 + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(b_p_full);
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok && n_kv > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(b_pv_done, (n_kv - 1) & 1, abort_flag));
+            tc_fence_after();
+        }
+        // ------------------------------------------------------------ epilogue
+        // Row r of the tile goes to row out_index[t * 128 + r] of out (the
+        // token's place in the sequence), or nowhere when that is negative.
+        const long long R = static_cast<long long>(t) * BM + r;
+        long long orow = p.out_index ? static_cast<long long>(p.out_index[R]) : R;
+        if (orow >= p.out_rows) {
+            if (p.status) atomicOr(p.status, kDevBadIndex);
+            orow = -1;
+        }
+        const bool row_valid = ok && orow >= 0;
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const long long obase = (orow * p.Hq + h) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            if (n_kv > 0 && ok) {
+                tmem_ld32(tl + C::TMEM_O + c * 32, o);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = 0u;
+            }
+            if (row_valid) {
+                if (p.out_f32) {
+                    float* dst = reinterpret_cast<float*>(p.out) + obase + c * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        st_global_v4(dst + e, __float_as_uint(__uint_as_float(o[e]) * inv_l),
+                                     __float_as_uint(__uint_as_float(o[e + 1]) * inv_l),
+                                     __float_as_uint(__uint_as_float(o[e + 2]) * inv_l),
+                                     __float_as_uint(__uint_as_float(o[e + 3]) * inv_l));
+                } else {
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + obase + c * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8)
+                        st_global_v4(dst + e,
+                                     pack_bf16x2(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l),
+                                     pack_bf16x2(__uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l),
+                                     pack_bf16x2(__uint_as_float(o[e + 4]) * inv_l, __uint_as_float(o[e + 5]) * inv_l),
+                                     pack_bf16x2(__uint_as_float(o[e + 6]) * inv_l, __uint_as_float(o[e + 7]) * inv_l));
+                }
+            }
+        }
+        if (row_valid && p.lse)
+            p.lse[static_cast<long long>(h) * p.out_rows + orow] = l > 0.f ? (m + __log2f(l)) * kVsaLn2 : -INFINITY;
+    }
+
+    // --------------------------------------------------------------- teardown
+    if (!ok) {
+        *abort_flag = 1;
+        if (p.status) atomicOr(p.status, kDevTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+using VsaCfg64 = VsaCfg<64, 8>;
+using VsaCfg128 = VsaCfg<128, 4>;
+
+// ------------------------------------------------------------------ launchers
+static int grid_for(long long units, int per_cta, int num_sms, int ctas_per_sm) {
+    long long g = (units + per_cta - 1) / per_cta;
+    const long long cap = static_cast<long long>(num_sms > 0 ? num_sms : 1) * ctas_per_sm;
+    return static_cast<int>(g < 1 ? 1 : (g > cap ? cap : g));
+}
+
+cudaError_t launch_gather_rows(const void* src, long long src_rows, const int32_t* index, long long dst_rows,
+                               int row_bytes, void* dst, uint32_t* status, int num_sms, cudaStream_t st) {
+    gather_rows_sm103a<<<grid_for(dst_rows, 8, num_sms, 8), 256, 0, st>>>(
+        static_cast<const uint4*>(src), src_rows, index, dst_rows, row_bytes / 16, static_cast<uint4*>(dst), status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_vsa_pool(const void* x, const int32_t* sizes, int nb, int H, int D, float* pooled,
+                            uint32_t* status, int num_sms, cudaStream_t st) {
+    const long long units = static_cast<long long>(nb) * H * (D / 8);
+    vsa_pool_sm103a<<<grid_for(units, 256, num_sms, 8), 256, 0, st>>>(static_cast<const uint4*>(x), sizes, nb, H, D,
+                                                                    pooled, status);
+    return cudaGetLastError();
+}
+
+int vsa_map_smem_bytes(int nb, int D, int qb) {
+    const long long words = (nb + 31) / 32;
+    const long long b = 4LL * (static_cast<long long>(qb) * D + static_cast<long long>(qb) * nb + qb * words) +
+                        4LL * kMapWarps * 256;
+    return b > 232448 ? -1 : static_cast<int>(b);
+}
+
+cudaError_t launch_vsa_block_map(const float* pq, const float* pk, const int32_t* sizes, const VsaGeom& g, int Hq,
+                                 int group, int D, float scale, int32_t* kv_list, int32_t* kv_num, uint32_t* status,
+                                 cudaStream_t st) {
+    int qb = 8;
+    while (qb > 2 && vsa_map_smem_bytes(g.nb, D, qb) < 0) qb >>= 1;
+    const int bytes = vsa_map_smem_bytes(g.nb, D, qb);
+    if (bytes < 0) return cudaErrorInvalidValue;
+    static std::mutex mu;
+    {
+        std::lock_guard<std::mutex> lock(mu);  // the limit only grows; setting it per call is cheap
+        cudaError_t e = cudaFuncSetAttribute(vsa_block_map_sm103a, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+    }
+    VsaMapParams p{pq, pk, sizes, kv_list, kv_num, status, g, group, D, qb, scale};
+    dim3 grid((g.nb + qb - 1) / qb, Hq);
+    vsa_block_map_sm103a<<<grid, kMapWarps * 32, bytes, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <class C>
+static cudaError_t launch_vsa_cfg(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                  const VsaFwdParams& p, cudaStream_t st) {
+    static bool done[64];
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64 || !done[dev]) {
+            e = cudaFuncSetAttribute(vsa_fwd_sm103a<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) done[dev] = true;
+        }
+    }
+    dim3 grid(p.Hq, p.g.nt);
+    vsa_fwd_sm103a<C><<<grid, 192, C::SMEM_BYTES, st>>>(tmQ, tmK, tmV, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_vsa_fwd(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                           const VsaFwdParams& p, cudaStream_t st) {
+    switch (D) {
+        case 64: return launch_vsa_cfg<VsaCfg64>(tmQ, tmK, tmV, p, st);
+        case 128: return launch_vsa_cfg<VsaCfg128>(tmQ, tmK, tmV, p, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gbattn

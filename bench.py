@@ -18,7 +18,7 @@ same workload on this machine's host cores (there is no other reference
 implementation of this path).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--only all|prefill|decode|kv_write|paged_prefill|masked] [--prefill WORKLOAD]
+                       [--only all|prefill|decode|kv_write|paged_prefill|masked|vsa] [--prefill WORKLOAD]
                        [--paged-prefill chunked_prefill|spec_decode] [--no-cpu]
 """
 
@@ -822,6 +822,154 @@ def run_masked(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def vsa_kept_pairs(kv_list, kv_num, nb, npre, topk, sizes):
+    """Query-key pairs the block-sparse attention computes, counted from its
+    per-tile lists: per entry, the key block's tokens times the tokens of
+    each query block of the tile that keeps it (list placement as stated
+    with attn_vsa_block_map)."""
+    import attention_forward_09_gb300 as gb
+
+    kl, kn = kv_list.cpu().numpy().astype(np.int64), kv_num.cpu().numpy()
+    sz = np.asarray(sizes, dtype=np.int64)
+    sz_pad = np.append(sz, 0)
+    nt, keep = (nb + 1) // 2, min(topk, nb - npre)
+    td = nt if keep == nb - npre else min(nt, (npre + 1) // 2)
+    c2 = min(nb, npre + 2 * keep)
+    per_head = gb.attn_vsa_list_size(nb, npre, topk, 1)
+    pairs = 0
+    for h in range(kn.shape[0]):
+        for t in range(nt):
+            off = h * per_head + (t * nb if t < td else td * nb + (t - td) * c2)
+            e = kl[off:off + int(kn[h, t])]
+            q0, q1 = sz[2 * t], sz_pad[2 * t + 1]
+            pairs += int((sz[e >> 9] * (((e & 1) != 0) * q0 + ((e & 2) != 0) * q1)).sum())
+    return pairs
+
+
+def run_vsa(args, world, rank, local):
+    """`--only vsa`: block-sparse video attention of one sequence (tile q, k,
+    v; pool; block map; attention), TFLOP/s on the query-key pairs it keeps."""
+    import attention_forward_09_gb300 as gb
+    from attention_forward_09_gb300 import _build
+
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier(world)
+    gb.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk, peak_kind = peaks()
+    w = workloads.vsa_video()
+    q, k, v = w.make()
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    plan = gb.VsaPlan(w.prefix, w.video, dev)
+    nb, npre = plan.num_blocks, plan.num_prefix_blocks
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fwd_ev = []
+
+    def run(time_fwd=False):
+        qt, kt, vt = (gb.attn_gather_rows(x, plan.tile_index, status, stream) for x in (qd, kd, vd))
+        pq = gb.attn_vsa_pool(qt, plan.block_sizes, status, stream)
+        pkk = gb.attn_vsa_pool(kt, plan.block_sizes, status, stream)
+        kl, kn = gb.attn_vsa_block_map(pq, pkk, plan.block_sizes, npre, w.topk, w.scale, status, stream)
+        if time_fwd:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            e[0].record(stream)
+        out, lse = gb.attn_fwd_vsa(qt, kt, vt, kl, kn, nb, npre, w.topk, out_index=plan.tile_index,
+                                   out_rows=w.tokens, softmax_scale=w.scale, lse=True, dev_status=status,
+                                   stream=stream)
+        if time_fwd:
+            e[1].record(stream)
+            fwd_ev.append(e)
+        return out, lse, kl, kn
+
+    for _ in range(args.warmup):
+        _, _, kl0, kn0 = run()
+    torch.cuda.synchronize()
+    flops = 4.0 * w.D * vsa_kept_pairs(kl0, kn0, nb, npre, w.topk, plan.block_sizes.cpu().tolist())
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            run(time_fwd=True)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world)
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev)
+    value = sum_over_ranks(flops, world) / (ms * 1e-3) / 1e12
+    tf_fwd = flops / (fwd_ms * 1e-3) / 1e12
+
+    hq_, hk_, hv_ = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    out0, lse0, _, _ = run()
+    hout, hlse = torch.empty(out0.shape).pin_memory(), torch.empty(lse0.shape).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for d_, h_ in ((qd, hq_), (kd, hk_), (vd, hv_)):
+            d_.copy_(h_, non_blocking=True)
+        o, l, _, _ = run()
+        hout.copy_(o, non_blocking=True)
+        hlse.copy_(l, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+
+    cpu = None
+    if world == 1 and not args.no_cpu:  # the oracle: one head's block map, then query blocks for about 10 s
+        import oracle
+
+        t0 = time.perf_counter()
+        blocks, n_pre = oracle.vsa_blocks(w.prefix, w.video)
+        bm = oracle.vsa_block_map(q[:, :1], k[:, :1], blocks, n_pre, w.topk, w.scale)[0]
+        fl, done = 0.0, 0
+        for i in range(n_pre, nb):
+            keys = torch.from_numpy(np.concatenate([blocks[j] for j in np.nonzero(bm[i])[0]]))
+            oracle.attention_single(q[torch.from_numpy(blocks[i]), :1], k[keys, :1], v[keys, :1], w.scale, False)
+            fl += 4.0 * w.D * len(blocks[i]) * len(keys)
+            done += 1
+            if time.perf_counter() - t0 > 10.0:
+                break
+        dt = time.perf_counter() - t0
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+               "sample": f"head 0: the block map of all {nb} blocks, then {done} video query blocks "
+                         f"({dt:.1f} s, map time included)"}
+    if rank != 0:
+        return
+    peak_tf = float(pk["bf16_tflops"])
+    line = {
+        "metric": "block-sparse video attention TFLOP/s (kept pairs) & % bf16 TC peak", "value": value,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "prefix": w.prefix, "video": list(w.video), "tokens": w.tokens,
+                   "blocks": nb, "topk": w.topk, "heads": w.Hq, "head_dim": w.D,
+                   "density": flops / (4.0 * w.D * w.Hq * w.tokens ** 2),
+                   "l2": "inputs larger than L2 (3 x 780 MB, tiled copies rewritten every step)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "vsa_fwd_sm103a", "achieved": tf_fwd, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": tf_fwd / peak_tf, "peak_kind": f"{peak_kind} bf16 burst",
+                     "flops_per_launch": flops, "fwd_ms": fwd_ms,
+                     "traffic": traffic_for("vsa_fwd_sm103a@" + w.name, "vsa.cu")},
+        "cpu_baseline": cpu,
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,
+                "d2h_bytes_per_step": hout.numel() * 4 + hlse.numel() * 4},
+        "gpu_launches": 7 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -832,7 +980,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--paged-prefill", choices=sorted(PAGED_PREFILL_WORKLOADS), default="chunked_prefill",
                     help="workload of --only paged_prefill")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "kv_write", "paged_prefill", "masked"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "kv_write", "paged_prefill", "masked", "vsa"],
+                    default="all",
                     help="run one part of the step (profiling captures), or the KV cache write alone; "
                          "the default line needs 'all'")
     ap.add_argument("--decode-seqs", type=int, default=0,
@@ -849,6 +998,8 @@ def main():
         run_paged_prefill(args, world, rank, local)
     elif args.only == "masked":
         run_masked(args, world, rank, local)
+    elif args.only == "vsa":
+        run_vsa(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

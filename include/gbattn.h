@@ -64,7 +64,7 @@ typedef enum {
 } gbattn_dtype;
 
 /* Bits the kernels OR into *dev_status. */
-#define GBATTN_DEV_BAD_INDEX 1u   /* block_table entry or slot outside the cache (token skipped) */
+#define GBATTN_DEV_BAD_INDEX 1u   /* block_table entry, slot or row index out of range (skipped) */
 #define GBATTN_DEV_TIMEOUT 2u     /* a pipeline wait gave up; that tile's output is invalid */
 #define GBATTN_DEV_BAD_SEQLEN 4u  /* cu_seqlens / seq_lens inconsistent or above the stated max */
 
@@ -321,6 +321,100 @@ gbattn_status attn_fwd_paged_noalloc(const void* q, const void* kv_cache, int nu
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* attn_status_string(gbattn_status status);
+
+/*
+ * Block-sparse video attention, device path (vllm-omni fastvideo_vsa.py,
+ * _forward_h3 without the trained gate branch).  The steps, each a call:
+ *
+ *   attn_vsa_tile_map    (host) the tiled layout of a geometry;
+ *   attn_gather_rows     q, k, v -> block-padded tiled q, k, v;
+ *   attn_vsa_pool        block means of the tiled q and k (_pool_h3_tiles);
+ *   attn_vsa_block_map   pooled scores -> the key blocks each query block
+ *                        keeps (_build_h3_block_map), as per-tile lists;
+ *   attn_fwd_vsa         block-sparse attention over those lists, each row
+ *                        written back to its token's place.
+ *
+ * Tiled layout: nb blocks of at most 64 tokens (the layout of
+ * attn_vsa_layout with 64-token blocks), padded to nbp = nb + (nb & 1)
+ * blocks; block b occupies tiled rows [64 b, 64 b + 64), its first
+ * block_sizes[b] rows real, the rest zero.  A tile is 128 rows: query blocks
+ * 2 t and 2 t + 1 (the last an empty partner when nb is odd).
+ *
+ * attn_vsa_tile_map -- host function, arguments as attn_vsa_layout with
+ *   64-token blocks (tile_t * tile_h * tile_w <= 64).
+ *   tile_index   out, host int32 [nbp * 64]: token of each tiled row, -1 at
+ *                padding rows
+ *   block_sizes  out, host int32 [nb]: tokens of each block
+ *   With tile_index or block_sizes NULL only the counts are written.
+ *
+ * attn_gather_rows -- dst[w] = src[index[w]] (rows of row_bytes bytes,
+ *   a positive multiple of 16; src and dst 16-byte aligned device memory;
+ *   index device int32 [dst_rows]).  A negative index gives a zero row; one
+ *   at or past src_rows a zero row and GBATTN_DEV_BAD_INDEX.
+ *
+ * attn_vsa_pool -- x_tiled device bf16 [nb * 64 (or more), H, D]; pooled
+ *   out, device fp32 [H, nb, D]: the mean of each block's real rows
+ *   (pooled / block size, as the page divides by the true size).
+ *   block_sizes device int32 [nb]; a size outside [0, 64] is clamped and
+ *   sets GBATTN_DEV_BAD_INDEX.  pooled 16-byte aligned.
+ *
+ * attn_vsa_list_size -- host: *entries = the int32 count of the kv_list
+ *   array for these sizes (all Hq heads).
+ *
+ * attn_vsa_block_map -- pooled_q fp32 [Hq, nb, D], pooled_k fp32 [Hkv, nb,
+ *   D] (attn_vsa_pool's output).  Scores scale * pooled_q . pooled_k in fp32;
+ *   a prefix query block (index < num_prefix_blocks) keeps every key block; a
+ *   video query block keeps every prefix key block and its min(topk,
+ *   nb - num_prefix_blocks) best video key blocks, ties to the lower block
+ *   index (with topk >= the video block count every block is kept).  topk
+ *   must be >= 1, as the page requires.
+ *   kv_list  out, device int32 [attn_vsa_list_size entries]: per head h and
+ *            tile t, the union of the key blocks that query blocks 2 t and
+ *            2 t + 1 keep, ascending, each entry (block << 9) | (block size
+ *            << 2) | bits, bit 0 set if block 2 t keeps it, bit 1 if 2 t + 1
+ *            does
+ *   kv_num   out, device int32 [Hq, (nb + 1) / 2]: entries of each list
+ *   Placement: with keep = min(topk, nb - num_prefix_blocks), nt = (nb + 1)
+ *   / 2, td = nt if keep == nb - num_prefix_blocks else min(nt,
+ *   (num_prefix_blocks + 1) / 2) tiles that list every block, and c2 =
+ *   min(nb, num_prefix_blocks + 2 keep), head h's lists start at h * E (E =
+ *   the list size for Hq = 1) and tile t's at t * nb (t < td) or td * nb +
+ *   (t - td) * c2, holding at most nb or c2 entries.
+ *   Errors: GBATTN_ERR_UNSUPPORTED if the scores of two query blocks against
+ *   every key block do not fit in shared memory (nb above about 26000).
+ *
+ * attn_fwd_vsa -- q_tiled [nbp * 64, Hq, D], k_tiled / v_tiled [nbp * 64,
+ *   Hkv, D], device bf16, D = 64 or 128; the padding rows of v_tiled must be
+ *   finite (attn_gather_rows writes zeros).  kv_list / kv_num from
+ *   attn_vsa_block_map with the same nb, num_prefix_blocks, topk and Hq.
+ *   Row r of query block b attends the real rows of every key block its
+ *   block keeps.  out_index device int32 [nbp * 64]: the out row of each
+ *   tiled row (attn_vsa_tile_map's tile_index), -1 = not written; NULL writes
+ *   out in the tiled layout (out_rows = nbp * 64).  out [out_rows, Hq, D]
+ *   (bf16 or fp32), lse optional fp32 [Hq, out_rows]; a row that keeps no key
+ *   gets out = 0, lse = -inf.  An entry naming a block outside [0, nb) or a
+ *   list longer than its capacity sets GBATTN_DEV_BAD_INDEX, as does an
+ *   out_index at or past out_rows (row skipped).
+ *
+ * Errors of the device calls: GBATTN_ERR_INVALID_ARG, GBATTN_ERR_UNSUPPORTED
+ * (head size, more than 65535 tiles), GBATTN_ERR_ALIGNMENT, GBATTN_ERR_DEVICE
+ * / _CUDA.  None allocates or synchronises.
+ */
+gbattn_status attn_vsa_tile_map(const int32_t* prefix_segments, int num_segments, int T, int H, int W, int tile_t,
+                                int tile_h, int tile_w, int32_t* tile_index, int32_t* block_sizes, int* num_blocks,
+                                int* num_prefix_blocks);
+gbattn_status attn_gather_rows(const void* src, long long src_rows, const int32_t* index, long long dst_rows,
+                               int row_bytes, void* dst, uint32_t* dev_status, void* stream);
+gbattn_status attn_vsa_pool(const void* x_tiled, int num_blocks, int H, int D, const int32_t* block_sizes,
+                            float* pooled, uint32_t* dev_status, void* stream);
+gbattn_status attn_vsa_list_size(int num_blocks, int num_prefix_blocks, int topk, int Hq, long long* entries);
+gbattn_status attn_vsa_block_map(const float* pooled_q, const float* pooled_k, int num_blocks, int num_prefix_blocks,
+                                 int Hq, int Hkv, int D, int topk, float softmax_scale, const int32_t* block_sizes,
+                                 int32_t* kv_list, int32_t* kv_num, uint32_t* dev_status, void* stream);
+gbattn_status attn_fwd_vsa(const void* q_tiled, const void* k_tiled, const void* v_tiled, int num_blocks,
+                           int num_prefix_blocks, int topk, const int32_t* kv_list, const int32_t* kv_num,
+                           const int32_t* out_index, long long out_rows, int Hq, int Hkv, int D, float softmax_scale,
+                           void* out, gbattn_dtype out_dtype, float* lse, uint32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -18,5 +18,6 @@ from .attention import (  # noqa: F401
     softmax_weights,
     visible_mask,
     vsa_block_map,
+    vsa_pool,
     vsa_blocks,
 )

@@ -313,6 +313,14 @@ def vsa_blocks(prefix_segments, video_shape, tile=(4, 4, 4), block=64):
     return blocks, n_prefix
 
 
+def vsa_pool(x, blocks):
+    """Mean token of every block (``fastvideo_vsa.py``, ``_pool_h3_tiles``:
+    the block's sum divided by its true token count).  x: [S, H, D].
+    Returns [NB, H, D] float64."""
+    x = _f64(x)
+    return np.stack([x[b].mean(axis=0) for b in blocks])
+
+
 def vsa_block_map(q, k, blocks, n_prefix, topk: int, scale: float):
     """Block selection (``fastvideo_vsa.py``, ``_pool_h3_tiles`` and
     ``_build_h3_block_map``): the mean query and key of every block, block
@@ -326,8 +334,8 @@ def vsa_block_map(q, k, blocks, n_prefix, topk: int, scale: float):
     hq, hkv = q.shape[1], k.shape[1]
     g = hq // hkv
     nb = len(blocks)
-    mq = np.stack([q[b].mean(axis=0) for b in blocks])  # [NB, Hq, D]
-    mk = np.stack([k[b].mean(axis=0) for b in blocks])  # [NB, Hkv, D]
+    mq = vsa_pool(q, blocks)  # [NB, Hq, D]
+    mk = vsa_pool(k, blocks)  # [NB, Hkv, D]
     n_video = nb - n_prefix
     keep = min(topk, n_video)
     bm = np.zeros((hq, nb, nb), dtype=bool)

@@ -40,3 +40,57 @@ def bf16_half_ulp(x):
     x = np.abs(np.asarray(x, dtype=np.float64))
     e = np.floor(np.log2(np.maximum(x, 2.0 ** -126)))
     return 0.5 * 2.0 ** (e - 7)
+
+
+# ---- block-sparse video attention: the per-tile list format of attn_vsa_block_map
+def _list_size(nb, npre, topk, hq):
+    import attention_forward_09_gb300 as gb
+    return gb.attn_vsa_list_size(nb, npre, topk, hq)
+
+
+def vsa_tile_offsets(nb, npre, topk):
+    """Start and capacity of each tile's list within one head (the placement
+    rule stated with attn_vsa_block_map)."""
+    nt, keep = (nb + 1) // 2, min(topk, nb - npre)
+    td = nt if keep == nb - npre else min(nt, (npre + 1) // 2)
+    c2 = min(nb, npre + 2 * keep)
+    return [(t * nb, nb) if t < td else (td * nb + (t - td) * c2, c2) for t in range(nt)]
+
+
+def vsa_lists_from_map(bm, sizes, npre, topk):
+    """Host encoding of a bool block map [Hq, nb, nb] into the kernel's lists
+    (CPU tensors)."""
+    hq, nb, _ = bm.shape
+    per_head = _list_size(nb, npre, topk, 1)
+    kl = np.zeros(max(hq * per_head, 1), dtype=np.int32)
+    kn = np.zeros((hq, (nb + 1) // 2), dtype=np.int32)
+    for h in range(hq):
+        for t, (off, cap) in enumerate(vsa_tile_offsets(nb, npre, topk)):
+            r1 = bm[h, 2 * t + 1] if 2 * t + 1 < nb else np.zeros(nb, bool)
+            ent = [(j << 9) | (int(sizes[j]) << 2) | int(bm[h, 2 * t, j]) | (int(r1[j]) << 1)
+                   for j in range(nb) if bm[h, 2 * t, j] or r1[j]]
+            assert len(ent) <= cap
+            kl[h * per_head + off:h * per_head + off + len(ent)] = ent
+            kn[h, t] = len(ent)
+    return torch.from_numpy(kl), torch.from_numpy(kn)
+
+
+def vsa_map_from_lists(kv_list, kv_num, nb, npre, topk, sizes):
+    """The kernel's lists -> bool map [Hq, nb, nb], checking their format."""
+    kl, kn = kv_list.cpu().numpy(), kv_num.cpu().numpy()
+    hq = kn.shape[0]
+    per_head = _list_size(nb, npre, topk, 1)
+    bm = np.zeros((hq, nb, nb), dtype=bool)
+    for h in range(hq):
+        for t, (off, cap) in enumerate(vsa_tile_offsets(nb, npre, topk)):
+            n = int(kn[h, t])
+            assert 0 <= n <= cap
+            e = kl[h * per_head + off:h * per_head + off + n].astype(np.int64)
+            blk, sz, bits = e >> 9, (e >> 2) & 127, e & 3
+            assert np.all(np.diff(blk) > 0) and np.all(bits != 0) and np.array_equal(sz, np.asarray(sizes)[blk])
+            bm[h, 2 * t, blk[(bits & 1) != 0]] = True
+            if 2 * t + 1 < nb:
+                bm[h, 2 * t + 1, blk[(bits & 2) != 0]] = True
+            else:
+                assert not np.any(bits & 2)
+    return bm

@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
         ["attn_fwd_dense", "attn_fwd_varlen", "attn_fwd_paged", "attn_fwd_paged_workspace_size",
          "attn_status_string", "attn_fwd_paged_noalloc", "attn_fwd_dense_plan", "attn_kv_cache_write",
          "attn_fwd_paged_prefill", "attn_mask_to_varlen", "attn_pack_rows", "attn_unpack_rows",
-         "attn_unpack_lse", "attn_vsa_layout"])
+         "attn_unpack_lse", "attn_vsa_layout", "attn_vsa_tile_map", "attn_gather_rows", "attn_vsa_pool",
+         "attn_vsa_list_size", "attn_vsa_block_map", "attn_fwd_vsa"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -204,3 +205,57 @@ def test_vsa_layout_validation(lib):
     seg = (ctypes.c_int32 * 1)(-1)
     assert lib.attn_vsa_layout(seg, 1, 4, 4, 4, 4, 4, 4, 64, None, None, ctypes.byref(nb), ctypes.byref(npre)) == 1
     assert lib.attn_vsa_layout(None, 0, 4, 4, 4, 8, 4, 4, 64, None, None, ctypes.byref(nb), ctypes.byref(npre)) == 1
+
+
+@pytest.mark.parametrize("prefix,shape", [([100, 37], (5, 9, 10)), ([], (8, 12, 12)), ([3], (9, 2, 13))])
+def test_vsa_tile_map_equals_the_oracle_blocks(lib, prefix, shape):
+    """Host computation: tiled row 64 b + r holds token r of block b, -1 past
+    the block's end and in the empty partner of an odd block count."""
+    import oracle
+    index, sizes, npre = gb.attn_vsa_tile_map(prefix, shape)
+    blocks, n_prefix = oracle.vsa_blocks(prefix, shape)
+    nb = len(blocks)
+    assert npre == n_prefix and sizes.tolist() == [len(b) for b in blocks]
+    assert index.numel() == (nb + nb % 2) * 64
+    for b, ref in enumerate(blocks):
+        assert index[64 * b:64 * b + len(ref)].tolist() == ref.tolist()
+        assert (index[64 * b + len(ref):64 * b + 64] == -1).all()
+    assert (index[64 * nb:] == -1).all()
+
+
+def test_vsa_list_size_counts_the_tiles(lib):
+    # 21 blocks, 3 prefix, topk 5: tiles 0-1 list all 21 blocks, tiles 2-10 at most 3 + 2 * 5
+    assert gb.attn_vsa_list_size(21, 3, 5, 1) == 2 * 21 + 9 * 13
+    assert gb.attn_vsa_list_size(21, 3, 5, 4) == 4 * (2 * 21 + 9 * 13)
+    assert gb.attn_vsa_list_size(18, 0, 7, 1) == 9 * 14
+    assert gb.attn_vsa_list_size(5, 1, 100, 2) == 2 * 3 * 5      # every block kept: every tile lists all
+    n = ctypes.c_longlong()
+    assert lib.attn_vsa_list_size(21, 3, 0, 1, ctypes.byref(n)) == 1  # topk must be positive
+    assert lib.attn_vsa_list_size(21, 22, 5, 1, ctypes.byref(n)) == 1
+
+
+def test_vsa_device_calls_validate_before_touching_a_device(lib):
+    assert lib.attn_gather_rows(P, 10, P, 10, 24, P, None, None) == 1           # row bytes not a multiple of 16
+    assert lib.attn_gather_rows(UNALIGNED, 10, P, 10, 256, P, None, None) == 3
+    assert lib.attn_gather_rows(P, 10, P, 0, 256, P, None, None) == 0           # nothing to copy
+    assert lib.attn_vsa_pool(P, 4, 2, 80, P, P, None, None) == 2                # head size
+    assert lib.attn_vsa_pool(P, 4, 2, 128, P, UNALIGNED, None, None) == 3
+    assert lib.attn_vsa_block_map(P, P, 21, 3, 4, 3, 128, 5, 0.1, P, P, P, None, None) == 1  # Hq % Hkv
+    assert lib.attn_vsa_block_map(P, P, 21, 3, 4, 2, 128, 0, 0.1, P, P, P, None, None) == 1  # topk 0
+    assert lib.attn_vsa_block_map(P, P, 30000, 0, 4, 2, 256, 5, 0.1, P, P, P, None, None) == 2  # scores too big
+
+    def fwd(**kw):
+        a = dict(q=P, k=P, v=P, nb=21, npre=3, topk=5, kl=P, kn=P, idx=P, rows=587, hq=4, hkv=2, d=128,
+                 scale=0.1, out=P, odt=1, lse=None)
+        a.update(kw)
+        return lib.attn_fwd_vsa(a["q"], a["k"], a["v"], a["nb"], a["npre"], a["topk"], a["kl"], a["kn"], a["idx"],
+                                a["rows"], a["hq"], a["hkv"], a["d"], a["scale"], a["out"], a["odt"], a["lse"],
+                                None, None)
+    assert fwd(d=96) == 2                # the attention kernel serves D = 64 and 128
+    assert fwd(odt=7) == 2
+    assert fwd(idx=None) == 1            # a tiled output needs out_rows = nbp * 64
+    assert fwd(idx=None, rows=22 * 64, nb=0, npre=0) == 1
+    assert fwd(nb=0, npre=0, rows=0) == 0  # nothing to compute
+    assert fwd(k=UNALIGNED) == 3
+    assert fwd(nb=200000) == 2           # more than 65535 tiles
+    assert fwd(scale=-1.0) == 1

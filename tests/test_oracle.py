@@ -577,3 +577,25 @@ def test_vsa_pooling_divides_by_the_true_block_size():
     k[blocks[1], 0, 0] = 1.0
     bm = oracle.vsa_block_map(q.to(torch.bfloat16), k.to(torch.bfloat16), blocks, npre, topk=1, scale=1.0)
     assert bm[0, :, 1].all() and not bm[0, :, 0].any()
+
+
+def test_vsa_pool_of_a_linear_ramp_is_the_box_centre():
+    """x = a + b t + c h + d w over the video grid: the mean of an axis-aligned
+    box is the value at the box's centre, whatever its (edge-clipped) size;
+    a prefix chunk's mean is the mean of its token positions."""
+    prefix, shape = [70], (5, 6, 7)
+    blocks, npre = oracle.vsa_blocks(prefix, shape)
+    n = 70 + 5 * 6 * 7
+    x = np.zeros((n, 2, 1))
+    x[:70, 0, 0] = np.arange(70)
+    t, h, w = np.meshgrid(*[np.arange(a) for a in shape], indexing="ij")
+    x[70:, 0, 0] = (1.0 + 2.0 * t + 3.0 * h + 5.0 * w).ravel()
+    x[:, 1, 0] = 7.0  # a constant head pools to the constant
+    pooled = oracle.vsa_pool(x, blocks)
+    assert pooled.shape == (len(blocks), 2, 1)
+    assert np.allclose(pooled[:, 1, 0], 7.0, rtol=0, atol=0)
+    assert pooled[0, 0, 0] == 31.5 and pooled[1, 0, 0] == 66.5  # chunks [0, 64) and [64, 70)
+    for b in range(npre, len(blocks)):
+        tt, hh, ww = np.unravel_index(blocks[b] - 70, shape)
+        centre = 1.0 + 2.0 * (tt.min() + tt.max()) / 2 + 3.0 * (hh.min() + hh.max()) / 2 + 5.0 * (ww.min() + ww.max()) / 2
+        assert abs(pooled[b, 0, 0] - centre) < 1e-12

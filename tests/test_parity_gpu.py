@@ -11,7 +11,8 @@ import torch
 import attention_forward_09_gb300 as gb
 import oracle
 import workloads
-from _helpers import LSE_TOL, OUT_TOL, assert_close, bf16_half_ulp, dev, max_err, status_word, to_np
+from _helpers import (LSE_TOL, OUT_TOL, assert_close, bf16_half_ulp, dev, max_err, status_word, to_np,
+                      vsa_lists_from_map, vsa_map_from_lists)
 
 pytestmark = pytest.mark.gpu
 
@@ -690,3 +691,187 @@ def test_config_spec_decode_sampled():
         ks, vs = oracle.paged_gather(cache, bt[s:s + 1], sl[s:s + 1])
         ro, rl = oracle.attention_single(q[a:b], ks[0], vs[0], w.scale, True)
         assert_close(out[a:b], lse[:, a:b], ro, rl, what=f"spec decode sequence {s}")
+
+
+# ------------------------------------------------- block-sparse video attention
+def _vsa_inputs(seed, prefix, video, hq, hkv, d):
+    n = sum(prefix) + int(np.prod(video))
+    g = torch.Generator().manual_seed(seed)
+    return (workloads.randn_bf16(g, n, hq, d), workloads.randn_bf16(g, n, hkv, d),
+            workloads.randn_bf16(g, n, hkv, d))
+
+
+def _vsa_check_map(bm_gpu, q, k, blocks, npre, topk, scale, heads=None):
+    """GPU block map against the oracle's: rows whose topk-th and (topk+1)-th
+    oracle scores are more than 1e-5 apart must be equal; the others must be
+    a valid choice (prefix kept, topk video blocks, none worse than a block
+    left out by more than 1e-5).  Returns the oracle map of the heads."""
+    heads = list(range(q.shape[1])) if heads is None else heads
+    g = q.shape[1] // k.shape[1]
+    nb = len(blocks)
+    keep = min(topk, nb - npre)
+    ref = np.zeros((len(heads), nb, nb), dtype=bool)
+    for x, h in enumerate(heads):
+        qh, kh = q[:, h:h + 1], k[:, h // g:h // g + 1]
+        ref[x] = oracle.vsa_block_map(qh, kh, blocks, npre, topk, scale)[0]
+        sc = scale * oracle.vsa_pool(qh, blocks)[:, 0, :] @ oracle.vsa_pool(kh, blocks)[:, 0, :].T
+        for i in range(nb):
+            if np.array_equal(bm_gpu[x, i], ref[x, i]):
+                continue
+            assert i >= npre and keep < nb - npre, f"head {h} dense row {i} differs"
+            s = np.sort(sc[i, npre:])[::-1]
+            assert s[keep - 1] - s[keep] <= 1e-5, f"head {h} row {i}: unambiguous top-{keep} differs"
+            chosen = bm_gpu[x, i, npre:]
+            assert bm_gpu[x, i, :npre].all() and chosen.sum() == keep
+            assert sc[i, npre:][chosen].min() >= sc[i, npre:][~chosen].max() - 1e-5
+    return ref
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_vsa_gather_and_pool_match_the_oracle(D):
+    prefix, video = [100, 37], (5, 9, 10)
+    q, _, _ = _vsa_inputs(60, prefix, video, 4, 2, D)
+    plan = gb.VsaPlan(prefix, video, dev())
+    blocks, npre = oracle.vsa_blocks(prefix, video)
+    assert plan.num_blocks == len(blocks) == 21 and plan.num_prefix_blocks == npre
+    st = status_word()
+    qt = gb.attn_gather_rows(q.to(dev()), plan.tile_index, dev_status=st)
+    pooled = gb.attn_vsa_pool(qt, plan.block_sizes, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    qt_h = qt.cpu()
+    for b, rows in enumerate(blocks):  # bit-exact rows, zeros at the padding
+        assert torch.equal(qt_h[64 * b:64 * b + len(rows)], q[torch.from_numpy(rows)])
+        assert not qt_h[64 * b + len(rows):64 * b + 64].any()
+    assert not qt_h[64 * len(blocks):].any()  # the odd count's empty partner block
+    ref = oracle.vsa_pool(q, blocks)  # [nb, H, D]
+    assert np.max(np.abs(to_np(pooled).transpose(1, 0, 2) - ref)) <= 1e-5
+
+
+@pytest.mark.parametrize("prefix,video,hq,hkv,D,topk", [
+    ([100, 37], (5, 9, 10), 4, 2, 128, 5),
+    ([100, 37], (5, 9, 10), 4, 2, 64, 1),
+    ([], (8, 12, 12), 2, 2, 128, 7),      # no prefix, 18 full blocks, even count
+    ([64], (4, 8, 8), 2, 1, 128, 100),    # topk above the video block count: every block kept
+])
+def test_vsa_block_map_matches_the_oracle(prefix, video, hq, hkv, D, topk):
+    q, k, _ = _vsa_inputs(61, prefix, video, hq, hkv, D)
+    plan = gb.VsaPlan(prefix, video, dev())
+    blocks, npre = oracle.vsa_blocks(prefix, video)
+    scale = 1.0 / math.sqrt(D)
+    st = status_word()
+    pq = gb.attn_vsa_pool(gb.attn_gather_rows(q.to(dev()), plan.tile_index), plan.block_sizes)
+    pk = gb.attn_vsa_pool(gb.attn_gather_rows(k.to(dev()), plan.tile_index), plan.block_sizes)
+    kv_list, kv_num = gb.attn_vsa_block_map(pq, pk, plan.block_sizes, npre, topk, scale, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    sizes = [len(b) for b in blocks]
+    bm = vsa_map_from_lists(kv_list, kv_num, len(blocks), npre, topk, sizes)
+    _vsa_check_map(bm, q, k, blocks, npre, topk, scale)
+
+
+@pytest.mark.parametrize("prefix,video,hq,hkv,D,topk,out_dtype,tiled", [
+    ([100, 37], (5, 9, 10), 4, 2, 128, 5, torch.float32, False),
+    ([100, 37], (5, 9, 10), 4, 2, 128, 5, torch.bfloat16, False),
+    ([100, 37], (5, 9, 10), 2, 2, 64, 3, torch.float32, False),
+    ([], (8, 12, 12), 2, 1, 128, 7, torch.float32, True),
+    ([64], (4, 8, 8), 2, 1, 64, 100, torch.float32, False),
+])
+def test_vsa_fwd_matches_the_oracle_on_the_oracle_map(prefix, video, hq, hkv, D, topk, out_dtype, tiled):
+    """The attention kernel alone, fed the oracle's own block map."""
+    q, k, v = _vsa_inputs(62, prefix, video, hq, hkv, D)
+    plan = gb.VsaPlan(prefix, video, dev())
+    blocks, npre = oracle.vsa_blocks(prefix, video)
+    scale = 1.0 / math.sqrt(D)
+    bm = oracle.vsa_block_map(q, k, blocks, npre, topk, scale)
+    ref_o, ref_l = oracle.attention_block_sparse(q, k, v, blocks, bm, scale)
+    kv_list, kv_num = (x.to(dev()) for x in vsa_lists_from_map(bm, [len(b) for b in blocks], npre, topk))
+    qt, kt, vt = (gb.attn_gather_rows(x.to(dev()), plan.tile_index) for x in (q, k, v))
+    st = status_word()
+    S = plan.tokens
+    out, lse = gb.attn_fwd_vsa(qt, kt, vt, kv_list, kv_num, plan.num_blocks, npre, topk,
+                               out_index=None if tiled else plan.tile_index, out_rows=None if tiled else S,
+                               softmax_scale=scale, lse=True, out_dtype=out_dtype, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    if tiled:  # rows stay in the tiled layout: take each token's row back out
+        idx = plan.tile_index.cpu().numpy()
+        tok = np.nonzero(idx >= 0)[0]
+        o = np.zeros((S, hq, D))
+        o[idx[tok]] = to_np(out)[tok]
+        l = np.zeros((hq, S))
+        l[:, idx[tok]] = to_np(lse)[:, tok]
+        out, lse = o, l
+    tol = OUT_TOL if out_dtype == torch.float32 else OUT_TOL + float(np.max(bf16_half_ulp(ref_o)))
+    assert_close(out, lse, ref_o, ref_l, out_tol=tol, what="vsa fwd")
+
+
+def test_vsa_end_to_end_matches_the_oracle():
+    prefix, video, hq, hkv, D, topk = [100, 37], (5, 9, 10), 4, 2, 128, 5
+    q, k, v = _vsa_inputs(63, prefix, video, hq, hkv, D)
+    plan = gb.VsaPlan(prefix, video, dev())
+    blocks, npre = oracle.vsa_blocks(prefix, video)
+    scale = 1.0 / math.sqrt(D)
+    st = status_word()
+    out, lse = gb.attn_vsa(q.to(dev()), k.to(dev()), v.to(dev()), plan, topk, scale, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    bm = oracle.vsa_block_map(q, k, blocks, npre, topk, scale)
+    ref_o, ref_l = oracle.attention_block_sparse(q, k, v, blocks, bm, scale)
+    assert_close(out, lse, ref_o, ref_l, what="vsa end to end")
+
+
+def test_vsa_bad_list_entry_sets_status():
+    prefix, video, D, topk = [], (4, 8, 8), 128, 1
+    q, k, v = _vsa_inputs(64, prefix, video, 2, 2, D)
+    plan = gb.VsaPlan(prefix, video, dev())
+    blocks, npre = oracle.vsa_blocks(prefix, video)
+    bm = oracle.vsa_block_map(q, k, blocks, npre, topk, 0.1)
+    kv_list, kv_num = (x.to(dev()) for x in vsa_lists_from_map(bm, [len(b) for b in blocks], npre, topk))
+    kv_list[0] = (len(blocks) + 5) << 9 | 64 << 2 | 1  # a block past the end
+    qt, kt, vt = (gb.attn_gather_rows(x.to(dev()), plan.tile_index) for x in (q, k, v))
+    st = status_word()
+    gb.attn_fwd_vsa(qt, kt, vt, kv_list, kv_num, plan.num_blocks, npre, topk, out_index=plan.tile_index,
+                    out_rows=plan.tokens, softmax_scale=0.1, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & gb.DEV_BAD_INDEX
+
+
+def test_config_vsa_video_sampled():
+    """The full-size video workload: the whole device path, its block map
+    checked on two heads, and rows of sampled query blocks against the oracle."""
+    w = workloads.vsa_video()
+    q, k, v = w.make()
+    plan = gb.VsaPlan(w.prefix, w.video, dev())
+    blocks, npre = oracle.vsa_blocks(w.prefix, w.video)
+    st = status_word()
+    qd, kd, vd = q.to(dev()), k.to(dev()), v.to(dev())
+    qt, kt, vt = (gb.attn_gather_rows(x, plan.tile_index, dev_status=st) for x in (qd, kd, vd))
+    pq, pk = gb.attn_vsa_pool(qt, plan.block_sizes, st), gb.attn_vsa_pool(kt, plan.block_sizes, st)
+    kv_list, kv_num = gb.attn_vsa_block_map(pq, pk, plan.block_sizes, npre, w.topk, w.scale, dev_status=st)
+    out, lse = gb.attn_fwd_vsa(qt, kt, vt, kv_list, kv_num, plan.num_blocks, npre, w.topk,
+                               out_index=plan.tile_index, out_rows=w.tokens, softmax_scale=w.scale, lse=True,
+                               dev_status=st)
+    out2, lse2 = gb.attn_vsa(qd, kd, vd, plan, w.topk, w.scale, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)  # the composed call is the same launches
+    heads = [0, w.Hq - 1]
+    sizes = [len(b) for b in blocks]
+    nb = len(blocks)
+    bm_all = vsa_map_from_lists(kv_list, kv_num, nb, npre, w.topk, sizes)
+    ref = _vsa_check_map(bm_all[heads], q, k, blocks, npre, w.topk, w.scale, heads)
+    rng = np.random.default_rng(16)
+    sample = [0, npre, nb - 1] + [int(x) for x in rng.integers(npre, nb, 4)]
+    out_h, lse_h = to_np(out), to_np(lse)
+    checked = 0
+    for x, h in enumerate(heads):
+        for i in sample:
+            if not np.array_equal(bm_all[h, i], ref[x, i]):
+                continue  # a near-tie resolved the other way; the map check covered it
+            rows = torch.from_numpy(blocks[i])
+            keys = torch.from_numpy(np.concatenate([blocks[j] for j in np.nonzero(ref[x, i])[0]]))
+            r_o, r_l = oracle.attention_single(q[rows, h:h + 1], k[keys, h:h + 1], v[keys, h:h + 1], w.scale, False)
+            assert_close(out_h[blocks[i], h:h + 1], lse_h[h:h + 1, blocks[i]], r_o, r_l, what=f"head {h} block {i}")
+            checked += 1
+    assert checked >= len(sample)

@@ -67,3 +67,24 @@ def test_generators_are_seeded_and_bf16():
     b = workloads.tiny_varlen().make()
     assert all(torch.equal(x, y) for x, y in zip(a, b))
     assert a[0].dtype == torch.bfloat16 and np.isfinite(a[0].float().numpy()).all()
+
+
+def test_vsa_kept_pairs_count_the_block_map():
+    """The block-sparse bench divides by 4 D x the query-key pairs its lists
+    keep; recounted here from the oracle's block map itself."""
+    import bench
+    from _helpers import vsa_lists_from_map
+
+    prefix, video, topk = [100, 37], (5, 9, 10), 5
+    blocks, npre = oracle.vsa_blocks(prefix, video)
+    n = sum(prefix) + int(np.prod(video))
+    g = torch.Generator().manual_seed(7)
+    q, k = torch.randn(n, 3, 16, generator=g), torch.randn(n, 3, 16, generator=g)
+    bm = oracle.vsa_block_map(q, k, blocks, npre, topk, 0.25)
+    sizes = [len(b) for b in blocks]
+    kl, kn = vsa_lists_from_map(bm, sizes, npre, topk)
+    expect = sum(sizes[i] * sum(sizes[j] for j in np.nonzero(bm[h, i])[0])
+                 for h in range(3) for i in range(len(blocks)))
+    assert bench.vsa_kept_pairs(kl, kn, len(blocks), npre, topk, sizes) == expect
+    w = workloads.vsa_video()
+    assert w.tokens == 512 + 21 * 45 * 80 and w.topk == 64

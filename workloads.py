@@ -353,6 +353,41 @@ def masked_dit() -> Masked:
     return Masked("masked_dit_b2_s4096_h24_d128_len4096_3072", [4096, 3072], 4096, 24, 24, 128, False, seed=15)
 
 
+@dataclass
+class Vsa:
+    """One sequence for block-sparse video attention: prefix segments, then a
+    T x H x W video latent grid; q [S, Hq, D], k / v [S, Hkv, D]; each video
+    query block keeps its topk best video key blocks plus the prefix."""
+    name: str
+    prefix: list
+    video: tuple
+    Hq: int
+    Hkv: int
+    D: int
+    topk: int
+    seed: int
+
+    @property
+    def tokens(self) -> int:
+        return sum(self.prefix) + self.video[0] * self.video[1] * self.video[2]
+
+    @property
+    def scale(self) -> float:
+        return default_scale(self.D)
+
+    def make(self):
+        g = torch.Generator().manual_seed(self.seed)
+        q = randn_bf16(g, self.tokens, self.Hq, self.D)
+        k = randn_bf16(g, self.tokens, self.Hkv, self.D)
+        v = randn_bf16(g, self.tokens, self.Hkv, self.D)
+        return q, k, v
+
+
+def vsa_video() -> Vsa:
+    """A 512-token prefix and a 21 x 45 x 80 video latent grid (76112 tokens,
+    1448 blocks), 40 heads, D=128, the page's default topk of 64 blocks."""
+    return Vsa("vsa_p512_t21h45w80_h40_d128_top64", [512], (21, 45, 80), 40, 40, 128, 64, seed=16)
+
 def _uniform_int(gen: torch.Generator, lo: int, hi: int, n: int) -> list:
     """n integers uniform in [lo, hi] (inclusive)."""
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=gen)]
