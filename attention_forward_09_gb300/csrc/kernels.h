@@ -143,7 +143,8 @@ constexpr int kVsaBlock = 64;
 
 // A key-block entry of a tile's list: (block << 9) | (its token count << 2)
 // | bits, bit 0 set when query block 2 t keeps the block, bit 1 when 2 t + 1
-// does.  Lists are in ascending block order.
+// does.  A list holds the blocks with bits 3, then 1, then 2, each group in
+// ascending block order.
 __host__ __device__ inline int vsa_entry(int blk, int size, int bits) { return (blk << 9) | (size << 2) | bits; }
 
 // Sizes of the per-head list array: tile t holds up to capacity(t) entries

@@ -16,7 +16,8 @@
 //                    of those query blocks against every key block in shared
 //                    memory, a 4-pass radix select of the topk-th score per
 //                    query block (ties to the lower block index), and, per
-//                    pair of query blocks, the union of their key blocks;
+//                    pair of query blocks, the union of their key blocks
+//                    (kept by both, then by the first only, then the second);
 //   vsa_fwd          CTA per (head, pair of query blocks = one 128-row tile):
 //                    Q tile by TMA, K/V tiles of two 64-row key blocks taken
 //                    from the pair's union list, S = Q K^T and O += P V by
@@ -257,17 +258,25 @@ __global__ void __launch_bounds__(kMapWarps * 32) vsa_block_map_sm103a(const Vsa
             const uint32_t* s1 = s0 + words;
             int32_t* dst = p.kv_list + static_cast<long long>(h) * p.g.per_head() + p.g.offset(t);
             const int cap = p.g.capacity(t);
+            // Blocks kept by both query blocks first, then those kept by the
+            // first only, then by the second only: a K/V tile of two blocks
+            // from one of the last two groups is skipped outright by the
+            // softmax warps of the other query block.
             int cnt = 0;
-            for (int w = 0; w < words; ++w) {
-                const int j = w * 32 + lane;
-                const uint32_t bits = ((s0[w] >> lane) & 1u) | (((s1[w] >> lane) & 1u) << 1);
-                const uint32_t any = __ballot_sync(0xffffffffu, bits != 0u);
-                if (bits) {
-                    const int at = cnt + __popc(any & ((1u << lane) - 1u));
-                    const int sz = block_size_at(p.sizes, j, p.status);
-                    if (at < cap) dst[at] = vsa_entry(j, sz, static_cast<int>(bits));
+#pragma unroll 1
+            for (uint32_t want = 3u; want != 0u; want = want == 3u ? 1u : (want == 1u ? 2u : 0u)) {
+                for (int w = 0; w < words; ++w) {
+                    const int j = w * 32 + lane;
+                    const uint32_t bits = ((s0[w] >> lane) & 1u) | (((s1[w] >> lane) & 1u) << 1);
+                    const bool mine = bits == want;
+                    const uint32_t sel_w = __ballot_sync(0xffffffffu, mine);
+                    if (mine) {
+                        const int at = cnt + __popc(sel_w & ((1u << lane) - 1u));
+                        const int sz = block_size_at(p.sizes, j, p.status);
+                        if (at < cap) dst[at] = vsa_entry(j, sz, static_cast<int>(bits));
+                    }
+                    cnt += __popc(sel_w);
                 }
-                cnt += __popc(any);
             }
             if (lane == 0) {
                 if (cnt > cap && p.status) atomicOr(p.status, kDevBadIndex);

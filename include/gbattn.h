@@ -370,9 +370,11 @@ const char* attn_status_string(gbattn_status status);
  *   must be >= 1, as the page requires.
  *   kv_list  out, device int32 [attn_vsa_list_size entries]: per head h and
  *            tile t, the union of the key blocks that query blocks 2 t and
- *            2 t + 1 keep, ascending, each entry (block << 9) | (block size
- *            << 2) | bits, bit 0 set if block 2 t keeps it, bit 1 if 2 t + 1
- *            does
+ *            2 t + 1 keep, each entry (block << 9) | (block size << 2) |
+ *            bits, bit 0 set if block 2 t keeps it, bit 1 if 2 t + 1 does;
+ *            the blocks both keep come first, then those only 2 t keeps,
+ *            then those only 2 t + 1 keeps, each group ascending (any order
+ *            is accepted by attn_fwd_vsa)
  *   kv_num   out, device int32 [Hq, (nb + 1) / 2]: entries of each list
  *   Placement: with keep = min(topk, nb - num_prefix_blocks), nt = (nb + 1)
  *   / 2, td = nt if keep == nb - num_prefix_blocks else min(nt,

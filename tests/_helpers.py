@@ -67,8 +67,8 @@ def vsa_lists_from_map(bm, sizes, npre, topk):
     for h in range(hq):
         for t, (off, cap) in enumerate(vsa_tile_offsets(nb, npre, topk)):
             r1 = bm[h, 2 * t + 1] if 2 * t + 1 < nb else np.zeros(nb, bool)
-            ent = [(j << 9) | (int(sizes[j]) << 2) | int(bm[h, 2 * t, j]) | (int(r1[j]) << 1)
-                   for j in range(nb) if bm[h, 2 * t, j] or r1[j]]
+            bits = bm[h, 2 * t].astype(int) | (r1.astype(int) << 1)
+            ent = [(j << 9) | (int(sizes[j]) << 2) | want for want in (3, 1, 2) for j in range(nb) if bits[j] == want]
             assert len(ent) <= cap
             kl[h * per_head + off:h * per_head + off + len(ent)] = ent
             kn[h, t] = len(ent)
@@ -87,7 +87,9 @@ def vsa_map_from_lists(kv_list, kv_num, nb, npre, topk, sizes):
             assert 0 <= n <= cap
             e = kl[h * per_head + off:h * per_head + off + n].astype(np.int64)
             blk, sz, bits = e >> 9, (e >> 2) & 127, e & 3
-            assert np.all(np.diff(blk) > 0) and np.all(bits != 0) and np.array_equal(sz, np.asarray(sizes)[blk])
+            assert np.all(bits != 0) and np.array_equal(sz, np.asarray(sizes)[blk])
+            rank = np.array([0, 1, 2, 0])[bits]  # groups: kept by both, by the first only, by the second only
+            assert np.all(np.diff(rank) >= 0) and np.all(np.diff(blk)[np.diff(rank) == 0] > 0)
             bm[h, 2 * t, blk[(bits & 1) != 0]] = True
             if 2 * t + 1 < nb:
                 bm[h, 2 * t + 1, blk[(bits & 2) != 0]] = True
