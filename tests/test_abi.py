@@ -3,6 +3,7 @@ bad arguments on the host before touching the GPU (these calls make no CUDA
 call, so they run on a machine without a GPU)."""
 
 import ctypes
+import json
 import os
 import re
 
@@ -198,6 +199,29 @@ def test_vsa_layout_equals_the_oracle_blocks(lib, prefix, shape):
     assert npre == n_prefix and start.numel() == len(blocks) + 1
     for b, ref in enumerate(blocks):
         assert order[int(start[b]):int(start[b + 1])].tolist() == ref.tolist()
+
+
+def _vsa_layout_cases():
+    with open(os.path.join(ROOT, "tests", "golden", "vsa_layout_examples.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _vsa_layout_cases(), ids=lambda c: c["name"])
+def test_vsa_host_layouts_match_the_hand_worked_layouts(lib, case):
+    """Both host layout calls against block layouts worked by hand from the
+    page's tiling functions (no oracle involved)."""
+    blocks = [[i for a, b in runs for i in range(a, b)] for runs in case["blocks"]]
+    order, start, npre = gb.attn_vsa_layout(case["prefix"], case["video"])
+    assert npre == case["n_prefix_blocks"]
+    assert [order[int(start[b]):int(start[b + 1])].tolist() for b in range(len(blocks))] == blocks
+    assert start.numel() == len(blocks) + 1
+    index, sizes, npre = gb.attn_vsa_tile_map(case["prefix"], case["video"])
+    assert npre == case["n_prefix_blocks"] and sizes.tolist() == case["block_sizes"]
+    nb = len(blocks)
+    expect = [-1] * ((nb + nb % 2) * 64)
+    for b, toks in enumerate(blocks):
+        expect[64 * b:64 * b + len(toks)] = toks
+    assert index.tolist() == expect
 
 
 def test_vsa_layout_validation(lib):

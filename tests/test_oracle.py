@@ -499,6 +499,26 @@ def test_masked_cross_keeps_every_query():
 
 # --------------------------------------------- block-sparse video attention (f4)
 
+def _vsa_layout_cases():
+    with open(os.path.join(GOLDEN, "vsa_layout_examples.json")) as f:
+        return json.load(f)["cases"]
+
+
+def _runs_to_tokens(runs):
+    return [i for a, b in runs for i in range(a, b)]
+
+
+@pytest.mark.parametrize("case", _vsa_layout_cases(), ids=lambda c: c["name"])
+def test_vsa_blocks_match_the_hand_worked_layouts(case):
+    """Block layouts worked by hand from the page's tiling functions: the
+    chunking of each prefix segment on its own, the T, H, W order of the
+    tiles, row-major order inside a tile, remainder tiles at the far edges."""
+    blocks, n_prefix = oracle.vsa_blocks(case["prefix"], tuple(case["video"]))
+    assert n_prefix == case["n_prefix_blocks"]
+    assert [len(b) for b in blocks] == case["block_sizes"]
+    assert [b.tolist() for b in blocks] == [_runs_to_tokens(r) for r in case["blocks"]]
+
+
 def test_vsa_blocks_partition_the_sequence_into_boxes():
     prefix, shape = [70, 5], (5, 6, 7)
     blocks, n_prefix = oracle.vsa_blocks(prefix, shape)
