@@ -519,6 +519,31 @@ def test_vsa_blocks_match_the_hand_worked_layouts(case):
     assert [b.tolist() for b in blocks] == [_runs_to_tokens(r) for r in case["blocks"]]
 
 
+def test_vsa_block_map_hand_worked_with_a_tie():
+    """Prefix of 2 tokens (one block) and a 1 x 1 x 16 grid (four video blocks
+    of 4 tokens).  Every query row is (1, 0); the key rows of block b are all
+    (s_b, 0) with s = (5, 1, 3, 3, 2), so the block means are exact and the
+    block scores at scale 1 are exactly s.  Top-1 among the video blocks is a
+    tie between blocks 2 and 3, which goes to block 2 (the lower index); top-2
+    takes both; the prefix key block is always kept and the prefix query block
+    keeps every block."""
+    blocks, n_prefix = oracle.vsa_blocks([2], (1, 1, 16))
+    assert n_prefix == 1 and [len(b) for b in blocks] == [2, 4, 4, 4, 4]
+    s = [5.0, 1.0, 3.0, 3.0, 2.0]
+    q = torch.zeros(18, 1, 2)
+    q[:, 0, 0] = 1.0
+    k = torch.zeros(18, 1, 2)
+    for b, rows in enumerate(blocks):
+        k[torch.from_numpy(rows), 0, 0] = s[b]
+    expect = {1: [True, False, True, False, False], 2: [True, False, True, True, False],
+              3: [True, False, True, True, True]}
+    for topk, row in expect.items():
+        bm = oracle.vsa_block_map(q, k, blocks, n_prefix, topk, 1.0)[0]
+        assert bm[0].all()  # the prefix query block keeps every block
+        for i in range(1, 5):
+            assert bm[i].tolist() == row, (topk, i)
+
+
 def test_vsa_blocks_partition_the_sequence_into_boxes():
     prefix, shape = [70, 5], (5, 6, 7)
     blocks, n_prefix = oracle.vsa_blocks(prefix, shape)
