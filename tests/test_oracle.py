@@ -544,6 +544,32 @@ def test_vsa_block_map_hand_worked_with_a_tie():
             assert bm[i].tolist() == row, (topk, i)
 
 
+def test_vsa_block_sparse_zero_query_is_the_mean_of_the_kept_tokens():
+    """q = 0 makes every score 0, so each query token's output is the plain
+    mean of V over the tokens of the key blocks its block keeps and its lse
+    is ln(their count): a closed form for any block map (here one chosen by
+    hand, unrelated to the scores), with GQA (head h reads KV head h // 2)."""
+    blocks, n_prefix = oracle.vsa_blocks([5], (2, 3, 6))  # sizes 5, 24, 12
+    assert [len(b) for b in blocks] == [5, 24, 12]
+    g = torch.Generator().manual_seed(7)
+    S = 41
+    q = torch.zeros(S, 4, 3)
+    k = torch.randn(S, 2, 3, generator=g)
+    v = torch.randn(S, 2, 3, generator=g).double()
+    bm = np.zeros((4, 3, 3), dtype=bool)
+    bm[0] = [[1, 0, 0], [1, 1, 0], [0, 0, 1]]
+    bm[1] = [[1, 1, 1], [0, 1, 0], [1, 0, 1]]
+    bm[2] = [[0, 1, 1], [0, 0, 1], [1, 1, 0]]
+    bm[3] = [[1, 0, 1], [1, 1, 1], [0, 1, 0]]
+    out, lse = oracle.attention_block_sparse(q, k, v, blocks, bm, 0.5)
+    for h in range(4):
+        for i, rows in enumerate(blocks):
+            keys = np.concatenate([blocks[j] for j in range(3) if bm[h, i, j]])
+            mean = v[torch.from_numpy(keys), h // 2].numpy().mean(axis=0)
+            assert np.allclose(out[rows, h], mean, rtol=0, atol=1e-12)
+            assert np.allclose(lse[h, rows], math.log(len(keys)), rtol=0, atol=1e-12)
+
+
 def test_vsa_blocks_partition_the_sequence_into_boxes():
     prefix, shape = [70, 5], (5, 6, 7)
     blocks, n_prefix = oracle.vsa_blocks(prefix, shape)
