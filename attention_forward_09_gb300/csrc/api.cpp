@@ -239,6 +239,10 @@ gbattn_status attn_kv_cache_write(const void* key, const void* value, const int3
     if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || Hkv <= 0) return GBATTN_ERR_INVALID_ARG;
     if (!head_size_ok(D)) return GBATTN_ERR_UNSUPPORTED;
     if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return GBATTN_ERR_UNSUPPORTED;
+    // The kernel counts the 2 * num_tokens (token, K or V) rows and a row's
+    // 16-byte pieces in 32-bit integers.
+    if (num_tokens >= (1 << 30) || static_cast<long long>(Hkv) * D * 2 > 0x7fffffffLL)
+        return GBATTN_ERR_UNSUPPORTED;
     if (num_tokens == 0) return GBATTN_OK;
     if (!key || !value || !slot_mapping || !kv_cache) return GBATTN_ERR_INVALID_ARG;
     if (!aligned16(key) || !aligned16(value) || !aligned16(kv_cache)) return GBATTN_ERR_ALIGNMENT;

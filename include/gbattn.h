@@ -236,8 +236,10 @@ gbattn_status attn_vsa_layout(const int32_t* prefix_segments, int num_segments, 
  * Two tokens with the same slot: one of them is stored, which one is not
  * defined.  A slot >= num_blocks * block_size is skipped and sets
  * GBATTN_DEV_BAD_INDEX in dev_status.  Errors: GBATTN_ERR_INVALID_ARG,
- * GBATTN_ERR_UNSUPPORTED (head size), GBATTN_ERR_ALIGNMENT (key, value,
- * kv_cache not 16-byte aligned), GBATTN_ERR_DEVICE / GBATTN_ERR_CUDA.
+ * GBATTN_ERR_UNSUPPORTED (head size; num_tokens >= 2^30, Hkv * D * 2 bytes
+ * per row or num_blocks * block_size slots past 2^31 - 1),
+ * GBATTN_ERR_ALIGNMENT (key, value, kv_cache not 16-byte aligned),
+ * GBATTN_ERR_DEVICE / GBATTN_ERR_CUDA.
  */
 gbattn_status attn_kv_cache_write(const void* key, const void* value, const int32_t* slot_mapping, int num_tokens,
                                   void* kv_cache, int num_blocks, int block_size, int Hkv, int D,

@@ -155,6 +155,8 @@ def test_kv_cache_write_validates_before_touching_a_device(lib):
     assert w(None, P, P, 4, P, 8, 128, 8, 128, None, None) == 1        # null key
     assert w(UNALIGNED, P, P, 4, P, 8, 128, 8, 128, None, None) == 3   # alignment
     assert w(P, P, P, 0, P, 8, 128, 8, 128, None, None) == 0           # nothing to write
+    assert w(P, P, P, 1 << 30, P, 8, 128, 8, 128, None, None) == 2     # row count past 32 bits
+    assert w(P, P, P, 4, P, 8, 128, 1 << 22, 256, None, None) == 2     # row bytes past 32 bits
 
 
 def test_paged_prefill_validates_before_touching_a_device(lib):
