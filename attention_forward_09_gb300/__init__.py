@@ -12,7 +12,7 @@ Entry points (same names as the C ABI):
     attn_fwd_paged(q, kv_cache, block_table, seq_lens, max_seq_len, ...)
     attn_fwd_paged_workspace_size(num_seqs, Hq, Hkv, D, max_seq_len)
     attn_kv_cache_write, attn_fwd_paged_prefill, attn_mask_to_varlen, attn_pack_rows,
-    attn_unpack_rows, attn_unpack_lse, attn_fwd_dense_plan, attn_fwd_paged_noalloc
+    attn_unpack_rows, attn_unpack_lse, attn_fwd_dense_plan, attn_fwd_varlen_plan, attn_fwd_paged_noalloc
     attn_vsa_layout, attn_vsa_tile_map, attn_gather_rows, attn_vsa_pool, attn_vsa_list_size,
     attn_vsa_block_map, attn_fwd_vsa
 Compositions of those calls: attn_fwd_masked (padding mask), attn_vsa (block-sparse
@@ -46,6 +46,7 @@ SIGNATURES = {
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_fwd_paged_noalloc": (_I, [_P, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _P]),
     "attn_fwd_dense_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
+    "attn_fwd_varlen_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
     "attn_kv_cache_write": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P]),
     "attn_fwd_paged_prefill": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P,
                                     _P, _P]),
@@ -146,6 +147,18 @@ def attn_fwd_dense_plan(B, Sq, Sk, Hq, Hkv, D, causal=False):
                                             ctypes.byref(sp))
     _check("attn_fwd_dense_plan", st)
     return n.value, sp.value
+
+
+def attn_fwd_varlen_plan(lens_q, D, causal=False, Hq=32, Hkv=8, lens_k=None):
+    """Kernel launches attn_fwd_varlen makes for documents of these lengths
+    on the current device (host sizes only)."""
+    lens_k = lens_q if lens_k is None else lens_k
+    n = ctypes.c_int(0)
+    st = load_library().attn_fwd_varlen_plan(len(lens_q), int(sum(lens_q)), int(max(list(lens_q) + [0])),
+                                             int(max(list(lens_k) + [0])), Hq, Hkv, D, int(bool(causal)),
+                                             ctypes.byref(n))
+    _check("attn_fwd_varlen_plan", st)
+    return n.value
 
 
 def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, softmax_scale=None,
@@ -421,6 +434,8 @@ def attn_vsa_pool(x_tiled, block_sizes, dev_status=None, stream=None):
     """x_tiled [rows >= nb * 64, H, D] bf16 CUDA, block_sizes int32 CUDA [nb]
     -> pooled [H, nb, D] fp32 block means."""
     _bf16_cuda("x_tiled", x_tiled)
+    if block_sizes.dtype != torch.int32 or not block_sizes.is_cuda or not block_sizes.is_contiguous():
+        raise ValueError("block_sizes must be a contiguous int32 CUDA tensor")
     nb = block_sizes.numel()
     _, H, D = x_tiled.shape
     if x_tiled.shape[0] < nb * 64:
@@ -444,8 +459,17 @@ def attn_vsa_block_map(pooled_q, pooled_k, block_sizes, num_prefix_blocks, topk,
     """pooled_q [Hq, nb, D], pooled_k [Hkv, nb, D] fp32 CUDA -> (kv_list, kv_num)
     int32: per head and tile (query blocks 2t, 2t+1), the union of the key
     blocks they keep, entries (block << 9) | (size << 2) | bits."""
+    if pooled_q.dim() != 3 or pooled_k.dim() != 3 or pooled_q.shape[1:] != pooled_k.shape[1:]:
+        raise ValueError("pooled_q must be [Hq, nb, D] and pooled_k [Hkv, nb, D] with the same nb and D")
+    if pooled_q.dtype != torch.float32 or pooled_k.dtype != torch.float32:
+        raise ValueError("pooled_q and pooled_k must be float32")
     Hq, nb, D = pooled_q.shape
     Hkv = pooled_k.shape[0]
+    if block_sizes.numel() != nb or block_sizes.dtype != torch.int32:
+        raise ValueError(f"block_sizes must hold {nb} int32 entries (one per block)")
+    for n_, t in (("pooled_q", pooled_q), ("pooled_k", pooled_k), ("block_sizes", block_sizes)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n_} must be a contiguous CUDA tensor")
     n = attn_vsa_list_size(nb, num_prefix_blocks, topk, Hq)
     kv_list = torch.empty(max(n, 1), dtype=torch.int32, device=pooled_q.device)
     kv_num = torch.empty(Hq, (nb + 1) // 2, dtype=torch.int32, device=pooled_q.device)
@@ -456,6 +480,36 @@ def attn_vsa_block_map(pooled_q, pooled_k, block_sizes, num_prefix_blocks, topk,
     return kv_list, kv_num
 
 
+def _check_vsa_fwd_shapes(q_tiled, k_tiled, v_tiled, kv_list, kv_num, num_blocks, num_prefix_blocks, topk,
+                          out_index, out_rows, out, lse):
+    """Raise ValueError unless the tensors have the sizes the C call derives
+    from (num_blocks, Hq, Hkv, D): its tensor maps and list reads trust them."""
+    if q_tiled.dim() != 3 or k_tiled.dim() != 3 or v_tiled.dim() != 3:
+        raise ValueError("q_tiled, k_tiled and v_tiled must be [rows, heads, D]")
+    rows, Hq, D = q_tiled.shape
+    want = (num_blocks + num_blocks % 2) * 64
+    if rows != want:
+        raise ValueError(f"q_tiled has {rows} rows; {num_blocks} blocks need {want} (64 per block, even count)")
+    if k_tiled.shape != v_tiled.shape or k_tiled.shape[0] != rows or k_tiled.shape[2] != D:
+        raise ValueError("k_tiled and v_tiled must both be [rows of q_tiled, Hkv, D of q_tiled]")
+    for n_, t in (("kv_list", kv_list), ("kv_num", kv_num)):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{n_} must be a contiguous int32 tensor")
+    need = attn_vsa_list_size(num_blocks, num_prefix_blocks, topk, Hq)
+    if kv_list.numel() < need:
+        raise ValueError(f"kv_list holds {kv_list.numel()} entries; these sizes need {need}")
+    if tuple(kv_num.shape) != (Hq, (num_blocks + 1) // 2):
+        raise ValueError(f"kv_num must be [Hq, (num_blocks + 1) // 2] = [{Hq}, {(num_blocks + 1) // 2}]")
+    if out_index is not None and (out_index.dtype != torch.int32 or out_index.numel() != rows):
+        raise ValueError(f"out_index must hold {rows} int32 entries (one per tiled row)")
+    if out_index is None and out_rows != rows:
+        raise ValueError("without out_index the output stays tiled: out_rows must equal the tiled row count")
+    if out is not None and tuple(out.shape) != (out_rows, Hq, D):
+        raise ValueError(f"out must be [out_rows, Hq, D] = [{out_rows}, {Hq}, {D}]")
+    if torch.is_tensor(lse) and (tuple(lse.shape) != (Hq, out_rows) or lse.dtype != torch.float32):
+        raise ValueError(f"lse must be float32 [Hq, out_rows] = [{Hq}, {out_rows}]")
+
+
 def attn_fwd_vsa(q_tiled, k_tiled, v_tiled, kv_list, kv_num, num_blocks, num_prefix_blocks, topk, out_index=None,
                  out_rows=None, softmax_scale=None, lse=None, out_dtype=torch.float32, out=None, dev_status=None,
                  stream=None):
@@ -463,12 +517,17 @@ def attn_fwd_vsa(q_tiled, k_tiled, v_tiled, kv_list, kv_num, num_blocks, num_pre
     (bf16 CUDA) and the lists of attn_vsa_block_map.  Row r of the tiled layout
     goes to out row out_index[r] (None: out stays tiled).  Returns (out
     [out_rows, Hq, D], lse [Hq, out_rows] or None)."""
+    if out_rows is None:
+        out_rows = q_tiled.shape[0]
+    _check_vsa_fwd_shapes(q_tiled, k_tiled, v_tiled, kv_list, kv_num, num_blocks, num_prefix_blocks, topk,
+                          out_index, out_rows, out, lse)
     for n_, t in (("q_tiled", q_tiled), ("k_tiled", k_tiled), ("v_tiled", v_tiled)):
         _bf16_cuda(n_, t)
+    for n_, t in (("kv_list", kv_list), ("kv_num", kv_num), ("out_index", out_index), ("out", out), ("lse", lse)):
+        if torch.is_tensor(t) and not t.is_cuda:
+            raise ValueError(f"{n_} must be a CUDA tensor")
     rows, Hq, D = q_tiled.shape
     Hkv = k_tiled.shape[1]
-    if out_rows is None:
-        out_rows = rows
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     if out is None:

@@ -198,6 +198,35 @@ gbattn_status attn_fwd_dense_plan(int B, int Sq, int Sk, int Hq, int Hkv, int D,
     return GBATTN_OK;
 }
 
+gbattn_status attn_fwd_varlen_plan(int num_docs, int Tq, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
+                                   int causal, int* launches) {
+    if (!launches) return GBATTN_ERR_INVALID_ARG;
+    *launches = 0;
+    if (num_docs < 0 || Tq < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+        return GBATTN_ERR_INVALID_ARG;
+    if (!head_size_ok(D)) return GBATTN_ERR_UNSUPPORTED;
+    if (num_docs > 65535) return GBATTN_ERR_UNSUPPORTED;
+    if (num_docs == 0 || Tq == 0 || max_seqlen_q == 0) return GBATTN_OK;
+    DeviceInfo di;
+    gbattn_status s = device_info(&di);
+    if (s != GBATTN_OK) return s;
+    int dummy = 0;
+    PrefillParams p{};
+    p.cu_q = p.cu_k = &dummy;  // only tested for presence: the plan reads no device memory
+    p.num_docs = num_docs;
+    p.Tq = Tq;
+    p.max_seqlen_q = max_seqlen_q;
+    p.max_seqlen_k = max_seqlen_k;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.group = Hq / Hkv;
+    p.causal = causal ? 1 : 0;
+    gbattn::PrefillPlan pl;
+    if (gbattn::prefill_plan(D, p, di.sms, &pl) != cudaSuccess) return GBATTN_ERR_CUDA;
+    *launches = pl.launches;
+    return GBATTN_OK;
+}
+
 gbattn_status attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
                               const int32_t* cu_seqlens_k, int num_docs, int Tq, int Tk, int max_seqlen_q,
                               int max_seqlen_k, int Hq, int Hkv, int D, float softmax_scale, int causal, void* out,

@@ -11,7 +11,10 @@
 // The array is device memory of every GPU on which this library's code is
 // loaded, held until the process exits.  Its host-side name is only a
 // stand-in: the device address is looked up with cudaGetSymbolAddress on
-// the first call on each device (with that device current) and cached.
+// the first call on each device (with that device current) and cached for
+// the life of the process.  cudaDeviceReset unloads the library's device
+// code, after which the array may live elsewhere: the cache does not notice,
+// so the entry point must not be used on a device after it was reset.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -27,9 +27,12 @@
 //
 // Both kernels have a paged instantiation (PAGED): K/V tiles come from the
 // paged cache through block_table (vllm-ascend attention_v1.py, chunked
-// prefill and speculative decode over the cache), V rows past seq_len are
-// zeroed before P.V, and the two-tile kernel can pack a GQA group into a
-// tile (128 / group tokens x group heads per 128 rows).
+// prefill and speculative decode over the cache), and the two-tile kernel
+// can pack a GQA group into a tile (128 / group tokens x group heads per 128
+// rows).  In every mode the V rows of a document's last KV tile that lie past
+// its last key are zeroed in shared memory before P.V, so a document's result
+// never depends on the bytes of its neighbours (no cross-document attention,
+// FlashAttentionImpl._forward_varlen_packed), NaN or not.
 //
 // Causal masking is bottom-right aligned (FlashAttentionImpl.forward_fa_npu:
 // key kp is blocked for query qp iff kp > qp + Sk - Sq); KV tiles past the
@@ -255,9 +258,11 @@ __global__ void __launch_bounds__(192, 1)
             if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
             if (!(ok = wait_all(b_p_full, j & 1))) break;
             if (!(ok = wait_all(b_kv_full(vs), vph))) break;
-            if (PAGED) {
-                // Cache slots past seq_len may hold anything, NaN included; P is 0
-                // there but 0 * NaN is not, so those V rows are zeroed first.
+            {
+                // Rows past the document's last key (the next document's, the
+                // next batch entry's, or cache slots past seq_len) may hold
+                // anything, NaN included; P is 0 there but 0 * NaN is not, so
+                // the last KV tile's V rows past the end are zeroed first.
                 const int lim = Lk - j * BN;
                 if (lim < BN) {
                     const uint32_t vb = sKV + vs * C::KV_BYTES;
@@ -927,9 +932,11 @@ __global__ void __launch_bounds__(384, 1)
                 const bool more = j + 1 < nmax;
                 bool k_ready = false;  // K_{j+1} is waited for only once an S product needs it
                 if (!(ok = wait_all(b_kv_full(vs), vph))) break;
-                if (PAGED) {
-                    // Cache slots past seq_len may hold anything, NaN included; P is 0
-                    // there but 0 * NaN is not, so those V rows are zeroed first.
+                {
+                    // Rows past the document's last key (the next document's, the
+                    // next batch entry's, or cache slots past seq_len) may hold
+                    // anything, NaN included; P is 0 there but 0 * NaN is not, so
+                    // the last KV tile's V rows past the end are zeroed first.
                     const int lim = I.Lk - (I.j0 + j) * BN;
                     if (lim < BN) {
                         const uint32_t vb = sKV + vs * C::KV_BYTES;

@@ -476,9 +476,25 @@ __global__ void __launch_bounds__(192, 1)
         ok = wait_all(b_q_full, 0);
         if (ok && n_kv > 0) ok = issue_s(0);
         for (int j = 0; ok && j < n_kv; ++j) {
+            // Real token counts of the tile's two key blocks (a missing second
+            // entry counts 0): V rows past them are padding, whatever they hold.
+            const int ea = list[2 * j], eb = 2 * j + 1 < n ? list[2 * j + 1] : -1;
+            const int za = min((ea >> 2) & 127, kVsaBlock), zb = eb < 0 ? 0 : min((eb >> 2) & 127, kVsaBlock);
             if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
             if (!(ok = wait_all(b_p_full, j & 1))) break;
             if (!(ok = wait_all(b_kv_full(vs), vph))) break;
+            if (za < kVsaBlock || zb < kVsaBlock) {
+                // P is 0 in the padding columns but 0 * NaN is not: zero those V rows.
+                const uint32_t vb = sKV + vs * C::KV_BYTES;
+                const int na = kVsaBlock - za, nz = na + kVsaBlock - zb;
+                for (int idx = lane; idx < nz * NCH * 8; idx += 32) {
+                    const int u = idx & 7, rc = idx >> 3, c = rc % NCH, k = rc / NCH;
+                    const int rr = k < na ? za + k : kVsaBlock + zb + (k - na);
+                    st_shared_v4(vb + c * BN * 128 + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
             tc_fence_after();
             if (leader) {
                 const uint64_t b0 = dV + static_cast<uint64_t>(vs * (C::KV_BYTES >> 4));
@@ -696,11 +712,21 @@ cudaError_t launch_vsa_block_map(const float* pq, const float* pk, const int32_t
     while (qb > 2 && vsa_map_smem_bytes(g.nb, D, qb) < 0) qb >>= 1;
     const int bytes = vsa_map_smem_bytes(g.nb, D, qb);
     if (bytes < 0) return cudaErrorInvalidValue;
+    // Per device, the kernel's dynamic shared-memory limit only ever rises
+    // (to the largest size asked for so far), so a launch made after another
+    // thread's smaller request still finds its own size allowed.
+    static int high[64];
     static std::mutex mu;
     {
-        std::lock_guard<std::mutex> lock(mu);  // the limit only grows; setting it per call is cheap
-        cudaError_t e = cudaFuncSetAttribute(vsa_block_map_sm103a, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64 || bytes > high[dev]) {
+            e = cudaFuncSetAttribute(vsa_block_map_sm103a, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) high[dev] = bytes;
+        }
     }
     VsaMapParams p{pq, pk, sizes, kv_list, kv_num, status, g, group, D, qb, scale};
     dim3 grid((g.nb + qb - 1) / qb, Hq);

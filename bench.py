@@ -255,6 +255,149 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def profile_for(kernel_prefix: str, workload: str):
+    """The committed ncu summary of a kernel on a workload, if there is one."""
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
+        return None
+    for f in sorted(os.listdir(d)):
+        if f.startswith(kernel_prefix) and f.endswith(f"__{workload}.md"):
+            return f"profiles/{f}"
+    return None
+
+
+def time_calls(fn, steps, warmup, flush, stream):
+    """Mean CUDA-event time (ms) of fn() over `steps` calls after `warmup`,
+    L2 flushed before every call (outside the events)."""
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        fn()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def measure_configs(gb, dev, stream, status, flush, steps, warmup, pk, peak_kind):
+    """Every workload of the headline metric, each timed on its own (inputs
+    resident, L2 flushed between calls): prefill TFLOP/s against the measured
+    bf16 burst peak, decode GB/s against the measured HBM copy bandwidth."""
+    peak_tf, peak_bw = float(pk["bf16_tflops"]), float(pk["hbm_gbs"])
+    res = {}
+
+    def prefill_entry(w, fn, launches, kernel):
+        ms = time_calls(fn, steps, warmup, flush, stream)
+        tf = w.flops() / (ms * 1e-3) / 1e12
+        return {"workload": w.name, "ms": ms, "value": tf, "unit": "TFLOP/s", "bound": "tensor", "peak": peak_tf,
+                "frac": tf / peak_tf, "peak_kind": f"{peak_kind} bf16 burst", "flops_per_call": w.flops(),
+                "launches_per_call": launches, "kernel": kernel,
+                "profile": profile_for(kernel.split("<")[0], w.name)}
+
+    def kernel_name(d):
+        return f"fmha2_fwd_sm103a<Prefill2Cfg<{d}>>" if d <= 128 else f"fmha_fwd_sm103a<PrefillCfg<{d}>>"
+
+    # 1: tiny packed documents (parity is checked in the tests; timed here for completeness)
+    w = workloads.tiny_varlen()
+    q, k, v, cq, ck = (x.to(dev) for x in w.make())
+    o = torch.empty(w.Tq, w.Hq, w.D, dtype=torch.float32, device=dev)
+    l = torch.empty(w.Hq, w.Tq, dtype=torch.float32, device=dev)
+    e = prefill_entry(w, lambda: gb.attn_fwd_varlen(q, k, v, cq, ck, max(w.lens_q), max(w.lens_k), w.scale, w.causal,
+                                                    out=o, lse=l, dev_status=status, stream=stream),
+                      gb.attn_fwd_varlen_plan(w.lens_q, w.D, w.causal, w.Hq, w.Hkv, w.lens_k), kernel_name(w.D))
+    e["note"] = "parity-only workload (a few microseconds of work); its fraction says nothing about the kernel"
+    res["1_tiny_varlen"] = e
+
+    # 2, 5a, 5b: dense
+    for key, w in (("2_dit_self", workloads.dit_self()), ("5a_cross", workloads.cross_attn()),
+                   ("5b_d64", workloads.head_sweep(64)), ("5b_d96", workloads.head_sweep(96)),
+                   ("5b_d192", workloads.head_sweep(192)), ("5b_d256", workloads.head_sweep(256))):
+        q, k, v = (x.to(dev) for x in w.make())
+        o = torch.empty(w.B, w.Sq, w.Hq, w.D, dtype=torch.float32, device=dev)
+        l = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
+        launches = gb.attn_fwd_dense_plan(w.B, w.Sq, w.Sk, w.Hq, w.Hkv, w.D, w.causal)[0]
+        res[key] = prefill_entry(w, lambda: gb.attn_fwd_dense(q, k, v, w.scale, w.causal, out=o, lse=l,
+                                                              dev_status=status, stream=stream),
+                                 launches, kernel_name(w.D))
+        del q, k, v, o, l
+
+    # 3: packed causal prefill with GQA
+    w = workloads.varlen_causal_gqa()
+    q, k, v, cq, ck = (x.to(dev) for x in w.make())
+    o = torch.empty(w.Tq, w.Hq, w.D, dtype=torch.float32, device=dev)
+    l = torch.empty(w.Hq, w.Tq, dtype=torch.float32, device=dev)
+    res["3_varlen_causal_gqa"] = prefill_entry(
+        w, lambda: gb.attn_fwd_varlen(q, k, v, cq, ck, max(w.lens_q), max(w.lens_k), w.scale, w.causal, out=o,
+                                      lse=l, dev_status=status, stream=stream),
+        gb.attn_fwd_varlen_plan(w.lens_q, w.D, w.causal, w.Hq, w.Hkv, w.lens_k), kernel_name(w.D))
+    res["3_varlen_causal_gqa"]["doc_lengths"] = list(w.lens_q)
+    del q, k, v, o, l
+
+    # 4: paged decode
+    w = workloads.paged_decode()
+    pq, cache, bt, sl = (x.to(dev) for x in w.make(chunk_rows=256))
+    mx = max(w.seq_lens)
+    ws = torch.empty(gb.attn_fwd_paged_workspace_size(len(w.seq_lens), w.Hq, w.Hkv, w.D, mx), dtype=torch.uint8,
+                     device=dev)
+    o = torch.empty(len(w.seq_lens), w.Hq, w.D, dtype=torch.float32, device=dev)
+    l = torch.empty(len(w.seq_lens), w.Hq, dtype=torch.float32, device=dev)
+    ms = time_calls(lambda: gb.attn_fwd_paged(pq, cache, bt, sl, mx, w.scale, out=o, lse=l, workspace=ws,
+                                              dev_status=status, stream=stream), steps, warmup, flush, stream)
+    nbytes = w.algorithmic_bytes(out_bytes_per_elem=4, with_lse=True)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    res["4_paged_decode"] = {"workload": w.name, "ms": ms, "value": gbs, "unit": "GB/s", "bound": "hbm",
+                             "peak": peak_bw, "frac": gbs / peak_bw, "peak_kind": f"{peak_kind} HBM copy",
+                             "bytes_per_call": nbytes, "launches_per_call": 3,
+                             "kernel": "paged_schedule + paged_decode_sm103a + paged_combine",
+                             "profile": profile_for("paged_decode_sm103a", w.name + "_first16")}
+    del pq, cache, bt, sl, ws, o, l
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} while timing the workloads")
+    return res
+
+
+def sustained_prefill(gb, dev, stream, status, seconds, pk, peak_kind, clock_gpu):
+    """The headline prefill back to back for `seconds` (no flush: a serving
+    loop's steady state), against the measured sustained bf16 peak, with its
+    own clock record."""
+    w = workloads.dit_self()
+    q, k, v = (x.to(dev) for x in w.make())
+    o = torch.empty(w.B, w.Sq, w.Hq, w.D, dtype=torch.float32, device=dev)
+    l = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
+
+    def call():
+        gb.attn_fwd_dense(q, k, v, w.scale, w.causal, out=o, lse=l, dev_status=status, stream=stream)
+
+    for _ in range(20):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    n = max(50, int(seconds / (e0.elapsed_time(e1) * 1e-3)))
+    with ClockSampler(clock_gpu) as clk:
+        e0.record(stream)
+        for _ in range(n):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    tf = w.flops() / (ms * 1e-3) / 1e12
+    peak = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the sustained leg")
+    return {"workload": w.name, "calls": n, "seconds": n * ms * 1e-3, "ms_per_call": ms, "value": tf,
+            "unit": "TFLOP/s", "peak": peak, "frac": tf / peak, "peak_kind": f"{peak_kind} bf16 sustained",
+            "frac_of_burst_peak": tf / float(pk["bf16_tflops"]), "clocks": clk.summary()}
+
+
 def run_ours(args, world, rank, local):
     import attention_forward_09_gb300 as gb
     from attention_forward_09_gb300 import _build
@@ -449,6 +592,12 @@ def run_ours(args, world, rank, local):
                "sequential": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "ms_per_step": e2e_ms},
                "result_matches_device_run": same}
 
+    # ---- every workload of the metric on its own, then the headline prefill sustained
+    configs, sustained = None, None
+    if args.only == "all" and not args.no_configs:
+        configs = measure_configs(gb, dev, stream, status, flush, args.steps, args.warmup, pk, peak_kind)
+        sustained = sustained_prefill(gb, dev, stream, status, args.sustained_s, pk, peak_kind, local)
+
     # ---- oracle on the host cores (rank 0, N=1 only)
     cpu, cpu_dec = None, None
     if world == 1 and not args.no_cpu:
@@ -504,6 +653,8 @@ def run_ours(args, world, rank, local):
                          "traffic": traffic_for(f"paged_decode_sm103a@{wd.name}", "decode.cu")},
             "cpu_baseline": cpu_dec,
         },
+        "configs": configs,
+        "sustained": sustained,
         "cpu_baseline": cpu,
         "e2e": e2e,
         # per step: the prefill launches (full waves, then the split last wave);
@@ -987,6 +1138,10 @@ def main():
     ap.add_argument("--decode-seqs", type=int, default=0,
                     help="use only the first N sequences of the decode workload (profiling captures)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle timing")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing every workload of the metric and the sustained leg (profiling captures)")
+    ap.add_argument("--sustained-s", type=float, default=3.0,
+                    help="seconds of back-to-back headline prefill in the sustained leg")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     world, rank, local = dist_setup(args.gpus)

@@ -77,7 +77,9 @@ typedef enum {
  *   out  device [B, Sq, Hq, D] in out_dtype
  *   lse  device fp32 [B, Hq, Sq] or NULL
  *
- * Batch b attends only its own keys.  Equivalent to attn_fwd_varlen with
+ * Batch b attends only its own keys, and its result depends only on its own
+ * rows of q, k and v (NaN or Inf in another batch entry does not reach it).
+ * Equivalent to attn_fwd_varlen with
  * cu_seqlens_q = arange(0, (B+1)*Sq, Sq) and cu_seqlens_k likewise
  * (FlashAttentionImpl._flash_varlen_wrapper), except for the LSE layout.
  * B, Sq or Sk equal to 0 is allowed (Sk = 0 writes zeros and -inf; k and v
@@ -110,7 +112,8 @@ gbattn_status attn_fwd_dense_plan(int B, int Sq, int Sk, int Hq, int Hkv, int D,
  *
  *   q              device bf16 [Tq, Hq, D]
  *   k, v           device bf16 [Tk, Hkv, D]
- *   cu_seqlens_q/k device int32 [num_docs + 1]: 0 = c[0] <= c[1] <= ... <= c[N] = Tq (Tk)
+ *   cu_seqlens_q/k device int32 [num_docs + 1]: 0 = c[0] <= c[1] <= ... <= c[N] <= Tq (Tk);
+ *                  rows past c[N] belong to no document (never read into a result, never written)
  *   max_seqlen_q/k host ints, >= every document's length (they size the grid;
  *                  no device read happens on the host)
  *   out            device [Tq, Hq, D] in out_dtype
@@ -120,9 +123,10 @@ gbattn_status attn_fwd_dense_plan(int B, int Sq, int Sk, int Hq, int Hkv, int D,
  * [cu_k[n], cu_k[n+1]); no row attends across documents.  Empty documents
  * are allowed (with Tk = 0, k and v may be NULL).  A document longer than max_seqlen, or cu_seqlens that
  * decrease or run past Tq/Tk, set GBATTN_DEV_BAD_SEQLEN and that document's
- * rows are left unwritten.  Keys past a document's end are masked in the
- * scores and multiplied by zero weight, so every bf16 value in k and v must
- * be finite.
+ * rows are left unwritten.  A document's result depends only on its own
+ * rows of q, k and v: the key and value rows past its end (the next
+ * document's, or rows of k and v past cu_seqlens_k[N]) are never mixed in,
+ * whatever they hold, NaN and Inf included.
  */
 gbattn_status attn_fwd_varlen(const void* q, const void* k, const void* v,
                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
@@ -130,6 +134,15 @@ gbattn_status attn_fwd_varlen(const void* q, const void* k, const void* v,
                               int Hq, int Hkv, int D, float softmax_scale, int causal,
                               void* out, gbattn_dtype out_dtype, float* lse,
                               uint32_t* dev_status, void* stream);
+
+/*
+ * attn_fwd_varlen_plan -- how many kernel launches attn_fwd_varlen makes for
+ * these sizes on the current device (launch accounting and tests; it reads
+ * no device memory, launches and allocates nothing, and has no counterpart
+ * on the pages).  Arguments as for attn_fwd_varlen; launches is an output.
+ */
+gbattn_status attn_fwd_varlen_plan(int num_docs, int Tq, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
+                                   int causal, int* launches);
 
 /*
  * attn_fwd_paged_prefill -- several query tokens per sequence against the
@@ -306,7 +319,10 @@ gbattn_status attn_fwd_paged(const void* q, const void* kv_cache, int num_blocks
  *    are refused with GBATTN_ERR_SCRATCH_LIMIT before any CUDA call.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture on the device.
+ *    before any stream capture on the device.  The address is kept for the
+ *    life of the process: after cudaDeviceReset on a device the library's
+ *    device code is loaded anew and the array may move, so do not call this
+ *    entry point on that device again in the same process.
  *  - The call itself allocates nothing and frees nothing.
  *  - Every call on a device shares the same array, and the array keeps the
  *    previous call's contents (nothing in it needs to start at zero).  Calls
@@ -388,8 +404,11 @@ const char* attn_status_string(gbattn_status status);
  *   every key block do not fit in shared memory (nb above about 26000).
  *
  * attn_fwd_vsa -- q_tiled [nbp * 64, Hq, D], k_tiled / v_tiled [nbp * 64,
- *   Hkv, D], device bf16, D = 64 or 128; the padding rows of v_tiled must be
- *   finite (attn_gather_rows writes zeros).  kv_list / kv_num from
+ *   Hkv, D], device bf16, D = 64 or 128; the padding rows of a block (those
+ *   past its token count) are never used, whatever they hold.  The real value
+ *   rows of every key block in a tile's list enter the P.V product of both
+ *   query blocks of the tile (with weight zero for the one that does not
+ *   keep the block), so they must be finite.  kv_list / kv_num from
  *   attn_vsa_block_map with the same nb, num_prefix_blocks, topk and Hq.
  *   Row r of query block b attends the real rows of every key block its
  *   block keeps.  out_index device int32 [nbp * 64]: the out row of each

@@ -33,7 +33,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(
         ["attn_fwd_dense", "attn_fwd_varlen", "attn_fwd_paged", "attn_fwd_paged_workspace_size",
-         "attn_status_string", "attn_fwd_paged_noalloc", "attn_fwd_dense_plan", "attn_kv_cache_write",
+         "attn_status_string", "attn_fwd_paged_noalloc", "attn_fwd_dense_plan", "attn_fwd_varlen_plan",
+         "attn_kv_cache_write",
          "attn_fwd_paged_prefill", "attn_mask_to_varlen", "attn_pack_rows", "attn_unpack_rows",
          "attn_unpack_lse", "attn_vsa_layout", "attn_vsa_tile_map", "attn_gather_rows", "attn_vsa_pool",
          "attn_vsa_list_size", "attn_vsa_block_map", "attn_fwd_vsa"])
@@ -285,3 +286,68 @@ def test_vsa_device_calls_validate_before_touching_a_device(lib):
     assert fwd(k=UNALIGNED) == 3
     assert fwd(nb=200000) == 2           # more than 65535 tiles
     assert fwd(scale=-1.0) == 1
+
+
+# The binding checks every tensor size the C calls of block-sparse video
+# attention derive from their integer arguments, before any device check, so
+# a mismatched tensor is refused on the host (CPU tensors suffice here).
+
+def _vsa_fwd_args(nb=21, npre=3, topk=5, hq=4, hkv=2, d=128):
+    import torch
+
+    rows = (nb + nb % 2) * 64
+    q = torch.zeros(rows, hq, d, dtype=torch.bfloat16)
+    kv = torch.zeros(rows, hkv, d, dtype=torch.bfloat16)
+    kl = torch.zeros(gb.attn_vsa_list_size(nb, npre, topk, hq), dtype=torch.int32)
+    kn = torch.zeros(hq, (nb + 1) // 2, dtype=torch.int32)
+    idx = torch.zeros(rows, dtype=torch.int32)
+    return dict(q_tiled=q, k_tiled=kv, v_tiled=kv.clone(), kv_list=kl, kv_num=kn, num_blocks=nb,
+                num_prefix_blocks=npre, topk=topk, out_index=idx, out_rows=1000)
+
+
+@pytest.mark.parametrize("change,message", [
+    (lambda a: a.update(q_tiled=a["q_tiled"][:-64]), "rows"),
+    (lambda a: a.update(k_tiled=a["k_tiled"][:-1]), "k_tiled and v_tiled"),
+    (lambda a: a.update(v_tiled=a["v_tiled"][..., :64].contiguous()), "k_tiled and v_tiled"),
+    (lambda a: a.update(kv_list=a["kv_list"][:-1]), "kv_list holds"),
+    (lambda a: a.update(kv_list=a["kv_list"].long()), "kv_list must be"),
+    (lambda a: a.update(kv_num=a["kv_num"][:, :-1].contiguous()), "kv_num must be"),
+    (lambda a: a.update(out_index=a["out_index"][:-1]), "out_index"),
+    (lambda a: a.update(out_index=None), "out_rows must equal"),
+    (lambda a: a.update(out=__import__("torch").zeros(999, 4, 128)), "out must be"),
+    (lambda a: a.update(lse=__import__("torch").zeros(4, 999)), "lse must be"),
+])
+def test_vsa_fwd_binding_refuses_mismatched_tensors(lib, change, message):
+    a = _vsa_fwd_args()
+    change(a)
+    with pytest.raises(ValueError, match=message):
+        gb.attn_fwd_vsa(**a)
+
+
+def test_vsa_fwd_binding_shape_check_accepts_matching_tensors(lib):
+    a = _vsa_fwd_args()
+    with pytest.raises(ValueError, match="CUDA"):  # past the size checks, stopped by the device check
+        gb.attn_fwd_vsa(**a)
+
+
+def test_vsa_block_map_binding_refuses_mismatched_tensors(lib):
+    import torch
+
+    pq, pk = torch.zeros(4, 21, 128), torch.zeros(2, 21, 128)
+    sizes = torch.full((21,), 64, dtype=torch.int32)
+    with pytest.raises(ValueError, match="same nb and D"):
+        gb.attn_vsa_block_map(pq, torch.zeros(2, 20, 128), sizes, 3, 5, 0.1)
+    with pytest.raises(ValueError, match="same nb and D"):
+        gb.attn_vsa_block_map(pq, torch.zeros(2, 21, 64), sizes, 3, 5, 0.1)
+    with pytest.raises(ValueError, match="float32"):
+        gb.attn_vsa_block_map(pq.double(), pk, sizes, 3, 5, 0.1)
+    with pytest.raises(ValueError, match="block_sizes"):
+        gb.attn_vsa_block_map(pq, pk, sizes[:-1], 3, 5, 0.1)
+
+
+def test_varlen_plan_validates_before_touching_a_device(lib):
+    n = ctypes.c_int(7)
+    assert lib.attn_fwd_varlen_plan(8, 1000, 200, 200, 32, 8, 80, 1, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.attn_fwd_varlen_plan(8, 1000, 200, 200, 6, 4, 128, 1, ctypes.byref(n)) == INVALID
+    assert lib.attn_fwd_varlen_plan(8, 1000, 200, 200, 32, 8, 128, 1, None) == INVALID
+    assert lib.attn_fwd_varlen_plan(0, 0, 0, 0, 32, 8, 128, 1, ctypes.byref(n)) == OK and n.value == 0

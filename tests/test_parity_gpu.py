@@ -207,6 +207,97 @@ def test_varlen_odd_lengths_and_empty_docs(causal):
     assert_close(out, lse, ro, rl, what=f"varlen causal={causal}")
 
 
+# Packed documents at every head size: both prefill kernels (two query
+# tiles per CTA for D <= 128, one for D = 192 / 256) in their varlen mode,
+# documents with Lq != Lk, an empty document, and lengths on both sides of
+# the 128-row tile and the 256-row item.
+
+VARLEN_EDGE_Q = [127, 128, 0, 129, 255, 257, 1, 300]
+VARLEN_EDGE_K = [128, 127, 5, 129, 300, 255, 1, 257]
+
+
+@pytest.mark.parametrize("D", workloads.HEAD_SIZES)
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_all_head_sizes_at_tile_boundaries(D, causal):
+    (q, k, v, cq, ck, s), out, lse = _varlen_case(VARLEN_EDGE_Q, VARLEN_EDGE_K, 6, 2, D, causal, seed=3 * D + causal)
+    ro, rl = oracle.attention_varlen(q, k, v, cq, ck, s, causal)
+    assert_close(out, lse, ro, rl, what=f"varlen D={D} causal={causal}")
+
+
+@pytest.mark.parametrize("D", [96, 192, 256])
+def test_varlen_bf16_output(D):
+    g = torch.Generator().manual_seed(D)
+    lq, lk = [300, 128, 77], [129, 256, 300]
+    q, k, v = workloads.randn_bf16(g, sum(lq), 4, D), workloads.randn_bf16(g, sum(lk), 4, D), \
+        workloads.randn_bf16(g, sum(lk), 4, D)
+    cq, ck = workloads.cu_from_lengths(lq), workloads.cu_from_lengths(lk)
+    s = 1.0 / math.sqrt(D)
+    st = status_word()
+    out, lse = gb.attn_fwd_varlen(q.to(dev()), k.to(dev()), v.to(dev()), cq.to(dev()), ck.to(dev()), max(lq),
+                                  max(lk), s, True, lse=True, out_dtype=torch.bfloat16, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ro, rl = oracle.attention_varlen(q, k, v, cq, ck, s, True)
+    assert np.all(np.abs(to_np(out) - ro) <= OUT_TOL + bf16_half_ulp(ro))
+    assert max_err(to_np(lse), rl) <= LSE_TOL
+
+
+# No cross-document attention, whatever the neighbours hold: a document's
+# last KV tile reaches into the next document's rows (or past the last
+# document), and those rows are NaN or Inf here.  Every other document must
+# still match the oracle.
+
+@pytest.mark.parametrize("D", workloads.HEAD_SIZES)
+@pytest.mark.parametrize("poison", [float("nan"), float("inf")])
+def test_varlen_poisoned_neighbours_do_not_leak(D, poison):
+    lq, lk = [100, 77, 129, 60], [130, 50, 200, 33]
+    g = torch.Generator().manual_seed(D + 1)
+    extra = 40  # rows of k / v (and q) past the last document
+    q = workloads.randn_bf16(g, sum(lq) + extra, 4, D)
+    k = workloads.randn_bf16(g, sum(lk) + extra, 2, D)
+    v = workloads.randn_bf16(g, sum(lk) + extra, 2, D)
+    cq, ck = workloads.cu_from_lengths(lq), workloads.cu_from_lengths(lk)
+    for t, cu in ((q, cq), (k, ck), (v, ck)):
+        t[int(cu[1]):int(cu[2])] = poison  # document 1
+        t[int(cu[-1]):] = poison           # rows past the last document
+    s = 1.0 / math.sqrt(D)
+    for causal in (False, True):
+        st = status_word()
+        out, lse = gb.attn_fwd_varlen(q.to(dev()), k.to(dev()), v.to(dev()), cq.to(dev()), ck.to(dev()), max(lq),
+                                      max(lk), s, causal, lse=True, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        for n in (0, 2, 3):
+            a, b, c, d = int(cq[n]), int(cq[n + 1]), int(ck[n]), int(ck[n + 1])
+            ro, rl = oracle.attention_single(q[a:b], k[c:d], v[c:d], s, causal)
+            assert_close(out[a:b], lse[:, a:b], ro, rl, what=f"document {n} D={D} causal={causal}")
+
+
+@pytest.mark.parametrize("D,B,Sq,Sk,Hq,Hkv", [
+    (64, 3, 200, 200, 4, 2), (96, 3, 200, 200, 4, 2), (128, 3, 200, 200, 4, 2), (192, 3, 200, 200, 4, 2),
+    (256, 3, 200, 200, 4, 2),
+    (128, 2, 256, 1100, 4, 2),   # the last wave split along the keys over 2-CTA clusters
+    (64, 2, 256, 200, 160, 8),   # a persistent grid of one CTA per SM
+])
+def test_dense_poisoned_batch_entry_does_not_leak(D, B, Sq, Sk, Hq, Hkv):
+    g = torch.Generator().manual_seed(D + B + Sk)
+    q = workloads.randn_bf16(g, B, Sq, Hq, D)
+    k = workloads.randn_bf16(g, B, Sk, Hkv, D)
+    v = workloads.randn_bf16(g, B, Sk, Hkv, D)
+    for t in (q, k, v):
+        t[1] = float("nan")
+    s = 1.0 / math.sqrt(D)
+    st = status_word()
+    out, lse = gb.attn_fwd_dense(q.to(dev()), k.to(dev()), v.to(dev()), s, False, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for b in range(B):
+        if b == 1:
+            continue
+        ro, rl = oracle.attention_single(q[b], k[b], v[b], s, False)
+        assert_close(out[b], lse[b], ro, rl, what=f"batch {b} D={D}")
+
+
 def test_varlen_pack_equals_documents_alone_bit_exact():
     lens = [129, 37, 300]
     (q, k, v, cq, ck, s), out, lse = _varlen_case(lens, lens, 4, 4, 64, True, seed=5)
@@ -804,6 +895,30 @@ def test_vsa_fwd_matches_the_oracle_on_the_oracle_map(prefix, video, hq, hkv, D,
         out, lse = o, l
     tol = OUT_TOL if out_dtype == torch.float32 else OUT_TOL + float(np.max(bf16_half_ulp(ref_o)))
     assert_close(out, lse, ref_o, ref_l, out_tol=tol, what="vsa fwd")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_vsa_fwd_padding_rows_are_never_used(D):
+    """The padding rows of every 64-row block (past its token count) and the
+    odd count's empty partner block hold NaN: the result is unchanged."""
+    prefix, video, hq, hkv, topk = [100, 37], (5, 9, 10), 4, 2, 5
+    q, k, v = _vsa_inputs(65, prefix, video, hq, hkv, D)
+    plan = gb.VsaPlan(prefix, video, dev())
+    blocks, npre = oracle.vsa_blocks(prefix, video)
+    scale = 1.0 / math.sqrt(D)
+    bm = oracle.vsa_block_map(q, k, blocks, npre, topk, scale)
+    ref_o, ref_l = oracle.attention_block_sparse(q, k, v, blocks, bm, scale)
+    kv_list, kv_num = (x.to(dev()) for x in vsa_lists_from_map(bm, [len(b) for b in blocks], npre, topk))
+    pad = (plan.tile_index < 0).to(dev())
+    qt, kt, vt = (gb.attn_gather_rows(x.to(dev()), plan.tile_index) for x in (q, k, v))
+    for t in (qt, kt, vt):
+        t[pad] = float("nan")
+    st = status_word()
+    out, lse = gb.attn_fwd_vsa(qt, kt, vt, kv_list, kv_num, plan.num_blocks, npre, topk, out_index=plan.tile_index,
+                               out_rows=plan.tokens, softmax_scale=scale, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert_close(out, lse, ref_o, ref_l, what="vsa fwd, NaN padding rows")
 
 
 def test_vsa_end_to_end_matches_the_oracle():

@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import attention_forward_09_gb300 as gb
+import oracle
 import workloads
 from _helpers import LSE_TOL, OUT_TOL, max_err, to_np
 
@@ -36,6 +37,7 @@ def _inputs(w):
 def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row(lib):
     w = workloads.Paged("noalloc", [300, 1, 2500, 129, 4096], 16, 4, 128, seed=21)
     q, cache, bt, sl = _inputs(w)
+    ora_out, ora_lse = oracle.attention_paged(*w.make(), w.scale)  # the float64 oracle on the same inputs
     max_len = max(w.seq_lens)
     ref_out, ref_lse = gb.attn_fwd_paged(q, cache, bt, sl, max_len, w.scale, lse=True)
     torch.cuda.synchronize()
@@ -54,6 +56,8 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row(lib):
         assert st == 0 and int(status.item()) == 0
         assert max_err(to_np(out), to_np(ref_out)) <= OUT_TOL
         assert max_err(to_np(lse), to_np(ref_lse)) <= LSE_TOL
+        assert max_err(to_np(out), ora_out) <= OUT_TOL
+        assert max_err(to_np(lse), ora_lse) <= LSE_TOL
 
 
 def test_noalloc_binding_and_size_limit(lib):
@@ -63,6 +67,8 @@ def test_noalloc_binding_and_size_limit(lib):
     b, lb = gb.attn_fwd_paged_noalloc(q, cache, bt, sl, max(w.seq_lens), w.scale, lse=True)
     torch.cuda.synchronize()
     assert max_err(to_np(b), to_np(a)) <= OUT_TOL and max_err(to_np(lb), to_np(la)) <= LSE_TOL
+    ro, rl = oracle.attention_paged(*w.make(), w.scale)
+    assert max_err(to_np(b), ro) <= OUT_TOL and max_err(to_np(lb), rl) <= LSE_TOL
     with pytest.raises(gb.GbattnError) as e:  # more sequences than the scratch can hold partials for
         gb.attn_fwd_paged_noalloc(q[:1].expand(4096, -1, -1).contiguous(), cache, bt[:1].expand(4096, -1).contiguous(),
                                   sl[:1].expand(4096).contiguous(), 131072, w.scale)
