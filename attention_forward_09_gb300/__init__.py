@@ -12,7 +12,8 @@ Entry points (same names as the C ABI):
     attn_fwd_paged(q, kv_cache, block_table, seq_lens, max_seq_len, ...)
     attn_fwd_paged_workspace_size(num_seqs, Hq, Hkv, D, max_seq_len)
     attn_kv_cache_write, attn_fwd_paged_prefill, attn_mask_to_varlen, attn_pack_rows,
-    attn_unpack_rows, attn_unpack_lse, attn_fwd_dense_plan, attn_fwd_varlen_plan, attn_fwd_paged_noalloc
+    attn_unpack_rows, attn_unpack_lse, attn_fwd_dense_plan, attn_fwd_varlen_plan, attn_fwd_paged_noalloc,
+    attn_set_wait_give_up
     attn_vsa_layout, attn_vsa_tile_map, attn_gather_rows, attn_vsa_pool, attn_vsa_list_size,
     attn_vsa_block_map, attn_fwd_vsa
 Compositions of those calls: attn_fwd_masked (padding mask), attn_vsa (block-sparse
@@ -47,6 +48,7 @@ SIGNATURES = {
     "attn_fwd_paged_noalloc": (_I, [_P, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _P]),
     "attn_fwd_dense_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "attn_fwd_varlen_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
+    "attn_set_wait_give_up": (_I, [_I, ctypes.POINTER(ctypes.c_int)]),
     "attn_kv_cache_write": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P]),
     "attn_fwd_paged_prefill": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P,
                                     _P, _P]),
@@ -147,6 +149,15 @@ def attn_fwd_dense_plan(B, Sq, Sk, Hq, Hkv, D, causal=False):
                                             ctypes.byref(sp))
     _check("attn_fwd_dense_plan", st)
     return n.value, sp.value
+
+
+def attn_set_wait_give_up(on) -> bool:
+    """Make the prefill kernels launched from now on give up their pipeline
+    waits at once (a test of the failure path: GBATTN_DEV_TIMEOUT is set,
+    the call returns, outputs are undefined); returns the previous setting."""
+    prev = ctypes.c_int(0)
+    _check("attn_set_wait_give_up", load_library().attn_set_wait_give_up(int(bool(on)), ctypes.byref(prev)))
+    return bool(prev.value)
 
 
 def attn_fwd_varlen_plan(lens_q, D, causal=False, Hq=32, Hkv=8, lens_k=None):

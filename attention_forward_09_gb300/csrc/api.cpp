@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
@@ -116,9 +117,21 @@ gbattn_status run_prefill(const void* q, const void* k, const void* v, long long
     return gbattn::launch_prefill(D, tq, tk, tv, to, p, di.sms, st) == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 
+// 1: the prefill kernels give up every pipeline wait (attn_set_wait_give_up).
+std::atomic<int> g_give_up{0};
+
 }  // namespace
 
+int gbattn::prefill_give_up() { return g_give_up.load(std::memory_order_relaxed); }
+
 extern "C" {
+
+gbattn_status attn_set_wait_give_up(int on, int* previous) {
+    if (on != 0 && on != 1) return GBATTN_ERR_INVALID_ARG;
+    const int old = g_give_up.exchange(on);
+    if (previous) *previous = old;
+    return GBATTN_OK;
+}
 
 const char* attn_status_string(gbattn_status s) {
     switch (s) {
@@ -145,6 +158,7 @@ gbattn_status attn_fwd_dense(const void* q, const void* k, const void* v, int B,
         return GBATTN_ERR_UNSUPPORTED;  // row counts are 32-bit on the device
     if (B == 0 || Sq == 0) return GBATTN_OK;
     PrefillParams p{};
+    p.give_up = gbattn::prefill_give_up();
     p.out = out;
     p.lse = lse;
     p.status = dev_status;
@@ -239,6 +253,7 @@ gbattn_status attn_fwd_varlen(const void* q, const void* k, const void* v, const
     if (num_docs > 65535) return GBATTN_ERR_UNSUPPORTED;
     if (num_docs == 0 || Tq == 0 || max_seqlen_q == 0) return GBATTN_OK;
     PrefillParams p{};
+    p.give_up = gbattn::prefill_give_up();
     p.out = out;
     p.lse = lse;
     p.status = dev_status;
@@ -310,6 +325,7 @@ gbattn_status attn_fwd_paged_prefill(const void* q, const void* kv_cache, int nu
     s = device_info(&di);
     if (s != GBATTN_OK) return s;
     PrefillParams p{};
+    p.give_up = gbattn::prefill_give_up();
     p.out = out;
     p.lse = lse;
     p.status = dev_status;

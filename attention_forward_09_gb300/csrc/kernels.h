@@ -35,7 +35,7 @@ struct PrefillParams {
     // Dense batches on the two-tile kernel use a 1D grid of items
     // (query tile, head, batch), tile fastest; varlen keeps the 3D grid
     // (tile, head, document).  Set by launch_prefill, not by callers.
-    int linear;     // 1: blockIdx.x counts items from item_base
+    int linear;     // 1: blockIdx.x counts items from item_base; 2: persistent walk of packed documents
     int tiles;      // query tiles (2 x 128 rows) per (batch, head)
     int item_base;  // first item of this launch
     int split;      // > 1: each item is shared by a cluster of `split` CTAs, one key range each
@@ -54,7 +54,13 @@ struct PrefillParams {
     // 128 rows are 128 / group tokens x the group's query heads (the Q and
     // out maps then have boxes {64 or 128 B, group, 128 / group}).
     int gqa_pack;
+    // 1: every pipeline wait gives up at once (attn_set_wait_give_up, a test
+    // of the failure path).  Set by the host API.
+    int give_up;
 };
+
+// The give-up setting the host API passes to the prefill kernels (process-wide).
+int prefill_give_up();
 
 // Tensor maps are built by the host (api.cpp) over q [Tq, Hq, D] and
 // k / v [Tk, Hkv, D] (box {64, 1, rows}) and over out [Tq, Hq, D] (box

@@ -23,7 +23,8 @@
 //       warp 5     TMEM allocator and MMA issuer (one elected lane)
 //     S double-buffered in TMEM (S_{j+1} is issued before PV_j, so the tensor
 //     core works on the next scores while the softmax warps exponentiate the
-//     current ones) and P staged in shared memory as bf16.
+//     current ones); P written back over S_j's buffer and read by P.V from
+//     TMEM, as in the two-tile kernel.
 //
 // Both kernels have a paged instantiation (PAGED): K/V tiles come from the
 // paged cache through block_table (vllm-ascend attention_v1.py, chunked
@@ -41,9 +42,10 @@
 // Shared-memory operand layout: every operand is a stack of 64-column
 // chunks, each chunk [rows x 128 B] with the 128-byte swizzle that TMA
 // writes (16-byte piece c of row r at position c ^ (r % 8)).  Q and K are
-// K-major operands; V is the MN-major B operand of P V; P (one-tile kernel)
-// is written by the softmax threads in the same K-major layout as Q.  Output
-// staged for TMA stores uses the same swizzle, 128-byte boxes of columns.
+// K-major operands; V is the MN-major B operand of P V.  P never touches
+// shared memory in either kernel (it goes from the softmax threads to TMEM).
+// Output staged for TMA stores uses the same swizzle, 128-byte boxes of
+// columns.
 #include <math.h>
 #include <algorithm>
 #include <mutex>
@@ -62,9 +64,8 @@ struct PrefillCfg {
     static constexpr int NCH = (D + 63) / 64;           // 64-column chunks per row
     static constexpr int Q_BYTES = NCH * BM * 128;
     static constexpr int KV_BYTES = NCH * BN * 128;     // one K or one V tile
-    static constexpr int P_BYTES = (BN / 64) * BM * 128;
     static constexpr int NUM_BARS = 2 * STAGES + 6;
-    static constexpr int SMEM_BYTES = 1024 + Q_BYTES + STAGES * KV_BYTES + P_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int SMEM_BYTES = 1024 + Q_BYTES + STAGES * KV_BYTES + NUM_BARS * 8 + 16;
     static constexpr int TMEM_S = 0;        // S buffers at columns [0, BN) and [BN, 2BN)
     static constexpr int TMEM_O = 2 * BN;   // O at [2BN, 2BN + D)
     static constexpr int TMEM_COLS = (2 * BN + D) <= 256 ? 256 : 512;
@@ -89,8 +90,7 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem);
     const uint32_t sKV = sQ + C::Q_BYTES;
-    const uint32_t sP = sKV + STAGES * C::KV_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Q_BYTES + STAGES * C::KV_BYTES + C::P_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Q_BYTES + STAGES * C::KV_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const uint32_t b_q_full = smem_u32(&bars[0]);
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(b_p_full, 128);
         mbar_init(b_pv_done, 1);
         mbar_init(b_drain, 1);
-        *abort_flag = 0;
+        *abort_flag = p.give_up ? 1 : 0;  // 1: give up every wait (failure-path test)
         fence_mbar_init();
     }
     if (warp == 5) {
@@ -217,7 +217,6 @@ __global__ void __launch_bounds__(192, 1)
         constexpr uint32_t kIdO = idesc_bf16_f32(BM, D, false, true);
         const bool leader = elect_one();
         const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
-        const uint64_t dP = sdesc_sw128(sP, 16, 1024);
         const uint64_t dK = sdesc_sw128(sKV, 16, 1024);
         const uint64_t dV = sdesc_sw128(sKV, BN * 128, 1024);
         auto wait_all = [&](uint32_t bar, uint32_t ph) {
@@ -252,7 +251,9 @@ __global__ void __launch_bounds__(192, 1)
             adv(ks, kph);
             return true;
         };
-        ok = wait_all(b_q_full, 0);
+        // A launch told to give up (p.give_up) stops here, before any MMA; the
+        // other warps' waits then never complete and run out at once.
+        ok = !*abort_flag && wait_all(b_q_full, 0);
         if (ok && n_kv > 0) ok = issue_s(0);
         for (int j = 0; ok && j < n_kv; ++j) {
             if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
@@ -276,13 +277,13 @@ __global__ void __launch_bounds__(192, 1)
             }
             tc_fence_after();
             if (leader) {
+                // O += P_j V_j, P_j (bf16 pairs) read from the first BN / 2 columns of S_j's buffer
                 const uint64_t b0 = dV + static_cast<uint64_t>(vs * (C::KV_BYTES >> 4));
+                const uint32_t a = tmem + C::TMEM_S + (j & 1) * BN;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint32_t oa = ((kk >> 2) * BM * 128 + (kk & 3) * 32) >> 4;
-                    mma_bf16_ss(tmem + C::TMEM_O, dP + oa, b0 + ((kk * 16 * 128) >> 4), kIdO,
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_bf16_ts(tmem + C::TMEM_O, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdO,
                                 (j > 0 || kk > 0) ? 1u : 0u);
-                }
                 mma_commit(b_pv_done);
                 mma_commit(b_kv_empty(vs));
             }
@@ -334,23 +335,15 @@ __global__ void __launch_bounds__(192, 1)
                 m = m_new;
             }
             l *= alpha;
-            const float msub = (m == -INFINITY) ? 0.f : m;
-            uint32_t pk[BN / 2];
-            const float2 c2x2 = make_float2(c2, c2), negm = make_float2(-msub, -msub);
-            float2 rsp[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                             make_float2(0.f, 0.f)};  // independent partial row sums, in pairs
-#pragma unroll
-            for (int c = 0; c < BN; c += 2) {
-                const float2 t =
-                    __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2x2, negm);
-                const float2 pp = make_float2(ex2(t.x), ex2(t.y));
-                rsp[(c >> 1) & 3] = __fadd2_rn(rsp[(c >> 1) & 3], pp);
-                pk[c >> 1] = pack_bf16x2(pp.x, pp.y);
-            }
-            const float2 rr = __fadd2_rn(__fadd2_rn(rsp[0], rsp[1]), __fadd2_rn(rsp[2], rsp[3]));
-            l += rr.x + rr.y;
-            // PV_{j-1} has to be finished before O is rescaled or P overwritten.
-            if (j > 0) {
+            // O must hold PV_{j-1} before it is rescaled.  S_j was issued after
+            // PV_{j-2} only, so here PV_0 .. PV_{j-2} are complete and PV_j not
+            // yet issued: pv_done has completed j - 1 or j phases, and a wait
+            // on the parity of phase j - 1 is exact whichever it is.  It is
+            // made when O is rescaled, and on the last step, so that after the
+            // loop pv_done is again within one phase of the final wait.  P_j
+            // goes over S_j's own buffer, whose previous P (P_{j-2}) PV_{j-2}
+            // read before S_j was written.
+            if (j > 0 && (warp_need || j + 1 == n_kv)) {
                 if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_pv_done, (j - 1) & 1, abort_flag)))) break;
                 tc_fence_after();
                 if (warp_need) {
@@ -363,18 +356,30 @@ __global__ void __launch_bounds__(192, 1)
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                         tmem_st32(tl + C::TMEM_O + c * 32, o);
                     }
-                    tmem_wait_st();
                 }
             }
+            // P = 2^(S c - m) as bf16 pairs over the first BN / 2 columns of S_j
+            const float msub = (m == -INFINITY) ? 0.f : m;
+            const float2 c2x2 = make_float2(c2, c2), negm = make_float2(-msub, -msub);
+            float2 rsp[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};  // independent partial row sums, in pairs
+            const uint32_t tS = tl + C::TMEM_S + (j & 1) * BN;
 #pragma unroll
-            for (int a = 0; a < BN / 64; ++a) {
-                const uint32_t rowp = sP + a * BM * 128 + r * 128;
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_shared_v4(rowp + ((q ^ (r & 7)) << 4), pk[a * 32 + q * 4 + 0], pk[a * 32 + q * 4 + 1],
-                                 pk[a * 32 + q * 4 + 2], pk[a * 32 + q * 4 + 3]);
+                for (int e = 0; e < 32; e += 2) {
+                    const float2 t = __ffma2_rn(
+                        make_float2(__uint_as_float(sr[c * 32 + e]), __uint_as_float(sr[c * 32 + e + 1])), c2x2, negm);
+                    const float2 pp = make_float2(ex2(t.x), ex2(t.y));
+                    rsp[(e >> 1) & 3] = __fadd2_rn(rsp[(e >> 1) & 3], pp);
+                    pk[e >> 1] = pack_bf16x2(pp.x, pp.y);
+                }
+                tmem_st16(tS + c * 16, pk);
             }
-            fence_proxy_async_smem();
+            const float2 rr = __fadd2_rn(__fadd2_rn(rsp[0], rsp[1]), __fadd2_rn(rsp[2], rsp[3]));
+            l += rr.x + rr.y;
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(b_p_full);
         }
@@ -503,7 +508,7 @@ __global__ void __launch_bounds__(192, 1)
 // to item; Q of the next item is loaded once the current item's last S
 // products are done, its K_0 while the current epilogue runs.
 // Registers: launched at 168 per thread; the third warpgroup gives back
-// down to 72 so each softmax thread can hold a whole 128-column S row (216).
+// down to 88 so each softmax thread can hold a whole 128-column S row (208).
 // TMEM: S_A [0,128) S_B [128,256) O_A [256, 256+D) O_B [256+D, 256+2D).
 // P_X (bf16 pairs) is written back over the first 64 columns of S_X and
 // read from there by the P.V product (tcgen05.mma with A in tensor memory),
@@ -511,6 +516,9 @@ __global__ void __launch_bounds__(192, 1)
 // tcgen05.mma in order, so once S_X(j) is complete PV_X(j-1) is complete
 // too: the softmax warps may then rescale O_X and overwrite P_X without a
 // separate wait.
+// Most documents a persistent varlen launch walks (beyond: one CTA per item).
+constexpr int kWalkMaxDocs = 512;
+
 template <int D_, int STAGES_>
 struct Prefill2Cfg {
     static constexpr int D = D_;
@@ -521,14 +529,16 @@ struct Prefill2Cfg {
     static constexpr int QT_BYTES = NCH * BM * 128;  // one Q tile
     static constexpr int KV_BYTES = NCH * BN * 128;
     static constexpr int NUM_BARS = 2 * STAGES + 10;
-    static constexpr int SMEM_BYTES = 1024 + 2 * QT_BYTES + STAGES * KV_BYTES + NUM_BARS * 8 + 16;
+    // + 16 bytes: TMEM address and abort flag; + 12 x 16: each warp's cursor of the persistent varlen walk
+    static constexpr int SMEM_BYTES = 1024 + 2 * QT_BYTES + STAGES * KV_BYTES + NUM_BARS * 8 + 16 + 12 * 16;
     static constexpr int TMEM_S = 0;          // S_X at X * BN
     static constexpr int TMEM_O = 2 * BN;     // O_X at TMEM_O + X * D
     static constexpr int TMEM_COLS = 512;
     // setmaxnreg split of the 384 x 168 launched registers: softmax warpgroups
-    // / producer + MMA warpgroup (the MMA warp needs more than 56)
-    static constexpr int REG_SOFTMAX = 216;
-    static constexpr int REG_OTHER = 72;
+    // / producer + MMA warpgroup (with the item walk of packed documents the
+    // MMA and producer code needs more than 72; the softmax code fits in 208)
+    static constexpr int REG_SOFTMAX = 208;
+    static constexpr int REG_OTHER = 88;
     static_assert(2 * 128 * REG_SOFTMAX + 128 * REG_OTHER <= 384 * 168, "register split");
     static_assert(2 * BN + 2 * D <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -641,7 +651,7 @@ __device__ __forceinline__ void split_merge(uint8_t* smem, uint32_t sO, uint32_t
     cluster_sync();  // no CTA leaves while another still reads its shared memory
 }
 
-template <class C, bool PAGED>
+template <class C, bool PAGED, bool WALK>
 __global__ void __launch_bounds__(384, 1)
     fmha2_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -684,11 +694,90 @@ __global__ void __launch_bounds__(384, 1)
         int h, doc, kvh, q_start, Lq, k_start, Lk, q0, diag, nA, nB, nmax, j0;
         bool valid;  // false: no such item, or one with nothing to do (CTA-uniform)
     };
-    auto item_at = [&](int i) -> Item {
+    // Persistent varlen walk (linear == 2).  The items are listed tile-major:
+    // level r holds tile t = T - 1 - r (T = tile pairs of the longest
+    // document) of every document that has it, heads fastest, so the heavy
+    // causal tiles come first across all documents.  CTA b takes list
+    // positions k * G + b (k even) and k * G + G - 1 - b (k odd), G CTAs: a
+    // snake over the list that keeps the CTAs' loads within a few percent of
+    // each other.  Each role walks the list with its own cursor (positions
+    // only grow); a document with inconsistent cu_seqlens has no tiles, and
+    // CTA 0 reports it.
+    // A cursor is three ints in shared memory, one per warp, so that it holds
+    // no register in the softmax loop: {level, documents in the level (-1:
+    // not started), list position of the level's first item (the host keeps
+    // the list under 2^31)}.  The lanes in `mask` (every lane of the warp, or
+    // lane 0 alone for the producer) read and write it together, between
+    // __syncwarp(mask), so they always see the same values.
+    struct Walk {
+        volatile int* c;
+        unsigned mask;
+    };
+    auto walk_here = [&](unsigned mask) {
+        Walk W{reinterpret_cast<volatile int*>(tmem_slot + 4) + 4 * (threadIdx.x >> 5), mask};
+        if (WALK) {
+            W.c[1] = -1;
+            __syncwarp(mask);
+        }
+        return W;
+    };
+    const int walk_T = (p.max_seqlen_q + 2 * BM - 1) / (2 * BM);
+    auto doc_tiles = [&](int d, bool report) -> int {
+        const int qs = p.cu_q[d], qe = p.cu_q[d + 1], ks = p.cu_k[d], ke = p.cu_k[d + 1];
+        const bool bad = qs < 0 || qe < qs || qe > p.Tq || qe - qs > p.max_seqlen_q || ks < 0 || ke < ks ||
+                         ke > p.Tk || ke - ks > p.max_seqlen_k;
+        if (bad) {
+            if (report && p.status) atomicOr(p.status, kDevBadSeqlen);
+            return 0;
+        }
+        return (qe - qs + 2 * BM - 1) / (2 * BM);
+    };
+    auto level_docs = [&](int t, bool report) {
+        int n = 0;
+        for (int d = 0; d < p.num_docs; ++d) n += doc_tiles(d, report) > t ? 1 : 0;
+        return n;
+    };
+    auto item_at = [&](int i, Walk& W) -> Item {
         Item I{};
         I.valid = false;
         int tile;
-        if (p.linear) {
+        // (the run-time test of linear keeps the register allocation of the walk
+        // kernel free of spills; linear is always 2 in it)
+        if (WALK && p.linear == 2) {
+            const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+            const long long gl = static_cast<long long>(i) * G + ((i & 1) ? G - 1 - b : b);
+            if (gl > 0x7fffffffLL) return I;
+            const int g = static_cast<int>(gl);
+            __syncwarp(W.mask);
+            int wr = W.c[0], wn = W.c[1], wbase = W.c[2];
+            __syncwarp(W.mask);
+            if (wn < 0) {
+                wr = 0;
+                wbase = 0;
+                wn = walk_T > 0 ? level_docs(walk_T - 1, blockIdx.x == 0 && threadIdx.x == 0) : 0;
+            }
+            bool past = false;
+            while (!past && g - wbase >= wn * p.Hq) {
+                wbase += wn * p.Hq;
+                if (++wr >= walk_T)
+                    past = true;
+                else
+                    wn = level_docs(walk_T - 1 - wr, false);
+            }
+            W.c[0] = wr;
+            W.c[1] = wn;
+            W.c[2] = wbase;
+            __syncwarp(W.mask);
+            if (past) return I;
+            tile = walk_T - 1 - wr;
+            const int k = g - wbase;
+            int rank = k / p.Hq;
+            I.h = k % p.Hq;
+            I.doc = -1;
+            for (int d = 0; d < p.num_docs && I.doc < 0; ++d)
+                if (doc_tiles(d, false) > tile && rank-- == 0) I.doc = d;
+            if (I.doc < 0) return I;
+        } else if (p.linear) {
             long long item;
             if (persist)
                 item = p.item_base + static_cast<long long>(blockIdx.x) + static_cast<long long>(i) * gridDim.x;
@@ -764,8 +853,12 @@ __global__ void __launch_bounds__(384, 1)
         return I;
     };
     // Before any barrier or TMEM use; never taken by a split cluster, and a
-    // persistent CTA always has a first item.
-    if (!item_at(0).valid) return;
+    // persistent CTA always has a first item (but for a varlen walk whose
+    // list is shorter than the grid).
+    {
+        Walk W0 = walk_here(0xffffffffu);  // set again by each role below, after the setup barrier
+        if (!item_at(0, W0).valid) return;
+    }
     if (!split && status_has_timeout(p.status, kDevTimeout)) return;
 
     // ------------------------------------------------------------------ setup
@@ -783,7 +876,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(b_drain, 1);
         mbar_init(b_q_empty, 1);
         mbar_init(b_staged, 2);
-        *abort_flag = 0;
+        *abort_flag = p.give_up ? 1 : 0;  // 1: give up every wait (failure-path test)
         fence_mbar_init();
     }
     if (warp == 9) {
@@ -804,8 +897,9 @@ __global__ void __launch_bounds__(384, 1)
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             int t = 0, nq = 0;  // K/V loads and Q loads issued, over all items
+            Walk W = walk_here(1u);  // lane 0 alone
             for (int i = 0; ok; ++i) {
-                const Item I = item_at(i);
+                const Item I = item_at(i, W);
                 if (!I.valid) break;
                 // Q_A, Q_B of item i replace item i-1's once its S products are done
                 if (i > 0 && !mbar_wait(b_q_empty, (i - 1) & 1, abort_flag)) {
@@ -818,6 +912,13 @@ __global__ void __launch_bounds__(384, 1)
                         tma_load_3d(sQ + x * C::QT_BYTES + c * BM * 128, &tmQ, b_q_full, c * 64, I.h,
                                     I.q_start + I.q0 + x * TPT);
                 ++nq;
+                // An item with no K/V tile still waits for the previous item's
+                // staging here, so that the producer meets every b_staged phase
+                // in order (a wait may never fall two phases behind).
+                if (I.nmax == 0 && i > 0 && persist && !mbar_wait(b_staged, (i - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 for (int tt = 0; tt < 2 * I.nmax; ++tt, ++t) {
                     // The previous item's output may be staged in every K/V stage but
                     // the one K_0 goes to, until its stores have read it.
@@ -906,13 +1007,15 @@ __global__ void __launch_bounds__(384, 1)
         };
         int tbase = 0;             // ring index of the current item's K_0 (K_j: tbase + 2j, V_j: + 1)
         uint32_t pa = 0, pb = 0;   // softmax steps of tiles A and B in earlier items
+        Walk W = walk_here(0xffffffffu);
         for (int i = 0; ok; ++i) {
-            const Item I = item_at(i);
+            const Item I = item_at(i, W);
             if (!I.valid) break;
             const int nA = I.nA, nB = I.nB, nmax = I.nmax;
             int ks = tbase % STAGES, vs = (tbase + 1) % STAGES;
             uint32_t kph = (tbase / STAGES) & 1, vph = ((tbase + 1) / STAGES) & 1;
-            if (!(ok = wait_all(b_q_full, i & 1))) break;
+            // A launch told to give up (p.give_up) stops at its first wait, before any MMA.
+            if (!(ok = (i > 0 || !*abort_flag) && wait_all(b_q_full, i & 1))) break;
             if (nmax > 0) {
                 if ((ok = wait_all(b_kv_full(ks), kph))) {
                     tc_fence_after();
@@ -1005,8 +1108,9 @@ __global__ void __launch_bounds__(384, 1)
         const float c2 = p.scale_log2;
         uint32_t sdone = 0;  // S_X products of earlier items (phase count of s_full and pv_done)
         int tbase = 0;       // ring index of the item's K_0 (as the producer and MMA warps count)
+        Walk W = walk_here(0xffffffffu);
         for (int i = 0; ok; ++i) {
-        const Item I = item_at(i);
+        const Item I = item_at(i, W);
         if (!I.valid) break;
         const int h = I.h, doc = I.doc, q_start = I.q_start, Lq = I.Lq, Lk = I.Lk, q0 = I.q0, diag = I.diag;
         const int nA = I.nA, nB = I.nB, nmax = I.nmax, j0 = I.j0;
@@ -1096,7 +1200,7 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_drain, 0, abort_flag));  // all MMAs done
             tc_fence_after();
             split_merge<D>(smem, sKV, tO, x * BM + r, m, l, n_kv > 0, ok, crank, q0, Lq, q_start, h, doc, p);
-        } else if (qfirst + TPT <= Lq && (x == 1 || nA >= nB)) {
+        } else if (nmax > 0 && qfirst + TPT <= Lq && (x == 1 || nA >= nB)) {
             // A tile wholly inside its document leaves through shared memory:
             // its rows are staged in the TMA 128-byte-swizzled box layout
             // (128 rows x 128 bytes per 16 KB box) in slots of the K/V area
@@ -1240,8 +1344,8 @@ using Cfg192 = PrefillCfg<192, 128, 3>;
 using Cfg256 = PrefillCfg<256, 128, 2>;
 
 // Sets the dynamic shared-memory limit of `kernel` once per device (one flag
-// set per configuration: the kernels of several configurations share a type).
-template <class C, bool PAGED, class K>
+// set per instantiation: the kernels of several configurations share a type).
+template <class C, bool PAGED, bool WALK = false, class K>
 static cudaError_t set_smem_attr(K kernel, int bytes) {
     static bool done[64];
     static std::mutex mu;
@@ -1314,6 +1418,11 @@ static cudaError_t plan_two_tile(K kernel, const PrefillParams& p, int num_sms, 
         pl->n_items = pl->n_full =
             static_cast<long long>((p.max_seqlen_q + 2 * tpt - 1) / (2 * tpt)) * (p.gqa_pack ? p.Hkv : p.Hq) * p.num_docs;
         pl->launches = pl->n_items > 0 ? 1 : 0;
+        // Packed documents whose grid would run more than one wave: one CTA
+        // per SM walks the tile-major item list (the walk rescans cu_seqlens
+        // per level, so very many documents keep the one-CTA-per-item grid).
+        pl->persist = !PAGED && num_sms > 0 && pl->n_items > num_sms && pl->n_items <= 0x7fffffffLL &&
+                      p.num_docs <= kWalkMaxDocs;
         return cudaSuccess;
     }
     cudaError_t e = set_smem_attr<C, PAGED>(kernel, C::SMEM_BYTES);
@@ -1347,6 +1456,15 @@ static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUten
     PrefillParams q = p;
     q.split = 0;
     q.item_base = 0;
+    if (p.cu_q && pl.persist) {  // the walk is its own instantiation (non-paged only)
+        if (PAGED) return cudaErrorInvalidValue;
+        auto walk = fmha2_fwd_sm103a<C, false, true>;
+        if ((e = set_smem_attr<C, false, true>(walk, C::SMEM_BYTES)) != cudaSuccess) return e;
+        q.linear = 2;
+        q.persist = 1;
+        walk<<<static_cast<unsigned>(num_sms), 384, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, q);
+        return cudaGetLastError();
+    }
     if (p.cu_q) {
         q.linear = 0;
         const int tpt = p.gqa_pack ? 128 / p.group : 128;  // tokens per tile
@@ -1390,8 +1508,8 @@ static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUten
 template <class C>
 static cudaError_t two_tile(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             const CUtensorMap& tmO, const PrefillParams& p, int num_sms, cudaStream_t stream) {
-    return p.block_table ? launch_two_tile<C, true>(fmha2_fwd_sm103a<C, true>, tmQ, tmK, tmV, tmO, p, num_sms, stream)
-                         : launch_two_tile<C, false>(fmha2_fwd_sm103a<C, false>, tmQ, tmK, tmV, tmO, p, num_sms,
+    return p.block_table ? launch_two_tile<C, true>(fmha2_fwd_sm103a<C, true, false>, tmQ, tmK, tmV, tmO, p, num_sms, stream)
+                         : launch_two_tile<C, false>(fmha2_fwd_sm103a<C, false, false>, tmQ, tmK, tmV, tmO, p, num_sms,
                                                      stream);
 }
 
@@ -1404,8 +1522,8 @@ static cudaError_t one_tile(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
 
 template <class C>
 static cudaError_t plan_for(const PrefillParams& p, int num_sms, PrefillPlan* pl) {
-    return p.block_table ? plan_two_tile<C, true>(fmha2_fwd_sm103a<C, true>, p, num_sms, pl)
-                         : plan_two_tile<C, false>(fmha2_fwd_sm103a<C, false>, p, num_sms, pl);
+    return p.block_table ? plan_two_tile<C, true>(fmha2_fwd_sm103a<C, true, false>, p, num_sms, pl)
+                         : plan_two_tile<C, false>(fmha2_fwd_sm103a<C, false, false>, p, num_sms, pl);
 }
 
 int prefill_block_n(int D) { return (D == 64 || D == 96 || D == 128 || D == 192 || D == 256) ? 128 : 0; }

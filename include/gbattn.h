@@ -337,6 +337,22 @@ gbattn_status attn_fwd_paged_noalloc(const void* q, const void* kv_cache, int nu
                                      void* out, gbattn_dtype out_dtype, float* lse,
                                      uint32_t* dev_status, void* stream);
 
+/*
+ * attn_set_wait_give_up -- a switch for testing the failure path of the
+ * prefill kernels (attn_fwd_dense, attn_fwd_varlen, attn_fwd_paged_prefill),
+ * process-wide, for the launches made after the call.  on = 1: each CTA
+ * gives up its pipeline waits at once, as if they had run out of time: it
+ * issues no MMA, lets its copies land, frees its tensor memory, sets
+ * GBATTN_DEV_TIMEOUT in dev_status and returns; the call comes back with
+ * GBATTN_OK and the outputs undefined, and the context stays usable.  on = 0
+ * (the default): waits give up only after one second, far above any
+ * legitimate wait.  previous (may be NULL) receives the old setting.  No
+ * counterpart on the pages (whose errors are raised, never rerouted:
+ * fastvideo_vsa.py forward_cuda).  Errors: GBATTN_ERR_INVALID_ARG unless on
+ * is 0 or 1.
+ */
+gbattn_status attn_set_wait_give_up(int on, int* previous);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* attn_status_string(gbattn_status status);
 

@@ -34,6 +34,7 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted(
         ["attn_fwd_dense", "attn_fwd_varlen", "attn_fwd_paged", "attn_fwd_paged_workspace_size",
          "attn_status_string", "attn_fwd_paged_noalloc", "attn_fwd_dense_plan", "attn_fwd_varlen_plan",
+         "attn_set_wait_give_up",
          "attn_kv_cache_write",
          "attn_fwd_paged_prefill", "attn_mask_to_varlen", "attn_pack_rows", "attn_unpack_rows",
          "attn_unpack_lse", "attn_vsa_layout", "attn_vsa_tile_map", "attn_gather_rows", "attn_vsa_pool",
@@ -351,3 +352,11 @@ def test_varlen_plan_validates_before_touching_a_device(lib):
     assert lib.attn_fwd_varlen_plan(8, 1000, 200, 200, 6, 4, 128, 1, ctypes.byref(n)) == INVALID
     assert lib.attn_fwd_varlen_plan(8, 1000, 200, 200, 32, 8, 128, 1, None) == INVALID
     assert lib.attn_fwd_varlen_plan(0, 0, 0, 0, 32, 8, 128, 1, ctypes.byref(n)) == OK and n.value == 0
+
+
+def test_wait_give_up_switch_is_host_only_and_restores(lib):
+    prev = ctypes.c_int(-5)
+    assert lib.attn_set_wait_give_up(2, ctypes.byref(prev)) == INVALID
+    assert lib.attn_set_wait_give_up(1, ctypes.byref(prev)) == OK and prev.value == 0
+    assert gb.attn_set_wait_give_up(False) is True
+    assert gb.attn_set_wait_give_up(False) is False

@@ -298,6 +298,49 @@ def test_dense_poisoned_batch_entry_does_not_leak(D, B, Sq, Sk, Hq, Hkv):
         assert_close(out[b], lse[b], ro, rl, what=f"batch {b} D={D}")
 
 
+# Packed documents whose one-CTA-per-item grid would exceed a wave run on a
+# persistent grid that walks the items tile-major (the heavy causal tiles of
+# every document first).  The lengths include an empty document, a document
+# with no keys (items with nothing to load), Lq > Lk and Lq < Lk documents.
+
+WALK_Q = [300, 1000, 77, 2000, 0, 513, 100, 129, 257]
+WALK_K = [300, 1000, 77, 2000, 9, 513, 0, 260, 128]
+
+
+@pytest.mark.parametrize("D", [64, 96, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_persistent_walk(D, causal):
+    (q, k, v, cq, ck, s), out, lse = _varlen_case(WALK_Q, WALK_K, 32, 8, D, causal, seed=5 * D + causal)
+    ro, rl = oracle.attention_varlen(q, k, v, cq, ck, s, causal)
+    assert_close(out, lse, ro, rl, what=f"persistent varlen D={D} causal={causal}")
+
+
+def test_varlen_persistent_walk_bf16_output_and_repeat():
+    g = torch.Generator().manual_seed(71)
+    q, k, v = (workloads.randn_bf16(g, sum(x), h, 128) for x, h in ((WALK_Q, 16), (WALK_K, 4), (WALK_K, 4)))
+    cq, ck = workloads.cu_from_lengths(WALK_Q).to(dev()), workloads.cu_from_lengths(WALK_K).to(dev())
+    qd, kd, vd = q.to(dev()), k.to(dev()), v.to(dev())
+    st = status_word()
+    outs = [gb.attn_fwd_varlen(qd, kd, vd, cq, ck, max(WALK_Q), max(WALK_K), 0.09, True, lse=True,
+                               out_dtype=torch.bfloat16, dev_status=st) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ro, rl = oracle.attention_varlen(q, k, v, cq.cpu(), ck.cpu(), 0.09, True)
+    assert np.all(np.abs(to_np(outs[0][0]) - ro) <= OUT_TOL + bf16_half_ulp(ro))
+    assert max_err(to_np(outs[0][1]), rl) <= LSE_TOL
+    for o, l in outs[1:]:  # the same bits on every launch
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
+def test_varlen_many_short_documents():
+    """More documents than the persistent walk takes: the one-CTA-per-item grid."""
+    rng = np.random.default_rng(8)
+    lens = [int(x) for x in rng.integers(0, 40, 600)]
+    (q, k, v, cq, ck, s), out, lse = _varlen_case(lens, lens, 4, 2, 64, True, seed=72)
+    ro, rl = oracle.attention_varlen(q, k, v, cq, ck, s, True)
+    assert_close(out, lse, ro, rl, what="600 short documents")
+
+
 def test_varlen_pack_equals_documents_alone_bit_exact():
     lens = [129, 37, 300]
     (q, k, v, cq, ck, s), out, lse = _varlen_case(lens, lens, 4, 4, 64, True, seed=5)
