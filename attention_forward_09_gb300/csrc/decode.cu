@@ -305,7 +305,12 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
 
     for (int g = 0;; ++g) {
         const int slot = g % STAGES, use = g / STAGES;
-        if (!mbar_wait(b_full(slot), use & 1, abort_flag)) {
+        // A warp stops at the first slice whose wait failed, or that it reaches
+        // after another warp gave up (the flag is read even after a wait that
+        // succeeded).  Slots are refilled only after every warp has released
+        // them, so all warps stop at the same slice: the one whose data did
+        // not come.  They then pass the same number of barriers below.
+        if (!mbar_wait(b_full(slot), use & 1, abort_flag) || *abort_flag) {
             ok = false;
             *abort_flag = 1;
         }
@@ -436,7 +441,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
         }
         __syncwarp();
     }
-    if (cur_item >= 0) finish_item();
+    if (cur_item >= 0 && ok) finish_item();  // after a give-up no partial is written (the status reports it)
     if (!ok) {
         *abort_flag = 1;
         if (p.status) atomicOr(p.status, kDevTimeout);

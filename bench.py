@@ -1010,7 +1010,7 @@ def run_vsa(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pk, peak_kind = peaks()
-    w = workloads.vsa_video()
+    w = workloads.vsa_video(args.vsa_frames)
     q, k, v = w.make()
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     plan = gb.VsaPlan(w.prefix, w.video, dev)
@@ -1138,6 +1138,8 @@ def main():
     ap.add_argument("--decode-seqs", type=int, default=0,
                     help="use only the first N sequences of the decode workload (profiling captures)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle timing")
+    ap.add_argument("--vsa-frames", type=int, default=21,
+                    help="frames of the video grid of --only vsa (fewer: a smaller profiling capture)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip timing every workload of the metric and the sustained leg (profiling captures)")
     ap.add_argument("--sustained-s", type=float, default=3.0,

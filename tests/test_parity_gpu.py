@@ -398,6 +398,23 @@ def test_deterministic():
     assert torch.equal(o2, out) and torch.equal(l2, lse)
 
 
+@pytest.mark.parametrize("D,causal", [(192, False), (256, True), (128, True)])
+def test_deterministic_one_tile_and_walk(D, causal):
+    """Repeated launches give the same bits: the one-tile kernel (D = 192,
+    256, P in TMEM, many KV steps) and the persistent varlen walk (D = 128)."""
+    if D == 128:
+        (q, k, v, cq, ck, s), out, lse = _varlen_case(WALK_Q, WALK_K, 16, 4, D, causal, seed=43)
+        args = (q.to(dev()), k.to(dev()), v.to(dev()), cq.to(dev()), ck.to(dev()), max(WALK_Q), max(WALK_K), s,
+                causal)
+        runs = [gb.attn_fwd_varlen(*args, lse=True) for _ in range(4)]
+    else:
+        (q, k, v, s), out, lse = _dense_case(2, 700, 1500, 8, 2, D, causal, seed=42)
+        runs = [gb.attn_fwd_dense(q.to(dev()), k.to(dev()), v.to(dev()), s, causal, lse=True) for _ in range(4)]
+    torch.cuda.synchronize()
+    for o2, l2 in runs:
+        assert torch.equal(o2, out) and torch.equal(l2, lse)
+
+
 def test_constant_values_give_constant_output():
     """Weights sum to one.  The P V product uses P rounded to bf16 while the
     normaliser sums the fp32 weights, so this holds to 2^-8 relative, not

@@ -383,10 +383,11 @@ class Vsa:
         return q, k, v
 
 
-def vsa_video() -> Vsa:
+def vsa_video(frames: int = 21) -> Vsa:
     """A 512-token prefix and a 21 x 45 x 80 video latent grid (76112 tokens,
-    1448 blocks), 40 heads, D=128, the page's default topk of 64 blocks."""
-    return Vsa("vsa_p512_t21h45w80_h40_d128_top64", [512], (21, 45, 80), 40, 40, 128, 64, seed=16)
+    1448 blocks), 40 heads, D=128, the page's default topk of 64 blocks.
+    ``frames`` shortens the grid's T axis (smaller profiling captures)."""
+    return Vsa(f"vsa_p512_t{frames}h45w80_h40_d128_top64", [512], (frames, 45, 80), 40, 40, 128, 64, seed=16)
 
 def _uniform_int(gen: torch.Generator, lo: int, hi: int, n: int) -> list:
     """n integers uniform in [lo, hi] (inclusive)."""
