@@ -305,12 +305,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
 
     for (int g = 0;; ++g) {
         const int slot = g % STAGES, use = g / STAGES;
-        // A warp stops at the first slice whose wait failed, or that it reaches
-        // after another warp gave up (the flag is read even after a wait that
-        // succeeded).  Slots are refilled only after every warp has released
-        // them, so all warps stop at the same slice: the one whose data did
-        // not come.  They then pass the same number of barriers below.
-        if (!mbar_wait(b_full(slot), use & 1, abort_flag) || *abort_flag) {
+        if (!mbar_wait(b_full(slot), use & 1, abort_flag)) {
             ok = false;
             *abort_flag = 1;
         }
@@ -319,6 +314,16 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
         const int item = ok ? sinfo[slot].item : -1;
         if (item < 0) break;
         if (item != cur_item) {
+            // The barriers of the kernel are those of finish_item.  A warp whose
+            // wait succeeded after another warp gave up (data arriving just
+            // after the give-up) reads the abort flag here, before any barrier,
+            // and leaves too: no warp finishes an item another warp abandoned,
+            // and no partial is written after a give-up (the status word
+            // reports it), so every warp passes the same number of barriers.
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+                ok = false;
+                break;
+            }
             if (cur_item >= 0) finish_item();
             cur_item = item;
             cur_s = sinfo[slot].s;
