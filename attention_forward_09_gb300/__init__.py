@@ -13,7 +13,7 @@ Entry points (same names as the C ABI):
     attn_fwd_paged_workspace_size(num_seqs, Hq, Hkv, D, max_seq_len)
     attn_kv_cache_write, attn_fwd_paged_prefill, attn_mask_to_varlen, attn_pack_rows,
     attn_unpack_rows, attn_unpack_lse, attn_fwd_dense_plan, attn_fwd_varlen_plan, attn_fwd_paged_noalloc,
-    attn_set_wait_give_up
+    attn_set_wait_give_up, attn_fwd_padded
     attn_vsa_layout, attn_vsa_tile_map, attn_gather_rows, attn_vsa_pool, attn_vsa_list_size,
     attn_vsa_block_map, attn_fwd_vsa
 Compositions of those calls: attn_fwd_masked (padding mask), attn_vsa (block-sparse
@@ -48,6 +48,7 @@ SIGNATURES = {
     "attn_fwd_paged_noalloc": (_I, [_P, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _P]),
     "attn_fwd_dense_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "attn_fwd_varlen_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
+    "attn_fwd_padded": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P, _P]),
     "attn_set_wait_give_up": (_I, [_I, ctypes.POINTER(ctypes.c_int)]),
     "attn_kv_cache_write": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P]),
     "attn_fwd_paged_prefill": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P,
@@ -139,6 +140,33 @@ def attn_fwd_dense(q, k, v, softmax_scale=None, causal=False, out=None, lse=None
                                        _ptr(out), _out_code(out.dtype), _ptr(lse), _ptr(dev_status),
                                        _stream_handle(stream))
     _check("attn_fwd_dense", st)
+    return out, lse
+
+
+def attn_fwd_padded(q, k, v, lens_q=None, lens_k=None, softmax_scale=None, causal=False, out=None, lse=None,
+                    out_dtype=torch.float32, dev_status=None, stream=None):
+    """Right-padded batch: entry b uses its first lens_q[b] query rows and
+    lens_k[b] keys (int32 CUDA tensors [B], or None for all rows).  q [B, Sq,
+    Hq, D], k/v [B, Sk, Hkv, D].  Returns (out [B, Sq, Hq, D], lse [B, Hq, Sq]
+    or None); padded query rows get zeros and -inf."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _bf16_cuda(n, t)
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Sk, Hkv, D] matching q")
+    for n, t in (("lens_q", lens_q), ("lens_k", lens_k)):
+        if t is not None and (t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous() or t.numel() != B):
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor of {B} entries")
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    if out is None:
+        out = torch.empty(B, Sq, Hq, D, dtype=out_dtype, device=q.device)
+    if lse is True:
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device=q.device)
+    st = load_library().attn_fwd_padded(_ptr(q), _ptr(k), _ptr(v), _ptr(lens_q), _ptr(lens_k), B, Sq, Sk, Hq, Hkv, D,
+                                        scale, int(bool(causal)), _ptr(out), _out_code(out.dtype), _ptr(lse),
+                                        _ptr(dev_status), _stream_handle(stream))
+    _check("attn_fwd_padded", st)
     return out, lse
 
 

@@ -183,6 +183,45 @@ gbattn_status attn_fwd_dense(const void* q, const void* k, const void* v, int B,
                        static_cast<cudaStream_t>(stream));
 }
 
+gbattn_status attn_fwd_padded(const void* q, const void* k, const void* v, const int32_t* lens_q,
+                              const int32_t* lens_k, int B, int Sq, int Sk, int Hq, int Hkv, int D,
+                              float softmax_scale, int causal, void* out, gbattn_dtype out_dtype, float* lse,
+                              uint32_t* dev_status, void* stream) {
+    gbattn_status s = check_common(q, k, v, out, Hq, Hkv, D, softmax_scale, out_dtype, Sk != 0);
+    if (s != GBATTN_OK) return s;
+    if (B < 0 || Sq < 0 || Sk < 0) return GBATTN_ERR_INVALID_ARG;
+    if (B > 65535) return GBATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * Sq > 0x7fffffffLL || static_cast<long long>(B) * Sk > 0x7fffffffLL)
+        return GBATTN_ERR_UNSUPPORTED;  // row counts are 32-bit on the device
+    if (B == 0 || Sq == 0) return GBATTN_OK;
+    PrefillParams p{};
+    p.give_up = gbattn::prefill_give_up();
+    p.out = out;
+    p.lse = lse;
+    p.status = dev_status;
+    p.cu_q = p.cu_k = nullptr;
+    p.lens_q = lens_q;
+    p.lens_k = lens_k;
+    p.num_docs = B;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.Tq = B * Sq;
+    p.Tk = B * Sk;
+    p.max_seqlen_q = Sq;
+    p.max_seqlen_k = Sk;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.group = Hq / Hkv;
+    p.scale_log2 = softmax_scale * kLog2e;
+    p.causal = causal ? 1 : 0;
+    p.out_f32 = out_dtype == GBATTN_OUT_F32;
+    p.lse_bstride = static_cast<long long>(Hq) * Sq;
+    p.lse_hstride = Sq;
+    p.lse_row_global = 0;
+    return run_prefill(q, k, v, static_cast<long long>(B) * Sq, static_cast<long long>(B) * Sk, D, p,
+                       static_cast<cudaStream_t>(stream));
+}
+
 gbattn_status attn_fwd_dense_plan(int B, int Sq, int Sk, int Hq, int Hkv, int D, int causal, int* launches,
                                   int* split) {
     if (!launches || !split) return GBATTN_ERR_INVALID_ARG;

@@ -57,6 +57,10 @@ struct PrefillParams {
     // 1: every pipeline wait gives up at once (attn_set_wait_give_up, a test
     // of the failure path).  Set by the host API.
     int give_up;
+    // Padded batch (dense mode only, attn_fwd_padded): batch entry b uses its
+    // first lens_q[b] query rows and lens_k[b] keys (null: all of them).
+    const int32_t* lens_q;
+    const int32_t* lens_k;
 };
 
 // The give-up setting the host API passes to the prefill kernels (process-wide).

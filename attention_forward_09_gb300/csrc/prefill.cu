@@ -78,6 +78,18 @@ struct PrefillCfg {
 };
 
 constexpr float kLn2 = 0.6931471805599453f;
+
+// Used length of padded batch entry b: lens[b] clamped to [0, full] (a value
+// outside is flagged), or full when lens is null.
+__device__ __forceinline__ int padded_len(const int32_t* lens, int b, int full, uint32_t* status, bool report) {
+    if (!lens) return full;
+    const int n = lens[b];
+    if (n < 0 || n > full) {
+        if (report && status) atomicOr(status, kDevBadSeqlen);
+        return n < 0 ? 0 : full;
+    }
+    return n;
+}
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: tolerate P up to 2^8 before rescaling O
 
 template <class C, bool PAGED>
@@ -139,12 +151,19 @@ __global__ void __launch_bounds__(192, 1)
         k_start = doc * p.Sk;
         Lk = p.Sk;
     }
+    // Padded batch (lens_q / lens_k): entry doc uses its first Lqu query rows
+    // and Lk keys; the rows past Lqu see no key (out 0, lse -inf).
+    int Lqu = Lq;
+    if (!PAGED && !p.cu_q && (p.lens_q || p.lens_k)) {
+        Lqu = padded_len(p.lens_q, doc, Lq, p.status, threadIdx.x == 0);
+        Lk = padded_len(p.lens_k, doc, Lk, p.status, threadIdx.x == 0);
+    }
     const int q0 = tile * BM;
     if (q0 >= Lq) return;  // CTA-uniform, before any barrier or TMEM use
     if (status_has_timeout(p.status, kDevTimeout)) return;
-    const int diag = Lk - Lq;
-    int kend = Lk;
-    if (p.causal) kend = min(Lk, min(q0 + BM - 1, Lq - 1) + diag + 1);
+    const int diag = Lk - Lqu;
+    int kend = q0 < Lqu ? Lk : 0;
+    if (p.causal && q0 < Lqu) kend = min(Lk, min(q0 + BM - 1, Lqu - 1) + diag + 1);
     const int n_kv = kend > 0 ? (kend + BN - 1) / BN : 0;
 
     // ------------------------------------------------------------------ setup
@@ -299,7 +318,8 @@ __global__ void __launch_bounds__(192, 1)
         const int r = threadIdx.x;  // row within the tile == TMEM lane
         const int row = q0 + r;     // row within the document
         const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const int row_lim = p.causal ? min(Lk, row + diag + 1) : Lk;  // keys [0, row_lim) visible
+        // keys [0, row_lim) visible
+        const int row_lim = row >= Lqu ? 0 : (p.causal ? min(Lk, row + diag + 1) : Lk);
         const float c2 = p.scale_log2;
         float m = -INFINITY, l = 0.f;
         for (int j = 0; j < n_kv; ++j) {
@@ -311,7 +331,7 @@ __global__ void __launch_bounds__(192, 1)
                 tmem_ld32(tl + C::TMEM_S + (j & 1) * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
             tmem_wait_ld();
             const int kbase = j * BN;
-            const bool edge = (kbase + BN > Lk) || (p.causal && kbase + BN - 1 > q0 + diag);
+            const bool edge = (kbase + BN > Lk) || (p.causal && kbase + BN - 1 > q0 + diag) || q0 + BM > Lqu;
             if (edge) {
                 const int lim = row_lim - kbase;
 #pragma unroll
@@ -528,7 +548,7 @@ struct Prefill2Cfg {
     static constexpr int NCH = (D + 63) / 64;
     static constexpr int QT_BYTES = NCH * BM * 128;  // one Q tile
     static constexpr int KV_BYTES = NCH * BN * 128;
-    static constexpr int NUM_BARS = 2 * STAGES + 10;
+    static constexpr int NUM_BARS = 2 * STAGES + 11;
     // + 16 bytes: TMEM address and abort flag; + 12 x 16: each warp's cursor of the persistent varlen walk
     static constexpr int SMEM_BYTES = 1024 + 2 * QT_BYTES + STAGES * KV_BYTES + NUM_BARS * 8 + 16 + 12 * 16;
     static constexpr int TMEM_S = 0;          // S_X at X * BN
@@ -672,7 +692,8 @@ __global__ void __launch_bounds__(384, 1)
     auto b_pv_done = [&](int x) { return smem_u32(&bars[5 + 2 * STAGES + x]); };
     const uint32_t b_drain = smem_u32(&bars[7 + 2 * STAGES]);
     const uint32_t b_q_empty = smem_u32(&bars[8 + 2 * STAGES]);  // Q tiles read by every S of an item
-    const uint32_t b_staged = smem_u32(&bars[9 + 2 * STAGES]);   // persistent: both tiles' output staging read
+    // persistent: tile X's output staging has been read by its TMA stores
+    auto b_staged = [&](int x) { return smem_u32(&bars[9 + 2 * STAGES + x]); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -691,7 +712,7 @@ __global__ void __launch_bounds__(384, 1)
     const bool persist = p.persist != 0;
     const int crank = split ? static_cast<int>(cluster_ctarank()) : 0;
     struct Item {
-        int h, doc, kvh, q_start, Lq, k_start, Lk, q0, diag, nA, nB, nmax, j0;
+        int h, doc, kvh, q_start, Lq, Lqu, k_start, Lk, q0, diag, nA, nB, nmax, j0;  // Lqu: used query rows
         bool valid;  // false: no such item, or one with nothing to do (CTA-uniform)
     };
     // Persistent varlen walk (linear == 2).  The items are listed tile-major:
@@ -826,14 +847,23 @@ __global__ void __launch_bounds__(384, 1)
             I.k_start = I.doc * p.Sk;
             I.Lk = p.Sk;
         }
+        // Padded batch (lens_q / lens_k): entry doc uses its first Lqu query
+        // rows and Lk keys; its rows past Lqu see no key (out 0, lse -inf)
+        // and its tiles wholly past Lqu load no K/V.
+        I.Lqu = I.Lq;
+        if (!PAGED && !WALK && !p.cu_q && (p.lens_q || p.lens_k)) {
+            const bool report = threadIdx.x == 0;  // any CTA that meets a bad length flags it
+            I.Lqu = padded_len(p.lens_q, I.doc, I.Lq, p.status, report);
+            I.Lk = padded_len(p.lens_k, I.doc, I.Lk, p.status, report);
+        }
         I.q0 = tile * 2 * TPT;
         if (I.q0 >= I.Lq) return I;
-        I.diag = I.Lk - I.Lq;
-        // KV tiles each query tile needs (0 for a tile with no rows)
+        I.diag = I.Lk - I.Lqu;
+        // KV tiles each query tile needs (0 for a tile with no used rows)
         auto kv_tiles = [&](int first_row) {
-            if (first_row >= I.Lq) return 0;
+            if (first_row >= I.Lqu) return 0;
             int kend = I.Lk;
-            if (p.causal) kend = min(I.Lk, min(first_row + TPT - 1, I.Lq - 1) + I.diag + 1);
+            if (p.causal) kend = min(I.Lk, min(first_row + TPT - 1, I.Lqu - 1) + I.diag + 1);
             return kend > 0 ? (kend + BN - 1) / BN : 0;
         };
         I.nA = kv_tiles(I.q0);
@@ -851,6 +881,13 @@ __global__ void __launch_bounds__(384, 1)
         I.nmax = max(I.nA, I.nB);
         I.valid = true;
         return I;
+    };
+    // Whether tile x of item I leaves through staged TMA stores in the K/V
+    // area in a persistent launch (the softmax warps' epilogue condition):
+    // a full tile, with KV tiles, that finishes last or with the other tile.
+    auto stages_output = [&](const Item& I, int x) -> bool {
+        const int nx = x ? I.nB : I.nA, ny = x ? I.nA : I.nB;
+        return persist && !split && I.nmax > 0 && I.q0 + (x + 1) * TPT <= I.Lq && nx >= ny;
     };
     // Before any barrier or TMEM use; never taken by a split cluster, and a
     // persistent CTA always has a first item (but for a varlen walk whose
@@ -875,7 +912,8 @@ __global__ void __launch_bounds__(384, 1)
         }
         mbar_init(b_drain, 1);
         mbar_init(b_q_empty, 1);
-        mbar_init(b_staged, 2);
+        mbar_init(b_staged(0), 1);
+        mbar_init(b_staged(1), 1);
         *abort_flag = p.give_up ? 1 : 0;  // 1: give up every wait (failure-path test)
         fence_mbar_init();
     }
@@ -897,6 +935,10 @@ __global__ void __launch_bounds__(384, 1)
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             int t = 0, nq = 0;  // K/V loads and Q loads issued, over all items
+            // Tiles whose staged output the next loads must wait for, and the
+            // staging phases of each tile waited so far (persistent launches).
+            bool pend[2] = {false, false};
+            uint32_t staged_waits[2] = {0u, 0u};
             Walk W = walk_here(1u);  // lane 0 alone
             for (int i = 0; ok; ++i) {
                 const Item I = item_at(i, W);
@@ -912,19 +954,19 @@ __global__ void __launch_bounds__(384, 1)
                         tma_load_3d(sQ + x * C::QT_BYTES + c * BM * 128, &tmQ, b_q_full, c * 64, I.h,
                                     I.q_start + I.q0 + x * TPT);
                 ++nq;
-                // An item with no K/V tile still waits for the previous item's
-                // staging here, so that the producer meets every b_staged phase
-                // in order (a wait may never fall two phases behind).
-                if (I.nmax == 0 && i > 0 && persist && !mbar_wait(b_staged, (i - 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
                 for (int tt = 0; tt < 2 * I.nmax; ++tt, ++t) {
-                    // The previous item's output may be staged in every K/V stage but
-                    // the one K_0 goes to, until its stores have read it.
-                    if (tt == 1 && i > 0 && !mbar_wait(b_staged, (i - 1) & 1, abort_flag)) {
-                        ok = false;
-                        break;
+                    // The output of earlier items may be staged in every K/V stage
+                    // but the one K_0 goes to, until its stores have read it.
+                    // Each tile that staged arrives once on its own barrier, so
+                    // these waits meet every phase in order.
+                    if (tt == 1 && (pend[0] || pend[1])) {
+                        for (int x = 0; x < 2 && ok; ++x)
+                            if (pend[x]) {
+                                ok = mbar_wait(b_staged(x), staged_waits[x] & 1, abort_flag);
+                                ++staged_waits[x];
+                                pend[x] = false;
+                            }
+                        if (!ok) break;
                     }
                     const int s = t % STAGES, u = t / STAGES;
                     if (u > 0 && !mbar_wait(b_kv_empty(s), (u - 1) & 1, abort_flag)) {
@@ -945,6 +987,7 @@ __global__ void __launch_bounds__(384, 1)
                     for (int c = 0; c < NCH; ++c)
                         tma_load_3d(sKV + s * C::KV_BYTES + c * BN * 128, m, b_kv_full(s), c * 64, I.kvh, row);
                 }
+                for (int x = 0; x < 2; ++x) pend[x] = pend[x] || stages_output(I, x);
             }
             if (!ok || *abort_flag) {
                 // Let every copy this thread started land before the CTA retires.
@@ -1112,19 +1155,22 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = 0; ok; ++i) {
         const Item I = item_at(i, W);
         if (!I.valid) break;
-        const int h = I.h, doc = I.doc, q_start = I.q_start, Lq = I.Lq, Lk = I.Lk, q0 = I.q0, diag = I.diag;
+        const int h = I.h, doc = I.doc, q_start = I.q_start, Lq = I.Lq, Lqu = I.Lqu, Lk = I.Lk, q0 = I.q0,
+                  diag = I.diag;
         const int nA = I.nA, nB = I.nB, nmax = I.nmax, j0 = I.j0;
         const int row = q0 + x * TPT + r / gq;  // token within the document
         const int hh = h + r % gq;              // query head of this row
         const int n_kv = x ? nB : nA;
         const int qfirst = q0 + x * TPT;
-        const int row_lim = p.causal ? min(Lk, row + diag + 1) : Lk;  // keys [0, row_lim) visible
+        // keys [0, row_lim) visible
+        const int row_lim = row >= Lqu ? 0 : (p.causal ? min(Lk, row + diag + 1) : Lk);
         float m = -INFINITY, l = 0.f;
         for (int j = 0; j < n_kv; ++j) {
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_s_full(x), (sdone + j) & 1, abort_flag)))) break;
             tc_fence_after();
             const int kbase = (j0 + j) * BN;
-            const bool edge = (kbase + BN > Lk) || (p.causal && kbase + BN - 1 > qfirst + diag);
+            const bool edge =
+                (kbase + BN > Lk) || (p.causal && kbase + BN - 1 > qfirst + diag) || qfirst + TPT > Lqu;
             const int lim = row_lim - kbase;  // columns >= lim are masked (edge tiles only)
             uint32_t sr[BN];
 #pragma unroll
@@ -1200,15 +1246,17 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_drain, 0, abort_flag));  // all MMAs done
             tc_fence_after();
             split_merge<D>(smem, sKV, tO, x * BM + r, m, l, n_kv > 0, ok, crank, q0, Lq, q_start, h, doc, p);
-        } else if (nmax > 0 && qfirst + TPT <= Lq && (x == 1 || nA >= nB)) {
+        } else if (nmax > 0 && qfirst + TPT <= Lq && (x == 1 ? nB >= nA : nA >= nB)) {
             // A tile wholly inside its document leaves through shared memory:
             // its rows are staged in the TMA 128-byte-swizzled box layout
             // (128 rows x 128 bytes per 16 KB box) in slots of the K/V area
-            // and written by tiled TMA stores.  Once PV_X(last) is complete
-            // the only MMA that may still read the K/V area is PV_B(last),
-            // when tile A finishes with nA == nB: it reads V_{n-1}, whose
-            // stage no slot uses.  (Tile A with nA < nB, causal, stores
-            // directly instead, while tile B computes on.)
+            // and written by tiled TMA stores.  Only a tile that finishes last
+            // (or with the other) stages: once PV_X(last) is complete the only
+            // MMA that may still read the K/V area is PV_B(last), when tile A
+            // finishes with nA == nB: it reads V_{n-1}, whose stage no slot
+            // uses.  A tile with fewer KV tiles than the other (tile A of a
+            // causal item, or tile B wholly in the padding of a padded batch)
+            // stores directly instead, while the other tile computes on.
             const bool f32 = p.out_f32 != 0;
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             const int boxes = f32 ? D / 32 : (D + 63) / 64, cols = f32 ? 32 : 64;  // 128-byte boxes per row
@@ -1269,7 +1317,7 @@ __global__ void __launch_bounds__(384, 1)
                 for (int b = 0; b < boxes; ++b) tma_store_3d(&tmO, slot_addr(b), b * cols, h, q_start + qfirst);
                 bulk_commit();
                 bulk_wait_read0();  // the staging area must outlive the reads
-                if (persist) mbar_arrive(b_staged);
+                if (persist) mbar_arrive(b_staged(x));
             }
             if (ok && p.lse) {
                 const long long lrow = p.lse_row_global ? (q_start + row) : row;
@@ -1277,7 +1325,6 @@ __global__ void __launch_bounds__(384, 1)
                     l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
             }
         } else {
-        if (persist && r == 0) mbar_arrive(b_staged);  // nothing staged
         const bool row_valid = ok && row < Lq;
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         const long long orow = static_cast<long long>(q_start + row) * p.Hq + hh;

@@ -886,8 +886,11 @@ def run_paged_prefill(args, world, rank, local):
 
 
 def run_masked(args, world, rank, local):
-    """`--only masked`: a padded batch through attn_fwd_masked (mask ->
-    cu_seqlens, pack, varlen attention, unpack), TFLOP/s on the kept tokens."""
+    """`--only masked`: a right-padded batch (each row keeps its first tokens)
+    two ways: attn_fwd_padded, which reads the padded tensors in place with
+    per-row lengths (the headline value), and attn_fwd_masked, the general
+    padding-mask pipeline (mask -> cu_seqlens, pack, varlen attention,
+    unpack), in `general_mask`; TFLOP/s on the kept tokens."""
     import attention_forward_09_gb300 as gb
     from attention_forward_09_gb300 import _build
 
@@ -901,49 +904,67 @@ def run_masked(args, world, rank, local):
     w = workloads.masked_dit()
     q, k, v, mask = w.make()
     qd, kd, vd, md = q.to(dev), k.to(dev), v.to(dev), mask.to(dev)
+    lens = torch.tensor(w.lens, dtype=torch.int32)
+    lensd = lens.to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    outd = torch.empty(w.B, w.S, w.Hq, w.D, dtype=torch.float32, device=dev)
+    lsed = torch.empty(w.B, w.Hq, w.S, dtype=torch.float32, device=dev)
 
-    def run():
+    def run_padded():
+        return gb.attn_fwd_padded(qd, kd, vd, lensd, lensd, w.scale, w.causal, out=outd, lse=lsed,
+                                  dev_status=status, stream=stream)
+
+    def run_general():
         return gb.attn_fwd_masked(qd, kd, vd, md, w.scale, w.causal, lse=True, dev_status=status, stream=stream)
 
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
-        run()
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t_wall = time.perf_counter()
+    def timed(fn):
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            fn()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize()
         for i in range(args.steps):
             flush.fill_(float(i))
             ev[i][0].record(stream)
-            run()
+            fn()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world)
+
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        ms = timed(run_padded)
         t_wall = time.perf_counter() - t_wall
-    barrier(world)
+        ms_general = timed(run_general)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
-    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world)
+    # the two routes give the same result on a right-padded batch
+    o1, l1 = run_padded()
+    o2, l2 = run_general()
+    torch.cuda.synchronize()
+    max_diff = float((o1 - o2).abs().max())
+    same_padding = bool(torch.equal(torch.isinf(l1), torch.isinf(l2)))
     flops = w.flops()
     tf_rank = flops / (ms * 1e-3) / 1e12
     value = sum_over_ranks(flops, world) / (ms * 1e-3) / 1e12
+    tf_general = flops / (ms_general * 1e-3) / 1e12
 
-    hq_, hk_, hv_, hm_ = q.pin_memory(), k.pin_memory(), v.pin_memory(), mask.pin_memory()
-    out0, lse0 = run()
-    hout, hlse = torch.empty(out0.shape).pin_memory(), torch.empty(lse0.shape).pin_memory()
+    hq_, hk_, hv_, hl_ = q.pin_memory(), k.pin_memory(), v.pin_memory(), lens.pin_memory()
+    hout, hlse = torch.empty(outd.shape).pin_memory(), torch.empty(lsed.shape).pin_memory()
     e2e_steps = max(3, min(args.steps, 20))
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     e0.record(stream)
     for _ in range(e2e_steps):
-        for d_, h_ in ((qd, hq_), (kd, hk_), (vd, hv_), (md, hm_)):
+        for d_, h_ in ((qd, hq_), (kd, hk_), (vd, hv_), (lensd, hl_)):
             d_.copy_(h_, non_blocking=True)
-        o, l = run()
+        o, l = run_padded()
         hout.copy_(o, non_blocking=True)
         hlse.copy_(l, non_blocking=True)
     e1.record(stream)
@@ -952,21 +973,27 @@ def run_masked(args, world, rank, local):
     if rank != 0:
         return
     peak_tf = float(pk["bf16_tflops"])
+    launches = gb.attn_fwd_dense_plan(w.B, w.S, w.S, w.Hq, w.Hkv, w.D, w.causal)[0]
     line = {
         "metric": "masked attention TFLOP/s & % bf16 TC peak", "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "seq_len": w.S, "kept": w.lens, "heads": w.Hq, "head_dim": w.D,
-                   "causal": w.causal, "l2": "512 MiB buffer rewritten between steps (flush)",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "kernel": "mask_to_varlen + 3 x pack_rows + fmha2 + unpack_rows + unpack_lse",
-                     "achieved": tf_rank, "peak": peak_tf, "unit": "TFLOP/s", "frac": tf_rank / peak_tf,
-                     "peak_kind": f"{peak_kind} bf16 burst", "flops_per_launch": flops, "traffic": None},
+                   "causal": w.causal, "route": "attn_fwd_padded (per-row lengths, tensors read in place)",
+                   "l2": "512 MiB buffer rewritten between steps (flush)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": f"fmha2_fwd_sm103a<Prefill2Cfg<{w.D}>> (padded batch)",
+                     "launches_per_call": launches, "achieved": tf_rank, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": tf_rank / peak_tf, "peak_kind": f"{peak_kind} bf16 burst", "flops_per_launch": flops,
+                     "traffic": None},
+        "general_mask": {"route": "attn_fwd_masked: mask_to_varlen + 3 x pack_rows + varlen attention + "
+                                  "unpack_rows + unpack_lse", "value": tf_general, "unit": "TFLOP/s",
+                         "ms": ms_general, "frac": tf_general / peak_tf, "launches_per_call": 7,
+                         "max_abs_out_diff_vs_padded": max_diff, "same_padded_rows_as_padded": same_padding},
         "cpu_baseline": None,
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2 + mask.numel(),
+                "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2 + lens.numel() * 4,
                 "d2h_bytes_per_step": hout.numel() * 4 + hlse.numel() * 4},
-        "gpu_launches": 7 * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": t_wall,
     }

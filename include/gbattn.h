@@ -92,6 +92,32 @@ gbattn_status attn_fwd_dense(const void* q, const void* k, const void* v,
                              uint32_t* dev_status, void* stream);
 
 /*
+ * attn_fwd_padded -- a padded batch whose padding mask keeps each row's first
+ * tokens (right padding): the case of FlashAttentionImpl._forward_varlen_masked
+ * (vllm-omni flash_attn.py) where the unpad -> varlen -> pad pipeline of
+ * attn_fwd_masked needs no packing, since each row's kept tokens already lie
+ * together.  Results equal that pipeline's for such a mask.
+ *
+ *   q, k, v, out, lse  as for attn_fwd_dense ([B, Sq, Hq, D], [B, Sk, Hkv, D],
+ *                      [B, Sq, Hq, D], [B, Hq, Sq])
+ *   lens_q   device int32 [B] or NULL: batch entry b's queries are its first
+ *            lens_q[b] rows (NULL: all Sq rows, the key-only mask of
+ *            cross-attention)
+ *   lens_k   device int32 [B] or NULL: its keys are its first lens_k[b] rows
+ *            (NULL: all Sk)
+ *
+ * Query rows past lens_q[b] get out = 0 and lse = -inf; key and value rows
+ * past lens_k[b] never reach a result, whatever they hold.  Causal masking is
+ * bottom-right within the used lengths: query i of entry b sees key j iff
+ * j <= i + lens_k[b] - lens_q[b].  A length outside [0, S] sets
+ * GBATTN_DEV_BAD_SEQLEN and is clamped.  Host errors as for attn_fwd_dense.
+ */
+gbattn_status attn_fwd_padded(const void* q, const void* k, const void* v, const int32_t* lens_q,
+                              const int32_t* lens_k, int B, int Sq, int Sk, int Hq, int Hkv, int D,
+                              float softmax_scale, int causal, void* out, gbattn_dtype out_dtype, float* lse,
+                              uint32_t* dev_status, void* stream);
+
+/*
  * attn_fwd_dense_plan -- how attn_fwd_dense runs these sizes on the current
  * device, for launch accounting and tests; it launches and allocates nothing
  * and has no counterpart on the pages.

@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted(
         ["attn_fwd_dense", "attn_fwd_varlen", "attn_fwd_paged", "attn_fwd_paged_workspace_size",
          "attn_status_string", "attn_fwd_paged_noalloc", "attn_fwd_dense_plan", "attn_fwd_varlen_plan",
-         "attn_set_wait_give_up",
+         "attn_set_wait_give_up", "attn_fwd_padded",
          "attn_kv_cache_write",
          "attn_fwd_paged_prefill", "attn_mask_to_varlen", "attn_pack_rows", "attn_unpack_rows",
          "attn_unpack_lse", "attn_vsa_layout", "attn_vsa_tile_map", "attn_gather_rows", "attn_vsa_pool",
@@ -360,3 +360,21 @@ def test_wait_give_up_switch_is_host_only_and_restores(lib):
     assert lib.attn_set_wait_give_up(1, ctypes.byref(prev)) == OK and prev.value == 0
     assert gb.attn_set_wait_give_up(False) is True
     assert gb.attn_set_wait_give_up(False) is False
+
+
+def test_padded_validation(lib):
+    def padded(**kw):
+        a = dict(q=P, k=P, v=P, lq=None, lk=P, B=2, Sq=8, Sk=8, Hq=4, Hkv=2, D=128, scale=0.1, causal=0, out=P,
+                 odt=1, lse=None)
+        a.update(kw)
+        return lib.attn_fwd_padded(a["q"], a["k"], a["v"], a["lq"], a["lk"], a["B"], a["Sq"], a["Sk"], a["Hq"],
+                                   a["Hkv"], a["D"], a["scale"], a["causal"], a["out"], a["odt"], a["lse"], None,
+                                   None)
+    assert padded(D=80) == UNSUPPORTED
+    assert padded(Hq=6, Hkv=4) == INVALID
+    assert padded(q=None) == INVALID
+    assert padded(scale=0.0) == INVALID
+    assert padded(v=UNALIGNED) == ALIGN
+    assert padded(B=-1) == INVALID
+    assert padded(B=70000) == UNSUPPORTED
+    assert padded(B=0) == OK  # nothing to compute, no device touched

@@ -816,6 +816,106 @@ def test_masked_matches_oracle(kind, causal, D, hq, hkv, S):
     assert_close(out, lse, ro, rl, what=f"masked {kind}")
 
 
+# Right-padded batches through attn_fwd_padded: the same results as the
+# unpad -> varlen -> pad pipeline (the oracle's attention_masked) for a mask
+# that keeps each row's first tokens, with NaN in every padded row (it must
+# never reach a result).
+
+PAD_LENS = [[300, 129, 0, 1], [257, 256, 255, 128], [127, 300, 13, 200]]
+
+
+def _prefix_mask(lens, S):
+    mask = torch.zeros(len(lens), S, dtype=torch.uint8)
+    for i, n in enumerate(lens):
+        mask[i, :n] = 1
+    return mask
+
+
+@pytest.mark.parametrize("D", workloads.HEAD_SIZES)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("kind", ["self", "cross"])
+def test_padded_matches_the_masked_oracle(D, causal, kind):
+    S = 300
+    lens = PAD_LENS[(D // 32 + causal) % 3]
+    B, Sq = len(lens), (200 if kind == "cross" else S)
+    g = torch.Generator().manual_seed(D + 3 * causal + (kind == "cross"))
+    q = workloads.randn_bf16(g, B, Sq, 4, D)
+    k = workloads.randn_bf16(g, B, S, 2, D)
+    v = workloads.randn_bf16(g, B, S, 2, D)
+    mask = _prefix_mask(lens, S)
+    ro, rl = oracle.attention_masked(q, k, v, mask, 1.0 / math.sqrt(D), causal, cross=(kind == "cross"))
+    for i, n in enumerate(lens):  # padding rows hold NaN: never read into a result
+        k[i, n:] = float("nan")
+        v[i, n:] = float("nan")
+        if kind == "self":
+            q[i, n:] = float("nan")
+    L = torch.tensor(lens, dtype=torch.int32, device=dev())
+    st = status_word()
+    out, lse = gb.attn_fwd_padded(q.to(dev()), k.to(dev()), v.to(dev()), L if kind == "self" else None, L,
+                                  1.0 / math.sqrt(D), causal, lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert_close(out, lse, ro, rl, what=f"padded {kind} D={D} causal={causal}")
+
+
+@pytest.mark.parametrize("D,Sk", [(128, 1100), (64, 300)])
+def test_padded_split_and_persistent_paths(D, Sk):
+    """Many heads (a persistent grid) and a partly filled last wave (its
+    items split along the keys over a cluster): rows padded at every place."""
+    g = torch.Generator().manual_seed(D + Sk)
+    B, S, H = 2, 512, 160 if D == 64 else 4
+    lens_q, lens_k = [512, 300], [Sk, 700 if Sk > 700 else 150]
+    q = workloads.randn_bf16(g, B, S, H, D)
+    k = workloads.randn_bf16(g, B, Sk, H // 4, D)
+    v = workloads.randn_bf16(g, B, Sk, H // 4, D)
+    s = 1.0 / math.sqrt(D)
+    st = status_word()
+    out, lse = gb.attn_fwd_padded(q.to(dev()), k.to(dev()), v.to(dev()),
+                                  torch.tensor(lens_q, dtype=torch.int32, device=dev()),
+                                  torch.tensor(lens_k, dtype=torch.int32, device=dev()), s, False, lse=True,
+                                  dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for b in range(B):
+        ro, rl = oracle.attention_single(q[b, :lens_q[b]], k[b, :lens_k[b]], v[b, :lens_k[b]], s, False)
+        assert_close(out[b, :lens_q[b]], lse[b][:, :lens_q[b]], ro, rl, what=f"padded batch {b}")
+        assert torch.all(out[b, lens_q[b]:] == 0) and torch.all(lse[b][:, lens_q[b]:] == -math.inf)
+
+
+@pytest.mark.parametrize("lens_q,lens_k", [([0, 512, 100], [512, 512, 0]), ([512, 0, 257], [200, 512, 300])])
+def test_padded_persistent_runs_of_empty_items(lens_q, lens_k):
+    """A persistent grid (160 heads) over batch entries that are wholly or
+    partly padding: long runs of items that stage nothing between items that
+    do, and items whose second tile lies in the padding."""
+    g = torch.Generator().manual_seed(sum(lens_q))
+    B, S, H, D = 3, 512, 160, 64
+    q = workloads.randn_bf16(g, B, S, H, D)
+    k = workloads.randn_bf16(g, B, S, H // 8, D)
+    v = workloads.randn_bf16(g, B, S, H // 8, D)
+    s = 1.0 / math.sqrt(D)
+    for causal in (False, True):
+        st = status_word()
+        out, lse = gb.attn_fwd_padded(q.to(dev()), k.to(dev()), v.to(dev()),
+                                      torch.tensor(lens_q, dtype=torch.int32, device=dev()),
+                                      torch.tensor(lens_k, dtype=torch.int32, device=dev()), s, causal, lse=True,
+                                      dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        for b in range(B):
+            ro, rl = oracle.attention_single(q[b, :lens_q[b]], k[b, :lens_k[b]], v[b, :lens_k[b]], s, causal)
+            assert_close(out[b, :lens_q[b]], lse[b][:, :lens_q[b]], ro, rl, what=f"entry {b} causal={causal}")
+            assert torch.all(out[b, lens_q[b]:] == 0) and torch.all(lse[b][:, lens_q[b]:] == -math.inf)
+
+
+def test_padded_bad_length_sets_status():
+    q = _gen(1, 2, 64, 2, 64).to(dev())
+    st = status_word()
+    gb.attn_fwd_padded(q, q, q, torch.tensor([64, 70], dtype=torch.int32, device=dev()), None, 0.1, False,
+                       dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & gb.DEV_BAD_SEQLEN
+
+
 def test_masked_bf16_output():
     g = torch.Generator().manual_seed(10)
     q, k, v = (workloads.randn_bf16(g, 2, 256, 2, 128) for _ in range(3))
