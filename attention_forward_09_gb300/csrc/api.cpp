@@ -111,7 +111,8 @@ gbattn_status run_prefill(const void* q, const void* k, const void* v, long long
     const bool no_keys = Tk == 0;
     if (!encode_rows_heads_d(&tq, q, Tq, p.Hq, D, 128) ||
         !encode_rows_heads_d(&tk, no_keys ? q : k, no_keys ? Tq : Tk, no_keys ? p.Hq : p.Hkv, D, bn) ||
-        !encode_rows_heads_d(&tv, no_keys ? q : v, no_keys ? Tq : Tk, no_keys ? p.Hq : p.Hkv, D, bn) ||
+        !encode_rows_heads_d(&tv, no_keys ? q : v, no_keys ? Tq : Tk, no_keys ? p.Hq : p.Hkv, D,
+                             gbattn::prefill_v_box_rows(D)) ||
         !encode_rows_heads_d(&to, p.out, Tq, p.Hq, D, 128, p.out_f32 != 0))
         return GBATTN_ERR_CUDA;
     return gbattn::launch_prefill(D, tq, tk, tv, to, p, di.sms, st) == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
@@ -394,13 +395,14 @@ gbattn_status attn_fwd_paged_prefill(const void* q, const void* kv_cache, int nu
     const int g = Hq / Hkv;
     p.gqa_pack = (D <= 128 && g >= 2 && 128 % g == 0) ? 1 : 0;
     const int box_heads = p.gqa_pack ? g : 1, box_rows = 128 / box_heads;
-    CUtensorMap tq, tkv, to;
+    CUtensorMap tq, tk, tv, to;
     const long long cache_rows = 2LL * num_blocks * 128;
     if (!encode_rows_heads_d(&tq, q, Tq, Hq, D, box_rows, false, box_heads) ||
-        !encode_rows_heads_d(&tkv, kv_cache, cache_rows, Hkv, D, 128) ||
+        !encode_rows_heads_d(&tk, kv_cache, cache_rows, Hkv, D, 128) ||
+        !encode_rows_heads_d(&tv, kv_cache, cache_rows, Hkv, D, gbattn::prefill_v_box_rows(D)) ||
         !encode_rows_heads_d(&to, out, Tq, Hq, D, box_rows, p.out_f32 != 0, box_heads))
         return GBATTN_ERR_CUDA;
-    return gbattn::launch_prefill(D, tq, tkv, tkv, to, p, di.sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+    return gbattn::launch_prefill(D, tq, tk, tv, to, p, di.sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? GBATTN_OK
                : GBATTN_ERR_CUDA;
 }

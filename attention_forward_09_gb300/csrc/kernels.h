@@ -71,7 +71,8 @@ int prefill_give_up();
 // {128 bytes of columns, 1, 128}), all with 128-byte swizzle.
 cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            const CUtensorMap& tmO, const PrefillParams& p, int num_sms, cudaStream_t stream);
-int prefill_block_n(int D);  // keys per KV tile for head size D
+int prefill_block_n(int D);    // keys per KV tile for head size D
+int prefill_v_box_rows(int D); // rows of the V map's TMA box for head size D
 
 // How launch_prefill runs these sizes: kernel launches, items (CTAs of work),
 // items launched whole, and the key split of the rest (0: none).

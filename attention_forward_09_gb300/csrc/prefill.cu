@@ -19,12 +19,24 @@
 //   fmha_fwd_sm103a (D = 192, 256): one tile per CTA (two O accumulators of
 //     that width do not fit in TMEM next to the S buffers), 192 threads:
 //       warps 0-3  softmax + O correction + epilogue; warp w owns TMEM lanes 32w..32w+31
-//       warp 4     TMA producer: Q once, then K_0 V_0 K_1 V_1 ... into a ring of slots
+//       warp 4     TMA producer: Q once, then K and V in the order the MMAs
+//                  read them (K_0, K_1 V_0, K_2 V_1, ...) into a ring of 16 KB
+//                  slots: a K tile is D / 64 slots of 64 columns x 128 keys, a
+//                  V tile the same at D = 192 and 4 slots of 32 keys x 256
+//                  columns at D = 256
 //       warp 5     TMEM allocator and MMA issuer (one elected lane)
 //     S double-buffered in TMEM (S_{j+1} is issued before PV_j, so the tensor
 //     core works on the next scores while the softmax warps exponentiate the
 //     current ones); P written back over S_j's buffer and read by P.V from
-//     TMEM, as in the two-tile kernel.
+//     TMEM, as in the two-tile kernel.  The MMAs of each slot release it as
+//     they complete, so the ring refills a slot at a time, several slots
+//     ahead of the MMAs.  K is cut along D (each slot feeds a full-width
+//     N = 128 score product).  P.V runs as N = D products: at D = 256 V is
+//     cut along the keys, each slot a whole product; at D = 192 a V tile's
+//     three column slots are read by one product when they lie in
+//     consecutive slots, and as three N = 64 products when the tile wraps
+//     around the ring (32-key V slots would leave a quarter of each slot
+//     empty at D = 192).
 //
 // Both kernels have a paged instantiation (PAGED): K/V tiles come from the
 // paged cache through block_table (vllm-ascend attention_v1.py, chunked
@@ -55,24 +67,31 @@
 
 namespace gbattn {
 
-template <int D_, int BN_, int STAGES_>
+template <int D_, int BN_, int SLOTS_>
 struct PrefillCfg {
     static constexpr int D = D_;
     static constexpr int BN = BN_;
-    static constexpr int STAGES = STAGES_;
+    static constexpr int SLOTS = SLOTS_;                // K/V ring slots, one 64-column chunk each
     static constexpr int BM = 128;
     static constexpr int NCH = (D + 63) / 64;           // 64-column chunks per row
     static constexpr int Q_BYTES = NCH * BM * 128;
-    static constexpr int KV_BYTES = NCH * BN * 128;     // one K or one V tile
-    static constexpr int NUM_BARS = 2 * STAGES + 6;
-    static constexpr int SMEM_BYTES = 1024 + Q_BYTES + STAGES * KV_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int SLOT_BYTES = BN * 128;         // 64 columns of a K tile
+    // V cut along the keys (VR keys x D per slot) when that fills a slot, else
+    // into 64-column chunks like K
+    static constexpr bool VKEYS = 32 * D * 2 == BN * 128;
+    static constexpr int VR = VKEYS ? 32 : BN;          // keys of a V tile per slot
+    static constexpr int V_SLOTS = VKEYS ? BN / VR : NCH;
+    static constexpr int V_SLOT_BYTES = VR * (VKEYS ? D : 64) * 2;
+    static constexpr int NUM_BARS = 2 * SLOTS + 6;
+    static constexpr int SMEM_BYTES = 1024 + Q_BYTES + SLOTS * SLOT_BYTES + NUM_BARS * 8 + 16;
     static constexpr int TMEM_S = 0;        // S buffers at columns [0, BN) and [BN, 2BN)
     static constexpr int TMEM_O = 2 * BN;   // O at [2BN, 2BN + D)
     static constexpr int TMEM_COLS = (2 * BN + D) <= 256 ? 256 : 512;
     static_assert(2 * BN + D <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(D % 32 == 0 && BN % 64 == 0, "tile shape");
-    static_assert(D % 64 == 0 && (D / 32) * BM * 128 <= STAGES * KV_BYTES, "output staging in the K/V area");
+    static_assert(D % 64 == 0 && BM == BN && (D / 32) * BM * 128 <= SLOTS * SLOT_BYTES, "output staging in the ring");
+    static_assert(V_SLOT_BYTES == SLOT_BYTES && VR % 16 == 0 && BN % VR == 0 && NCH <= SLOTS, "V slots");
     // TMA-store epilogue for full tiles: measured +1.5% at D = 192, -0.8% at D = 256
     static constexpr bool TMA_OUT = D < 256;
 };
@@ -97,21 +116,21 @@ __global__ void __launch_bounds__(192, 1)
     fmha_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     const PrefillParams p) {
-    constexpr int D = C::D, BN = C::BN, STAGES = C::STAGES, BM = C::BM, NCH = C::NCH;
+    constexpr int D = C::D, BN = C::BN, SLOTS = C::SLOTS, BM = C::BM, NCH = C::NCH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem);
     const uint32_t sKV = sQ + C::Q_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Q_BYTES + STAGES * C::KV_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Q_BYTES + SLOTS * C::SLOT_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const uint32_t b_q_full = smem_u32(&bars[0]);
     auto b_kv_full = [&](int s) { return smem_u32(&bars[1 + s]); };
-    auto b_kv_empty = [&](int s) { return smem_u32(&bars[1 + STAGES + s]); };
-    auto b_s_full = [&](int b) { return smem_u32(&bars[1 + 2 * STAGES + b]); };
-    const uint32_t b_p_full = smem_u32(&bars[3 + 2 * STAGES]);
-    const uint32_t b_pv_done = smem_u32(&bars[4 + 2 * STAGES]);
-    const uint32_t b_drain = smem_u32(&bars[5 + 2 * STAGES]);
+    auto b_kv_empty = [&](int s) { return smem_u32(&bars[1 + SLOTS + s]); };
+    auto b_s_full = [&](int b) { return smem_u32(&bars[1 + 2 * SLOTS + b]); };
+    const uint32_t b_p_full = smem_u32(&bars[3 + 2 * SLOTS]);
+    const uint32_t b_pv_done = smem_u32(&bars[4 + 2 * SLOTS]);
+    const uint32_t b_drain = smem_u32(&bars[5 + 2 * SLOTS]);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -169,7 +188,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
         mbar_init(b_q_full, 1);
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < SLOTS; ++s) {
             mbar_init(b_kv_full(s), 1);
             mbar_init(b_kv_empty(s), 1);
         }
@@ -199,33 +218,45 @@ __global__ void __launch_bounds__(192, 1)
             tma_prefetch_desc(&tmV);
             mbar_arrive_expect_tx(b_q_full, C::Q_BYTES);
             for (int c = 0; c < NCH; ++c) tma_load_3d(sQ + c * BM * 128, &tmQ, b_q_full, c * 64, h, q_start + q0);
+            // Load t of the MMAs' order: K_0, then K_{j+1} and V_j for each j,
+            // V_{n-1} last.  Chunk g of the sequence goes to slot g % SLOTS.
             int issued = 0;
-            for (int t = 0; t < 2 * n_kv; ++t) {
-                const int s = t % STAGES, u = t / STAGES;
-                if (u > 0 && !mbar_wait(b_kv_empty(s), (u - 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const CUtensorMap* m = (t & 1) ? &tmV : &tmK;
-                int row = k_start + (t >> 1) * BN;
-                if (PAGED) {  // cache block of KV tile j; a bad entry is flagged, block 0 read
-                    int blk = p.block_table[static_cast<long long>(doc) * p.max_blocks + (t >> 1)];
+            for (int t = 0; ok && t < 2 * n_kv; ++t) {
+                const bool isv = t == 2 * n_kv - 1 || (t > 0 && (t & 1) == 0);
+                const int jt = isv ? (t == 2 * n_kv - 1 ? n_kv - 1 : t / 2 - 1) : (t + 1) / 2;
+                const CUtensorMap* m = isv ? &tmV : &tmK;
+                int row = k_start + jt * BN;
+                if (PAGED) {  // cache block of KV tile jt; a bad entry is flagged, block 0 read
+                    int blk = p.block_table[static_cast<long long>(doc) * p.max_blocks + jt];
                     if (blk < 0 || blk >= p.num_blocks) {
                         if (p.status) atomicOr(p.status, kDevBadIndex);
                         blk = 0;
                     }
-                    row = ((t & 1) ? p.num_blocks + blk : blk) * BN;
+                    row = (isv ? p.num_blocks + blk : blk) * BN;
                 }
-                mbar_arrive_expect_tx(b_kv_full(s), C::KV_BYTES);
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_3d(sKV + s * C::KV_BYTES + c * BN * 128, m, b_kv_full(s), c * 64, kvh, row);
-                ++issued;
+                for (int q = 0; q < (isv ? C::V_SLOTS : NCH); ++q) {
+                    const int s = issued % SLOTS, u = issued / SLOTS;
+                    if (u > 0 && !mbar_wait(b_kv_empty(s), (u - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = sKV + s * C::SLOT_BYTES;
+                    if (isv && C::VKEYS) {  // keys [q VR, q VR + VR): NCH blocks of 64 columns (V map box: VR rows)
+                        mbar_arrive_expect_tx(b_kv_full(s), C::V_SLOT_BYTES);
+                        for (int c = 0; c < NCH; ++c)
+                            tma_load_3d(dst + c * (C::VR * 128), m, b_kv_full(s), c * 64, kvh, row + q * C::VR);
+                    } else {    // columns [64 q, 64 q + 64) of all BN keys
+                        mbar_arrive_expect_tx(b_kv_full(s), C::SLOT_BYTES);
+                        tma_load_3d(dst, m, b_kv_full(s), q * 64, kvh, row);
+                    }
+                    ++issued;
+                }
             }
             if (!ok || *abort_flag) {
                 // Let every copy this thread started land before the CTA retires.
                 mbar_wait_drain(b_q_full, 0);
-                for (int t = (issued > STAGES ? issued - STAGES : 0); t < issued; ++t)
-                    mbar_wait_drain(b_kv_full(t % STAGES), (t / STAGES) & 1);
+                for (int g = (issued > SLOTS ? issued - SLOTS : 0); g < issued; ++g)
+                    mbar_wait_drain(b_kv_full(g % SLOTS), (g / SLOTS) & 1);
             }
         }
     } else if (warp == 5) {
@@ -237,37 +268,41 @@ __global__ void __launch_bounds__(192, 1)
         const bool leader = elect_one();
         const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
         const uint64_t dK = sdesc_sw128(sKV, 16, 1024);
-        const uint64_t dV = sdesc_sw128(sKV, BN * 128, 1024);
+        // V operand: VR-key blocks of 64 columns (VKEYS), or the tile's column
+        // chunks in consecutive slots
+        const uint64_t dV = sdesc_sw128(sKV, C::VKEYS ? C::VR * 128 : C::SLOT_BYTES, 1024);
+        constexpr uint32_t kIdO64 = idesc_bf16_f32(BM, 64, false, true);
         auto wait_all = [&](uint32_t bar, uint32_t ph) {
             return __all_sync(0xffffffffu, mbar_wait(bar, ph, abort_flag));
         };
-        // K_j is load 2j of the ring, V_j load 2j + 1 (STAGES >= 2)
-        int ks = 0, vs = 1;
-        uint32_t kph = 0, vph = 0;
-        auto adv = [](int& s, uint32_t& ph) {
-            s += 2;
-            if (s >= STAGES) {
-                s -= STAGES;
-                ph ^= 1u;
+        // Slots are read in the producer's order; cs / cph: the next one's slot and phase.
+        int cs = 0;
+        uint32_t cph = 0;
+        auto next_slot = [&]() {
+            if (++cs == SLOTS) {
+                cs = 0;
+                cph ^= 1u;
             }
         };
         auto issue_s = [&](int j) -> bool {
-            if (!wait_all(b_kv_full(ks), kph)) return false;
-            tc_fence_after();
-            if (leader) {
-                const uint32_t dS = tmem + C::TMEM_S + (j & 1) * BN;
-                const uint64_t b0 = dK + static_cast<uint64_t>(ks * (C::KV_BYTES >> 4));
+            const uint32_t dS = tmem + C::TMEM_S + (j & 1) * BN;
+#pragma unroll 1
+            for (int c = 0; c < NCH; ++c) {
+                if (!wait_all(b_kv_full(cs), cph)) return false;
+                tc_fence_after();
+                if (leader) {
+                    const uint64_t b0 = dK + static_cast<uint64_t>(cs * (C::SLOT_BYTES >> 4));
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t oa = ((kk >> 2) * BM * 128 + (kk & 3) * 32) >> 4;
-                    const uint32_t ob = ((kk >> 2) * BN * 128 + (kk & 3) * 32) >> 4;
-                    mma_bf16_ss(dS, dQ + oa, b0 + ob, kIdS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(dS, dQ + ((c * BM * 128 + kk * 32) >> 4), b0 + ((kk * 32) >> 4), kIdS,
+                                    (c > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(b_kv_empty(cs));
                 }
-                mma_commit(b_s_full(j & 1));
-                mma_commit(b_kv_empty(ks));
+                __syncwarp();
+                next_slot();
             }
+            if (leader) mma_commit(b_s_full(j & 1));
             __syncwarp();
-            adv(ks, kph);
             return true;
         };
         // A launch told to give up (p.give_up) stops here, before any MMA; the
@@ -277,37 +312,93 @@ __global__ void __launch_bounds__(192, 1)
         for (int j = 0; ok && j < n_kv; ++j) {
             if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
             if (!(ok = wait_all(b_p_full, j & 1))) break;
-            if (!(ok = wait_all(b_kv_full(vs), vph))) break;
-            {
-                // Rows past the document's last key (the next document's, the
-                // next batch entry's, or cache slots past seq_len) may hold
-                // anything, NaN included; P is 0 there but 0 * NaN is not, so
-                // the last KV tile's V rows past the end are zeroed first.
-                const int lim = Lk - j * BN;
+            // O += P_j V_j; P_j (bf16 pairs) read from the first BN / 2 columns
+            // of S_j's buffer.  Rows past the document's last key (the next
+            // document's, the next batch entry's, or cache slots past
+            // seq_len) may hold anything, NaN included; P is 0 there but
+            // 0 * NaN is not, so V rows past the end are zeroed first.
+            const uint32_t a = tmem + C::TMEM_S + (j & 1) * BN;
+            const int lim = Lk - j * BN;  // keys of this tile inside the document
+            if (C::VKEYS) {
+#pragma unroll 1
+                for (int q = 0; q < C::V_SLOTS; ++q) {
+                    if (!(ok = wait_all(b_kv_full(cs), cph))) break;
+                    const uint32_t vb = sKV + cs * C::SLOT_BYTES;
+                    const int ql = lim - q * C::VR;  // keys of this slot inside the document
+                    if (ql < C::VR) {
+                        const int r0 = ql > 0 ? ql : 0;
+                        for (int idx = lane; idx < (C::VR - r0) * NCH * 8; idx += 32) {
+                            const int u = idx & 7, rc = idx >> 3, c = rc % NCH, rr = r0 + rc / NCH;
+                            st_shared_v4(vb + c * (C::VR * 128) + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    tc_fence_after();
+                    if (leader) {
+                        const uint64_t b0 = dV + static_cast<uint64_t>(cs * (C::SLOT_BYTES >> 4));
+#pragma unroll
+                        for (int kk = 0; kk < C::VR / 16; ++kk)
+                            mma_bf16_ts(tmem + C::TMEM_O, a + (q * (C::VR / 16) + kk) * 8,
+                                        b0 + ((kk * 16 * 128) >> 4), kIdO, (j > 0 || q > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(b_kv_empty(cs));
+                    }
+                    __syncwarp();
+                    next_slot();
+                }
+            } else if (cs + NCH <= SLOTS) {
+                // the tile's chunks lie in slots cs .. cs + NCH - 1 (one phase)
+#pragma unroll 1
+                for (int c = 0; ok && c < NCH; ++c) ok = wait_all(b_kv_full(cs + c), cph);
+                if (!ok) break;
                 if (lim < BN) {
-                    const uint32_t vb = sKV + vs * C::KV_BYTES;
                     for (int idx = lane; idx < (BN - lim) * NCH * 8; idx += 32) {
                         const int u = idx & 7, rc = idx >> 3, c = rc % NCH, rr = lim + rc / NCH;
-                        st_shared_v4(vb + c * BN * 128 + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
+                        st_shared_v4(sKV + (cs + c) * C::SLOT_BYTES + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
-            }
-            tc_fence_after();
-            if (leader) {
-                // O += P_j V_j, P_j (bf16 pairs) read from the first BN / 2 columns of S_j's buffer
-                const uint64_t b0 = dV + static_cast<uint64_t>(vs * (C::KV_BYTES >> 4));
-                const uint32_t a = tmem + C::TMEM_S + (j & 1) * BN;
+                tc_fence_after();
+                if (leader) {
+                    const uint64_t b0 = dV + static_cast<uint64_t>(cs * (C::SLOT_BYTES >> 4));
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_bf16_ts(tmem + C::TMEM_O, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdO,
-                                (j > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(b_pv_done);
-                mma_commit(b_kv_empty(vs));
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_bf16_ts(tmem + C::TMEM_O, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdO,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) mma_commit(b_kv_empty(cs + c));
+                }
+                __syncwarp();
+                for (int c = 0; c < NCH; ++c) next_slot();
+            } else {
+                // the tile wraps around the ring: one N = 64 product per chunk
+#pragma unroll 1
+                for (int c = 0; c < NCH; ++c) {
+                    if (!(ok = wait_all(b_kv_full(cs), cph))) break;
+                    const uint32_t vb = sKV + cs * C::SLOT_BYTES;
+                    if (lim < BN) {
+                        for (int idx = lane; idx < (BN - lim) * 8; idx += 32)
+                            st_shared_v4(vb + (lim + (idx >> 3)) * 128 + (idx & 7) * 16, 0u, 0u, 0u, 0u);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    tc_fence_after();
+                    if (leader) {
+                        const uint64_t b0 = dV + static_cast<uint64_t>(cs * (C::SLOT_BYTES >> 4));
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk)
+                            mma_bf16_ts(tmem + C::TMEM_O + c * 64, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdO64,
+                                        (j > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(b_kv_empty(cs));
+                    }
+                    __syncwarp();
+                    next_slot();
+                }
             }
+            if (!ok) break;
+            if (leader) mma_commit(b_pv_done);
             __syncwarp();
-            adv(vs, vph);
         }
         // Everything issued above must finish before TMEM is released.
         if (leader) mma_commit(b_drain);
@@ -1387,8 +1478,8 @@ __global__ void __launch_bounds__(384, 1)
 using Cfg64 = Prefill2Cfg<64, 10>;
 using Cfg96 = Prefill2Cfg<96, 5>;
 using Cfg128 = Prefill2Cfg<128, 5>;
-using Cfg192 = PrefillCfg<192, 128, 3>;
-using Cfg256 = PrefillCfg<256, 128, 2>;
+using Cfg192 = PrefillCfg<192, 128, 11>;
+using Cfg256 = PrefillCfg<256, 128, 10>;
 
 // Sets the dynamic shared-memory limit of `kernel` once per device (one flag
 // set per instantiation: the kernels of several configurations share a type).
@@ -1574,6 +1665,7 @@ static cudaError_t plan_for(const PrefillParams& p, int num_sms, PrefillPlan* pl
 }
 
 int prefill_block_n(int D) { return (D == 64 || D == 96 || D == 128 || D == 192 || D == 256) ? 128 : 0; }
+int prefill_v_box_rows(int D) { return D == 256 ? Cfg256::VR : D == 192 ? Cfg192::VR : prefill_block_n(D); }
 
 cudaError_t launch_prefill(int D, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            const CUtensorMap& tmO, const PrefillParams& p, int num_sms, cudaStream_t stream) {
