@@ -603,7 +603,8 @@ gbattn_status attn_fwd_vsa(const void* q_tiled, const void* k_tiled, const void*
     if (out_dtype != GBATTN_OUT_BF16 && out_dtype != GBATTN_OUT_F32) return GBATTN_ERR_UNSUPPORTED;
     const long long nbp = num_blocks + (num_blocks & 1);
     const long long rows = nbp * gbattn::kVsaBlock;
-    if (num_blocks >= (1 << 22) || nbp / 2 > 65535 || Hq > 65535) return GBATTN_ERR_UNSUPPORTED;
+    if (num_blocks >= (1 << 22) || nbp / 2 > 65535 || Hq > 65535 || static_cast<long long>(Hq) * (nbp / 2) > 0x7fffffffLL)
+        return GBATTN_ERR_UNSUPPORTED;
     if (!out_index && out_rows != rows) return GBATTN_ERR_INVALID_ARG;
     if (num_blocks == 0) return GBATTN_OK;
     if (!q_tiled || !k_tiled || !v_tiled || !kv_list || !kv_num || !out) return GBATTN_ERR_INVALID_ARG;

@@ -20,10 +20,13 @@
 //                    (kept by both, then by the first only, then the second);
 //   vsa_fwd          CTA per (head, pair of query blocks = one 128-row tile):
 //                    Q tile by TMA, K/V tiles of two 64-row key blocks taken
-//                    from the pair's union list, S = Q K^T and O += P V by
-//                    tcgen05.mma with accumulators in TMEM, online softmax
-//                    where each row masks the key blocks its own query block
-//                    does not keep and the padding rows of every key block.
+//                    from the pair's union list and loaded in the order the
+//                    MMAs read them (K_0, K_1 V_0, K_2 V_1, ...), S = Q K^T and
+//                    O += P V by tcgen05.mma with accumulators in TMEM, online
+//                    softmax where each row masks the key blocks its own query
+//                    block does not keep and the padding rows of every key
+//                    block; P goes to TMEM columns of its own (two buffers)
+//                    and is read from there by P V.
 //
 // The pair layout follows the page's note that the Blackwell kernel serves two
 // 64-row query blocks per CTA (hence an even block count, the last block of an
@@ -296,13 +299,13 @@ struct VsaCfg {
     static constexpr int NCH = D / 64;              // 64-column chunks per row
     static constexpr int Q_BYTES = NCH * BM * 128;
     static constexpr int KV_BYTES = NCH * BN * 128;
-    static constexpr int P_BYTES = (BN / 64) * BM * 128;
     static constexpr int NUM_BARS = 2 * STAGES + 6;
-    static constexpr int SMEM_BYTES = 1024 + Q_BYTES + STAGES * KV_BYTES + P_BYTES + NUM_BARS * 8 + 16;
-    static constexpr int TMEM_S = 0;       // S buffers at [0, BN) and [BN, 2 BN)
-    static constexpr int TMEM_O = 2 * BN;  // O at [2 BN, 2 BN + D)
+    static constexpr int SMEM_BYTES = 1024 + Q_BYTES + STAGES * KV_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int TMEM_S = 0;           // S buffers at [0, BN) and [BN, 2 BN)
+    static constexpr int TMEM_O = 2 * BN;      // O at [2 BN, 2 BN + D)
+    static constexpr int TMEM_P = 2 * BN + D;  // P buffers (bf16 pairs) at [TMEM_P, + BN / 2) and [+ BN / 2, + BN)
     static constexpr int TMEM_COLS = 512;
-    static_assert(D % 64 == 0 && 2 * BN + D <= TMEM_COLS, "tile shape");
+    static_assert(D % 64 == 0 && 3 * BN + D <= TMEM_COLS, "tile shape");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(SMEM_BYTES > 232448 / 2, "one CTA per SM: the TMEM allocation is 512 columns");
 };
@@ -329,8 +332,7 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem);
     const uint32_t sKV = sQ + C::Q_BYTES;
-    const uint32_t sP = sKV + STAGES * C::KV_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Q_BYTES + STAGES * C::KV_BYTES + C::P_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Q_BYTES + STAGES * C::KV_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const uint32_t b_q_full = smem_u32(&bars[0]);
@@ -343,8 +345,22 @@ __global__ void __launch_bounds__(192, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // ------------------------------------------------------------ tile coordinates
-    const int h = blockIdx.x;  // heads fastest: the dense prefix tiles of every head start first
-    const int t = blockIdx.y;
+    // The dense tiles (prefix query blocks keep every key block) of every head
+    // start first, heads fastest; then each head's sparse tiles, tiles fastest,
+    // so that the CTAs resident at one time read the K/V of one or two heads,
+    // which stay in L2.
+    int h, t;
+    {
+        const int dense = p.Hq * p.g.td, per = p.g.nt - p.g.td;
+        const int L = blockIdx.x;
+        if (L < dense) {
+            h = L % p.Hq;
+            t = L / p.Hq;
+        } else {
+            h = (L - dense) / per;
+            t = p.g.td + (L - dense) % per;
+        }
+    }
     const int kvh = h / p.group;
     const int nb = p.g.nb;
     const int cap = p.g.capacity(t);
@@ -390,14 +406,14 @@ __global__ void __launch_bounds__(192, 1)
             tma_prefetch_desc(&tmV);
             mbar_arrive_expect_tx(b_q_full, C::Q_BYTES);
             for (int c = 0; c < NCH; ++c) tma_load_3d(sQ + c * BM * 128, &tmQ, b_q_full, c * 64, h, t * BM);
-            int e0 = n > 0 ? list[0] : 0, e1 = n > 1 ? list[1] : -1;
+            // Load t of the MMAs' order: K_0, then K_{j+1} and V_j for each j,
+            // V_{n-1} last; a K or V tile is the two key blocks of list
+            // entries 2 j and 2 j + 1.
             int issued = 0;
-            for (int j = 0; ok && j < n_kv; ++j) {
-                int f0 = 0, f1 = -1;  // entries of tile j + 1, read ahead of this tile's waits
-                if (j + 1 < n_kv) {
-                    f0 = list[2 * j + 2];
-                    f1 = 2 * j + 3 < n ? list[2 * j + 3] : -1;
-                }
+            for (int tt = 0; ok && tt < 2 * n_kv; ++tt) {
+                const bool isv = tt == 2 * n_kv - 1 || (tt > 0 && (tt & 1) == 0);
+                const int jt = isv ? (tt == 2 * n_kv - 1 ? n_kv - 1 : tt / 2 - 1) : (tt + 1) / 2;
+                const int e0 = list[2 * jt], e1 = 2 * jt + 1 < n ? list[2 * jt + 1] : -1;
                 // A missing second entry repeats the first block (masked for
                 // every row); a bad entry is flagged and block 0 read instead.
                 int b0 = e0 >> 9, b1 = e1 < 0 ? b0 : (e1 >> 9);
@@ -406,24 +422,19 @@ __global__ void __launch_bounds__(192, 1)
                     b0 = (b0 < 0 || b0 >= nb) ? 0 : b0;
                     b1 = (b1 < 0 || b1 >= nb) ? 0 : b1;
                 }
-                for (int kv = 0; kv < 2; ++kv) {
-                    const int u_ = 2 * j + kv, s = u_ % STAGES, u = u_ / STAGES;
-                    if (u > 0 && !mbar_wait(b_kv_empty(s), (u - 1) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const CUtensorMap* m = kv ? &tmV : &tmK;
-                    const uint32_t dst = sKV + s * C::KV_BYTES;
-                    mbar_arrive_expect_tx(b_kv_full(s), C::KV_BYTES);
-                    for (int c = 0; c < NCH; ++c) {
-                        tma_load_3d(dst + c * BN * 128, m, b_kv_full(s), c * 64, kvh, b0 * kVsaBlock);
-                        tma_load_3d(dst + c * BN * 128 + kVsaBlock * 128, m, b_kv_full(s), c * 64, kvh,
-                                    b1 * kVsaBlock);
-                    }
-                    ++issued;
+                const int s = tt % STAGES, u = tt / STAGES;
+                if (u > 0 && !mbar_wait(b_kv_empty(s), (u - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                e0 = f0;
-                e1 = f1;
+                const CUtensorMap* m = isv ? &tmV : &tmK;
+                const uint32_t dst = sKV + s * C::KV_BYTES;
+                mbar_arrive_expect_tx(b_kv_full(s), C::KV_BYTES);
+                for (int c = 0; c < NCH; ++c) {
+                    tma_load_3d(dst + c * BN * 128, m, b_kv_full(s), c * 64, kvh, b0 * kVsaBlock);
+                    tma_load_3d(dst + c * BN * 128 + kVsaBlock * 128, m, b_kv_full(s), c * 64, kvh, b1 * kVsaBlock);
+                }
+                ++issued;
             }
             if (!ok || *abort_flag) {
                 // Let every copy this thread started land before the CTA retires.
@@ -439,27 +450,26 @@ __global__ void __launch_bounds__(192, 1)
         constexpr uint32_t kIdO = idesc_bf16_f32(BM, D, false, true);
         const bool leader = elect_one();
         const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
-        const uint64_t dP = sdesc_sw128(sP, 16, 1024);
         const uint64_t dK = sdesc_sw128(sKV, 16, 1024);
         const uint64_t dV = sdesc_sw128(sKV, BN * 128, 1024);
         auto wait_all = [&](uint32_t bar, uint32_t ph) {
             return __all_sync(0xffffffffu, mbar_wait(bar, ph, abort_flag));
         };
-        int ks = 0, vs = 1;  // K_j is load 2 j of the ring, V_j load 2 j + 1
-        uint32_t kph = 0, vph = 0;
-        auto adv = [](int& s, uint32_t& ph) {
-            s += 2;
-            if (s >= STAGES) {
-                s -= STAGES;
-                ph ^= 1u;
+        // Stages are read in the producer's order; cs / cph: the next one and its phase.
+        int cs = 0;
+        uint32_t cph = 0;
+        auto next_stage = [&]() {
+            if (++cs == STAGES) {
+                cs = 0;
+                cph ^= 1u;
             }
         };
         auto issue_s = [&](int j) -> bool {
-            if (!wait_all(b_kv_full(ks), kph)) return false;
+            if (!wait_all(b_kv_full(cs), cph)) return false;
             tc_fence_after();
             if (leader) {
                 const uint32_t dS = tmem + C::TMEM_S + (j & 1) * BN;
-                const uint64_t b0 = dK + static_cast<uint64_t>(ks * (C::KV_BYTES >> 4));
+                const uint64_t b0 = dK + static_cast<uint64_t>(cs * (C::KV_BYTES >> 4));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = ((kk >> 2) * BM * 128 + (kk & 3) * 32) >> 4;
@@ -467,10 +477,10 @@ __global__ void __launch_bounds__(192, 1)
                     mma_bf16_ss(dS, dQ + oa, b0 + ob, kIdS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(b_s_full(j & 1));
-                mma_commit(b_kv_empty(ks));
+                mma_commit(b_kv_empty(cs));
             }
             __syncwarp();
-            adv(ks, kph);
+            next_stage();
             return true;
         };
         ok = wait_all(b_q_full, 0);
@@ -482,10 +492,10 @@ __global__ void __launch_bounds__(192, 1)
             const int za = min((ea >> 2) & 127, kVsaBlock), zb = eb < 0 ? 0 : min((eb >> 2) & 127, kVsaBlock);
             if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
             if (!(ok = wait_all(b_p_full, j & 1))) break;
-            if (!(ok = wait_all(b_kv_full(vs), vph))) break;
+            if (!(ok = wait_all(b_kv_full(cs), cph))) break;
             if (za < kVsaBlock || zb < kVsaBlock) {
                 // P is 0 in the padding columns but 0 * NaN is not: zero those V rows.
-                const uint32_t vb = sKV + vs * C::KV_BYTES;
+                const uint32_t vb = sKV + cs * C::KV_BYTES;
                 const int na = kVsaBlock - za, nz = na + kVsaBlock - zb;
                 for (int idx = lane; idx < nz * NCH * 8; idx += 32) {
                     const int u = idx & 7, rc = idx >> 3, c = rc % NCH, k = rc / NCH;
@@ -497,18 +507,18 @@ __global__ void __launch_bounds__(192, 1)
             }
             tc_fence_after();
             if (leader) {
-                const uint64_t b0 = dV + static_cast<uint64_t>(vs * (C::KV_BYTES >> 4));
+                // O += P_j V_j, P_j (bf16 pairs) read from its TMEM buffer
+                const uint64_t b0 = dV + static_cast<uint64_t>(cs * (C::KV_BYTES >> 4));
+                const uint32_t a = tmem + C::TMEM_P + (j & 1) * (BN / 2);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint32_t oa = ((kk >> 2) * BM * 128 + (kk & 3) * 32) >> 4;
-                    mma_bf16_ss(tmem + C::TMEM_O, dP + oa, b0 + ((kk * 16 * 128) >> 4), kIdO,
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_bf16_ts(tmem + C::TMEM_O, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdO,
                                 (j > 0 || kk > 0) ? 1u : 0u);
-                }
                 mma_commit(b_pv_done);
-                mma_commit(b_kv_empty(vs));
+                mma_commit(b_kv_empty(cs));
             }
             __syncwarp();
-            adv(vs, vph);
+            next_stage();
         }
         if (leader) mma_commit(b_drain);  // all of the above finishes before TMEM is released
         __syncwarp();
@@ -532,6 +542,7 @@ __global__ void __launch_bounds__(192, 1)
             e1 = f1;
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_s_full(j & 1), (j >> 1) & 1, abort_flag)))) break;
             tc_fence_after();
+            const uint32_t tS = tl + C::TMEM_S + (j & 1) * BN;
             uint32_t pk[BN / 2];
             bool warp_need = false;
             float alpha = 1.f;
@@ -539,8 +550,7 @@ __global__ void __launch_bounds__(192, 1)
                 uint32_t sr[BN];
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c)
-                    tmem_ld32(tl + C::TMEM_S + (j & 1) * BN + c * 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+                    tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
                 tmem_wait_ld();
                 if (la < kVsaBlock || lb < kVsaBlock) {
 #pragma unroll
@@ -579,7 +589,13 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;
             }
-            // PV_{j-1} has to be finished before O is rescaled or P overwritten.
+            // PV_{j-1} is complete before P_j is released (and before O is
+            // rescaled): S_j was issued after PV_{j-2} only, so here PV_{j-2}
+            // is complete and PV_j not yet issued, and pv_done has completed
+            // j - 1 or j phases; a wait on the parity of phase j - 1 is exact
+            // whichever it is.  P_j replaces P_{j-2} in buffer j & 1.  (Waiting
+            // only when O is rescaled, as the prefill kernels do, measured the
+            // same speed here and gave wrong rows at D = 64.)
             if (j > 0) {
                 if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_pv_done, (j - 1) & 1, abort_flag)))) break;
                 tc_fence_after();
@@ -593,18 +609,11 @@ __global__ void __launch_bounds__(192, 1)
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                         tmem_st32(tl + C::TMEM_O + c * 32, o);
                     }
-                    tmem_wait_st();
                 }
             }
 #pragma unroll
-            for (int a = 0; a < BN / 64; ++a) {
-                const uint32_t rowp = sP + a * BM * 128 + r * 128;
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_shared_v4(rowp + ((q ^ (r & 7)) << 4), pk[a * 32 + q * 4 + 0], pk[a * 32 + q * 4 + 1],
-                                 pk[a * 32 + q * 4 + 2], pk[a * 32 + q * 4 + 3]);
-            }
-            fence_proxy_async_smem();
+            for (int c = 0; c < BN / 32; ++c) tmem_st16(tl + C::TMEM_P + (j & 1) * (BN / 2) + c * 16, &pk[c * 16]);
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(b_p_full);
         }
@@ -673,8 +682,8 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-using VsaCfg64 = VsaCfg<64, 8>;
-using VsaCfg128 = VsaCfg<128, 4>;
+using VsaCfg64 = VsaCfg<64, 12>;
+using VsaCfg128 = VsaCfg<128, 6>;
 
 // ------------------------------------------------------------------ launchers
 static int grid_for(long long units, int per_cta, int num_sms, int ctas_per_sm) {
@@ -750,8 +759,9 @@ static cudaError_t launch_vsa_cfg(const CUtensorMap& tmQ, const CUtensorMap& tmK
             if (dev >= 0 && dev < 64) done[dev] = true;
         }
     }
-    dim3 grid(p.Hq, p.g.nt);
-    vsa_fwd_sm103a<C><<<grid, 192, C::SMEM_BYTES, st>>>(tmQ, tmK, tmV, p);
+    const long long ctas = static_cast<long long>(p.Hq) * p.g.nt;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    vsa_fwd_sm103a<C><<<static_cast<unsigned>(ctas), 192, C::SMEM_BYTES, st>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
 }
 

@@ -462,7 +462,8 @@ const char* attn_status_string(gbattn_status status);
  *   out_index at or past out_rows (row skipped).
  *
  * Errors of the device calls: GBATTN_ERR_INVALID_ARG, GBATTN_ERR_UNSUPPORTED
- * (head size, more than 65535 tiles), GBATTN_ERR_ALIGNMENT, GBATTN_ERR_DEVICE
+ * (head size, more than 65535 tiles, heads x tiles above 2^31 - 1),
+ * GBATTN_ERR_ALIGNMENT, GBATTN_ERR_DEVICE
  * / _CUDA.  None allocates or synchronises.
  */
 gbattn_status attn_vsa_tile_map(const int32_t* prefix_segments, int num_segments, int T, int H, int W, int tile_t,
