@@ -20,23 +20,23 @@
 //     that width do not fit in TMEM next to the S buffers), 192 threads:
 //       warps 0-3  softmax + O correction + epilogue; warp w owns TMEM lanes 32w..32w+31
 //       warp 4     TMA producer: Q once, then K and V in the order the MMAs
-//                  read them (K_0, K_1 V_0, K_2 V_1, ...) into a ring of 16 KB
-//                  slots: a K tile is D / 64 slots of 64 columns x 128 keys, a
-//                  V tile the same at D = 192 and 4 slots of 32 keys x 256
-//                  columns at D = 256
+//                  read them (K_0, K_1 V_0, K_2 V_1, ...) into a ring of slots:
+//                  at D = 192 three 48 KB slots, one whole K or V tile each; at
+//                  D = 256 five 32 KB slots, a K tile two slots of 128 columns,
+//                  a V tile two slots of 64 keys x 256 columns
 //       warp 5     TMEM allocator and MMA issuer (one elected lane)
 //     S double-buffered in TMEM (S_{j+1} is issued before PV_j, so the tensor
 //     core works on the next scores while the softmax warps exponentiate the
 //     current ones); P written back over S_j's buffer and read by P.V from
 //     TMEM, as in the two-tile kernel.  The MMAs of each slot release it as
-//     they complete, so the ring refills a slot at a time, several slots
-//     ahead of the MMAs.  K is cut along D (each slot feeds a full-width
-//     N = 128 score product).  P.V runs as N = D products: at D = 256 V is
-//     cut along the keys, each slot a whole product; at D = 192 a V tile's
-//     three column slots are read by one product when they lie in
-//     consecutive slots, and as three N = 64 products when the tile wraps
-//     around the ring (32-key V slots would leave a quarter of each slot
-//     empty at D = 192).
+//     they complete, so the ring refills a slot at a time, ahead of the
+//     MMAs.  K is cut along D (each slot feeds full-width N = 128 score
+//     products) and P.V runs as full-width N = D products (at D = 256 V is
+//     cut along the keys).  Slots are as large as the ring allows: measured
+//     on this part, one SM's TMA rate grows with the bytes each barrier
+//     covers (16 KB: about 21 B/cycle, 32 KB: 40, 48 KB: 57), and 16 KB
+//     slots held these kernels to 1180 / 1270 TFLOP/s against 1640 / 1600
+//     with these.
 //
 // Both kernels have a paged instantiation (PAGED): K/V tiles come from the
 // paged cache through block_table (vllm-ascend attention_v1.py, chunked
@@ -67,21 +67,23 @@
 
 namespace gbattn {
 
-template <int D_, int BN_, int SLOTS_>
+template <int D_, int BN_, int SLOTS_, int SCH_>
 struct PrefillCfg {
     static constexpr int D = D_;
     static constexpr int BN = BN_;
-    static constexpr int SLOTS = SLOTS_;                // K/V ring slots, one 64-column chunk each
+    static constexpr int SLOTS = SLOTS_;                // K/V ring slots
+    static constexpr int SCH = SCH_;                    // 64-column chunks of a K tile per slot
     static constexpr int BM = 128;
     static constexpr int NCH = (D + 63) / 64;           // 64-column chunks per row
     static constexpr int Q_BYTES = NCH * BM * 128;
-    static constexpr int SLOT_BYTES = BN * 128;         // 64 columns of a K tile
+    static constexpr int SLOT_BYTES = SCH * BN * 128;
+    static constexpr int K_SLOTS = NCH / SCH;           // slots of one K tile
     // V cut along the keys (VR keys x D per slot) when that fills a slot, else
     // into 64-column chunks like K
-    static constexpr bool VKEYS = 32 * D * 2 == BN * 128;
-    static constexpr int VR = VKEYS ? 32 : BN;          // keys of a V tile per slot
-    static constexpr int V_SLOTS = VKEYS ? BN / VR : NCH;
-    static constexpr int V_SLOT_BYTES = VR * (VKEYS ? D : 64) * 2;
+    static constexpr bool VKEYS = 32 * SCH * D * 2 == SLOT_BYTES;
+    static constexpr int VR = VKEYS ? 32 * SCH : BN;    // keys of a V tile per slot
+    static constexpr int V_SLOTS = VKEYS ? BN / VR : K_SLOTS;
+    static constexpr int V_SLOT_BYTES = VKEYS ? VR * D * 2 : SLOT_BYTES;
     static constexpr int NUM_BARS = 2 * SLOTS + 6;
     static constexpr int SMEM_BYTES = 1024 + Q_BYTES + SLOTS * SLOT_BYTES + NUM_BARS * 8 + 16;
     static constexpr int TMEM_S = 0;        // S buffers at columns [0, BN) and [BN, 2BN)
@@ -91,7 +93,8 @@ struct PrefillCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(D % 32 == 0 && BN % 64 == 0, "tile shape");
     static_assert(D % 64 == 0 && BM == BN && (D / 32) * BM * 128 <= SLOTS * SLOT_BYTES, "output staging in the ring");
-    static_assert(V_SLOT_BYTES == SLOT_BYTES && VR % 16 == 0 && BN % VR == 0 && NCH <= SLOTS, "V slots");
+    static_assert(V_SLOT_BYTES == SLOT_BYTES && VR % 16 == 0 && BN % VR == 0 && NCH % SCH == 0 && K_SLOTS <= SLOTS,
+                  "V slots");
     // TMA-store epilogue for full tiles: measured +1.5% at D = 192, -0.8% at D = 256
     static constexpr bool TMA_OUT = D < 256;
 };
@@ -234,7 +237,7 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     row = (isv ? p.num_blocks + blk : blk) * BN;
                 }
-                for (int q = 0; q < (isv ? C::V_SLOTS : NCH); ++q) {
+                for (int q = 0; q < (isv ? C::V_SLOTS : C::K_SLOTS); ++q) {
                     const int s = issued % SLOTS, u = issued / SLOTS;
                     if (u > 0 && !mbar_wait(b_kv_empty(s), (u - 1) & 1, abort_flag)) {
                         ok = false;
@@ -245,9 +248,10 @@ __global__ void __launch_bounds__(192, 1)
                         mbar_arrive_expect_tx(b_kv_full(s), C::V_SLOT_BYTES);
                         for (int c = 0; c < NCH; ++c)
                             tma_load_3d(dst + c * (C::VR * 128), m, b_kv_full(s), c * 64, kvh, row + q * C::VR);
-                    } else {    // columns [64 q, 64 q + 64) of all BN keys
+                    } else {    // columns [64 SCH q, 64 SCH (q + 1)) of all BN keys
                         mbar_arrive_expect_tx(b_kv_full(s), C::SLOT_BYTES);
-                        tma_load_3d(dst, m, b_kv_full(s), q * 64, kvh, row);
+                        for (int i = 0; i < C::SCH; ++i)
+                            tma_load_3d(dst + i * (BN * 128), m, b_kv_full(s), (q * C::SCH + i) * 64, kvh, row);
                     }
                     ++issued;
                 }
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint64_t dK = sdesc_sw128(sKV, 16, 1024);
         // V operand: VR-key blocks of 64 columns (VKEYS), or the tile's column
         // chunks in consecutive slots
-        const uint64_t dV = sdesc_sw128(sKV, C::VKEYS ? C::VR * 128 : C::SLOT_BYTES, 1024);
+        const uint64_t dV = sdesc_sw128(sKV, C::VKEYS ? C::VR * 128 : BN * 128, 1024);
         constexpr uint32_t kIdO64 = idesc_bf16_f32(BM, 64, false, true);
         auto wait_all = [&](uint32_t bar, uint32_t ph) {
             return __all_sync(0xffffffffu, mbar_wait(bar, ph, abort_flag));
@@ -287,15 +291,17 @@ __global__ void __launch_bounds__(192, 1)
         auto issue_s = [&](int j) -> bool {
             const uint32_t dS = tmem + C::TMEM_S + (j & 1) * BN;
 #pragma unroll 1
-            for (int c = 0; c < NCH; ++c) {
+            for (int q = 0; q < C::K_SLOTS; ++q) {
                 if (!wait_all(b_kv_full(cs), cph)) return false;
                 tc_fence_after();
                 if (leader) {
                     const uint64_t b0 = dK + static_cast<uint64_t>(cs * (C::SLOT_BYTES >> 4));
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss(dS, dQ + ((c * BM * 128 + kk * 32) >> 4), b0 + ((kk * 32) >> 4), kIdS,
-                                    (c > 0 || kk > 0) ? 1u : 0u);
+                    for (int i = 0; i < C::SCH; ++i)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss(dS, dQ + ((((q * C::SCH + i) * BM) * 128 + kk * 32) >> 4),
+                                        b0 + ((i * BN * 128 + kk * 32) >> 4), kIdS, (q > 0 || i > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(b_kv_empty(cs));
                 }
                 __syncwarp();
@@ -346,15 +352,16 @@ __global__ void __launch_bounds__(192, 1)
                     __syncwarp();
                     next_slot();
                 }
-            } else if (cs + NCH <= SLOTS) {
-                // the tile's chunks lie in slots cs .. cs + NCH - 1 (one phase)
+            } else if (cs + C::V_SLOTS <= SLOTS) {
+                // the tile's chunks lie in slots cs .. cs + V_SLOTS - 1 (one
+                // phase), chunk c at sKV + cs SLOT_BYTES + c BN 128
 #pragma unroll 1
-                for (int c = 0; ok && c < NCH; ++c) ok = wait_all(b_kv_full(cs + c), cph);
+                for (int q = 0; ok && q < C::V_SLOTS; ++q) ok = wait_all(b_kv_full(cs + q), cph);
                 if (!ok) break;
                 if (lim < BN) {
                     for (int idx = lane; idx < (BN - lim) * NCH * 8; idx += 32) {
                         const int u = idx & 7, rc = idx >> 3, c = rc % NCH, rr = lim + rc / NCH;
-                        st_shared_v4(sKV + (cs + c) * C::SLOT_BYTES + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
+                        st_shared_v4(sKV + cs * C::SLOT_BYTES + c * (BN * 128) + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -367,29 +374,34 @@ __global__ void __launch_bounds__(192, 1)
                         mma_bf16_ts(tmem + C::TMEM_O, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdO,
                                     (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c) mma_commit(b_kv_empty(cs + c));
+                    for (int q = 0; q < C::V_SLOTS; ++q) mma_commit(b_kv_empty(cs + q));
                 }
                 __syncwarp();
-                for (int c = 0; c < NCH; ++c) next_slot();
+                for (int q = 0; q < C::V_SLOTS; ++q) next_slot();
             } else {
                 // the tile wraps around the ring: one N = 64 product per chunk
 #pragma unroll 1
-                for (int c = 0; c < NCH; ++c) {
+                for (int q = 0; q < C::V_SLOTS; ++q) {
                     if (!(ok = wait_all(b_kv_full(cs), cph))) break;
                     const uint32_t vb = sKV + cs * C::SLOT_BYTES;
                     if (lim < BN) {
-                        for (int idx = lane; idx < (BN - lim) * 8; idx += 32)
-                            st_shared_v4(vb + (lim + (idx >> 3)) * 128 + (idx & 7) * 16, 0u, 0u, 0u, 0u);
+                        for (int idx = lane; idx < (BN - lim) * C::SCH * 8; idx += 32) {
+                            const int u = idx & 7, rc = idx >> 3, i = rc % C::SCH, rr = lim + rc / C::SCH;
+                            st_shared_v4(vb + i * (BN * 128) + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
+                        }
                         fence_proxy_async_smem();
                         __syncwarp();
                     }
                     tc_fence_after();
                     if (leader) {
-                        const uint64_t b0 = dV + static_cast<uint64_t>(cs * (C::SLOT_BYTES >> 4));
 #pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk)
-                            mma_bf16_ts(tmem + C::TMEM_O + c * 64, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdO64,
-                                        (j > 0 || kk > 0) ? 1u : 0u);
+                        for (int i = 0; i < C::SCH; ++i) {
+                            const uint64_t b0 = dV + static_cast<uint64_t>((cs * C::SLOT_BYTES + i * BN * 128) >> 4);
+#pragma unroll
+                            for (int kk = 0; kk < BN / 16; ++kk)
+                                mma_bf16_ts(tmem + C::TMEM_O + (q * C::SCH + i) * 64, a + kk * 8,
+                                            b0 + ((kk * 16 * 128) >> 4), kIdO64, (j > 0 || kk > 0) ? 1u : 0u);
+                        }
                         mma_commit(b_kv_empty(cs));
                     }
                     __syncwarp();
@@ -1478,8 +1490,8 @@ __global__ void __launch_bounds__(384, 1)
 using Cfg64 = Prefill2Cfg<64, 10>;
 using Cfg96 = Prefill2Cfg<96, 5>;
 using Cfg128 = Prefill2Cfg<128, 5>;
-using Cfg192 = PrefillCfg<192, 128, 11>;
-using Cfg256 = PrefillCfg<256, 128, 10>;
+using Cfg192 = PrefillCfg<192, 128, 3, 3>;
+using Cfg256 = PrefillCfg<256, 128, 5, 2>;
 
 // Sets the dynamic shared-memory limit of `kernel` once per device (one flag
 // set per instantiation: the kernels of several configurations share a type).
