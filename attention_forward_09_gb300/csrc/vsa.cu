@@ -313,6 +313,14 @@ struct VsaCfg {
 constexpr float kVsaLn2 = 0.6931471805599453f;
 constexpr float kVsaRescale = 8.0f;  // log2 units: tolerate P up to 2^8 before rescaling O
 
+// Token count of the key block of list entry e (clamped to [0, 64]; 0 for no block).
+__device__ __forceinline__ int entry_rows_of(int e, int nb) {
+    const int blk = e >> 9;
+    if (e < 0 || blk >= nb) return 0;
+    const int s = (e >> 2) & 127;
+    return s < kVsaBlock ? s : kVsaBlock;
+}
+
 // Visible keys of a 64-row key block for the rows of query block qb (0 or 1)
 // of the tile: its token count if that query block keeps it, else 0.
 __device__ __forceinline__ int entry_keys(int e, int qb, int nb) {
@@ -410,10 +418,25 @@ __global__ void __launch_bounds__(192, 1)
             // V_{n-1} last; a K or V tile is the two key blocks of list
             // entries 2 j and 2 j + 1.
             int issued = 0;
+            auto tile_of = [&](int tt) {
+                const bool isv = tt == 2 * n_kv - 1 || (tt > 0 && (tt & 1) == 0);
+                return isv ? (tt == 2 * n_kv - 1 ? n_kv - 1 : tt / 2 - 1) : (tt + 1) / 2;
+            };
+            // the entries of the next load, read one load ahead
+            int ne0 = 0, ne1 = -1;
+            if (n_kv > 0) {
+                ne0 = list[0];
+                ne1 = n > 1 ? list[1] : -1;
+            }
             for (int tt = 0; ok && tt < 2 * n_kv; ++tt) {
                 const bool isv = tt == 2 * n_kv - 1 || (tt > 0 && (tt & 1) == 0);
-                const int jt = isv ? (tt == 2 * n_kv - 1 ? n_kv - 1 : tt / 2 - 1) : (tt + 1) / 2;
-                const int e0 = list[2 * jt], e1 = 2 * jt + 1 < n ? list[2 * jt + 1] : -1;
+                const int jt = tile_of(tt);
+                const int e0 = ne0, e1 = ne1;
+                if (tt + 1 < 2 * n_kv) {
+                    const int jn = tile_of(tt + 1);
+                    ne0 = list[2 * jn];
+                    ne1 = 2 * jn + 1 < n ? list[2 * jn + 1] : -1;
+                }
                 // A missing second entry repeats the first block (masked for
                 // every row); a bad entry is flagged and block 0 read instead.
                 int b0 = e0 >> 9, b1 = e1 < 0 ? b0 : (e1 >> 9);
@@ -486,25 +509,10 @@ __global__ void __launch_bounds__(192, 1)
         ok = wait_all(b_q_full, 0);
         if (ok && n_kv > 0) ok = issue_s(0);
         for (int j = 0; ok && j < n_kv; ++j) {
-            // Real token counts of the tile's two key blocks (a missing second
-            // entry counts 0): V rows past them are padding, whatever they hold.
-            const int ea = list[2 * j], eb = 2 * j + 1 < n ? list[2 * j + 1] : -1;
-            const int za = min((ea >> 2) & 127, kVsaBlock), zb = eb < 0 ? 0 : min((eb >> 2) & 127, kVsaBlock);
             if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
+            // p_full(j) also reports V_j's padding rows zeroed (softmax warps)
             if (!(ok = wait_all(b_p_full, j & 1))) break;
             if (!(ok = wait_all(b_kv_full(cs), cph))) break;
-            if (za < kVsaBlock || zb < kVsaBlock) {
-                // P is 0 in the padding columns but 0 * NaN is not: zero those V rows.
-                const uint32_t vb = sKV + cs * C::KV_BYTES;
-                const int na = kVsaBlock - za, nz = na + kVsaBlock - zb;
-                for (int idx = lane; idx < nz * NCH * 8; idx += 32) {
-                    const int u = idx & 7, rc = idx >> 3, c = rc % NCH, k = rc / NCH;
-                    const int rr = k < na ? za + k : kVsaBlock + zb + (k - na);
-                    st_shared_v4(vb + c * BN * 128 + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
             tc_fence_after();
             if (leader) {
                 // O += P_j V_j, P_j (bf16 pairs) read from its TMEM buffer
@@ -538,6 +546,7 @@ __global__ void __launch_bounds__(192, 1)
                 f1 = 2 * j + 3 < n ? list[2 * j + 3] : -1;
             }
             const int la = entry_keys(e0, qb, nb), lb = entry_keys(e1, qb, nb);
+            const int cur0 = e0, cur1 = e1;
             e0 = f0;
             e1 = f1;
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_s_full(j & 1), (j >> 1) & 1, abort_flag)))) break;
@@ -609,6 +618,27 @@ __global__ void __launch_bounds__(192, 1)
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                         tmem_st32(tl + C::TMEM_O + c * 32, o);
                     }
+                }
+            }
+            {
+                // V_j's rows past each block's token count are padding, which
+                // may hold anything, NaN included; P is 0 there but 0 * NaN is
+                // not, so the 128 softmax threads zero those rows (V_j is load
+                // 2j + 2 of the ring, or 2n - 1 for the last tile) before they
+                // release P_j, which the MMA warp waits for before P_j V_j.
+                const int za = entry_rows_of(cur0, nb), zb = cur1 < 0 ? 0 : entry_rows_of(cur1, nb);
+                if (za < kVsaBlock || zb < kVsaBlock) {
+                    const int vl = j + 1 == n_kv ? 2 * n_kv - 1 : 2 * j + 2;
+                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_kv_full(vl % STAGES), (vl / STAGES) & 1, abort_flag))))
+                        break;
+                    const uint32_t vb = sKV + (vl % STAGES) * C::KV_BYTES;
+                    const int na = kVsaBlock - za, nz = na + kVsaBlock - zb;
+                    for (int idx = r; idx < nz * NCH * 8; idx += 128) {
+                        const int u = idx & 7, rc = idx >> 3, c = rc % NCH, k = rc / NCH;
+                        const int rr = k < na ? za + k : kVsaBlock + zb + (k - na);
+                        st_shared_v4(vb + c * BN * 128 + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
                 }
             }
 #pragma unroll
