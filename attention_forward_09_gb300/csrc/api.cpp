@@ -581,6 +581,7 @@ gbattn_status attn_vsa_block_map(const float* pooled_q, const float* pooled_k, i
     if (num_blocks >= (1 << 22) || Hq > 65535) return GBATTN_ERR_UNSUPPORTED;
     if (num_blocks == 0) return GBATTN_OK;
     if (!pooled_q || !pooled_k || !block_sizes || !kv_list || !kv_num) return GBATTN_ERR_INVALID_ARG;
+    if (!aligned16(pooled_q) || !aligned16(pooled_k)) return GBATTN_ERR_ALIGNMENT;
     if (gbattn::vsa_map_smem_bytes(num_blocks, D, 2) < 0) return GBATTN_ERR_UNSUPPORTED;
     DeviceInfo di;
     gbattn_status s = device_info(&di);

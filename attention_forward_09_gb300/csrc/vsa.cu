@@ -12,9 +12,10 @@
 //
 //   gather_rows      warp per destination row: dst[w] = src[index[w]] or zeros;
 //   vsa_pool         thread per (block, head, 8 columns): fp32 block means;
-//   vsa_block_map    CTA per (head, 8 / 4 / 2 query blocks): the pooled scores
-//                    of those query blocks against every key block in shared
-//                    memory, a 4-pass radix select of the topk-th score per
+//   vsa_block_map    CTA per (head, 8 / 4 / 2 query blocks): the pooled
+//                    scores of those query blocks against every key block
+//                    (fp32 FMA, two key blocks x 8 query blocks per thread)
+//                    in shared memory, a 4-pass radix select of the topk-th score per
 //                    query block (ties to the lower block index), and, per
 //                    pair of query blocks, the union of their key blocks
 //                    (kept by both, then by the first only, then the second);
@@ -123,52 +124,83 @@ struct VsaMapParams {
 };
 
 constexpr int kMapWarps = 8;
+constexpr int kMapQB = 8;                     // most query blocks per CTA
+constexpr int kMapKeys = 2 * kMapWarps * 32;  // key blocks per scoring pass (two per thread)
+constexpr int kMapDC = 16;                    // dimensions per staged chunk of pooled keys
+constexpr int kMapKS = kMapDC + 4;            // staged row stride in floats (conflict-free float4 reads)
 
 __global__ void __launch_bounds__(kMapWarps * 32) vsa_block_map_sm103a(const VsaMapParams p) {
     extern __shared__ float4 map_smem[];
     const int QB = p.qb, D = p.D, nb = p.g.nb, n_prefix = p.g.n_prefix, keep = p.g.keep;
     const int words = (nb + 31) >> 5;
-    float* pq_s = reinterpret_cast<float*>(map_smem);                  // [QB][D]
-    float* sc = pq_s + QB * D;                                         // [QB][nb]
+    float* pq_s = reinterpret_cast<float*>(map_smem);                  // [kMapQB][D]
+    float* stage = pq_s + kMapQB * D;                                  // [kMapKeys][kMapKS]
+    float* sc = stage + kMapKeys * kMapKS;                             // [QB][nb]
     uint32_t* sel = reinterpret_cast<uint32_t*>(sc + QB * nb);         // [QB][words] kept key blocks
     int* hist = reinterpret_cast<int*>(sel + QB * words);              // [kMapWarps][256]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y, kvh = h / p.group;
     const int i0 = blockIdx.x * QB;
 
-    for (int x = threadIdx.x; x < QB * D; x += blockDim.x) {
+    for (int x = threadIdx.x; x < kMapQB * D; x += blockDim.x) {
         const int i = x / D;
-        pq_s[x] = (i0 + i < nb) ? p.pq[(static_cast<long long>(h) * nb + i0 + i) * D + x % D] : 0.f;
+        pq_s[x] = (i < QB && i0 + i < nb) ? p.pq[(static_cast<long long>(h) * nb + i0 + i) * D + x % D] : 0.f;
     }
-    __syncthreads();
 
-    // scores of the QB query blocks against key block j (warp per key block)
+    // Scores of the query blocks against every key block: thread t takes key
+    // blocks kb + t and kb + t + 256 of each pass against all kMapQB query
+    // blocks (16 fp32 sums in registers, each over d in ascending order); the
+    // pooled keys pass through shared memory kMapDC dimensions at a time, the
+    // pooled queries are read from there as broadcasts.
     const float* pkh = p.pk + static_cast<long long>(kvh) * nb * D;
-    for (int j = warp; j < nb; j += kMapWarps) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int d = lane; d < D; d += 32) {
-            const float kv = pkh[static_cast<long long>(j) * D + d];
+    const int tid = threadIdx.x;
+    for (int kb = 0; kb < nb; kb += kMapKeys) {
+        float acc[2][kMapQB];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (i < QB) acc[i] = fmaf(pq_s[i * D + d], kv, acc[i]);
+        for (int i = 0; i < kMapQB; ++i) acc[0][i] = acc[1][i] = 0.f;
+        for (int d0 = 0; d0 < D; d0 += kMapDC) {
+            __syncthreads();  // the previous chunk has been read (and pq_s written, the first time)
+            for (int f = tid; f < kMapKeys * (kMapDC / 4); f += kMapWarps * 32) {
+                const int key = f / (kMapDC / 4), c4 = f % (kMapDC / 4);
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (kb + key < nb)
+                    v = *reinterpret_cast<const float4*>(pkh + static_cast<long long>(kb + key) * D + d0 + 4 * c4);
+                *reinterpret_cast<float4*>(stage + key * kMapKS + 4 * c4) = v;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int dd = 0; dd < kMapDC; dd += 4) {
+                const float4 k0 = *reinterpret_cast<const float4*>(stage + tid * kMapKS + dd);
+                const float4 k1 = *reinterpret_cast<const float4*>(stage + (tid + kMapWarps * 32) * kMapKS + dd);
+#pragma unroll
+                for (int i = 0; i < kMapQB; ++i) {
+                    const float4 q = *reinterpret_cast<const float4*>(pq_s + i * D + d0 + dd);
+                    acc[0][i] = fmaf(q.x, k0.x, acc[0][i]);
+                    acc[1][i] = fmaf(q.x, k1.x, acc[1][i]);
+                    acc[0][i] = fmaf(q.y, k0.y, acc[0][i]);
+                    acc[1][i] = fmaf(q.y, k1.y, acc[1][i]);
+                    acc[0][i] = fmaf(q.z, k0.z, acc[0][i]);
+                    acc[1][i] = fmaf(q.z, k1.z, acc[1][i]);
+                    acc[0][i] = fmaf(q.w, k0.w, acc[0][i]);
+                    acc[1][i] = fmaf(q.w, k1.w, acc[1][i]);
+                }
+            }
         }
-        float mine = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float a = acc[i];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-            if (lane == i) mine = a;
+        for (int i = 0; i < kMapQB; ++i) {
+            if (i < QB) {
+                if (kb + tid < nb) sc[i * nb + kb + tid] = p.scale * acc[0][i];
+                if (kb + tid + kMapWarps * 32 < nb) sc[i * nb + kb + tid + kMapWarps * 32] = p.scale * acc[1][i];
+            }
         }
-        if (lane < QB) sc[lane * nb + j] = p.scale * mine;
     }
     __syncthreads();
 
     // kept key blocks of each query block (warp per query block)
-    if (warp < QB) {
-        const int qi = i0 + warp;
-        uint32_t* srow = sel + warp * words;
-        const float* row = sc + warp * nb;
+    for (int qw = warp; qw < QB; qw += kMapWarps) {
+        const int qi = i0 + qw;
+        uint32_t* srow = sel + qw * words;
+        const float* row = sc + qw * nb;
         if (qi >= nb) {
             for (int w = lane; w < words; w += 32) srow[w] = 0u;
         } else if (qi < n_prefix || keep == nb - n_prefix) {  // dense rows
@@ -253,7 +285,7 @@ __global__ void __launch_bounds__(kMapWarps * 32) vsa_block_map_sm103a(const Vsa
     }
     __syncthreads();
 
-    // union list of each pair of query blocks (warp per pair)
+    // union list of each pair of query blocks (warp per pair; QB / 2 <= kMapWarps)
     if (warp < QB / 2) {
         const int t = (i0 >> 1) + warp;
         if (t < p.g.nt) {
@@ -739,7 +771,8 @@ cudaError_t launch_vsa_pool(const void* x, const int32_t* sizes, int nb, int H, 
 
 int vsa_map_smem_bytes(int nb, int D, int qb) {
     const long long words = (nb + 31) / 32;
-    const long long b = 4LL * (static_cast<long long>(qb) * D + static_cast<long long>(qb) * nb + qb * words) +
+    const long long b = 4LL * (static_cast<long long>(kMapQB) * D + kMapKeys * kMapKS + static_cast<long long>(qb) * nb +
+                               qb * words) +
                         4LL * kMapWarps * 256;
     return b > 232448 ? -1 : static_cast<int>(b);
 }
@@ -747,7 +780,7 @@ int vsa_map_smem_bytes(int nb, int D, int qb) {
 cudaError_t launch_vsa_block_map(const float* pq, const float* pk, const int32_t* sizes, const VsaGeom& g, int Hq,
                                  int group, int D, float scale, int32_t* kv_list, int32_t* kv_num, uint32_t* status,
                                  cudaStream_t st) {
-    int qb = 8;
+    int qb = kMapQB;
     while (qb > 2 && vsa_map_smem_bytes(g.nb, D, qb) < 0) qb >>= 1;
     const int bytes = vsa_map_smem_bytes(g.nb, D, qb);
     if (bytes < 0) return cudaErrorInvalidValue;

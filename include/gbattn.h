@@ -422,7 +422,8 @@ const char* attn_status_string(gbattn_status status);
  *   array for these sizes (all Hq heads).
  *
  * attn_vsa_block_map -- pooled_q fp32 [Hq, nb, D], pooled_k fp32 [Hkv, nb,
- *   D] (attn_vsa_pool's output).  Scores scale * pooled_q . pooled_k in fp32;
+ *   D] (attn_vsa_pool's output), both 16-byte aligned.  Scores scale *
+ *   pooled_q . pooled_k in fp32;
  *   a prefix query block (index < num_prefix_blocks) keeps every key block; a
  *   video query block keeps every prefix key block and its min(topk,
  *   nb - num_prefix_blocks) best video key blocks, ties to the lower block
@@ -443,7 +444,8 @@ const char* attn_status_string(gbattn_status status);
  *   the list size for Hq = 1) and tile t's at t * nb (t < td) or td * nb +
  *   (t - td) * c2, holding at most nb or c2 entries.
  *   Errors: GBATTN_ERR_UNSUPPORTED if the scores of two query blocks against
- *   every key block do not fit in shared memory (nb above about 26000).
+ *   every key block do not fit in shared memory (nb above about 21000);
+ *   GBATTN_ERR_ALIGNMENT for a pooled array not 16-byte aligned.
  *
  * attn_fwd_vsa -- q_tiled [nbp * 64, Hq, D], k_tiled / v_tiled [nbp * 64,
  *   Hkv, D], device bf16, D = 64 or 128; the padding rows of a block (those

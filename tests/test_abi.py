@@ -271,6 +271,8 @@ def test_vsa_device_calls_validate_before_touching_a_device(lib):
     assert lib.attn_vsa_block_map(P, P, 21, 3, 4, 3, 128, 5, 0.1, P, P, P, None, None) == 1  # Hq % Hkv
     assert lib.attn_vsa_block_map(P, P, 21, 3, 4, 2, 128, 0, 0.1, P, P, P, None, None) == 1  # topk 0
     assert lib.attn_vsa_block_map(P, P, 30000, 0, 4, 2, 256, 5, 0.1, P, P, P, None, None) == 2  # scores too big
+    assert lib.attn_vsa_block_map(UNALIGNED, P, 21, 3, 4, 2, 128, 5, 0.1, P, P, P, None, None) == 3
+    assert lib.attn_vsa_block_map(P, UNALIGNED, 21, 3, 4, 2, 128, 5, 0.1, P, P, P, None, None) == 3
 
     def fwd(**kw):
         a = dict(q=P, k=P, v=P, nb=21, npre=3, topk=5, kl=P, kn=P, idx=P, rows=587, hq=4, hkv=2, d=128,
