@@ -27,7 +27,8 @@
 //                    softmax where each row masks the key blocks its own query
 //                    block does not keep and the padding rows of every key
 //                    block; P goes to TMEM columns of its own (two buffers)
-//                    and is read from there by P V.
+//                    and is read from there by P V; a warp of its own zeroes
+//                    the padding rows of each V tile once it has landed.
 //
 // The pair layout follows the page's note that the Blackwell kernel serves two
 // 64-row query blocks per CTA (hence an even block count, the last block of an
@@ -331,7 +332,7 @@ struct VsaCfg {
     static constexpr int NCH = D / 64;              // 64-column chunks per row
     static constexpr int Q_BYTES = NCH * BM * 128;
     static constexpr int KV_BYTES = NCH * BN * 128;
-    static constexpr int NUM_BARS = 2 * STAGES + 6;
+    static constexpr int NUM_BARS = 3 * STAGES + 6;
     static constexpr int SMEM_BYTES = 1024 + Q_BYTES + STAGES * KV_BYTES + NUM_BARS * 8 + 16;
     static constexpr int TMEM_S = 0;           // S buffers at [0, BN) and [BN, 2 BN)
     static constexpr int TMEM_O = 2 * BN;      // O at [2 BN, 2 BN + D)
@@ -364,7 +365,7 @@ __device__ __forceinline__ int entry_keys(int e, int qb, int nb) {
 }
 
 template <class C>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     vsa_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const VsaFwdParams p) {
     constexpr int D = C::D, BN = C::BN, STAGES = C::STAGES, BM = C::BM, NCH = C::NCH;
@@ -382,6 +383,8 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t b_p_full = smem_u32(&bars[3 + 2 * STAGES]);
     const uint32_t b_pv_done = smem_u32(&bars[4 + 2 * STAGES]);
     const uint32_t b_drain = smem_u32(&bars[5 + 2 * STAGES]);
+    // stage s's load has landed and, for a V tile, its padding rows are zeroed
+    auto b_v_ready = [&](int s) { return smem_u32(&bars[6 + 2 * STAGES + s]); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // ------------------------------------------------------------ tile coordinates
@@ -419,6 +422,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(b_kv_full(s), 1);
             mbar_init(b_kv_empty(s), 1);
+            mbar_init(b_v_ready(s), 1);
         }
         mbar_init(b_s_full(0), 1);
         mbar_init(b_s_full(1), 1);
@@ -542,9 +546,8 @@ __global__ void __launch_bounds__(192, 1)
         if (ok && n_kv > 0) ok = issue_s(0);
         for (int j = 0; ok && j < n_kv; ++j) {
             if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
-            // p_full(j) also reports V_j's padding rows zeroed (softmax warps)
             if (!(ok = wait_all(b_p_full, j & 1))) break;
-            if (!(ok = wait_all(b_kv_full(cs), cph))) break;
+            if (!(ok = wait_all(b_v_ready(cs), cph))) break;  // V_j landed, padding rows zeroed
             tc_fence_after();
             if (leader) {
                 // O += P_j V_j, P_j (bf16 pairs) read from its TMEM buffer
@@ -563,6 +566,37 @@ __global__ void __launch_bounds__(192, 1)
         if (leader) mma_commit(b_drain);  // all of the above finishes before TMEM is released
         __syncwarp();
         mbar_wait_drain(b_drain, 0);
+    } else if (warp == 6) {
+        // ----------------------------------------------------------- V padding
+        // Rows of a V tile past each key block's token count are padding,
+        // which may hold anything, NaN included; P is 0 there but 0 * NaN is
+        // not.  This warp follows the ring in load order: once a load has
+        // landed it zeroes a V tile's padding rows, then passes the stage on
+        // (b_v_ready), which the MMA warp waits for before P V.  It passes K
+        // loads on too, only after they land, so that no stage's b_v_ready
+        // runs a phase ahead of its loads.
+        for (int tt = 0; ok && tt < 2 * n_kv; ++tt) {
+            const int s = tt % STAGES;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_kv_full(s), (tt / STAGES) & 1, abort_flag)))) break;
+            const bool isv = tt == 2 * n_kv - 1 || (tt > 0 && (tt & 1) == 0);
+            if (isv) {
+                const int jv = tt == 2 * n_kv - 1 ? n_kv - 1 : tt / 2 - 1;
+                const int ea = list[2 * jv], eb = 2 * jv + 1 < n ? list[2 * jv + 1] : -1;
+                const int za = entry_rows_of(ea, nb), zb = eb < 0 ? 0 : entry_rows_of(eb, nb);
+                if (za < kVsaBlock || zb < kVsaBlock) {
+                    const uint32_t vb = sKV + s * C::KV_BYTES;
+                    const int na = kVsaBlock - za, nz = na + kVsaBlock - zb;
+                    for (int idx = lane; idx < nz * NCH * 8; idx += 32) {
+                        const int u = idx & 7, rc = idx >> 3, c = rc % NCH, k = rc / NCH;
+                        const int rr = k < na ? za + k : kVsaBlock + zb + (k - na);
+                        st_shared_v4(vb + c * BN * 128 + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_v_ready(s));
+        }
     } else {
         // ------------------------------------------------------------- softmax
         const int r = threadIdx.x;  // row within the tile == TMEM lane
@@ -578,7 +612,6 @@ __global__ void __launch_bounds__(192, 1)
                 f1 = 2 * j + 3 < n ? list[2 * j + 3] : -1;
             }
             const int la = entry_keys(e0, qb, nb), lb = entry_keys(e1, qb, nb);
-            const int cur0 = e0, cur1 = e1;
             e0 = f0;
             e1 = f1;
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_s_full(j & 1), (j >> 1) & 1, abort_flag)))) break;
@@ -650,27 +683,6 @@ __global__ void __launch_bounds__(192, 1)
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                         tmem_st32(tl + C::TMEM_O + c * 32, o);
                     }
-                }
-            }
-            {
-                // V_j's rows past each block's token count are padding, which
-                // may hold anything, NaN included; P is 0 there but 0 * NaN is
-                // not, so the 128 softmax threads zero those rows (V_j is load
-                // 2j + 2 of the ring, or 2n - 1 for the last tile) before they
-                // release P_j, which the MMA warp waits for before P_j V_j.
-                const int za = entry_rows_of(cur0, nb), zb = cur1 < 0 ? 0 : entry_rows_of(cur1, nb);
-                if (za < kVsaBlock || zb < kVsaBlock) {
-                    const int vl = j + 1 == n_kv ? 2 * n_kv - 1 : 2 * j + 2;
-                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_kv_full(vl % STAGES), (vl / STAGES) & 1, abort_flag))))
-                        break;
-                    const uint32_t vb = sKV + (vl % STAGES) * C::KV_BYTES;
-                    const int na = kVsaBlock - za, nz = na + kVsaBlock - zb;
-                    for (int idx = r; idx < nz * NCH * 8; idx += 128) {
-                        const int u = idx & 7, rc = idx >> 3, c = rc % NCH, k = rc / NCH;
-                        const int rr = k < na ? za + k : kVsaBlock + zb + (k - na);
-                        st_shared_v4(vb + c * BN * 128 + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
-                    }
-                    fence_proxy_async_smem();
                 }
             }
 #pragma unroll
@@ -824,7 +836,7 @@ static cudaError_t launch_vsa_cfg(const CUtensorMap& tmQ, const CUtensorMap& tmK
     }
     const long long ctas = static_cast<long long>(p.Hq) * p.g.nt;
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-    vsa_fwd_sm103a<C><<<static_cast<unsigned>(ctas), 192, C::SMEM_BYTES, st>>>(tmQ, tmK, tmV, p);
+    vsa_fwd_sm103a<C><<<static_cast<unsigned>(ctas), 224, C::SMEM_BYTES, st>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
 }
 
