@@ -323,17 +323,21 @@ __global__ void __launch_bounds__(kMapWarps * 32) vsa_block_map_sm103a(const Vsa
 }
 
 // --------------------------------------------------------------- attention
-template <int D_, int STAGES_>
+template <int D_, int SLOTS_>
 struct VsaCfg {
     static constexpr int D = D_;
-    static constexpr int STAGES = STAGES_;
+    // Ring slots, each one load: K_{u} (its first half) and V_{u-1} (its
+    // second half), so that one barrier covers a step's bytes (slot u = 0
+    // holds K_0 alone, slot u = n V_{n-1} alone).
+    static constexpr int STAGES = SLOTS_;
     static constexpr int BM = 128;                  // two query blocks
     static constexpr int BN = 128;                  // two key blocks
     static constexpr int NCH = D / 64;              // 64-column chunks per row
     static constexpr int Q_BYTES = NCH * BM * 128;
-    static constexpr int KV_BYTES = NCH * BN * 128;
+    static constexpr int KV_BYTES = NCH * BN * 128;  // one K or V tile
+    static constexpr int SLOT_BYTES = 2 * KV_BYTES;
     static constexpr int NUM_BARS = 3 * STAGES + 6;
-    static constexpr int SMEM_BYTES = 1024 + Q_BYTES + STAGES * KV_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int SMEM_BYTES = 1024 + Q_BYTES + STAGES * SLOT_BYTES + NUM_BARS * 8 + 16;
     static constexpr int TMEM_S = 0;           // S buffers at [0, BN) and [BN, 2 BN)
     static constexpr int TMEM_O = 2 * BN;      // O at [2 BN, 2 BN + D)
     static constexpr int TMEM_P = 2 * BN + D;  // P buffers (bf16 pairs) at [TMEM_P, + BN / 2) and [+ BN / 2, + BN)
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(224, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem);
     const uint32_t sKV = sQ + C::Q_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Q_BYTES + STAGES * C::KV_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Q_BYTES + STAGES * C::SLOT_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const uint32_t b_q_full = smem_u32(&bars[0]);
@@ -450,49 +454,55 @@ __global__ void __launch_bounds__(224, 1)
             tma_prefetch_desc(&tmV);
             mbar_arrive_expect_tx(b_q_full, C::Q_BYTES);
             for (int c = 0; c < NCH; ++c) tma_load_3d(sQ + c * BM * 128, &tmQ, b_q_full, c * 64, h, t * BM);
-            // Load t of the MMAs' order: K_0, then K_{j+1} and V_j for each j,
-            // V_{n-1} last; a K or V tile is the two key blocks of list
-            // entries 2 j and 2 j + 1.
+            // Slot load u: K_u (entries 2u, 2u + 1) in its first half for u < n,
+            // V_{u-1} (the previous K tile's blocks) in its second for u >= 1.
+            // A missing second entry repeats the first block (masked for every
+            // row); a bad entry is flagged and block 0 read instead.
             int issued = 0;
-            auto tile_of = [&](int tt) {
-                const bool isv = tt == 2 * n_kv - 1 || (tt > 0 && (tt & 1) == 0);
-                return isv ? (tt == 2 * n_kv - 1 ? n_kv - 1 : tt / 2 - 1) : (tt + 1) / 2;
-            };
-            // the entries of the next load, read one load ahead
-            int ne0 = 0, ne1 = -1;
+            int vb0 = 0, vb1 = 0;  // blocks of the previous K tile
+            int ne0 = 0, ne1 = -1;  // entries of the next K tile, read one load ahead
             if (n_kv > 0) {
                 ne0 = list[0];
                 ne1 = n > 1 ? list[1] : -1;
             }
-            for (int tt = 0; ok && tt < 2 * n_kv; ++tt) {
-                const bool isv = tt == 2 * n_kv - 1 || (tt > 0 && (tt & 1) == 0);
-                const int jt = tile_of(tt);
-                const int e0 = ne0, e1 = ne1;
-                if (tt + 1 < 2 * n_kv) {
-                    const int jn = tile_of(tt + 1);
-                    ne0 = list[2 * jn];
-                    ne1 = 2 * jn + 1 < n ? list[2 * jn + 1] : -1;
+            for (int u = 0; ok && n_kv > 0 && u <= n_kv; ++u) {
+                const bool hk = u < n_kv, hv = u >= 1;
+                int b0 = 0, b1 = 0;
+                if (hk) {
+                    const int e0 = ne0, e1 = ne1;
+                    if (u + 1 < n_kv) {
+                        ne0 = list[2 * u + 2];
+                        ne1 = 2 * u + 3 < n ? list[2 * u + 3] : -1;
+                    }
+                    b0 = e0 >> 9;
+                    b1 = e1 < 0 ? b0 : (e1 >> 9);
+                    if (b0 < 0 || b0 >= nb || b1 < 0 || b1 >= nb) {
+                        if (p.status) atomicOr(p.status, kDevBadIndex);
+                        b0 = (b0 < 0 || b0 >= nb) ? 0 : b0;
+                        b1 = (b1 < 0 || b1 >= nb) ? 0 : b1;
+                    }
                 }
-                // A missing second entry repeats the first block (masked for
-                // every row); a bad entry is flagged and block 0 read instead.
-                int b0 = e0 >> 9, b1 = e1 < 0 ? b0 : (e1 >> 9);
-                if (b0 < 0 || b0 >= nb || b1 < 0 || b1 >= nb) {
-                    if (p.status) atomicOr(p.status, kDevBadIndex);
-                    b0 = (b0 < 0 || b0 >= nb) ? 0 : b0;
-                    b1 = (b1 < 0 || b1 >= nb) ? 0 : b1;
-                }
-                const int s = tt % STAGES, u = tt / STAGES;
-                if (u > 0 && !mbar_wait(b_kv_empty(s), (u - 1) & 1, abort_flag)) {
+                const int s = u % STAGES, w = u / STAGES;
+                if (w > 0 && !mbar_wait(b_kv_empty(s), (w - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const CUtensorMap* m = isv ? &tmV : &tmK;
-                const uint32_t dst = sKV + s * C::KV_BYTES;
-                mbar_arrive_expect_tx(b_kv_full(s), C::KV_BYTES);
+                const uint32_t dst = sKV + s * C::SLOT_BYTES;
+                mbar_arrive_expect_tx(b_kv_full(s), (hk ? C::KV_BYTES : 0) + (hv ? C::KV_BYTES : 0));
                 for (int c = 0; c < NCH; ++c) {
-                    tma_load_3d(dst + c * BN * 128, m, b_kv_full(s), c * 64, kvh, b0 * kVsaBlock);
-                    tma_load_3d(dst + c * BN * 128 + kVsaBlock * 128, m, b_kv_full(s), c * 64, kvh, b1 * kVsaBlock);
+                    if (hk) {
+                        tma_load_3d(dst + c * BN * 128, &tmK, b_kv_full(s), c * 64, kvh, b0 * kVsaBlock);
+                        tma_load_3d(dst + c * BN * 128 + kVsaBlock * 128, &tmK, b_kv_full(s), c * 64, kvh,
+                                    b1 * kVsaBlock);
+                    }
+                    if (hv) {
+                        tma_load_3d(dst + C::KV_BYTES + c * BN * 128, &tmV, b_kv_full(s), c * 64, kvh, vb0 * kVsaBlock);
+                        tma_load_3d(dst + C::KV_BYTES + c * BN * 128 + kVsaBlock * 128, &tmV, b_kv_full(s), c * 64,
+                                    kvh, vb1 * kVsaBlock);
+                    }
                 }
+                vb0 = b0;
+                vb1 = b1;
                 ++issued;
             }
             if (!ok || *abort_flag) {
@@ -510,25 +520,14 @@ __global__ void __launch_bounds__(224, 1)
         const bool leader = elect_one();
         const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
         const uint64_t dK = sdesc_sw128(sKV, 16, 1024);
-        const uint64_t dV = sdesc_sw128(sKV, BN * 128, 1024);
+        const uint64_t dV = sdesc_sw128(sKV + C::KV_BYTES, BN * 128, 1024);
         auto wait_all = [&](uint32_t bar, uint32_t ph) {
             return __all_sync(0xffffffffu, mbar_wait(bar, ph, abort_flag));
         };
-        // Stages are read in the producer's order; cs / cph: the next one and its phase.
-        int cs = 0;
-        uint32_t cph = 0;
-        auto next_stage = [&]() {
-            if (++cs == STAGES) {
-                cs = 0;
-                cph ^= 1u;
-            }
-        };
-        auto issue_s = [&](int j) -> bool {
-            if (!wait_all(b_kv_full(cs), cph)) return false;
-            tc_fence_after();
+        auto issue_s = [&](int j, int s) {  // S_j from the K half of slot s
             if (leader) {
                 const uint32_t dS = tmem + C::TMEM_S + (j & 1) * BN;
-                const uint64_t b0 = dK + static_cast<uint64_t>(cs * (C::KV_BYTES >> 4));
+                const uint64_t b0 = dK + static_cast<uint64_t>(s * (C::SLOT_BYTES >> 4));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = ((kk >> 2) * BM * 128 + (kk & 3) * 32) >> 4;
@@ -536,32 +535,38 @@ __global__ void __launch_bounds__(224, 1)
                     mma_bf16_ss(dS, dQ + oa, b0 + ob, kIdS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(b_s_full(j & 1));
-                mma_commit(b_kv_empty(cs));
             }
             __syncwarp();
-            next_stage();
-            return true;
         };
         ok = wait_all(b_q_full, 0);
-        if (ok && n_kv > 0) ok = issue_s(0);
+        if (ok && n_kv > 0 && (ok = wait_all(b_kv_full(0), 0))) {  // slot load 0: K_0 alone
+            tc_fence_after();
+            issue_s(0, 0);
+            if (leader) mma_commit(b_kv_empty(0));
+            __syncwarp();
+        }
         for (int j = 0; ok && j < n_kv; ++j) {
-            if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
+            // slot load j + 1: K_{j+1} (but for the last step) and V_j
+            const int s = (j + 1) % STAGES;
+            const uint32_t ph = static_cast<uint32_t>((j + 1) / STAGES) & 1u;
+            if (!(ok = wait_all(b_kv_full(s), ph))) break;
+            tc_fence_after();
+            if (j + 1 < n_kv) issue_s(j + 1, s);
             if (!(ok = wait_all(b_p_full, j & 1))) break;
-            if (!(ok = wait_all(b_v_ready(cs), cph))) break;  // V_j landed, padding rows zeroed
+            if (!(ok = wait_all(b_v_ready(s), ph))) break;  // V_j's padding rows zeroed
             tc_fence_after();
             if (leader) {
                 // O += P_j V_j, P_j (bf16 pairs) read from its TMEM buffer
-                const uint64_t b0 = dV + static_cast<uint64_t>(cs * (C::KV_BYTES >> 4));
+                const uint64_t b0 = dV + static_cast<uint64_t>(s * (C::SLOT_BYTES >> 4));
                 const uint32_t a = tmem + C::TMEM_P + (j & 1) * (BN / 2);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_bf16_ts(tmem + C::TMEM_O, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdO,
                                 (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(b_pv_done);
-                mma_commit(b_kv_empty(cs));
+                mma_commit(b_kv_empty(s));
             }
             __syncwarp();
-            next_stage();
         }
         if (leader) mma_commit(b_drain);  // all of the above finishes before TMEM is released
         __syncwarp();
@@ -570,26 +575,25 @@ __global__ void __launch_bounds__(224, 1)
         // ----------------------------------------------------------- V padding
         // Rows of a V tile past each key block's token count are padding,
         // which may hold anything, NaN included; P is 0 there but 0 * NaN is
-        // not.  This warp follows the ring in load order: once a load has
-        // landed it zeroes a V tile's padding rows, then passes the stage on
-        // (b_v_ready), which the MMA warp waits for before P V.  It passes K
-        // loads on too, only after they land, so that no stage's b_v_ready
-        // runs a phase ahead of its loads.
-        for (int tt = 0; ok && tt < 2 * n_kv; ++tt) {
-            const int s = tt % STAGES;
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_kv_full(s), (tt / STAGES) & 1, abort_flag)))) break;
-            const bool isv = tt == 2 * n_kv - 1 || (tt > 0 && (tt & 1) == 0);
-            if (isv) {
-                const int jv = tt == 2 * n_kv - 1 ? n_kv - 1 : tt / 2 - 1;
+        // not.  This warp follows the ring in load order: once a slot load
+        // has landed it zeroes the padding rows of its V tile, then passes
+        // the slot on (b_v_ready), which the MMA warp waits for before P V.
+        // It passes slot load 0 (K_0 alone) on too, after it lands, so that
+        // no slot's b_v_ready runs a phase ahead of its loads.
+        for (int u = 0; ok && n_kv > 0 && u <= n_kv; ++u) {
+            const int s = u % STAGES;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(b_kv_full(s), (u / STAGES) & 1, abort_flag)))) break;
+            if (u >= 1) {  // V_{u-1} in the slot's second half
+                const int jv = u - 1;
                 const int ea = list[2 * jv], eb = 2 * jv + 1 < n ? list[2 * jv + 1] : -1;
                 const int za = entry_rows_of(ea, nb), zb = eb < 0 ? 0 : entry_rows_of(eb, nb);
                 if (za < kVsaBlock || zb < kVsaBlock) {
-                    const uint32_t vb = sKV + s * C::KV_BYTES;
+                    const uint32_t vb = sKV + s * C::SLOT_BYTES + C::KV_BYTES;
                     const int na = kVsaBlock - za, nz = na + kVsaBlock - zb;
                     for (int idx = lane; idx < nz * NCH * 8; idx += 32) {
-                        const int u = idx & 7, rc = idx >> 3, c = rc % NCH, k = rc / NCH;
+                        const int uu = idx & 7, rc = idx >> 3, c = rc % NCH, k = rc / NCH;
                         const int rr = k < na ? za + k : kVsaBlock + zb + (k - na);
-                        st_shared_v4(vb + c * BN * 128 + rr * 128 + u * 16, 0u, 0u, 0u, 0u);
+                        st_shared_v4(vb + c * BN * 128 + rr * 128 + uu * 16, 0u, 0u, 0u, 0u);
                     }
                     fence_proxy_async_smem();
                 }
@@ -756,8 +760,8 @@ __global__ void __launch_bounds__(224, 1)
     }
 }
 
-using VsaCfg64 = VsaCfg<64, 12>;
-using VsaCfg128 = VsaCfg<128, 6>;
+using VsaCfg64 = VsaCfg<64, 6>;
+using VsaCfg128 = VsaCfg<128, 3>;
 
 // ------------------------------------------------------------------ launchers
 static int grid_for(long long units, int per_cta, int num_sms, int ctas_per_sm) {
