@@ -1021,6 +1021,25 @@ def test_vsa_block_map_matches_the_oracle(prefix, video, hq, hkv, D, topk):
     _vsa_check_map(bm, q, k, blocks, npre, topk, scale)
 
 
+def test_vsa_block_map_with_fewer_query_blocks_per_cta():
+    """6000 video blocks: the scores of eight query blocks against every key
+    block no longer fit in shared memory, so the kernel takes four per CTA."""
+    prefix, video, hq, hkv, D, topk = [], (4, 240, 400), 1, 1, 64, 8
+    q, k, _ = _vsa_inputs(66, prefix, video, hq, hkv, D)
+    plan = gb.VsaPlan(prefix, video, dev())
+    blocks, npre = oracle.vsa_blocks(prefix, video)
+    assert len(blocks) == 6000
+    scale = 1.0 / math.sqrt(D)
+    st = status_word()
+    pq = gb.attn_vsa_pool(gb.attn_gather_rows(q.to(dev()), plan.tile_index), plan.block_sizes)
+    pk = gb.attn_vsa_pool(gb.attn_gather_rows(k.to(dev()), plan.tile_index), plan.block_sizes)
+    kv_list, kv_num = gb.attn_vsa_block_map(pq, pk, plan.block_sizes, npre, topk, scale, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    bm = vsa_map_from_lists(kv_list, kv_num, len(blocks), npre, topk, [len(b) for b in blocks])
+    _vsa_check_map(bm, q, k, blocks, npre, topk, scale)
+
+
 @pytest.mark.parametrize("prefix,video,hq,hkv,D,topk,out_dtype,tiled", [
     ([100, 37], (5, 9, 10), 4, 2, 128, 5, torch.float32, False),
     ([100, 37], (5, 9, 10), 4, 2, 128, 5, torch.bfloat16, False),
