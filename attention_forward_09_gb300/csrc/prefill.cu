@@ -667,8 +667,7 @@ struct Prefill2Cfg {
     static_assert(2 * BN + 2 * D <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(2 * BM * D * 4 <= STAGES * KV_BYTES && 2 * BM * 8 <= 2 * QT_BYTES, "split-merge staging");
-    static_assert(KV_BYTES == NCH * BM * 128 && 2 * ((D + 31) / 32) <= (STAGES - 1) * NCH &&
-                      (D + 31) / 32 <= (STAGES - 2) * NCH, "output staging slots");
+    static_assert(KV_BYTES == NCH * BM * 128 && STAGES >= 3, "output staging stages");
 };
 
 // Merge of an item split along the keys over a cluster of p.split CTAs (the
@@ -1042,7 +1041,13 @@ __global__ void __launch_bounds__(384, 1)
             // Tiles whose staged output the next loads must wait for, and the
             // staging phases of each tile waited so far (persistent launches).
             bool pend[2] = {false, false};
+            int pend_stage[2] = {-1, -1};  // the K/V stage each pending tile's output occupies
             uint32_t staged_waits[2] = {0u, 0u};
+            auto wait_staged = [&](int x) {
+                ok = ok && mbar_wait(b_staged(x), staged_waits[x] & 1, abort_flag);
+                ++staged_waits[x];
+                pend[x] = false;
+            };
             Walk W = walk_here(1u);  // lane 0 alone
             for (int i = 0; ok; ++i) {
                 const Item I = item_at(i, W);
@@ -1059,20 +1064,14 @@ __global__ void __launch_bounds__(384, 1)
                                     I.q_start + I.q0 + x * TPT);
                 ++nq;
                 for (int tt = 0; tt < 2 * I.nmax; ++tt, ++t) {
-                    // The output of earlier items may be staged in every K/V stage
-                    // but the one K_0 goes to, until its stores have read it.
-                    // Each tile that staged arrives once on its own barrier, so
-                    // these waits meet every phase in order.
-                    if (tt == 1 && (pend[0] || pend[1])) {
-                        for (int x = 0; x < 2 && ok; ++x)
-                            if (pend[x]) {
-                                ok = mbar_wait(b_staged(x), staged_waits[x] & 1, abort_flag);
-                                ++staged_waits[x];
-                                pend[x] = false;
-                            }
-                        if (!ok) break;
-                    }
                     const int s = t % STAGES, u = t / STAGES;
+                    // An earlier item's output staged in this stage must have
+                    // been read by its stores first (each tile that staged
+                    // arrives once on its own barrier, so the waits meet every
+                    // phase in order).
+                    for (int x = 0; x < 2; ++x)
+                        if (pend[x] && pend_stage[x] == s) wait_staged(x);
+                    if (!ok) break;
                     if (u > 0 && !mbar_wait(b_kv_empty(s), (u - 1) & 1, abort_flag)) {
                         ok = false;
                         break;
@@ -1091,7 +1090,14 @@ __global__ void __launch_bounds__(384, 1)
                     for (int c = 0; c < NCH; ++c)
                         tma_load_3d(sKV + s * C::KV_BYTES + c * BN * 128, m, b_kv_full(s), c * 64, I.kvh, row);
                 }
-                for (int x = 0; x < 2; ++x) pend[x] = pend[x] || stages_output(I, x);
+                if (!ok) break;
+                for (int x = 0; x < 2; ++x)
+                    if (stages_output(I, x)) {
+                        if (pend[x]) wait_staged(x);  // an older staging not yet passed by the loads
+                        pend[x] = true;
+                        pend_stage[x] = (t + STAGES - 2 + x) % STAGES;  // t: the next item's K_0
+                    }
+                if (!ok) break;
             }
             if (!ok || *abort_flag) {
                 // Let every copy this thread started land before the CTA retires.
@@ -1353,31 +1359,24 @@ __global__ void __launch_bounds__(384, 1)
         } else if (nmax > 0 && qfirst + TPT <= Lq && (x == 1 ? nB >= nA : nA >= nB)) {
             // A tile wholly inside its document leaves through shared memory:
             // its rows are staged in the TMA 128-byte-swizzled box layout
-            // (128 rows x 128 bytes per 16 KB box) in slots of the K/V area
+            // (128 rows x 128 bytes per 16 KB box) in a stage of the K/V area
             // and written by tiled TMA stores.  Only a tile that finishes last
             // (or with the other) stages: once PV_X(last) is complete the only
             // MMA that may still read the K/V area is PV_B(last), when tile A
-            // finishes with nA == nB: it reads V_{n-1}, whose stage no slot
-            // uses.  A tile with fewer KV tiles than the other (tile A of a
-            // causal item, or tile B wholly in the padding of a padded batch)
-            // stores directly instead, while the other tile computes on.
+            // finishes with nA == nB: it reads V_{n-1}, whose stage tile A
+            // does not use.  A tile with fewer KV tiles than the other (tile A
+            // of a causal item, or tile B wholly in the padding of a padded
+            // batch) stores directly instead, while the other tile computes on.
             const bool f32 = p.out_f32 != 0;
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             const int boxes = f32 ? D / 32 : (D + 63) / 64, cols = f32 ? 32 : 64;  // 128-byte boxes per row
-            // Stages for the boxes: never the next item's K_0 stage (sk, loaded
-            // while this epilogue runs); tile A never V_{n-1}'s (sv), which
-            // PV_B(last) may still read: the stages other than sv and sk come
-            // first, sv last, and tile A's boxes fit in the first ones.
-            const int sv = (tbase + 2 * nmax - 1 + STAGES) % STAGES, sk = (tbase + 2 * nmax) % STAGES;
-            const int lo = min(sv, sk), hi = max(sv, sk);
-            auto slot_addr = [&](int b) {  // box b of this tile: the (x * boxes + b)-th usable 16 KB slot
-                const int i = x * boxes + b, k = i / NCH;
-                int st = k;
-                if (st >= lo) ++st;
-                if (st >= hi) ++st;
-                if (k == STAGES - 2) st = sv;
-                return sKV + static_cast<uint32_t>(st * NCH + i % NCH) * (BM * 128);
-            };
+            // One K/V stage per tile, NCH boxes at a time: tile B's is V_{n-1}'s
+            // (PV_B(last) is complete here), tile A's K_{n-1}'s (every S product
+            // is complete once PV_A(last) is; PV_B(last) reads only V_{n-1}).
+            // Neither is the next item's K_0 stage, nor those of its next loads
+            // but the last two of a ring turn, which wait for these stores.
+            const int sk = (tbase + 2 * nmax) % STAGES;
+            const uint32_t stage_base = sKV + static_cast<uint32_t>((sk + STAGES - 2 + x) % STAGES) * C::KV_BYTES;
             const int sw = r & 7;
             auto load_scaled = [&](int c, uint32_t (&o)[32]) {
                 if (n_kv > 0 && ok) {
@@ -1390,39 +1389,45 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
             };
-            if (f32) {  // 32 columns = one 128-byte box row, 8 units of 16 bytes
+            for (int b0 = 0; b0 < boxes; b0 += NCH) {
+                const int b1 = min(boxes, b0 + NCH);
+                if (b0 > 0) named_bar_sync(1 + x, 128);  // the previous boxes' stores have read the stage
+                if (f32) {  // 32 columns = one 128-byte box row, 8 units of 16 bytes
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    load_scaled(c, o);
-                    const uint32_t rb = slot_addr(c) + r * 128;
+                    for (int b = b0; b < b1; ++b) {
+                        uint32_t o[32];
+                        load_scaled(b, o);
+                        const uint32_t rb = stage_base + static_cast<uint32_t>(b - b0) * (BM * 128) + r * 128;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        st_shared_v4(rb + ((k ^ sw) << 4), o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                        for (int k = 0; k < 8; ++k)
+                            st_shared_v4(rb + ((k ^ sw) << 4), o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                    }
+                } else {    // 32 columns = half a box row
+#pragma unroll 1
+                    for (int c = 2 * b0; c < 2 * b1 && c < D / 32; ++c) {
+                        uint32_t o[32];
+                        load_scaled(c, o);
+                        const uint32_t rb = stage_base + static_cast<uint32_t>((c >> 1) - b0) * (BM * 128) + r * 128;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            st_shared_v4(rb + ((((c & 1) * 4 + k) ^ sw) << 4),
+                                         pack_bf16x2(__uint_as_float(o[8 * k]), __uint_as_float(o[8 * k + 1])),
+                                         pack_bf16x2(__uint_as_float(o[8 * k + 2]), __uint_as_float(o[8 * k + 3])),
+                                         pack_bf16x2(__uint_as_float(o[8 * k + 4]), __uint_as_float(o[8 * k + 5])),
+                                         pack_bf16x2(__uint_as_float(o[8 * k + 6]), __uint_as_float(o[8 * k + 7])));
+                    }
                 }
-            } else {    // 32 columns = half a box row
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    load_scaled(c, o);
-                    const uint32_t rb = slot_addr(c >> 1) + r * 128;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        st_shared_v4(rb + ((((c & 1) * 4 + k) ^ sw) << 4),
-                                     pack_bf16x2(__uint_as_float(o[8 * k]), __uint_as_float(o[8 * k + 1])),
-                                     pack_bf16x2(__uint_as_float(o[8 * k + 2]), __uint_as_float(o[8 * k + 3])),
-                                     pack_bf16x2(__uint_as_float(o[8 * k + 4]), __uint_as_float(o[8 * k + 5])),
-                                     pack_bf16x2(__uint_as_float(o[8 * k + 6]), __uint_as_float(o[8 * k + 7])));
+                fence_proxy_async_smem();  // generic-proxy writes -> the TMA engine
+                named_bar_sync(1 + x, 128);
+                if (r == 0) {
+                    for (int b = b0; b < b1; ++b)
+                        tma_store_3d(&tmO, stage_base + static_cast<uint32_t>(b - b0) * (BM * 128), b * cols, h,
+                                     q_start + qfirst);
+                    bulk_commit();
+                    bulk_wait_read0();  // the staging area must outlive the reads
                 }
             }
-            fence_proxy_async_smem();  // generic-proxy writes -> the TMA engine
-            named_bar_sync(1 + x, 128);
-            if (r == 0) {
-                for (int b = 0; b < boxes; ++b) tma_store_3d(&tmO, slot_addr(b), b * cols, h, q_start + qfirst);
-                bulk_commit();
-                bulk_wait_read0();  // the staging area must outlive the reads
-                if (persist) mbar_arrive(b_staged(x));
-            }
+            if (r == 0 && persist) mbar_arrive(b_staged(x));
             if (ok && p.lse) {
                 const long long lrow = p.lse_row_global ? (q_start + row) : row;
                 p.lse[doc * p.lse_bstride + hh * p.lse_hstride + lrow] =
