@@ -1000,6 +1000,9 @@ __global__ void __launch_bounds__(384, 1)
         if (!item_at(0, W0).valid) return;
     }
     if (!split && status_has_timeout(p.status, kDevTimeout)) return;
+    // The split last wave (launched behind this grid, independent of its
+    // results) may take each SM as soon as this grid's CTA there is done.
+    if (!split) grid_launch_dependents();
 
     // ------------------------------------------------------------------ setup
     if (threadIdx.x == 0) {
@@ -1488,6 +1491,9 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
+    // A split last wave overlaps the end of the grid before it: it finishes
+    // only after that grid, so the stream's later work still follows both.
+    if (split) grid_dependency_wait();
 }
 
 // ---------------------------------------------------------------- launchers
@@ -1642,17 +1648,20 @@ static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUten
         q.item_base = static_cast<int>(pl.n_full);
         q.split = pl.split;
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute at[1];
+        cudaLaunchAttribute at[2];
         at[0].id = cudaLaunchAttributeClusterDimension;
         at[0].val.clusterDim.x = pl.split;
         at[0].val.clusterDim.y = 1;
         at[0].val.clusterDim.z = 1;
+        // behind the full-wave launch: start as its CTAs finish
+        at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.gridDim = dim3(static_cast<unsigned>((pl.n_items - pl.n_full) * pl.split));
         cfg.blockDim = dim3(384);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = stream;
         cfg.attrs = at;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = pl.n_full > 0 ? 2 : 1;
         e = cudaLaunchKernelEx(&cfg, kernel, tmQ, tmK, tmV, tmO, q);
         if (e != cudaSuccess) return e;
     }
