@@ -774,7 +774,12 @@ __device__ __forceinline__ void split_merge(uint8_t* smem, uint32_t sO, uint32_t
     cluster_sync();  // no CTA leaves while another still reads its shared memory
 }
 
-template <class C, bool PAGED, bool WALK>
+// DEFER (dense launches of few KV tiles): the wait for the last staged
+// stores' reads, and the b_staged arrival, move from the end of the epilogue
+// to after the next item's first P hand-over, where they rarely wait.  Its
+// own instantiation: the extra code in the step loop costs the long-item
+// launches a little.
+template <class C, bool PAGED, bool WALK, bool DEFER = false>
 __global__ void __launch_bounds__(384, 1)
     fmha2_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -1264,6 +1269,14 @@ __global__ void __launch_bounds__(384, 1)
         const float c2 = p.scale_log2;
         uint32_t sdone = 0;  // S_X products of earlier items (phase count of s_full and pv_done)
         int tbase = 0;       // ring index of the item's K_0 (as the producer and MMA warps count)
+        bool owe_staged = false;  // (DEFER, thread r == 0) the previous item's last stores
+        auto settle_staged = [&]() {
+            if (owe_staged) {
+                bulk_wait_read0();
+                mbar_arrive(b_staged(x));
+                owe_staged = false;
+            }
+        };
         Walk W = walk_here(0xffffffffu);
         for (int i = 0; ok; ++i) {
         const Item I = item_at(i, W);
@@ -1347,7 +1360,9 @@ __global__ void __launch_bounds__(384, 1)
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(b_p_full(x));
+            if constexpr (DEFER) settle_staged();
         }
+        if constexpr (DEFER) settle_staged();  // (an item without KV tiles, or a loop left early)
         ok = __all_sync(0xffffffffu, ok);
         if (ok && n_kv > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(b_pv_done(x), (sdone + n_kv - 1) & 1, abort_flag));
@@ -1427,10 +1442,13 @@ __global__ void __launch_bounds__(384, 1)
                         tma_store_3d(&tmO, stage_base + static_cast<uint32_t>(b - b0) * (BM * 128), b * cols, h,
                                      q_start + qfirst);
                     bulk_commit();
-                    bulk_wait_read0();  // the staging area must outlive the reads
+                    if (DEFER && persist && b1 == boxes)
+                        owe_staged = true;  // waited for after the next item's first P
+                    else
+                        bulk_wait_read0();  // the staging area must outlive the reads
                 }
             }
-            if (r == 0 && persist) mbar_arrive(b_staged(x));
+            if (r == 0 && persist && !DEFER) mbar_arrive(b_staged(x));
             if (ok && p.lse) {
                 const long long lrow = p.lse_row_global ? (q_start + row) : row;
                 p.lse[doc * p.lse_bstride + hh * p.lse_hstride + lrow] =
@@ -1478,6 +1496,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         tbase += 2 * nmax;
         }  // items
+        if constexpr (DEFER) settle_staged();
     }
 
     // --------------------------------------------------------------- teardown
@@ -1507,7 +1526,7 @@ using Cfg256 = PrefillCfg<256, 128, 5, 2>;
 
 // Sets the dynamic shared-memory limit of `kernel` once per device (one flag
 // set per instantiation: the kernels of several configurations share a type).
-template <class C, bool PAGED, bool WALK = false, class K>
+template <class C, bool PAGED, bool WALK = false, bool DEFER = false, class K>
 static cudaError_t set_smem_attr(K kernel, int bytes) {
     static bool done[64];
     static std::mutex mu;
@@ -1572,7 +1591,7 @@ static int resident_clusters(K kernel, int c) {
 // full, its items go to a second launch in which a cluster of `split` CTAs
 // shares each item along the keys and merges the partial results on chip,
 // so that the wave lasts about 1/split of an item instead of a whole one.
-template <class C, bool PAGED, class K>
+template <class C, bool PAGED, bool DEFER = false, class K>
 static cudaError_t plan_two_tile(K kernel, const PrefillParams& p, int num_sms, PrefillPlan* pl) {
     *pl = PrefillPlan{};
     if (p.cu_q) {
@@ -1587,7 +1606,7 @@ static cudaError_t plan_two_tile(K kernel, const PrefillParams& p, int num_sms, 
                       p.num_docs <= kWalkMaxDocs;
         return cudaSuccess;
     }
-    cudaError_t e = set_smem_attr<C, PAGED>(kernel, C::SMEM_BYTES);
+    cudaError_t e = set_smem_attr<C, PAGED, false, DEFER>(kernel, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     pl->tiles = (p.Sq + 255) / 256;
     pl->n_items = static_cast<long long>(pl->tiles) * p.Hq * p.num_docs;
@@ -1607,13 +1626,13 @@ static cudaError_t plan_two_tile(K kernel, const PrefillParams& p, int num_sms, 
     return cudaSuccess;
 }
 
-template <class C, bool PAGED, class K>
+template <class C, bool PAGED, bool DEFER = false, class K>
 static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                    const CUtensorMap& tmO, const PrefillParams& p, int num_sms, cudaStream_t stream) {
     PrefillPlan pl;
-    cudaError_t e = plan_two_tile<C, PAGED>(kernel, p, num_sms, &pl);
+    cudaError_t e = plan_two_tile<C, PAGED, DEFER>(kernel, p, num_sms, &pl);
     if (e != cudaSuccess) return e;
-    e = set_smem_attr<C, PAGED>(kernel, C::SMEM_BYTES);
+    e = set_smem_attr<C, PAGED, false, DEFER>(kernel, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     PrefillParams q = p;
     q.split = 0;
@@ -1673,9 +1692,14 @@ static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUten
 template <class C>
 static cudaError_t two_tile(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             const CUtensorMap& tmO, const PrefillParams& p, int num_sms, cudaStream_t stream) {
-    return p.block_table ? launch_two_tile<C, true>(fmha2_fwd_sm103a<C, true, false>, tmQ, tmK, tmV, tmO, p, num_sms, stream)
-                         : launch_two_tile<C, false>(fmha2_fwd_sm103a<C, false, false>, tmQ, tmK, tmV, tmO, p, num_sms,
-                                                     stream);
+    if (p.block_table)
+        return launch_two_tile<C, true>(fmha2_fwd_sm103a<C, true, false>, tmQ, tmK, tmV, tmO, p, num_sms, stream);
+    // dense launches of at most 8 KV tiles per item spend much of an item in
+    // its epilogue: the instantiation that defers the staged stores' wait
+    if (!p.cu_q && !p.causal && (p.Sk + C::BN - 1) / C::BN <= 8)
+        return launch_two_tile<C, false, true>(fmha2_fwd_sm103a<C, false, false, true>, tmQ, tmK, tmV, tmO, p, num_sms,
+                                               stream);
+    return launch_two_tile<C, false>(fmha2_fwd_sm103a<C, false, false>, tmQ, tmK, tmV, tmO, p, num_sms, stream);
 }
 
 template <class C>
