@@ -1639,8 +1639,9 @@ static cudaError_t launch_two_tile(K kernel, const CUtensorMap& tmQ, const CUten
     q.item_base = 0;
     if (p.cu_q && pl.persist) {  // the walk is its own instantiation (non-paged only)
         if (PAGED) return cudaErrorInvalidValue;
-        auto walk = fmha2_fwd_sm103a<C, false, true>;
-        if ((e = set_smem_attr<C, false, true>(walk, C::SMEM_BYTES)) != cudaSuccess) return e;
+        // (packed documents give many items of few KV tiles: the DEFER form)
+        auto walk = fmha2_fwd_sm103a<C, false, true, true>;
+        if ((e = set_smem_attr<C, false, true, true>(walk, C::SMEM_BYTES)) != cudaSuccess) return e;
         q.linear = 2;
         q.persist = 1;
         walk<<<static_cast<unsigned>(num_sms), 384, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, q);
