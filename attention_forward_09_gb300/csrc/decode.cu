@@ -207,7 +207,6 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_hgroups = p.Hkv * (p.group / p.heads_per_cta);
     if (status_has_timeout(p.status, kDevTimeout)) return;
-    const int total = p.sched[1] * n_hgroups;  // items in this launch
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -219,6 +218,11 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmKV);
     }
+    // Launched behind paged_schedule, which may still run: its list and
+    // counters are read only past this point.
+    grid_dependency_wait();
+    grid_launch_dependents();  // paged_combine may queue up (it waits for this grid)
+    const int total = p.sched[1] * n_hgroups;  // items in this launch
     __syncthreads();
     if (threadIdx.x == 0) {  // prologue: the first STAGES slices
         Cursor cu;
@@ -464,6 +468,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1)
 // seq_lens outside [0, min(max_seq_len, 128 * max_blocks_per_seq)].
 __global__ void __launch_bounds__(1024) paged_schedule(const PagedParams p) {
     __shared__ int count[17], offset[17];
+    grid_launch_dependents();  // the decode grid sets up while this runs
     const int bps = p.blocks_per_split;
     const int cap = min(p.max_seq_len, p.max_blocks_per_seq * kBlk);
     if (threadIdx.x <= 16) count[threadIdx.x] = 0;
@@ -508,6 +513,7 @@ __global__ void __launch_bounds__(1024) paged_schedule(const PagedParams p) {
 
 // Merge the split partials of each (sequence, query head).
 __global__ void __launch_bounds__(128) paged_combine(const PagedParams p, int D) {
+    grid_dependency_wait();  // launched behind the decode grid, whose partials it reads
     const int s = blockIdx.x / p.Hq, h = blockIdx.x % p.Hq;
     int L = p.seq_lens[s];
     const int cap = min(p.max_seq_len, p.max_blocks_per_seq * kBlk);
@@ -576,10 +582,26 @@ static cudaError_t launch_paged_cfg(const CUtensorMap& tm, const PagedParams& p,
     paged_schedule<<<1, 1024, 0, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    paged_decode_sm103a<C><<<grid, 32 * kWarps, C::SMEM_BYTES, st>>>(tm, p);
-    e = cudaGetLastError();
+    // The decode and combine grids are programmatic dependents of the grid
+    // before them: they may start while it runs and wait for it
+    // (griddepcontrol.wait) before they read what it writes.
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(32 * kWarps);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, paged_decode_sm103a<C>, tm, p);
     if (e != cudaSuccess) return e;
-    paged_combine<<<p.num_seqs * p.Hq, 128, 0, st>>>(p, C::D);
+    cfg.gridDim = dim3(static_cast<unsigned>(p.num_seqs * p.Hq));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, paged_combine, p, static_cast<int>(C::D));
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
